@@ -1,0 +1,435 @@
+/*
+ * qmm_oracle.c -- plain, slow, CPU reference for the GGML block-quantized
+ * linear layer (Q8_0 and Q4_K).  TEST INFRASTRUCTURE ONLY: the tests, the
+ * package's smoke check and the CPU-baseline leg of the benchmark call this
+ * library; the product path never does.  It shares no code, header, table or
+ * constant with the CUDA library.
+ *
+ * Source of the method.  The mistral.rs documentation page "Quantization
+ * types" names the two formats and their nominal widths: table "Q*K family"
+ * (q4k, 4 bits) and table "Legacy GGML types" (q8_0, 8 bits); its section
+ * "Numeric shorthands" maps `--isq 8` to Q8_0 and `--isq 4` to Q4K on CUDA.
+ * The same page, in its opening section, defines ISQ as quantizing the
+ * unquantized weights at load time.  The pages give no byte layout and no
+ * quantizer formula; the ones written here are this library's stated reading:
+ *
+ *   Q8_0 block (32 weights, 34 bytes):
+ *     amax = max |x_i|; d = amax / 127 (fp32 division); d16 = fp16_rne(d);
+ *     q_i = clamp(roundf(x_i / float(d16)), -127, 127), or 0 when d16 == 0;
+ *     bytes: d16 little-endian, then int8 q[0..31].
+ *   Q4_K superblock (256 weights = 8 sub-blocks of 32, 144 bytes):
+ *     mn_j = min(0, min_i x_i); mx_j = max_i x_i;
+ *     s_j = (mx_j - mn_j) / 15;  m_j = 0 - mn_j;
+ *     d16 = fp16_rne(max_j s_j / 63); dmin16 = fp16_rne(max_j m_j / 63);
+ *     sc_j = clamp(roundf(s_j / d16), 0, 63)   (0 when d16 == 0);
+ *     mc_j = clamp(roundf(m_j / dmin16), 0, 63) (0 when dmin16 == 0);
+ *     S_j = d16 * sc_j; Mn_j = dmin16 * mc_j  (both exact in fp32);
+ *     q_i = clamp(roundf((x_i + Mn_j) / S_j), 0, 15), or 0 when S_j == 0;
+ *     dequantized value: S_j * q - Mn_j.
+ *     bytes 0-1 d16, 2-3 dmin16, 4-15 the twelve scale bytes s[]:
+ *       j<4: s[j]   = sc_j | (sc_{j+4} >> 4) << 6
+ *            s[j+4] = mc_j | (mc_{j+4} >> 4) << 6
+ *            s[j+8] = (sc_{j+4} & 15) | (mc_{j+4} & 15) << 4
+ *     bytes 16-143: four 32-byte chunks c; byte 32c+l holds weight l of
+ *       sub-block 2c in its low nibble and weight l of sub-block 2c+1 in its
+ *       high nibble.
+ *   matmul: Y[m][n] = sum_k double(w^[n][k]) * double(x[m][k]) over the exactly
+ *     dequantized weights w^ and the bf16 activations, summed in k order in
+ *     fp64; A[m][n] = sum_k |w^ x| in fp64 (the scale of the error bound).
+ *
+ * Build: plain C11, -O2 -ffp-contract=off (no fused multiply-add, IEEE single
+ * arithmetic on x86-64 SSE), optionally -fopenmp (rows are independent, so the
+ * thread count never changes a result).
+ *
+ * fp16 encoding is written here from the IEEE 754 binary16 definition
+ * (1 sign bit, 5 exponent bits with bias 15, 10 fraction bits, subnormals,
+ * round to nearest, ties to even); the tests pin it against two independent
+ * library conversions.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------ */
+/* IEEE 754 binary16 and bfloat16                                      */
+/* ------------------------------------------------------------------ */
+
+/* binary16 -> float.  E == 0: subnormal F * 2^-24; E == 31: inf / NaN;
+ * otherwise (1024 + F) * 2^(E - 25). */
+float orc_f16_to_f32(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int E = (h >> 10) & 31;
+    int F = h & 1023;
+    double v;
+    if (E == 0)
+        v = ldexp((double)F, -24);
+    else if (E == 31)
+        v = F ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + F), E - 25);
+    return (float)(sign ? -v : v);
+}
+
+/* float -> binary16, round to nearest, ties to even.
+ * For finite |f| with binary exponent e = floor(log2 |f|), clamped below at
+ * -14 (the subnormal range shares the exponent of the smallest normal), the
+ * representable neighbours are integer multiples of the quantum 2^(e-10).
+ * N = rint(|f| / 2^(e-10)) (exact scaling in double, rint rounds ties to
+ * even) is the significand; the encoding of N * 2^(e-10) is then
+ * (e + 14) * 1024 + N for every case: N < 1024 only happens for e == -14
+ * (a subnormal, field E = 0), N == 2048 is a carry into the next binade.
+ * A result of 2^16 or more (|f| >= 65520) is an overflow to infinity. */
+uint16_t orc_f32_to_f16(float f)
+{
+    uint16_t sign = signbit(f) ? 0x8000 : 0;
+    double a = fabs((double)f);
+    if (isnan(f))
+        return (uint16_t)(sign | 0x7E00);
+    if (a == 0.0)
+        return sign;
+    if (isinf(f) || a >= 65520.0)
+        return (uint16_t)(sign | 0x7C00);
+    int ex;
+    frexp(a, &ex);          /* a = m * 2^ex, m in [0.5, 1) */
+    int e = ex - 1;         /* a in [2^e, 2^(e+1)) */
+    if (e < -14)
+        e = -14;
+    double N = rint(ldexp(a, 10 - e));
+    long bits = (long)(e + 14) * 1024 + (long)N;
+    return (uint16_t)(sign | (uint16_t)bits);
+}
+
+/* Element-wise versions of the two conversions above (for the tests). */
+void orc_f32_to_f16_array(const float *x, uint16_t *h, int64_t n)
+{
+    for (int64_t i = 0; i < n; i++)
+        h[i] = orc_f32_to_f16(x[i]);
+}
+
+void orc_f16_to_f32_array(const uint16_t *h, float *x, int64_t n)
+{
+    for (int64_t i = 0; i < n; i++)
+        x[i] = orc_f16_to_f32(h[i]);
+}
+
+/* bfloat16 is the upper half of a binary32: widening is exact. */
+float orc_bf16_to_f32(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+static float load_src(int src_kind, const void *src, int64_t idx)
+{
+    if (src_kind == 0)
+        return orc_bf16_to_f32(((const uint16_t *)src)[idx]);
+    return ((const float *)src)[idx];
+}
+
+static float clampf(float v, float lo, float hi)
+{
+    if (v < lo)
+        return lo;
+    if (v > hi)
+        return hi;
+    return v;
+}
+
+static void put_u16(uint8_t *p, uint16_t v)
+{
+    p[0] = (uint8_t)(v & 0xFF);
+    p[1] = (uint8_t)(v >> 8);
+}
+
+static uint16_t get_u16(const uint8_t *p)
+{
+    return (uint16_t)(p[0] | (p[1] << 8));
+}
+
+/* ------------------------------------------------------------------ */
+/* Q8_0: 32 weights, fp16 scale d, int8 codes; 34 bytes                */
+/* ------------------------------------------------------------------ */
+
+enum { Q8_0_QK = 32, Q8_0_BYTES = 34, Q4_K_QK = 256, Q4_K_BYTES = 144 };
+
+static void quantize_q8_0_block(const float *x, uint8_t *out)
+{
+    float amax = 0.0f;
+    for (int i = 0; i < Q8_0_QK; i++) {
+        float a = fabsf(x[i]);
+        if (a > amax)
+            amax = a;
+    }
+    float d = amax / 127.0f;
+    uint16_t d16 = orc_f32_to_f16(d);
+    float df = orc_f16_to_f32(d16);
+    put_u16(out, d16);
+    for (int i = 0; i < Q8_0_QK; i++) {
+        float q = 0.0f;
+        if (df != 0.0f)
+            q = clampf(roundf(x[i] / df), -127.0f, 127.0f);
+        out[2 + i] = (uint8_t)(int8_t)(int)q;
+    }
+}
+
+static void dequantize_q8_0_block(const uint8_t *blk, float *y)
+{
+    float df = orc_f16_to_f32(get_u16(blk));
+    for (int i = 0; i < Q8_0_QK; i++)
+        y[i] = df * (float)(int8_t)blk[2 + i];
+}
+
+/* ------------------------------------------------------------------ */
+/* Q4_K: 256-weight superblock, 8 sub-blocks of 32; 144 bytes          */
+/* ------------------------------------------------------------------ */
+
+/* Write the eight 6-bit scale codes and eight 6-bit min codes into the
+ * twelve scale bytes (layout in the file header). */
+static void pack_scales_q4_k(const int sc[8], const int mc[8], uint8_t s[12])
+{
+    for (int j = 0; j < 4; j++) {
+        s[j] = (uint8_t)((sc[j] & 63) | ((sc[j + 4] >> 4) << 6));
+        s[j + 4] = (uint8_t)((mc[j] & 63) | ((mc[j + 4] >> 4) << 6));
+        s[j + 8] = (uint8_t)((sc[j + 4] & 15) | ((mc[j + 4] & 15) << 4));
+    }
+}
+
+static void unpack_scales_q4_k(const uint8_t s[12], int sc[8], int mc[8])
+{
+    for (int j = 0; j < 4; j++) {
+        sc[j] = s[j] & 63;
+        mc[j] = s[j + 4] & 63;
+        sc[j + 4] = (s[j + 8] & 15) | ((s[j] >> 6) << 4);
+        mc[j + 4] = (s[j + 8] >> 4) | ((s[j + 4] >> 6) << 4);
+    }
+}
+
+static void quantize_q4_k_superblock(const float *x, uint8_t *out)
+{
+    float s[8], m[8];
+    float smax = 0.0f, mmax = 0.0f;
+    for (int j = 0; j < 8; j++) {
+        const float *xs = x + 32 * j;
+        float mx = xs[0];
+        float mn = 0.0f; /* min(0, min_i x_i) */
+        for (int i = 0; i < 32; i++) {
+            if (xs[i] > mx)
+                mx = xs[i];
+            if (xs[i] < mn)
+                mn = xs[i];
+        }
+        float range = mx - mn;
+        s[j] = range / 15.0f;
+        m[j] = 0.0f - mn;
+        if (s[j] > smax)
+            smax = s[j];
+        if (m[j] > mmax)
+            mmax = m[j];
+    }
+    uint16_t d16 = orc_f32_to_f16(smax / 63.0f);
+    uint16_t dmin16 = orc_f32_to_f16(mmax / 63.0f);
+    float df = orc_f16_to_f32(d16);
+    float dminf = orc_f16_to_f32(dmin16);
+
+    int sc[8], mc[8];
+    for (int j = 0; j < 8; j++) {
+        sc[j] = df > 0.0f ? (int)clampf(roundf(s[j] / df), 0.0f, 63.0f) : 0;
+        mc[j] = dminf > 0.0f ? (int)clampf(roundf(m[j] / dminf), 0.0f, 63.0f) : 0;
+    }
+
+    put_u16(out, d16);
+    put_u16(out + 2, dmin16);
+    pack_scales_q4_k(sc, mc, out + 4);
+
+    int q[256];
+    for (int j = 0; j < 8; j++) {
+        float S = df * (float)sc[j];
+        float Mn = dminf * (float)mc[j];
+        for (int i = 0; i < 32; i++) {
+            float v = 0.0f;
+            if (S > 0.0f) {
+                float shifted = x[32 * j + i] + Mn;
+                v = clampf(roundf(shifted / S), 0.0f, 15.0f);
+            }
+            q[32 * j + i] = (int)v;
+        }
+    }
+    uint8_t *qs = out + 16;
+    for (int c = 0; c < 4; c++)
+        for (int l = 0; l < 32; l++)
+            qs[32 * c + l] = (uint8_t)(q[32 * (2 * c) + l] | (q[32 * (2 * c + 1) + l] << 4));
+}
+
+static void dequantize_q4_k_superblock(const uint8_t *blk, float *y)
+{
+    float df = orc_f16_to_f32(get_u16(blk));
+    float dminf = orc_f16_to_f32(get_u16(blk + 2));
+    int sc[8], mc[8];
+    unpack_scales_q4_k(blk + 4, sc, mc);
+    const uint8_t *qs = blk + 16;
+    for (int j = 0; j < 8; j++) {
+        float S = df * (float)sc[j];
+        float Mn = dminf * (float)mc[j];
+        int c = j / 2;
+        int hi = j % 2;
+        for (int l = 0; l < 32; l++) {
+            int q = hi ? (qs[32 * c + l] >> 4) : (qs[32 * c + l] & 15);
+            float prod = S * (float)q;
+            y[32 * j + l] = prod - Mn;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* Exported API                                                        */
+/* ------------------------------------------------------------------ */
+
+enum { ORC_Q8_0 = 8, ORC_Q4_K = 4 };
+
+static int qk_of(int fmt) { return fmt == ORC_Q8_0 ? Q8_0_QK : fmt == ORC_Q4_K ? Q4_K_QK : 0; }
+static int bytes_of(int fmt) { return fmt == ORC_Q8_0 ? Q8_0_BYTES : fmt == ORC_Q4_K ? Q4_K_BYTES : 0; }
+
+int64_t orc_packed_bytes(int fmt, int64_t rows, int64_t cols)
+{
+    int qk = qk_of(fmt);
+    if (qk == 0 || rows < 0 || cols < 0 || cols % qk != 0)
+        return -1;
+    return rows * (cols / qk) * bytes_of(fmt);
+}
+
+void orc_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0)
+        omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+int orc_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* src_kind: 0 = bf16 (raw uint16 bits), 1 = fp32.  Returns 0 on success. */
+int orc_quantize(int fmt, int src_kind, const void *src, uint8_t *dst, int64_t rows, int64_t cols)
+{
+    int qk = qk_of(fmt);
+    if (qk == 0 || cols % qk != 0 || (src_kind != 0 && src_kind != 1))
+        return -1;
+    int64_t nb = cols / qk;
+    int64_t row_bytes = nb * bytes_of(fmt);
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; r++) {
+        float x[256];
+        for (int64_t b = 0; b < nb; b++) {
+            for (int i = 0; i < qk; i++)
+                x[i] = load_src(src_kind, src, r * cols + b * qk + i);
+            uint8_t *out = dst + r * row_bytes + b * bytes_of(fmt);
+            if (fmt == ORC_Q8_0)
+                quantize_q8_0_block(x, out);
+            else
+                quantize_q4_k_superblock(x, out);
+        }
+    }
+    return 0;
+}
+
+int orc_dequantize(int fmt, const uint8_t *src, float *dst, int64_t rows, int64_t cols)
+{
+    int qk = qk_of(fmt);
+    if (qk == 0 || cols % qk != 0)
+        return -1;
+    int64_t nb = cols / qk;
+    int64_t row_bytes = nb * bytes_of(fmt);
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; r++) {
+        for (int64_t b = 0; b < nb; b++) {
+            const uint8_t *blk = src + r * row_bytes + b * bytes_of(fmt);
+            float *y = dst + r * cols + b * qk;
+            if (fmt == ORC_Q8_0)
+                dequantize_q8_0_block(blk, y);
+            else
+                dequantize_q4_k_superblock(blk, y);
+        }
+    }
+    return 0;
+}
+
+static void dequantize_row(int fmt, const uint8_t *src, float *dst, int64_t cols)
+{
+    int qk = qk_of(fmt);
+    for (int64_t b = 0; b < cols / qk; b++) {
+        if (fmt == ORC_Q8_0)
+            dequantize_q8_0_block(src + b * Q8_0_BYTES, dst + b * qk);
+        else
+            dequantize_q4_k_superblock(src + b * Q4_K_BYTES, dst + b * qk);
+    }
+}
+
+/* Y[m][t] and A[m][t] (row-major, M x count) for the output features n = ns[t]
+ * of X[M x K] (bf16 bits) times the packed W[N x K]: one weight row is
+ * dequantized exactly, then every activation row is dotted with it in k
+ * order in fp64.  A may be NULL.  Returns 0 on success. */
+int orc_matmul_columns(int fmt, const uint8_t *W, const uint16_t *X, int64_t M, int64_t K,
+                       const int64_t *ns, int64_t count, double *Y, double *A)
+{
+    int qk = qk_of(fmt);
+    if (qk == 0 || K % qk != 0)
+        return -1;
+    int64_t row_bytes = (K / qk) * bytes_of(fmt);
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 4) reduction(| : bad)
+    for (int64_t t = 0; t < count; t++) {
+        float *w = (float *)malloc((size_t)K * sizeof(float));
+        if (!w) {
+            bad |= 1;
+            continue;
+        }
+        dequantize_row(fmt, W + ns[t] * row_bytes, w, K);
+        for (int64_t m = 0; m < M; m++) {
+            double acc = 0.0, aacc = 0.0;
+            const uint16_t *xm = X + m * K;
+            for (int64_t k = 0; k < K; k++) {
+                double p = (double)w[k] * (double)orc_bf16_to_f32(xm[k]);
+                acc += p;
+                aacc += fabs(p);
+            }
+            Y[m * count + t] = acc;
+            if (A)
+                A[m * count + t] = aacc;
+        }
+        free(w);
+    }
+    return bad ? -2 : 0;
+}
+
+/* The full product: Y[M x N], A[M x N] in fp64 (A may be NULL). */
+int orc_matmul(int fmt, const uint8_t *W, const uint16_t *X, double *Y, double *A,
+               int64_t M, int64_t N, int64_t K)
+{
+    int64_t *ns = (int64_t *)malloc((size_t)(N > 0 ? N : 1) * sizeof(int64_t));
+    if (!ns)
+        return -2;
+    for (int64_t n = 0; n < N; n++)
+        ns[n] = n;
+    int rc = orc_matmul_columns(fmt, W, X, M, K, ns, N, Y, A);
+    free(ns);
+    return rc;
+}
+
+/* Debug access to the scale-byte packing of Q4_K (used by the layout pins). */
+void orc_q4_k_pack_scales(const int *sc, const int *mc, uint8_t *s12) { pack_scales_q4_k(sc, mc, s12); }
+void orc_q4_k_unpack_scales(const uint8_t *s12, int *sc, int *mc) { unpack_scales_q4_k(s12, sc, mc); }
