@@ -1,0 +1,415 @@
+// gemv.cu -- decode-shaped quantized matmul, Y[M x N] = X[M x K] * W^T,
+// for M <= 16 tokens over packed Q8_0 / Q4_K weights W[N x K].
+//
+// The mistral.rs documentation ("Quantization types", section NVFP4) splits
+// CUDA linears into a dedicated matrix-vector kernel for small decode
+// batches and tiled matrix multiplication for larger ones; this is the
+// small-batch kernel of that split, written for the Q8_0 / Q4_K formats.
+//
+// Design (HBM-bound: the packed weights are read exactly once):
+//  * A CTA owns 64 weight rows and a contiguous range of K; the CTAs that
+//    share a row tile form one thread-block cluster (split-K).  Their partial
+//    sums are reduced through distributed shared memory in rank order, so
+//    the result is deterministic and needs no workspace.
+//  * One producer warp streams the CTA's rows, 256 weights (272 / 144 bytes)
+//    per row per stage, with 1-D bulk copies (cp.async.bulk) into a ring of
+//    shared-memory stages guarded by mbarriers.
+//  * Four consumer warps (16 rows each) run warp-level tensor-core MMAs
+//    (m16n8k16, f16 inputs, fp32 accumulation) with the weight rows as the
+//    M side and the (padded) tokens as N.  The MMA operands are the integer
+//    codes, which binary16 holds exactly: an int8 code becomes 1152 + q and
+//    a 4-bit code 1024 + q (or 1024 + 16 q for a high nibble) through one
+//    PRMT / LOP3 that places the byte in the mantissa of a binary16 1024.
+//    The offsets and the per-block scales are applied in fp32 after each
+//    32-weight block:  sum_k w x = a * R - b * sum_k x,  with R the MMA
+//    result of the block, a the block scale (d, or S_j, S_j / 16) and
+//    b the offset term (1152 d, or 1024 S_j + Mn_j, 64 S_j + Mn_j).
+//    sum_k x per block and token comes from the staged activations.
+//  * The activations of the CTA's K range are converted once to binary16
+//    (round to nearest) in shared memory, each group of 4 stored in the
+//    order (0, 2, 1, 3) so that one 16-byte load yields both B fragments.
+#include "common.cuh"
+
+namespace qmm {
+
+constexpr int kGemvWarps = 4;                       // consumer warps
+constexpr int kGemvRows = 16 * kGemvWarps;          // weight rows per CTA
+constexpr int kGemvThreads = (kGemvWarps + 1) * 32; // + one producer warp
+constexpr int kGemvMaxStages = 4;
+
+struct GemvParams {
+    const uint8_t *W;
+    const uint16_t *X;
+    float *Y;
+    int M, N, K;
+    int64_t row_bytes;  // packed bytes per weight row
+    int nchunks;        // K / 256
+    int stages;         // shared-memory ring depth
+    int kr_max;         // activation window: K staged at once (multiple of 256)
+};
+
+struct GemvLayout {
+    int ring, xh, xs, coef, ypart, bars, total;
+};
+
+// Byte offsets of the shared-memory regions; identical on host and device.
+__host__ __device__ inline GemvLayout gemv_layout(int fmt, int nt, int stages, int kr_max) {
+    const int slot = (fmt == 8 ? kQ8GroupBytes : kQ4Bytes) + 16;  // padded row slot
+    const int mt = 8 * nt;
+    GemvLayout L;
+    int off = 0;
+    L.ring = off;
+    off += stages * kGemvRows * slot;
+    L.xh = off;
+    off += mt * (kr_max + 32) * 2;
+    L.xs = off;
+    off += (kr_max / 32) * mt * 4;
+    L.coef = off;
+    off += (fmt == 4 ? kGemvWarps * 16 * 16 * 4 : 0);
+    L.ypart = off;
+    off += kGemvRows * mt * 4;
+    off = (off + 15) & ~15;
+    L.bars = off;
+    off += 2 * stages * 8;
+    L.total = off;
+    return L;
+}
+
+__device__ __forceinline__ float h2f_bits(uint32_t b) {
+    return __half2float(__ushort_as_half((unsigned short)(b & 0xFFFF)));
+}
+
+// 8 code bytes of a Q8_0 block at smem address p (p mod 8 == kMod8).
+template <int kMod8>
+__device__ __forceinline__ void load_q8_codes(const uint8_t *p, uint32_t &w0, uint32_t &w1) {
+    if constexpr (kMod8 == 0) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(p);
+        w0 = v.x;
+        w1 = v.y;
+    } else if constexpr (kMod8 == 4) {
+        w0 = *reinterpret_cast<const uint32_t *>(p);
+        w1 = *reinterpret_cast<const uint32_t *>(p + 4);
+    } else {  // 2 mod 4
+        const uint32_t a = *reinterpret_cast<const uint32_t *>(p - 2);
+        const uint32_t b = *reinterpret_cast<const uint32_t *>(p + 2);
+        const uint32_t c = *reinterpret_cast<const uint32_t *>(p + 6);
+        w0 = __byte_perm(a, b, 0x5432);
+        w1 = __byte_perm(b, c, 0x5432);
+    }
+}
+
+// int8 codes -> binary16 (1152 + q): flip the sign bit (u = q + 128) and put
+// u under a binary16 exponent of 1024.  Lanes take positions (0,2) or (1,3).
+__device__ __forceinline__ uint32_t q8_pair02(uint32_t u) { return prmt(u, 0x64646464u, 0x4240u); }
+__device__ __forceinline__ uint32_t q8_pair13(uint32_t u) { return prmt(u, 0x64646464u, 0x4341u); }
+
+template <int kB, int kNT>
+__device__ __forceinline__ void q8_block(const uint8_t *r0, const uint8_t *r1, const __half *xrow,
+                                         int xstride, const float *xs, int blk, int t,
+                                         float (&acc)[kNT][4]) {
+    // code offset of this block inside the row slot: 34b + 2 + 8t
+    constexpr int kOff = kQ8Bytes * kB + 2;
+    constexpr int kMod8 = kOff % 8;
+    const float d0 = h2f_bits(*reinterpret_cast<const uint16_t *>(r0 + kQ8Bytes * kB));
+    const float d1 = h2f_bits(*reinterpret_cast<const uint16_t *>(r1 + kQ8Bytes * kB));
+    uint32_t a0, a1, b0, b1;  // rows g (a*) and g+8 (b*), words 0/1
+    load_q8_codes<kMod8>(r0 + kOff + 8 * t, a0, a1);
+    load_q8_codes<kMod8>(r1 + kOff + 8 * t, b0, b1);
+    a0 ^= 0x80808080u; a1 ^= 0x80808080u; b0 ^= 0x80808080u; b1 ^= 0x80808080u;
+    const uint32_t A0[4] = {q8_pair02(a0), q8_pair02(b0), q8_pair13(a0), q8_pair13(b0)};
+    const uint32_t A1[4] = {q8_pair02(a1), q8_pair02(b1), q8_pair13(a1), q8_pair13(b1)};
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt) {
+        const uint4 xv =
+            *reinterpret_cast<const uint4 *>(xrow + nt * 8 * xstride + kQ8Weights * kB + 8 * t);
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_f16_16816(c, A0, xv.x, xv.y);
+        mma_f16_16816(c, A1, xv.z, xv.w);
+        const float2 s = *reinterpret_cast<const float2 *>(xs + blk * (8 * kNT) + nt * 8 + 2 * t);
+        acc[nt][0] = fmaf(d0, fmaf(-1152.0f, s.x, c[0]), acc[nt][0]);
+        acc[nt][1] = fmaf(d0, fmaf(-1152.0f, s.y, c[1]), acc[nt][1]);
+        acc[nt][2] = fmaf(d1, fmaf(-1152.0f, s.x, c[2]), acc[nt][2]);
+        acc[nt][3] = fmaf(d1, fmaf(-1152.0f, s.y, c[3]), acc[nt][3]);
+    }
+}
+
+template <int kNT>
+__device__ __forceinline__ void q4k_chunk(const uint8_t *base, const uint8_t *r0, const uint8_t *r1,
+                                          const __half *xr, int xstride, const float *xs, int li,
+                                          float *cw, int lane, int g, int t, float (&acc)[kNT][4]) {
+    constexpr int kSlot = kQ4Bytes + 16;
+    constexpr int kMT = 8 * kNT;
+    // per-row coefficients (a_j, b_j) of the 8 sub-blocks; lane (row =
+    // lane / 2) decodes sub-blocks 4 * (lane & 1) .. + 3 of its row
+    {
+        const int rr = lane >> 1, half = lane & 1;
+        const uint4 h = *reinterpret_cast<const uint4 *>(base + rr * kSlot);
+        const float dsc = h2f_bits(h.x), dmn = h2f_bits(h.x >> 16);
+        const uint32_t sw[3] = {h.y, h.z, h.w};
+        auto sbyte = [&](int k) { return (sw[k >> 2] >> (8 * (k & 3))) & 0xFFu; };
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const int j = 4 * half + jj;
+            uint32_t sc, mc;
+            if (j < 4) {
+                sc = sbyte(j) & 63u;
+                mc = sbyte(j + 4) & 63u;
+            } else {
+                sc = (sbyte(j + 4) & 15u) | ((sbyte(j - 4) >> 6) << 4);
+                mc = (sbyte(j + 4) >> 4) | ((sbyte(j) >> 6) << 4);
+            }
+            const float S = dsc * (float)sc, Mn = dmn * (float)mc;
+            const bool hi = (j & 1) != 0;
+            cw[rr * 16 + 2 * j] = hi ? S * 0.0625f : S;
+            cw[rr * 16 + 2 * j + 1] = fmaf(hi ? 64.0f : 1024.0f, S, Mn);
+        }
+    }
+    __syncwarp();
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const uint2 qa = *reinterpret_cast<const uint2 *>(r0 + 16 + 32 * c + 8 * t);
+        const uint2 qb = *reinterpret_cast<const uint2 *>(r1 + 16 + 32 * c + 8 * t);
+        const float4 ca = *reinterpret_cast<const float4 *>(cw + g * 16 + 4 * c);
+        const float4 cb = *reinterpret_cast<const float4 *>(cw + (g + 8) * 16 + 4 * c);
+        const uint32_t M16 = 0x64006400u;
+        const uint32_t qa0s = qa.x >> 8, qa1s = qa.y >> 8, qb0s = qb.x >> 8, qb1s = qb.y >> 8;
+        const uint32_t L0[4] = {and_or(qa.x, 0x000F000Fu, M16), and_or(qb.x, 0x000F000Fu, M16),
+                                and_or(qa0s, 0x000F000Fu, M16), and_or(qb0s, 0x000F000Fu, M16)};
+        const uint32_t L1[4] = {and_or(qa.y, 0x000F000Fu, M16), and_or(qb.y, 0x000F000Fu, M16),
+                                and_or(qa1s, 0x000F000Fu, M16), and_or(qb1s, 0x000F000Fu, M16)};
+        const uint32_t H0[4] = {and_or(qa.x, 0x00F000F0u, M16), and_or(qb.x, 0x00F000F0u, M16),
+                                and_or(qa0s, 0x00F000F0u, M16), and_or(qb0s, 0x00F000F0u, M16)};
+        const uint32_t H1[4] = {and_or(qa.y, 0x00F000F0u, M16), and_or(qb.y, 0x00F000F0u, M16),
+                                and_or(qa1s, 0x00F000F0u, M16), and_or(qb1s, 0x00F000F0u, M16)};
+        const int blo = li * 8 + 2 * c;
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt) {
+            const __half *xq = xr + nt * 8 * xstride + 64 * c + 8 * t;
+            const uint4 xl = *reinterpret_cast<const uint4 *>(xq);
+            const uint4 xhv = *reinterpret_cast<const uint4 *>(xq + 32);
+            float cl[4] = {0.f, 0.f, 0.f, 0.f}, chh[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_f16_16816(cl, L0, xl.x, xl.y);
+            mma_f16_16816(cl, L1, xl.z, xl.w);
+            mma_f16_16816(chh, H0, xhv.x, xhv.y);
+            mma_f16_16816(chh, H1, xhv.z, xhv.w);
+            const float2 sl = *reinterpret_cast<const float2 *>(xs + blo * kMT + nt * 8 + 2 * t);
+            const float2 sh = *reinterpret_cast<const float2 *>(xs + (blo + 1) * kMT + nt * 8 + 2 * t);
+            acc[nt][0] += fmaf(ca.x, cl[0], -ca.y * sl.x) + fmaf(ca.z, chh[0], -ca.w * sh.x);
+            acc[nt][1] += fmaf(ca.x, cl[1], -ca.y * sl.y) + fmaf(ca.z, chh[1], -ca.w * sh.y);
+            acc[nt][2] += fmaf(cb.x, cl[2], -cb.y * sl.x) + fmaf(cb.z, chh[2], -cb.w * sh.x);
+            acc[nt][3] += fmaf(cb.x, cl[3], -cb.y * sl.y) + fmaf(cb.z, chh[3], -cb.w * sh.y);
+        }
+    }
+    __syncwarp();
+}
+
+template <int kFmt, int kNT>
+__global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const GemvParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    constexpr int kCB = kFmt == 8 ? kQ8GroupBytes : kQ4Bytes;  // bytes per row per chunk
+    constexpr int kSlot = kCB + 16;
+    constexpr int kMT = 8 * kNT;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t nsplit = cluster_nctarank(), rank = cluster_ctarank();
+    const int row0 = blockIdx.x * kGemvRows;
+    const int c_begin = (int)((int64_t)p.nchunks * rank / nsplit);
+    const int c_end = (int)((int64_t)p.nchunks * (rank + 1) / nsplit);
+    const int nloc = c_end - c_begin;
+    const int kbase = c_begin * kGroup;
+    const int xstride = p.kr_max + 32;
+    const GemvLayout L = gemv_layout(kFmt, kNT, p.stages, p.kr_max);
+    uint8_t *ring = smem + L.ring;
+    __half *xh = reinterpret_cast<__half *>(smem + L.xh);
+    float *xs = reinterpret_cast<float *>(smem + L.xs);
+    float *coef = reinterpret_cast<float *>(smem + L.coef);
+    float *ypart = reinterpret_cast<float *>(smem + L.ypart);
+    const uint32_t bar0 = smem_addr(smem + L.bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (p.stages + s); };
+
+    if (tid == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), kGemvWarps);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kGemvWarps) {
+        // ---------------- producer: bulk-copy the row tile, chunk by chunk
+        const int rows_valid = min(kGemvRows, p.N - row0);
+        const uint8_t *tile = p.W + (int64_t)row0 * p.row_bytes + (int64_t)c_begin * kCB;
+        for (int i = 0; i < nloc; ++i) {
+            const int s = i % p.stages;
+            if (i >= p.stages &&
+                !mbar_wait_warp(empty_bar(s), ((i / p.stages) - 1) & 1, kErrGemvEmptyWait))
+                break;  // bug path: consumers then time out on their full barriers
+            if (lane == 0) mbar_arrive_expect_tx(full_bar(s), (uint32_t)(rows_valid * kCB));
+            __syncwarp();
+            for (int r = lane; r < rows_valid; r += 32)
+                bulk_g2s(smem_addr(ring + (s * kGemvRows + r) * kSlot),
+                         tile + (int64_t)r * p.row_bytes + (int64_t)i * kCB, kCB, full_bar(s));
+        }
+    } else {
+        // ---------------- consumers
+        const int g = lane >> 2, t = lane & 3;
+        float acc[kNT][4];
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt)
+            acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+        const __half *xrow = xh + g * xstride;
+        float *cw = coef + warp * 16 * 16;
+        const int win = p.kr_max / kGroup;  // chunks per activation window
+        // `ok` is warp-uniform; after a timed-out wait the warp skips its
+        // remaining waits and MMAs but still takes every named barrier.
+        bool ok = true;
+        for (int w0 = 0; w0 < nloc; w0 += win) {
+            const int wn = min(win, nloc - w0);
+            if (w0 > 0) named_bar_sync(1, kGemvWarps * 32);  // previous window fully read
+            // stage the window's activations as binary16 (+ 32-weight block sums)
+            const int ngr = (wn * kGroup) / 8;  // 8-element groups per token
+            const int kw = kbase + w0 * kGroup;
+            for (int idx = tid; idx < kMT * ngr; idx += kGemvWarps * 32) {
+                const int m = idx / ngr, kg = idx - m * ngr;
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                if (m < p.M)
+                    v = __ldg(reinterpret_cast<const uint4 *>(p.X + (int64_t)m * p.K + kw + 8 * kg));
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                float f[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    f[2 * e] = __uint_as_float(w[e] << 16);
+                    f[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+                }
+                const __half2 h02 = __floats2half2_rn(f[0], f[2]);
+                const __half2 h13 = __floats2half2_rn(f[1], f[3]);
+                const __half2 h46 = __floats2half2_rn(f[4], f[6]);
+                const __half2 h57 = __floats2half2_rn(f[5], f[7]);
+                uint4 o;
+                o.x = *reinterpret_cast<const uint32_t *>(&h02);
+                o.y = *reinterpret_cast<const uint32_t *>(&h13);
+                o.z = *reinterpret_cast<const uint32_t *>(&h46);
+                o.w = *reinterpret_cast<const uint32_t *>(&h57);
+                *reinterpret_cast<uint4 *>(xh + m * xstride + 8 * kg) = o;
+                const float2 s02 = __half22float2(h02), s13 = __half22float2(h13);
+                const float2 s46 = __half22float2(h46), s57 = __half22float2(h57);
+                float sum = ((s02.x + s13.x) + (s02.y + s13.y)) + ((s46.x + s57.x) + (s46.y + s57.y));
+                sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+                sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+                if ((kg & 3) == 0) xs[(kg >> 2) * kMT + m] = sum;
+            }
+            named_bar_sync(1, kGemvWarps * 32);
+
+            // main loop over the window's K chunks
+            for (int li = 0; li < wn; ++li) {
+                const int i = w0 + li;
+                const int s = i % p.stages;
+                if (ok) ok = mbar_wait_warp(full_bar(s), (i / p.stages) & 1, kErrGemvFullWait);
+                if (!ok) continue;
+                const uint8_t *base = ring + (s * kGemvRows + 16 * warp) * kSlot;
+                const uint8_t *r0 = base + g * kSlot;
+                const uint8_t *r1 = base + (g + 8) * kSlot;
+                const __half *xr = xrow + li * kGroup;
+                if constexpr (kFmt == 8) {
+                    q8_block<0, kNT>(r0, r1, xr, xstride, xs, li * 8 + 0, t, acc);
+                    q8_block<1, kNT>(r0, r1, xr, xstride, xs, li * 8 + 1, t, acc);
+                    q8_block<2, kNT>(r0, r1, xr, xstride, xs, li * 8 + 2, t, acc);
+                    q8_block<3, kNT>(r0, r1, xr, xstride, xs, li * 8 + 3, t, acc);
+                    q8_block<4, kNT>(r0, r1, xr, xstride, xs, li * 8 + 4, t, acc);
+                    q8_block<5, kNT>(r0, r1, xr, xstride, xs, li * 8 + 5, t, acc);
+                    q8_block<6, kNT>(r0, r1, xr, xstride, xs, li * 8 + 6, t, acc);
+                    q8_block<7, kNT>(r0, r1, xr, xstride, xs, li * 8 + 7, t, acc);
+                } else {
+                    q4k_chunk<kNT>(base, r0, r1, xr, xstride, xs, li, cw, lane, g, t, acc);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty_bar(s));
+            }
+        }
+        // partial sums of this CTA: ypart[row][token]
+        const int rg = 16 * warp + g;
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt) {
+            *reinterpret_cast<float2 *>(ypart + rg * kMT + nt * 8 + 2 * t) = make_float2(acc[nt][0], acc[nt][1]);
+            *reinterpret_cast<float2 *>(ypart + (rg + 8) * kMT + nt * 8 + 2 * t) =
+                make_float2(acc[nt][2], acc[nt][3]);
+        }
+    }
+
+    // ---------------- split-K reduction across the cluster, in rank order
+    cluster_sync_all();
+    const int rpr = kGemvRows / (int)nsplit;
+    for (int idx = tid; idx < rpr * kMT; idx += kGemvThreads) {
+        const int r = (int)rank * rpr + idx / kMT, m = idx % kMT;
+        if (m < p.M && row0 + r < p.N) {
+            const uint32_t a = smem_addr(ypart + r * kMT + m);
+            float sum = 0.f;
+            for (uint32_t q = 0; q < nsplit; ++q) sum += ld_dsmem_f32(map_to_rank(a, q));
+            p.Y[(int64_t)m * p.N + row0 + r] = sum;
+        }
+    }
+    cluster_sync_all();
+}
+
+// ------------------------------------------------------------- launcher
+template <int kFmt, int kNT>
+static cudaError_t launch_gemv_t(const GemvParams &p0, int nsplit, int sms, cudaStream_t stream) {
+    GemvParams p = p0;
+    const GemvLayout L = gemv_layout(kFmt, kNT, p.stages, p.kr_max);
+    static bool attr_set = false;  // per process; the limit is the same on every device
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(gemv_kernel<kFmt, kNT>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    (void)sms;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((p.N + kGemvRows - 1) / kGemvRows), (unsigned)nsplit, 1);
+    cfg.blockDim = dim3(kGemvThreads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)L.total;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = (unsigned)nsplit;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<kFmt, kNT>, p);
+}
+
+// Split-K factor (cluster size along K) for an N x K problem.
+int gemv_split(int N, int K, int sms) {
+    const int tiles = (N + kGemvRows - 1) / kGemvRows;
+    const int nchunks = K / kGroup;
+    int s = 1;
+    while (s < 8 && tiles * s < 2 * sms && nchunks >= 4 * s) s *= 2;
+    return s;
+}
+
+// Activation window (in 256-weight chunks) staged in shared memory at once.
+constexpr int kGemvMaxWindow = 8;
+
+cudaError_t launch_gemv(int fmt, const void *W, const uint16_t *X, float *Y, int M, int N, int K,
+                        int sms, cudaStream_t stream) {
+    GemvParams p;
+    p.W = static_cast<const uint8_t *>(W);
+    p.X = X;
+    p.Y = Y;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.nchunks = K / kGroup;
+    p.row_bytes = (int64_t)p.nchunks * (fmt == 8 ? kQ8GroupBytes : kQ4Bytes);
+    const int nsplit = gemv_split(N, K, sms);
+    const int per = (p.nchunks + nsplit - 1) / nsplit;
+    p.stages = per < kGemvMaxStages ? per : kGemvMaxStages;
+    p.kr_max = (per < kGemvMaxWindow ? per : kGemvMaxWindow) * kGroup;
+    if (fmt == 8)
+        return M <= 8 ? launch_gemv_t<8, 1>(p, nsplit, sms, stream) : launch_gemv_t<8, 2>(p, nsplit, sms, stream);
+    return M <= 8 ? launch_gemv_t<4, 1>(p, nsplit, sms, stream) : launch_gemv_t<4, 2>(p, nsplit, sms, stream);
+}
+
+}  // namespace qmm

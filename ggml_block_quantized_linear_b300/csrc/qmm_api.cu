@@ -1,0 +1,139 @@
+// qmm_api.cu -- the C ABI declared in include/qmm.h: argument checks on the
+// host, kernel selection and launch.  Nothing here allocates or synchronises
+// (except qmm_device_error_take, which is documented to synchronise).
+#include <cstdint>
+#include <cstring>
+
+#include "common.cuh"
+#include "qmm.h"
+
+namespace qmm {
+
+cudaError_t launch_quantize(int fmt, int src_f32, const void *src, void *dst, int64_t nweights,
+                            int sms, cudaStream_t stream);
+cudaError_t launch_dequantize(int fmt, const void *src, float *dst, int64_t nweights, int sms,
+                              cudaStream_t stream);
+cudaError_t launch_gemv(int fmt, const void *W, const uint16_t *X, float *Y, int M, int N, int K,
+                        int sms, cudaStream_t stream);
+cudaError_t launch_gemm(int fmt, const void *W, const uint16_t *X, float *Y, int M, int N, int K,
+                        void *workspace, size_t workspace_bytes, int sms, cudaStream_t stream);
+size_t gemm_workspace_bytes(int fmt, int M, int N, int K);
+
+constexpr int kMaxDecodeM = 16;
+// Largest dimension accepted (keeps every 32-bit index in the kernels exact).
+constexpr int64_t kMaxDim = (int64_t)1 << 30;
+
+static int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (dev < 0 || dev >= 64) return 148;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static bool known_fmt(qmm_format f) { return f == QMM_Q8_0 || f == QMM_Q4_K; }
+
+static qmm_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA; }
+
+}  // namespace qmm
+
+using namespace qmm;
+
+extern "C" {
+
+size_t qmm_packed_bytes(qmm_format fmt, int64_t rows, int64_t cols) {
+    if (!known_fmt(fmt) || rows < 0 || cols < 0) return 0;
+    const int64_t qk = fmt == QMM_Q8_0 ? kQ8Weights : kQ4Weights;
+    const int64_t bb = fmt == QMM_Q8_0 ? kQ8Bytes : kQ4Bytes;
+    if (cols % qk != 0) return 0;
+    if (rows > kMaxDim || cols > kMaxDim) return 0;
+    return (size_t)(rows * (cols / qk) * bb);
+}
+
+qmm_status qmm_quantize(qmm_format fmt, qmm_src_dtype st, const void *src, void *dst_packed,
+                        int64_t rows, int64_t cols, qmm_stream_t stream) {
+    if (!known_fmt(fmt) || (st != QMM_SRC_BF16 && st != QMM_SRC_F32)) return QMM_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 0 || rows > kMaxDim || cols > kMaxDim) return QMM_ERR_INVALID_ARG;
+    if (cols == 0 || cols % kGroup != 0) return QMM_ERR_SHAPE;
+    if (rows == 0) return QMM_OK;
+    if (src == nullptr || dst_packed == nullptr) return QMM_ERR_INVALID_ARG;
+    if (!aligned16(src) || !aligned16(dst_packed)) return QMM_ERR_ALIGNMENT;
+    return from_cuda(launch_quantize((int)fmt, st == QMM_SRC_F32, src, dst_packed, rows * cols,
+                                     sm_count(), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+qmm_status qmm_dequantize(qmm_format fmt, const void *src_packed, float *dst, int64_t rows,
+                          int64_t cols, qmm_stream_t stream) {
+    if (!known_fmt(fmt)) return QMM_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 0 || rows > kMaxDim || cols > kMaxDim) return QMM_ERR_INVALID_ARG;
+    if (cols == 0 || cols % kGroup != 0) return QMM_ERR_SHAPE;
+    if (rows == 0) return QMM_OK;
+    if (src_packed == nullptr || dst == nullptr) return QMM_ERR_INVALID_ARG;
+    if (!aligned16(src_packed) || !aligned16(dst)) return QMM_ERR_ALIGNMENT;
+    return from_cuda(launch_dequantize((int)fmt, src_packed, dst, rows * cols, sm_count(),
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t qmm_matmul_workspace_bytes(qmm_format fmt, int64_t M, int64_t N, int64_t K) {
+    if (!known_fmt(fmt) || M <= kMaxDecodeM || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim ||
+        K > kMaxDim || K % kGroup != 0)
+        return 0;
+    return gemm_workspace_bytes((int)fmt, (int)M, (int)N, (int)K);
+}
+
+qmm_status qmm_matmul(qmm_format fmt, const void *W_packed, const uint16_t *X_bf16, float *Y,
+                      int64_t M, int64_t N, int64_t K, void *workspace, size_t workspace_bytes,
+                      qmm_stream_t stream) {
+    if (!known_fmt(fmt)) return QMM_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+        return QMM_ERR_INVALID_ARG;
+    if (K == 0 || K % kGroup != 0) return QMM_ERR_SHAPE;
+    if (M == 0 || N == 0) return QMM_OK;
+    if (W_packed == nullptr || X_bf16 == nullptr || Y == nullptr) return QMM_ERR_INVALID_ARG;
+    if (!aligned16(W_packed) || !aligned16(X_bf16) || !aligned16(Y)) return QMM_ERR_ALIGNMENT;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (M <= kMaxDecodeM)
+        return from_cuda(launch_gemv((int)fmt, W_packed, X_bf16, Y, (int)M, (int)N, (int)K,
+                                     sm_count(), s));
+    const size_t need = gemm_workspace_bytes((int)fmt, (int)M, (int)N, (int)K);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return QMM_ERR_WORKSPACE;
+    if (need > 0 && !aligned16(workspace)) return QMM_ERR_ALIGNMENT;
+    return from_cuda(launch_gemm((int)fmt, W_packed, X_bf16, Y, (int)M, (int)N, (int)K, workspace,
+                                 workspace_bytes, sm_count(), s));
+}
+
+const char *qmm_status_string(qmm_status s) {
+    switch (s) {
+    case QMM_OK: return "ok";
+    case QMM_ERR_INVALID_ARG: return "invalid argument (null pointer, negative size or unknown enum)";
+    case QMM_ERR_UNSUPPORTED: return "unsupported request";
+    case QMM_ERR_SHAPE: return "cols / K must be a positive multiple of 256";
+    case QMM_ERR_ALIGNMENT: return "pointers must be 16-byte aligned";
+    case QMM_ERR_WORKSPACE: return "workspace missing or too small";
+    case QMM_ERR_CUDA: return "CUDA runtime error";
+    case QMM_ERR_DEVICE: return "a kernel recorded an internal error";
+    }
+    return "unknown status";
+}
+
+int qmm_device_error_take(void) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)) != cudaSuccess) return -1;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess) return -1;
+    }
+    return v;
+}
+
+const char *qmm_version(void) { return "qmm 0.1.0 sm_103a"; }
+
+}  // extern "C"

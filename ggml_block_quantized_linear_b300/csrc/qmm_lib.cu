@@ -1,0 +1,6 @@
+// qmm_lib.cu -- the single translation unit of libqmm.so (the kernels share
+// the device error word, so they are compiled together).
+#include "qmm_api.cu"
+#include "quantize.cu"
+#include "gemv.cu"
+#include "gemm.cu"

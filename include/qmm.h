@@ -1,0 +1,147 @@
+/*
+ * qmm.h -- C ABI of the B300 (sm_103a) GGML block-quantized linear layer.
+ *
+ * What it computes.  The mistral.rs documentation page "Quantization types"
+ * describes in-situ quantization (ISQ): unquantized (bf16) weights are
+ * quantized at load time (opening section, `--isq N`), and on CUDA the
+ * shorthand 8 resolves to Q8_0 and 4 to Q4K (section "Numeric shorthands";
+ * widths in tables "Legacy GGML types" and "Q*K family").  This library
+ * provides that step and the linear layer that consumes it:
+ *
+ *   qmm_quantize    bf16 (or fp32) weights W[rows x cols] -> packed blocks
+ *   qmm_dequantize  packed blocks -> fp32 W^[rows x cols] (exact)
+ *   qmm_matmul      Y[M x N] = X[M x K] * W^[N x K]^T   (fp32 out, bf16 X)
+ *
+ * The pages give names and widths only.  The byte layouts and the quantizer
+ * used here (the library's reading, GGUF-shaped) are:
+ *
+ *   Q8_0  32 weights -> 34 bytes: binary16 d = fp16(max|x| / 127), then
+ *         int8 q_i = clamp(round_half_away(x_i / d), -127, 127).
+ *         Dequantized weight: d * q.
+ *   Q4_K  256 weights -> 144 bytes: binary16 d, binary16 dmin, 12 bytes of
+ *         eight 6-bit sub-block scale codes sc_j and eight 6-bit min codes
+ *         mc_j, 128 bytes of 4-bit codes q (byte 32c+l: weight l of sub-block
+ *         2c in the low nibble, of sub-block 2c+1 in the high nibble).
+ *         Per 32-weight sub-block: s_j = (max - min(0, min)) / 15,
+ *         m_j = -min(0, min); d = fp16(max_j s_j / 63), dmin = fp16(max_j
+ *         m_j / 63); sc_j, mc_j = round(s_j / d), round(m_j / dmin) in 0..63;
+ *         q = round((x + dmin*mc_j) / (d*sc_j)) in 0..15.
+ *         Dequantized weight: (d*sc_j) * q - dmin*mc_j.
+ *   Scale bytes of Q4_K, j = 0..3: byte j = sc_j | (sc_{j+4} >> 4) << 6;
+ *   byte j+4 = mc_j | (mc_{j+4} >> 4) << 6; byte j+8 = (sc_{j+4} & 15) |
+ *   (mc_{j+4} & 15) << 4.
+ *
+ * A packed matrix is row-major in blocks: row n holds cols/32 Q8_0 blocks
+ * (cols/32*34 bytes) or cols/256 Q4_K superblocks (cols/256*144 bytes),
+ * rows back to back.
+ *
+ * Conventions for every call:
+ *  - Pointers are DEVICE pointers owned by the caller.  The library allocates
+ *    nothing and never synchronises; work is enqueued on `stream` (NULL = the
+ *    legacy default stream) and completes asynchronously.
+ *  - Row-major, contiguous, 16-byte aligned buffers; buffers must not alias.
+ *  - cols (K) must be a positive multiple of 256 for both formats (this makes
+ *    every packed row a multiple of 16 bytes).  rows / N / M may be 0 (nothing
+ *    is launched) or any positive value.
+ *  - Arguments are checked on the host before anything is launched; on an
+ *    error nothing is enqueued and the status says why.  A launch failure
+ *    reported by the CUDA runtime maps to QMM_ERR_CUDA.  Faults during the
+ *    asynchronous execution surface at the caller's next synchronisation.
+ *  - NaN or infinite inputs give unspecified (but memory-safe) results.
+ *  - qmm_matmul converts the bf16 activations to binary16 for the tensor
+ *    cores: |x| must stay below 65504, and activations below 2^-14 in
+ *    magnitude keep an absolute precision of 2^-25.
+ *  - No C++ exception crosses this interface.
+ */
+#ifndef QMM_H
+#define QMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define QMM_API __attribute__((visibility("default")))
+#else
+#define QMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (cudaStream_t); declared here so that this header does not
+ * need the CUDA headers. */
+struct CUstream_st;
+typedef struct CUstream_st *qmm_stream_t;
+
+/* Block formats; the values mirror the ISQ shorthands `--isq 8` / `--isq 4`
+ * (mistral.rs "Quantization types", section "Numeric shorthands"). */
+typedef enum { QMM_Q8_0 = 8, QMM_Q4_K = 4 } qmm_format;
+
+/* Element type of the unquantized source of qmm_quantize.  BF16 is the ISQ
+ * source (model weights); F32 lets tests feed values that bf16 cannot hold. */
+typedef enum { QMM_SRC_BF16 = 0, QMM_SRC_F32 = 1 } qmm_src_dtype;
+
+typedef enum {
+    QMM_OK = 0,
+    QMM_ERR_INVALID_ARG = -1, /* NULL pointer, negative size, unknown enum  */
+    QMM_ERR_UNSUPPORTED = -2, /* valid request this build does not handle   */
+    QMM_ERR_SHAPE = -3,       /* cols / K not a positive multiple of 256     */
+    QMM_ERR_ALIGNMENT = -4,   /* a pointer is not 16-byte aligned            */
+    QMM_ERR_WORKSPACE = -5,   /* workspace missing or smaller than required  */
+    QMM_ERR_CUDA = -6,        /* the CUDA runtime reported an error          */
+    QMM_ERR_DEVICE = -7       /* a kernel recorded an internal error (below) */
+} qmm_status;
+
+/* Bytes of a packed [rows x cols] matrix; 0 if the format is unknown, a size
+ * is negative, or cols is not a multiple of the format's block (32 / 256). */
+QMM_API size_t qmm_packed_bytes(qmm_format fmt, int64_t rows, int64_t cols);
+
+/* ISQ: quantize src[rows x cols] (bf16 bit patterns or fp32, per `st`) into
+ * dst_packed (qmm_packed_bytes(fmt, rows, cols) bytes).  Bit-exact and
+ * deterministic: the same bytes as the plain CPU definition above (IEEE
+ * single arithmetic without contraction, round-half-away codes, binary16
+ * round-to-nearest-even scales).  One kernel launch. */
+QMM_API qmm_status qmm_quantize(qmm_format fmt, qmm_src_dtype st, const void *src, void *dst_packed,
+                        int64_t rows, int64_t cols, qmm_stream_t stream);
+
+/* dst[rows x cols] (fp32) = the exactly dequantized weights of src_packed.
+ * Every value is exact except the single rounding of Q4_K's final
+ * subtraction.  One kernel launch. */
+QMM_API qmm_status qmm_dequantize(qmm_format fmt, const void *src_packed, float *dst, int64_t rows,
+                          int64_t cols, qmm_stream_t stream);
+
+/* Workspace qmm_matmul needs for this problem, in bytes (0 = none; then
+ * workspace may be NULL). */
+QMM_API size_t qmm_matmul_workspace_bytes(qmm_format fmt, int64_t M, int64_t N, int64_t K);
+
+/* Y[M x N] (fp32, row-major) = X[M x K] (bf16 bit patterns, row-major) times
+ * the transpose of the packed weights W[N x K].  M <= 16 runs the decode
+ * kernel (split-K over a thread-block cluster, reduced in distributed shared
+ * memory in a fixed order: deterministic).  Larger M runs the prefill kernel
+ * (tcgen05 tensor cores, TMEM accumulators).  Accuracy: per element
+ * |y - y_exact| <= 1e-3 * sum_k |w^_k x_k| + 1e-6, where w^ are the
+ * dequantized weights.  `workspace` must hold
+ * qmm_matmul_workspace_bytes(fmt, M, N, K) bytes (or be NULL when that is 0). */
+QMM_API qmm_status qmm_matmul(qmm_format fmt, const void *W_packed, const uint16_t *X_bf16, float *Y,
+                      int64_t M, int64_t N, int64_t K, void *workspace, size_t workspace_bytes,
+                      qmm_stream_t stream);
+
+/* Static description of a status code (never NULL). */
+QMM_API const char *qmm_status_string(qmm_status s);
+
+/* Kernels never trap.  A wait inside a kernel that exceeds its time limit
+ * (about two seconds; it can only happen through a bug) makes the kernel
+ * record a nonzero code in a device word and return early.  This call
+ * synchronises the current device, returns that code (0 = none) and clears
+ * it. */
+QMM_API int qmm_device_error_take(void);
+
+/* Library version, e.g. "qmm 0.1.0 sm_103a". */
+QMM_API const char *qmm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMM_H */

@@ -1,0 +1,112 @@
+"""Host-only checks of the C ABI (no kernel is launched): the library builds
+and loads, exports every function include/qmm.h declares, and rejects bad
+arguments with the documented status before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import ggml_block_quantized_linear_b300 as q
+from ggml_block_quantized_linear_b300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return q.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "qmm.h")).read()
+    return re.findall(r"QMM_API\s+[\w\s\*]+?\b(qmm_\w+)\s*\(", text)
+
+
+def test_header_declares_the_boundary():
+    names = set(declared_functions())
+    assert {"qmm_quantize", "qmm_dequantize", "qmm_matmul", "qmm_packed_bytes",
+            "qmm_matmul_workspace_bytes", "qmm_status_string"} <= names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert q.qmm_version().startswith("qmm ")
+
+
+def test_packed_bytes(lib):
+    assert q.qmm_packed_bytes(q.QMM_Q8_0, 4096, 4096) == 17825792
+    assert q.qmm_packed_bytes(q.QMM_Q4_K, 4096, 4096) == 9437184
+    assert q.qmm_packed_bytes(q.QMM_Q8_0, 14336, 4096) == 62390272
+    assert q.qmm_packed_bytes(q.QMM_Q4_K, 14336, 4096) == 33030144
+    assert q.qmm_packed_bytes(q.QMM_Q8_0, 1, 48) == 0       # not a block multiple
+    assert q.qmm_packed_bytes(q.QMM_Q4_K, 1, 512 + 32) == 0
+    assert q.qmm_packed_bytes(7, 1, 256) == 0
+    assert q.qmm_packed_bytes(q.QMM_Q8_0, -1, 256) == 0
+    assert q.qmm_packed_bytes(q.QMM_Q8_0, 0, 256) == 0
+
+
+def test_status_strings(lib):
+    for s in range(-7, 1):
+        assert len(q.qmm_status_string(s)) > 0
+    assert q.qmm_status_string(99) == "unknown status"
+
+
+FAKE = ctypes.c_void_p(0x1000)        # never dereferenced: every case fails first
+MISALIGNED = ctypes.c_void_p(0x1008)
+NULL = ctypes.c_void_p(0)
+S0 = ctypes.c_void_p(0)
+
+
+def test_quantize_argument_errors(lib):
+    L = lib
+    assert L.qmm_quantize(5, 0, FAKE, FAKE, 4, 256, S0) == q.QMM_ERR_INVALID_ARG
+    assert L.qmm_quantize(8, 3, FAKE, FAKE, 4, 256, S0) == q.QMM_ERR_INVALID_ARG
+    assert L.qmm_quantize(8, 0, FAKE, FAKE, -1, 256, S0) == q.QMM_ERR_INVALID_ARG
+    assert L.qmm_quantize(8, 0, FAKE, FAKE, 4, 0, S0) == q.QMM_ERR_SHAPE
+    assert L.qmm_quantize(8, 0, FAKE, FAKE, 4, 288, S0) == q.QMM_ERR_SHAPE
+    assert L.qmm_quantize(4, 0, FAKE, FAKE, 4, 128, S0) == q.QMM_ERR_SHAPE
+    assert L.qmm_quantize(8, 0, NULL, FAKE, 4, 256, S0) == q.QMM_ERR_INVALID_ARG
+    assert L.qmm_quantize(8, 0, FAKE, NULL, 4, 256, S0) == q.QMM_ERR_INVALID_ARG
+    assert L.qmm_quantize(4, 1, MISALIGNED, FAKE, 4, 256, S0) == q.QMM_ERR_ALIGNMENT
+    assert L.qmm_quantize(4, 1, FAKE, MISALIGNED, 4, 256, S0) == q.QMM_ERR_ALIGNMENT
+    assert L.qmm_quantize(8, 0, NULL, NULL, 0, 256, S0) == q.QMM_OK  # empty: nothing to do
+
+
+def test_dequantize_argument_errors(lib):
+    L = lib
+    assert L.qmm_dequantize(3, FAKE, FAKE, 4, 256, S0) == q.QMM_ERR_INVALID_ARG
+    assert L.qmm_dequantize(8, FAKE, FAKE, 4, 100, S0) == q.QMM_ERR_SHAPE
+    assert L.qmm_dequantize(8, NULL, FAKE, 4, 256, S0) == q.QMM_ERR_INVALID_ARG
+    assert L.qmm_dequantize(4, FAKE, MISALIGNED, 4, 256, S0) == q.QMM_ERR_ALIGNMENT
+    assert L.qmm_dequantize(4, NULL, NULL, 0, 256, S0) == q.QMM_OK
+
+
+def test_matmul_argument_errors(lib):
+    L = lib
+    assert L.qmm_matmul(1, FAKE, FAKE, FAKE, 1, 64, 256, NULL, 0, S0) == q.QMM_ERR_INVALID_ARG
+    assert L.qmm_matmul(8, FAKE, FAKE, FAKE, -1, 64, 256, NULL, 0, S0) == q.QMM_ERR_INVALID_ARG
+    assert L.qmm_matmul(8, FAKE, FAKE, FAKE, 1, 64, 200, NULL, 0, S0) == q.QMM_ERR_SHAPE
+    assert L.qmm_matmul(4, FAKE, FAKE, FAKE, 1, 64, 0, NULL, 0, S0) == q.QMM_ERR_SHAPE
+    assert L.qmm_matmul(8, NULL, FAKE, FAKE, 1, 64, 256, NULL, 0, S0) == q.QMM_ERR_INVALID_ARG
+    assert L.qmm_matmul(8, FAKE, NULL, FAKE, 1, 64, 256, NULL, 0, S0) == q.QMM_ERR_INVALID_ARG
+    assert L.qmm_matmul(8, FAKE, FAKE, NULL, 1, 64, 256, NULL, 0, S0) == q.QMM_ERR_INVALID_ARG
+    assert L.qmm_matmul(8, MISALIGNED, FAKE, FAKE, 1, 64, 256, NULL, 0, S0) == q.QMM_ERR_ALIGNMENT
+    assert L.qmm_matmul(8, FAKE, MISALIGNED, FAKE, 1, 64, 256, NULL, 0, S0) == q.QMM_ERR_ALIGNMENT
+    assert L.qmm_matmul(8, FAKE, FAKE, MISALIGNED, 1, 64, 256, NULL, 0, S0) == q.QMM_ERR_ALIGNMENT
+    assert L.qmm_matmul(8, NULL, NULL, NULL, 0, 64, 256, NULL, 0, S0) == q.QMM_OK
+    assert L.qmm_matmul(8, NULL, NULL, NULL, 3, 0, 256, NULL, 0, S0) == q.QMM_OK
+
+
+def test_workspace_query(lib):
+    for fmt in (q.QMM_Q8_0, q.QMM_Q4_K):
+        for M in (1, 4, 16):  # decode shapes reduce in distributed shared memory
+            assert q.qmm_matmul_workspace_bytes(fmt, M, 4096, 4096) == 0
+        assert q.qmm_matmul_workspace_bytes(fmt, 512, 4096, 100) == 0  # invalid K
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError):
+        q.load(str(tmp_path / "nope.so"))

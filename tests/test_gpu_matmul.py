@@ -1,0 +1,119 @@
+"""GPU parity of qmm_matmul against the fp64 CPU oracle.
+
+Tolerance per element: |y - y_ref| <= 1e-3 * sum_k |w^_k x_k| + 1e-6, with
+y_ref and the sum computed by the oracle in fp64 over the exactly dequantized
+weights.  Small shapes compare every output; the full decode / prefill shapes
+compare sampled output features (all tokens) computed one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import ggml_block_quantized_linear_b300 as q
+from ggml_block_quantized_linear_b300 import inputs
+from qmm_testutil import DEV, bf16_from_bits, check_matmul, to_dev_u8
+
+pytestmark = pytest.mark.gpu
+FMTS = [q.QMM_Q8_0, q.QMM_Q4_K]
+
+
+def problem(fmt, n, k, m, seed):
+    w = inputs.weights(n, k, seed)
+    x = inputs.activations(m, k, seed)
+    packed = oracle.quantize(fmt, inputs.bf16_bits(w))
+    xb = inputs.bf16_bits(x)
+    return packed, xb
+
+
+def run(fmt, packed, xb, n):
+    return q.qmm_matmul(fmt, to_dev_u8(packed), bf16_from_bits(xb), n)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("n,k", [(64, 256), (100, 512), (1024, 1792), (192, 4096), (333, 2304)])
+@pytest.mark.parametrize("m", [1, 2, 4, 7, 8, 9, 16])
+def test_decode_small_full(fmt, n, k, m):
+    packed, xb = problem(fmt, n, k, m, 1000 + n + k + m)
+    Y, A = oracle.matmul(fmt, packed, xb, n, k)
+    check_matmul(run(fmt, packed, xb, n), Y, A, "fmt=%d n=%d k=%d m=%d" % (fmt, n, k, m))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_tiny_linear_config(fmt):
+    # fp32 W 256 x 512 quantized, X bf16 1 x 512
+    w = inputs.weights(256, 512, inputs.seed_for(1), fp32=True)
+    packed = oracle.quantize(fmt, w.numpy())
+    xb = inputs.bf16_bits(inputs.activations(1, 512, inputs.seed_for(1)))
+    Y, A = oracle.matmul(fmt, packed, xb, 256, 512)
+    check_matmul(run(fmt, packed, xb, 256), Y, A)
+
+
+def sample_rows(n, count, seed):
+    rng = np.random.default_rng(seed)
+    s = set(rng.choice(n, size=min(count, n), replace=False).tolist())
+    s.update([0, n - 1, min(63, n - 1), min(64, n - 1)])
+    return np.array(sorted(s), dtype=np.int64)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("shape", inputs.DECODE_SHAPES)
+@pytest.mark.parametrize("m", inputs.DECODE_MS)
+def test_decode_full_shapes_sampled(fmt, shape, m):
+    n, k = shape
+    cfg = 2 if fmt == q.QMM_Q8_0 else 3
+    si, mi = inputs.DECODE_SHAPES.index(shape), inputs.DECODE_MS.index(m)
+    w = inputs.weights(n, k, inputs.seed_for(cfg, si))
+    packed = oracle.quantize(fmt, inputs.bf16_bits(w))
+    xb = inputs.bf16_bits(inputs.activations(m, k, inputs.seed_for(cfg, si, mi)))
+    y = run(fmt, packed, xb, n).cpu()
+    ns = sample_rows(n, 192, si * 10 + mi)
+    Y, A = oracle.matmul_columns(fmt, packed, xb, k, ns)
+    check_matmul(y[:, torch.from_numpy(ns)], Y, A, "fmt=%d %s m=%d" % (fmt, shape, m))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_one_hot_and_zero(fmt):
+    n, k = 130, 1024
+    packed, _ = problem(fmt, n, k, 1, 5)
+    cols = [0, 1, 255, 256, 700, 1023, 31, 32, 33, 512, 513, 1000, 100, 200, 300, 400]
+    x = torch.zeros((len(cols), k), dtype=torch.bfloat16)
+    for i, c in enumerate(cols):
+        x[i, c] = 1.0
+    xb = inputs.bf16_bits(x)
+    Y, A = oracle.matmul(fmt, packed, xb, n, k)
+    y = run(fmt, packed, xb, n)
+    check_matmul(y, Y, A, "one-hot")
+    if fmt == q.QMM_Q8_0:  # d * q survives the offset arithmetic exactly
+        assert np.array_equal(y.cpu().double().numpy(), Y)
+    zp = oracle.quantize(fmt, np.zeros((n, k), dtype=np.float32))
+    xb2 = inputs.bf16_bits(inputs.activations(16, k, 3))
+    assert not run(fmt, zp, xb2, n).cpu().any()
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_deterministic_and_stream(fmt):
+    n, k, m = 4096, 4096, 4
+    packed, xb = problem(fmt, n, k, m, 77)
+    s = torch.cuda.Stream()
+    w, x = to_dev_u8(packed), bf16_from_bits(xb)
+    with torch.cuda.stream(s):
+        a = q.qmm_matmul(fmt, w, x, n)
+        b = q.qmm_matmul(fmt, w, x, n)
+    s.synchronize()
+    assert torch.equal(a, b)
+    assert q.qmm_device_error_take() == 0
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_activation_range(fmt):
+    n, k = 64, 512
+    packed, _ = problem(fmt, n, k, 1, 11)
+    rng = np.random.default_rng(4)
+    x = torch.from_numpy(rng.normal(0, 1, (3, k)).astype(np.float32))
+    x[0] *= 3000.0          # large but inside binary16 range
+    x[1] *= 1e-3
+    x[2, ::3] = 0.0
+    xb = inputs.bf16_bits(x.to(torch.bfloat16))
+    Y, A = oracle.matmul(fmt, packed, xb, n, k)
+    check_matmul(run(fmt, packed, xb, n), Y, A, "range")
