@@ -1,0 +1,588 @@
+#!/usr/bin/env python3
+"""Benchmark of the B300 GGML block-quantized linear layer (Q8_0, Q4_K).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  The headline metric is the packed-weight
+bandwidth of the decode GEMV at M = 1 over the decode-shaped linears
+(N x K = 4096x4096, 1024x4096, 14336x4096, 4096x14336) in both formats,
+with the weights cold in L2.  One step runs every stage of the path once,
+each stage captured as a CUDA graph and replayed back to back:
+
+  isq       quantize the four bf16 decode weights to Q8_0 and Q4_K
+  dequant   dequantize them to fp32
+  gemv_m1   decode GEMV, M = 1, all 8 linears          (-> value)
+  gemv_m4   ... M = 4
+  gemv_m16  ... M = 16
+  gemm      prefill GEMM, M = 512 and 2048, 3 shapes x 2 formats
+  model     synthetic 8B-shape decoder (32 layers x 7 linears): ISQ of all
+            224 bf16 weights to Q4_K and to Q8_0, then one M = 1 decode
+            step (224 GEMVs) in each format
+
+Inputs are seeded synthetic tensors (ggml_block_quantized_linear_b300.inputs);
+the packed weights rotate through more than 200 MB per GEMV sweep, so every
+GEMV reads its weights from HBM, not L2.
+
+Under torchrun (N > 1) every rank runs the same per-GPU workload on its own
+GPU (independent problems, weak scaling); there is no data-path collective,
+only a barrier and a max over ranks of the timings.
+
+`--impl reference` times the plain CPU oracle (oracle/) on the host cores on
+a bounded sample of the same workload and metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Q8_0/Q4_K qmatmul weight GB/s vs HBM peak (M=1); TFLOP/s at M=2048"
+UNIT = "GB/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+# --------------------------------------------------------------------- utils
+def env_rank():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "ggml_block_quantized_linear_b300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            h.update(name.encode())
+            h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic():
+    """Per-launch DRAM traffic measured by ncu (profiles/dram_traffic.txt),
+    valid only for the kernel sources it was measured on."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    out = {}
+    if not os.path.exists(p):
+        return out
+    src_hash = None
+    for line in open(p):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        k, _, v = line.partition("=")
+        if k.strip() == "source_hash":
+            src_hash = v.strip()
+        else:
+            try:
+                out[k.strip()] = float(v)
+            except ValueError:
+                pass
+    if src_hash != kernel_source_hash():
+        return {}
+    return out
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        try:
+            sm = [float(r[1]) for r in rows]
+            smax = max(float(r[2]) for r in rows)
+            power = [float(r[3]) for r in rows if r[3].replace(".", "", 1).isdigit()]
+        except ValueError:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        loaded = [s for s, r in zip(sm, rows)] if sm else []
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": smax, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------------- our workload
+class Workload:
+    def __init__(self, device, with_model=True):
+        import torch
+        import ggml_block_quantized_linear_b300 as q
+        from ggml_block_quantized_linear_b300 import inputs
+        self.torch, self.q, self.inputs = torch, q, inputs
+        self.dev = device
+        self.fmts = [q.QMM_Q8_0, q.QMM_Q4_K]
+        # decode-shaped linears: bf16 sources, packed weights, activations
+        self.w_bf16 = []
+        for si, (n, k) in enumerate(inputs.DECODE_SHAPES):
+            self.w_bf16.append(inputs.weights(n, k, inputs.seed_for(2, si), device=device))
+        self.packed = {f: [q.qmm_quantize(f, w) for w in self.w_bf16] for f in self.fmts}
+        self.isq_out = {f: [torch.empty_like(p) for p in self.packed[f]] for f in self.fmts}
+        self.deq_out = [torch.empty((n, k), dtype=torch.float32, device=device)
+                        for (n, k) in inputs.DECODE_SHAPES]
+        self.x = {}
+        self.y = {}
+        for mi, m in enumerate(inputs.DECODE_MS + inputs.PREFILL_MS):
+            self.x[m] = [inputs.activations(m, k, inputs.seed_for(2, si, mi), device=device)
+                         for si, (n, k) in enumerate(inputs.DECODE_SHAPES)]
+            self.y[m] = {f: [torch.empty((m, n), dtype=torch.float32, device=device)
+                             for (n, k) in inputs.DECODE_SHAPES] for f in self.fmts}
+        self.gemm_ok = self._probe_gemm()
+        self.model = None
+        if with_model:
+            self._make_model()
+
+    def _probe_gemm(self):
+        q = self.q
+        try:
+            q.qmm_matmul(q.QMM_Q8_0, self.packed[q.QMM_Q8_0][0], self.x[512][0], 4096,
+                         out=self.y[512][q.QMM_Q8_0][0])
+            self.torch.cuda.synchronize(self.dev)
+            return True
+        except q.QmmError:
+            return False
+
+    def _make_model(self):
+        torch, q, inputs = self.torch, self.q, self.inputs
+        self.model = {"w": [], "packed": {f: [] for f in self.fmts}, "x": [], "y": []}
+        for layer in range(inputs.MODEL_LAYERS):
+            for li, (name, n, k) in enumerate(inputs.MODEL_LINEARS):
+                w = inputs.weights(n, k, 50000 + 10 * layer + li, device=self.dev)
+                self.model["w"].append(w)
+                for f in self.fmts:
+                    self.model["packed"][f].append(q.qmm_quantize(f, w))
+                self.model["x"].append(inputs.activations(1, k, 60000 + 10 * layer + li,
+                                                          device=self.dev))
+                self.model["y"].append(torch.empty((1, n), dtype=torch.float32, device=self.dev))
+
+    # each stage: (name, callable, launches, algorithmic bytes, flops, kernel family)
+    def stages(self):
+        q, inputs = self.q, self.inputs
+        S = []
+        shapes = inputs.DECODE_SHAPES
+        bw = {q.QMM_Q8_0: 34 / 32, q.QMM_Q4_K: 144 / 256}
+
+        def isq():
+            for f in self.fmts:
+                for w, o in zip(self.w_bf16, self.isq_out[f]):
+                    q.qmm_quantize(f, w, out=o)
+        nw = sum(n * k for n, k in shapes)
+        S.append(("isq", isq, 8, sum(nw * (2 + bw[f]) for f in self.fmts), 0.0, "quantize"))
+
+        def deq():
+            for f in self.fmts:
+                for (n, k), p, o in zip(shapes, self.packed[f], self.deq_out):
+                    q.qmm_dequantize(f, p, n, k, out=o)
+        S.append(("dequant", deq, 8, sum(nw * (bw[f] + 4) for f in self.fmts), 0.0, "dequantize"))
+
+        for m in inputs.DECODE_MS:
+            def gemv(m=m):
+                for f in self.fmts:
+                    for (n, k), p, x, y in zip(shapes, self.packed[f], self.x[m], self.y[m][f]):
+                        q.qmm_matmul(f, p, x, n, out=y)
+            wbytes = sum(nw * bw[f] for f in self.fmts)
+            io = 2 * sum((2 * m * k + 4 * m * n) for n, k in shapes)
+            S.append(("gemv_m%d" % m, gemv, 8, wbytes + io, 2.0 * 2 * m * nw, "gemv"))
+
+        if self.gemm_ok:
+            pshapes = inputs.PREFILL_SHAPES
+            for m in inputs.PREFILL_MS:
+                def gemm(m=m):
+                    for f in self.fmts:
+                        for si, (n, k) in enumerate(shapes):
+                            if (n, k) in pshapes:
+                                q.qmm_matmul(f, self.packed[f][si], self.x[m][si], n,
+                                             out=self.y[m][f][si])
+                fl = 2 * 2.0 * m * sum(n * k for n, k in pshapes)
+                S.append(("gemm_m%d" % m, gemm, 6, 0, fl, "gemm"))
+
+        if self.model is not None:
+            mw = sum(n * k for _, n, k in inputs.MODEL_LINEARS) * inputs.MODEL_LAYERS
+            nl = len(self.model["w"])
+
+            def model_isq():
+                for f in self.fmts:
+                    for w, p in zip(self.model["w"], self.model["packed"][f]):
+                        q.qmm_quantize(f, w, out=p)
+            S.append(("model_isq", model_isq, 2 * nl, sum(mw * (2 + bw[f]) for f in self.fmts),
+                      0.0, "quantize"))
+            for f in self.fmts:
+                def model_decode(f=f):
+                    for (_, n, k), p, x, y in zip(inputs.MODEL_LINEARS * inputs.MODEL_LAYERS,
+                                                  self.model["packed"][f], self.model["x"],
+                                                  self.model["y"]):
+                        q.qmm_matmul(f, p, x, n, out=y)
+                name = "model_decode_" + ("q8_0" if f == q.QMM_Q8_0 else "q4_k")
+                S.append((name, model_decode, nl, mw * bw[f], 2.0 * mw, "gemv"))
+        return S
+
+
+def time_graphs(torch, graphs, steps, warmup, dev):
+    """Replay every stage graph once per step; per-stage CUDA-event times."""
+    names = [g[0] for g in graphs]
+    for _ in range(warmup):
+        for _, g in graphs:
+            g.replay()
+    torch.cuda.synchronize(dev)
+    per = {n: [] for n in names}
+    step_ms = []
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(steps):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(graphs) + 1)]
+        evs[0].record(stream)
+        for i, (_, g) in enumerate(graphs):
+            g.replay()
+            evs[i + 1].record(stream)
+        evs[-1].synchronize()
+        for i, n in enumerate(names):
+            per[n].append(evs[i].elapsed_time(evs[i + 1]))
+        step_ms.append(evs[0].elapsed_time(evs[-1]))
+    return per, step_ms
+
+
+def parity_check(wl):
+    """Sampled parity of the benchmarked kernels against the CPU oracle."""
+    import numpy as np
+    import oracle
+    q, inputs = wl.q, wl.inputs
+    worst = 0.0
+    for f in wl.fmts:
+        for si, (n, k) in enumerate(inputs.DECODE_SHAPES):
+            packed = wl.packed[f][si].cpu().numpy()
+            want = oracle.quantize(f, inputs.bf16_bits(wl.w_bf16[si][:64].cpu()))
+            if not np.array_equal(packed[:64], want):
+                return "FAIL: packed bytes differ (fmt %d shape %d)" % (f, si)
+            for m in (1, 16) + ((2048,) if wl.gemm_ok and (n, k) in inputs.PREFILL_SHAPES else ()):
+                ns = np.array([0, 1, n // 2, n - 1], dtype=np.int64)
+                xb = inputs.bf16_bits(wl.x[m][si])
+                Y, A = oracle.matmul_columns(f, packed, xb, k, ns)
+                y = wl.y[m][f][si][:, ns].double().cpu().numpy()
+                r = float((np.abs(y - Y) / (1e-3 * A + 1e-6)).max())
+                worst = max(worst, r)
+    return "ok (max err/bound %.3f)" % worst if worst <= 1.0 else "FAIL (max err/bound %.3f)" % worst
+
+
+def e2e_decode(wl, steps, warmup):
+    """M = 1 decode sweep through the public API with pinned host buffers:
+    per linear, H2D of x, qmm_matmul, D2H of y, inside the timed region."""
+    torch, q, inputs = wl.torch, wl.q, wl.inputs
+    hx, hy, dx, dy = [], [], [], []
+    for f in wl.fmts:
+        for si, (n, k) in enumerate(inputs.DECODE_SHAPES):
+            hx.append(wl.x[1][si].cpu().pin_memory())
+            hy.append(torch.empty((1, n), dtype=torch.float32).pin_memory())
+            dx.append(torch.empty((1, k), dtype=torch.bfloat16, device=wl.dev))
+            dy.append(torch.empty((1, n), dtype=torch.float32, device=wl.dev))
+    stream = torch.cuda.current_stream(wl.dev)
+    jobs = [(f, si, n) for f in wl.fmts for si, (n, k) in enumerate(inputs.DECODE_SHAPES)]
+
+    def one():
+        for j, (f, si, n) in enumerate(jobs):
+            dx[j].copy_(hx[j], non_blocking=True)
+            q.qmm_matmul(f, wl.packed[f][si], dx[j], n, out=dy[j])
+            hy[j].copy_(dy[j], non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(warmup):
+        one()
+    t = []
+    for _ in range(steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        one()
+        e1.record(stream)
+        e1.synchronize()
+        t.append(e0.elapsed_time(e1))
+    wbytes = sum(p.numel() for f in wl.fmts for p in wl.packed[f])
+    h2d = sum(x.numel() * 2 for x in hx)
+    d2h = sum(y.numel() * 4 for y in hy)
+    ms = statistics.median(t)
+    return {"value": round(wbytes / (ms * 1e-3) / 1e9, 1), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4),
+            "launches_per_step": len(jobs)}
+
+
+# ------------------------------------------------------------ CPU oracle arm
+def oracle_decode_sample(threads=None, min_seconds=10.0):
+    """Time the oracle's M = 1 matmul over the eight decode-shaped linears
+    (rows sampled evenly, so that the sample takes ~min_seconds)."""
+    import numpy as np
+    import torch
+    import oracle
+    from ggml_block_quantized_linear_b300 import inputs
+    if threads:
+        oracle.set_threads(threads)
+    cores = oracle.max_threads()
+    probs = []
+    for f in (oracle.Q8_0, oracle.Q4_K):
+        for si, (n, k) in enumerate(inputs.DECODE_SHAPES):
+            rows = 256  # weight rows per linear in the sample
+            w = inputs.weights(rows, k, inputs.seed_for(2, si))
+            packed = oracle.quantize(f, inputs.bf16_bits(w))
+            xb = inputs.bf16_bits(inputs.activations(1, k, inputs.seed_for(2, si, 0)))
+            probs.append((f, packed, xb, rows, k))
+    nbytes = sum(p[1].size for p in probs)
+    reps, total = 0, 0.0
+    while total < min_seconds:
+        t0 = time.perf_counter()
+        for f, packed, xb, rows, k in probs:
+            oracle.matmul(f, packed, xb, rows, k)
+        total += time.perf_counter() - t0
+        reps += 1
+    gbs = nbytes * reps / total / 1e9
+    return {"value": round(gbs, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": "oracle fp64 matmul at M=1 over 256 weight rows of each of the 8 decode "
+                      "linears (4 shapes x Q8_0/Q4_K), %d repetitions, %.1f s" % (reps, total)}
+
+
+def run_reference(args):
+    rank, world, _ = env_rank()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    cores = oracle.max_threads()
+    # each step: one pass of the oracle over the bounded decode sample
+    import numpy as np
+    from ggml_block_quantized_linear_b300 import inputs
+    probs = []
+    for f in (oracle.Q8_0, oracle.Q4_K):
+        for si, (n, k) in enumerate(inputs.DECODE_SHAPES):
+            rows = 256
+            w = inputs.weights(rows, k, inputs.seed_for(2, si))
+            packed = oracle.quantize(f, inputs.bf16_bits(w))
+            xb = inputs.bf16_bits(inputs.activations(1, k, inputs.seed_for(2, si, 0)))
+            probs.append((f, packed, xb, rows, k))
+    nbytes = sum(p[1].size for p in probs)
+
+    def step():
+        for f, packed, xb, rows, k in probs:
+            oracle.matmul(f, packed, xb, rows, k)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = nbytes * args.steps / dt / 1e9
+    sample = ("oracle fp64 matmul at M=1 over 256 weight rows of each of the 8 decode linears "
+              "(4 shapes x Q8_0/Q4_K) per step")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(),
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config():
+    return {"workload": "decode-shaped Q8_0/Q4_K linears (N x K = 4096x4096, 1024x4096, "
+                        "14336x4096, 4096x14336), GEMV at M=1 (headline) plus M=4/16, ISQ, "
+                        "dequant, prefill GEMM M=512/2048 and a 32-layer 8B-shape model "
+                        "(ISQ + 224-GEMV decode step) in each step",
+            "weights": "bf16 ~N(0,0.02) with 0.1% x20 outliers, seeded",
+            "activations": "bf16 ~N(0,1), seeded",
+            "l2": "inputs larger than L2: each GEMV sweep reads > 200 MB of distinct packed "
+                  "weights, the model step 11.3 GB",
+            "accumulate": "f32", "graphs": "each stage captured as one CUDA graph"}
+
+
+# --------------------------------------------------------------------- main
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-model", action="store_true", help="skip the 32-layer model stage")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+    rank, world, local = env_rank()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import ggml_block_quantized_linear_b300 as q
+    q.load()
+
+    wl = Workload(dev, with_model=not args.no_model)
+    stages = wl.stages()
+    # capture each stage as one graph (first call of every kernel happens in
+    # the workload set-up above, so capture sees no lazy initialisation)
+    for _, fn, *_ in stages:
+        fn()
+    torch.cuda.synchronize(dev)
+    graphs = []
+    cap = torch.cuda.Stream(dev)
+    with torch.cuda.stream(cap):
+        for name, fn, *_ in stages:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
+                fn()
+            graphs.append((name, g))
+    torch.cuda.synchronize(dev)
+    if q.qmm_device_error_take() != 0:
+        raise RuntimeError("device error during set-up")
+
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local)
+    clocks.start()
+    per, step_ms = time_graphs(torch, graphs, args.steps, args.warmup, dev)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    if q.qmm_device_error_take() != 0:
+        raise RuntimeError("device error during the timed region")
+
+    # median over steps per stage; max over ranks
+    med = {n: statistics.median(v) for n, v in per.items()}
+    ms_step = statistics.median(step_ms)
+    if world > 1:
+        vals = torch.tensor([ms_step] + [med[n] for n, *_ in stages], device=dev, dtype=torch.float64)
+        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
+        ms_step = float(vals[0])
+        for i, (n, *_) in enumerate(stages):
+            med[n] = float(vals[i + 1])
+
+    peaks, peak_kind = load_peaks()
+    traffic = load_traffic()
+    info = {s[0]: s for s in stages}
+    wbytes_m1 = sum(p.numel() for f in wl.fmts for p in wl.packed[f])
+    value = wbytes_m1 * world / (med["gemv_m1"] * 1e-3) / 1e9
+
+    rows = {}
+    fam_time = {}
+    for name, _, launches, nbytes, flops, fam in stages:
+        t = med[name] * 1e-3
+        r = {"ms": round(med[name], 4), "launches": launches}
+        if nbytes:
+            r["GBps"] = round(nbytes / t / 1e9, 1)
+        if fam == "gemm":
+            r["TFLOPs"] = round(flops / t / 1e12, 1)
+        rows[name] = r
+        fam_time[fam] = fam_time.get(fam, 0.0) + med[name]
+    for f, nm in ((q.QMM_Q8_0, "q8_0"), (q.QMM_Q4_K, "q4_k")):
+        key = "model_decode_" + nm
+        if key in rows:
+            rows[key]["weight_GBps"] = rows[key].pop("GBps")
+
+    def roofline_for(fam):
+        sel = [s for s in stages if s[5] == fam]
+        t = sum(med[s[0]] for s in sel) * 1e-3
+        launches = sum(s[2] for s in sel)
+        if fam == "gemm":
+            fl = sum(s[4] for s in sel)
+            peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+            ach = fl / t / 1e12
+            return {"bound": "tensor", "achieved": round(ach, 1), "peak": peak, "unit": "TFLOP/s",
+                    "frac": round(ach / peak, 4), "traffic": None,
+                    "peak_source": peak_kind + " bf16 burst (f16 same nominal rate)",
+                    "launches": launches}
+        nb = sum(s[3] for s in sel)
+        peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+        ach = nb / t / 1e9
+        tr = traffic.get(fam)
+        return {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(ach / peak, 4),
+                "traffic": tr, "traffic_ratio": round(tr / (nb / launches), 3) if tr else None,
+                "peak_source": peak_kind + " copy bandwidth", "launches": launches}
+
+    dominant = max(fam_time, key=fam_time.get)
+    rooflines = {fam: roofline_for(fam) for fam in fam_time}
+    gemv_roof = rooflines["gemv"]
+    # the headline kernel: M = 1 decode GEMV sweep alone
+    m1 = info["gemv_m1"]
+    m1_ach = m1[3] / (med["gemv_m1"] * 1e-3) / 1e9
+    rooflines["gemv_m1"] = {"bound": "hbm", "achieved": round(m1_ach, 1),
+                            "peak": peaks.get("hbm_gbs"), "unit": "GB/s",
+                            "frac": round(m1_ach / peaks.get("hbm_gbs"), 4),
+                            "weight_only_frac": round(value / world / peaks.get("hbm_gbs"), 4)}
+
+    line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+            "data": "synthetic", "config": workload_config(),
+            "roofline": dict(rooflines[dominant], kernel=dominant),
+            "rooflines": rooflines, "rows": rows,
+            "gemm_tflops_m2048": rows.get("gemm_m2048", {}).get("TFLOPs"),
+            "clocks": clk, "gpu_launches": sum(s[2] for s in stages) * args.steps,
+            "parity": None, "kernel_source": kernel_source_hash()}
+    if rank == 0:
+        line["parity"] = parity_check(wl)
+        line["e2e"] = e2e_decode(wl, max(3, args.steps), 3)
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = oracle_decode_sample()
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -4,9 +4,11 @@
 // warp-level MMA used by the decode kernel, and the device error word.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (types only; the driver is reached through the runtime)
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 #include <stdint.h>
 
 namespace qmm {
@@ -61,14 +63,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
 }
+// Suspend-time hint of one try_wait: the thread sleeps until the phase
+// completes or this many nanoseconds pass, instead of spinning.
+constexpr uint32_t kTryWaitHintNs = 20000;
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(kTryWaitHintNs)
         : "memory");
     return ok != 0;
 }
@@ -103,6 +108,45 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
             dst),
         "l"(src), "r"(bytes), "r"(bar)
         : "memory");
+}
+
+// 2-D tiled tensor copy global -> shared (this CTA), completing on an
+// mbarrier.  (x, y) are element coordinates of the box's first element; x *
+// element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// Host: encode a 2-D tiled tensor map (row-major [dim1][dim0] of `dtype`,
+// row pitch `stride1_bytes`, box [box1][box0], no swizzle, zero fill out of
+// bounds).  The driver function is looked up once through the runtime.
+inline cudaError_t encode_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype,
+                                  uint64_t dim0, uint64_t dim1, uint64_t stride1_bytes,
+                                  uint32_t box0, uint32_t box1,
+                                  CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE) {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        cudaDriverEntryPointQueryResult q;
+        void *p = nullptr;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                                         cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || p == nullptr)
+            return e != cudaSuccess ? e : cudaErrorNotSupported;
+        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    const cuuint64_t dims[2] = {dim0, dim1};
+    const cuuint64_t strides[1] = {stride1_bytes};
+    const cuuint32_t box[2] = {box0, box1};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, dtype, 2, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 // ------------------------------------------------------------------ cluster

@@ -11,9 +11,10 @@
 //    share a row tile form one thread-block cluster (split-K).  Their partial
 //    sums are reduced through distributed shared memory in rank order, so
 //    the result is deterministic and needs no workspace.
-//  * One producer warp streams the CTA's rows, 256 weights (272 / 144 bytes)
-//    per row per stage, with 1-D bulk copies (cp.async.bulk) into a ring of
-//    shared-memory stages guarded by mbarriers.
+//  * One producer thread streams the CTA's 64 rows, 256 weights (272 / 144
+//    bytes) per row per stage, as ONE 2-D tensor-map TMA copy per stage
+//    (cp.async.bulk.tensor) into a ring of shared-memory stages guarded by
+//    mbarriers.  Rows past N are zero-filled by the TMA unit.
 //  * Four consumer warps (16 rows each) run warp-level tensor-core MMAs
 //    (m16n8k16, f16 inputs, fp32 accumulation) with the weight rows as the
 //    M side and the (padded) tokens as N.  The MMA operands are the integer
@@ -53,15 +54,15 @@ struct GemvLayout {
 };
 
 // Byte offsets of the shared-memory regions; identical on host and device.
-__host__ __device__ inline GemvLayout gemv_layout(int fmt, int nt, int stages, int kr_max) {
-    const int slot = (fmt == 8 ? kQ8GroupBytes : kQ4Bytes) + 16;  // padded row slot
+__host__ __device__ inline GemvLayout gemv_layout(int fmt, int nt, int M, int stages, int kr_max) {
+    const int slot = fmt == 8 ? kQ8GroupBytes : kQ4Bytes;  // dense rows, as the TMA box lands
     const int mt = 8 * nt;
     GemvLayout L;
     int off = 0;
     L.ring = off;
     off += stages * kGemvRows * slot;
     L.xh = off;
-    off += mt * (kr_max + 32) * 2;
+    off += M * (kr_max + 32) * 2;  // only the real tokens are staged
     L.xs = off;
     off += (kr_max / 32) * mt * 4;
     L.coef = off;
@@ -103,9 +104,14 @@ __device__ __forceinline__ void load_q8_codes(const uint8_t *p, uint32_t &w0, ui
 __device__ __forceinline__ uint32_t q8_pair02(uint32_t u) { return prmt(u, 0x64646464u, 0x4240u); }
 __device__ __forceinline__ uint32_t q8_pair13(uint32_t u) { return prmt(u, 0x64646464u, 0x4341u); }
 
+// 16-byte B-fragment load of token row (g + 8 nt); tokens >= M are zero.
+__device__ __forceinline__ uint4 x_frag(const __half *p, bool valid) {
+    return valid ? *reinterpret_cast<const uint4 *>(p) : make_uint4(0u, 0u, 0u, 0u);
+}
+
 template <int kB, int kNT>
 __device__ __forceinline__ void q8_block(const uint8_t *r0, const uint8_t *r1, const __half *xrow,
-                                         int xstride, const float *xs, int blk, int t,
+                                         int xstride, const float *xs, int blk, int t, int gvalid,
                                          float (&acc)[kNT][4]) {
     // code offset of this block inside the row slot: 34b + 2 + 8t
     constexpr int kOff = kQ8Bytes * kB + 2;
@@ -120,8 +126,7 @@ __device__ __forceinline__ void q8_block(const uint8_t *r0, const uint8_t *r1, c
     const uint32_t A1[4] = {q8_pair02(a1), q8_pair02(b1), q8_pair13(a1), q8_pair13(b1)};
 #pragma unroll
     for (int nt = 0; nt < kNT; ++nt) {
-        const uint4 xv =
-            *reinterpret_cast<const uint4 *>(xrow + nt * 8 * xstride + kQ8Weights * kB + 8 * t);
+        const uint4 xv = x_frag(xrow + nt * 8 * xstride + kQ8Weights * kB + 8 * t, nt * 8 < gvalid);
         float c[4] = {0.f, 0.f, 0.f, 0.f};
         mma_f16_16816(c, A0, xv.x, xv.y);
         mma_f16_16816(c, A1, xv.z, xv.w);
@@ -136,8 +141,9 @@ __device__ __forceinline__ void q8_block(const uint8_t *r0, const uint8_t *r1, c
 template <int kNT>
 __device__ __forceinline__ void q4k_chunk(const uint8_t *base, const uint8_t *r0, const uint8_t *r1,
                                           const __half *xr, int xstride, const float *xs, int li,
-                                          float *cw, int lane, int g, int t, float (&acc)[kNT][4]) {
-    constexpr int kSlot = kQ4Bytes + 16;
+                                          float *cw, int lane, int g, int t, int gvalid,
+                                          float (&acc)[kNT][4]) {
+    constexpr int kSlot = kQ4Bytes;
     constexpr int kMT = 8 * kNT;
     // per-row coefficients (a_j, b_j) of the 8 sub-blocks; lane (row =
     // lane / 2) decodes sub-blocks 4 * (lane & 1) .. + 3 of its row
@@ -185,8 +191,8 @@ __device__ __forceinline__ void q4k_chunk(const uint8_t *base, const uint8_t *r0
 #pragma unroll
         for (int nt = 0; nt < kNT; ++nt) {
             const __half *xq = xr + nt * 8 * xstride + 64 * c + 8 * t;
-            const uint4 xl = *reinterpret_cast<const uint4 *>(xq);
-            const uint4 xhv = *reinterpret_cast<const uint4 *>(xq + 32);
+            const uint4 xl = x_frag(xq, nt * 8 < gvalid);
+            const uint4 xhv = x_frag(xq + 32, nt * 8 < gvalid);
             float cl[4] = {0.f, 0.f, 0.f, 0.f}, chh[4] = {0.f, 0.f, 0.f, 0.f};
             mma_f16_16816(cl, L0, xl.x, xl.y);
             mma_f16_16816(cl, L1, xl.z, xl.w);
@@ -204,10 +210,11 @@ __device__ __forceinline__ void q4k_chunk(const uint8_t *base, const uint8_t *r0
 }
 
 template <int kFmt, int kNT>
-__global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const GemvParams p) {
+__global__ void __launch_bounds__(kGemvThreads)
+gemv_kernel(const __grid_constant__ CUtensorMap wmap, const GemvParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int kCB = kFmt == 8 ? kQ8GroupBytes : kQ4Bytes;  // bytes per row per chunk
-    constexpr int kSlot = kCB + 16;
+    constexpr int kSlot = kCB;
     constexpr int kMT = 8 * kNT;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t nsplit = cluster_nctarank(), rank = cluster_ctarank();
@@ -217,7 +224,7 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const GemvParams p) 
     const int nloc = c_end - c_begin;
     const int kbase = c_begin * kGroup;
     const int xstride = p.kr_max + 32;
-    const GemvLayout L = gemv_layout(kFmt, kNT, p.stages, p.kr_max);
+    const GemvLayout L = gemv_layout(kFmt, kNT, p.M, p.stages, p.kr_max);
     uint8_t *ring = smem + L.ring;
     __half *xh = reinterpret_cast<__half *>(smem + L.xh);
     float *xs = reinterpret_cast<float *>(smem + L.xs);
@@ -234,22 +241,24 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const GemvParams p) 
         }
         fence_mbar_init();
     }
+    // block sums of padding tokens (m >= M) stay zero for the whole kernel
+    for (int idx = tid; idx < (p.kr_max / 32) * kMT; idx += kGemvThreads) xs[idx] = 0.f;
     __syncthreads();
 
     if (warp == kGemvWarps) {
-        // ---------------- producer: bulk-copy the row tile, chunk by chunk
-        const int rows_valid = min(kGemvRows, p.N - row0);
-        const uint8_t *tile = p.W + (int64_t)row0 * p.row_bytes + (int64_t)c_begin * kCB;
+        // ---------------- producer: one 2-D TMA copy of the row tile per chunk
+        if (lane == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wmap)) : "memory");
         for (int i = 0; i < nloc; ++i) {
             const int s = i % p.stages;
             if (i >= p.stages &&
                 !mbar_wait_warp(empty_bar(s), ((i / p.stages) - 1) & 1, kErrGemvEmptyWait))
                 break;  // bug path: consumers then time out on their full barriers
-            if (lane == 0) mbar_arrive_expect_tx(full_bar(s), (uint32_t)(rows_valid * kCB));
+            if (lane == 0) {
+                mbar_arrive_expect_tx(full_bar(s), (uint32_t)(kGemvRows * kCB));
+                tma_load_2d(smem_addr(ring + s * kGemvRows * kSlot), &wmap,
+                            (c_begin + i) * (kCB / 2), row0, full_bar(s));
+            }
             __syncwarp();
-            for (int r = lane; r < rows_valid; r += 32)
-                bulk_g2s(smem_addr(ring + (s * kGemvRows + r) * kSlot),
-                         tile + (int64_t)r * p.row_bytes + (int64_t)i * kCB, kCB, full_bar(s));
         }
     } else {
         // ---------------- consumers
@@ -258,7 +267,8 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const GemvParams p) 
 #pragma unroll
         for (int nt = 0; nt < kNT; ++nt)
             acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-        const __half *xrow = xh + g * xstride;
+        const __half *xrow = xh + g * xstride;  // token g (+ 8 nt); read only if < M
+        const int gvalid = p.M - g;             // token g + 8 nt is real iff 8 nt < gvalid
         float *cw = coef + warp * 16 * 16;
         const int win = p.kr_max / kGroup;  // chunks per activation window
         // `ok` is warp-uniform; after a timed-out wait the warp skips its
@@ -270,11 +280,10 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const GemvParams p) 
             // stage the window's activations as binary16 (+ 32-weight block sums)
             const int ngr = (wn * kGroup) / 8;  // 8-element groups per token
             const int kw = kbase + w0 * kGroup;
-            for (int idx = tid; idx < kMT * ngr; idx += kGemvWarps * 32) {
+            for (int idx = tid; idx < p.M * ngr; idx += kGemvWarps * 32) {
                 const int m = idx / ngr, kg = idx - m * ngr;
-                uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                if (m < p.M)
-                    v = __ldg(reinterpret_cast<const uint4 *>(p.X + (int64_t)m * p.K + kw + 8 * kg));
+                const uint4 v =
+                    __ldg(reinterpret_cast<const uint4 *>(p.X + (int64_t)m * p.K + kw + 8 * kg));
                 const uint32_t w[4] = {v.x, v.y, v.z, v.w};
                 float f[8];
 #pragma unroll
@@ -312,16 +321,16 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const GemvParams p) 
                 const uint8_t *r1 = base + (g + 8) * kSlot;
                 const __half *xr = xrow + li * kGroup;
                 if constexpr (kFmt == 8) {
-                    q8_block<0, kNT>(r0, r1, xr, xstride, xs, li * 8 + 0, t, acc);
-                    q8_block<1, kNT>(r0, r1, xr, xstride, xs, li * 8 + 1, t, acc);
-                    q8_block<2, kNT>(r0, r1, xr, xstride, xs, li * 8 + 2, t, acc);
-                    q8_block<3, kNT>(r0, r1, xr, xstride, xs, li * 8 + 3, t, acc);
-                    q8_block<4, kNT>(r0, r1, xr, xstride, xs, li * 8 + 4, t, acc);
-                    q8_block<5, kNT>(r0, r1, xr, xstride, xs, li * 8 + 5, t, acc);
-                    q8_block<6, kNT>(r0, r1, xr, xstride, xs, li * 8 + 6, t, acc);
-                    q8_block<7, kNT>(r0, r1, xr, xstride, xs, li * 8 + 7, t, acc);
+                    q8_block<0, kNT>(r0, r1, xr, xstride, xs, li * 8 + 0, t, gvalid, acc);
+                    q8_block<1, kNT>(r0, r1, xr, xstride, xs, li * 8 + 1, t, gvalid, acc);
+                    q8_block<2, kNT>(r0, r1, xr, xstride, xs, li * 8 + 2, t, gvalid, acc);
+                    q8_block<3, kNT>(r0, r1, xr, xstride, xs, li * 8 + 3, t, gvalid, acc);
+                    q8_block<4, kNT>(r0, r1, xr, xstride, xs, li * 8 + 4, t, gvalid, acc);
+                    q8_block<5, kNT>(r0, r1, xr, xstride, xs, li * 8 + 5, t, gvalid, acc);
+                    q8_block<6, kNT>(r0, r1, xr, xstride, xs, li * 8 + 6, t, gvalid, acc);
+                    q8_block<7, kNT>(r0, r1, xr, xstride, xs, li * 8 + 7, t, gvalid, acc);
                 } else {
-                    q4k_chunk<kNT>(base, r0, r1, xr, xstride, xs, li, cw, lane, g, t, acc);
+                    q4k_chunk<kNT>(base, r0, r1, xr, xstride, xs, li, cw, lane, g, t, gvalid, acc);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty_bar(s));
@@ -353,10 +362,50 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const GemvParams p) 
 }
 
 // ------------------------------------------------------------- launcher
+// Activation window (in 256-weight chunks) staged in shared memory at once,
+// and ring depth, per format / token tile.
+static int gemv_window(int nt) { return nt == 1 ? 8 : 4; }
+static int gemv_stages(int fmt) { return fmt == 8 ? 3 : 4; }
+
+struct GemvPlan {
+    int nsplit, stages, kr_max, smem;
+};
+
+// Split-K factor (cluster size along K) and shared-memory plan: the largest
+// power of two <= 8 that keeps every CTA on at least two chunks and the grid
+// within one wave of resident CTAs.
+static GemvPlan gemv_plan(int fmt, int M, int N, int K, int sms) {
+    const int nt = M <= 8 ? 1 : 2;
+    const int tiles = (N + kGemvRows - 1) / kGemvRows;
+    const int nchunks = K / kGroup;
+    GemvPlan best = {0, 0, 0, 0};
+    for (int s = 1; s <= 8; s *= 2) {
+        if (s > 1 && nchunks < 2 * s) break;
+        const int per = (nchunks + s - 1) / s;
+        GemvPlan pl;
+        pl.nsplit = s;
+        pl.stages = per < gemv_stages(fmt) ? per : gemv_stages(fmt);
+        pl.kr_max = (per < gemv_window(nt) ? per : gemv_window(nt)) * kGroup;
+        pl.smem = gemv_layout(fmt, nt, M, pl.stages, pl.kr_max).total;
+        const int by_smem = (228 * 1024) / (pl.smem + 1024);
+        const int by_warps = 64 / (kGemvThreads / 32);
+        const int per_sm = by_smem < by_warps ? by_smem : by_warps;
+        if (s == 1 || tiles * s <= sms * per_sm) best = pl;
+        else break;
+    }
+    return best;
+}
+
 template <int kFmt, int kNT>
-static cudaError_t launch_gemv_t(const GemvParams &p0, int nsplit, int sms, cudaStream_t stream) {
-    GemvParams p = p0;
-    const GemvLayout L = gemv_layout(kFmt, kNT, p.stages, p.kr_max);
+static cudaError_t launch_gemv_t(const GemvParams &p, const GemvPlan &pl, cudaStream_t stream) {
+    // packed weights viewed as uint16 [N][row_bytes / 2]; box = 64 rows x one
+    // 256-weight group
+    constexpr int kCB = kFmt == 8 ? kQ8GroupBytes : kQ4Bytes;
+    CUtensorMap wmap;
+    cudaError_t te = encode_tmap_2d(&wmap, p.W, CU_TENSOR_MAP_DATA_TYPE_UINT16,
+                                    (uint64_t)(p.row_bytes / 2), (uint64_t)p.N,
+                                    (uint64_t)p.row_bytes, kCB / 2, kGemvRows);
+    if (te != cudaSuccess) return te;
     static bool attr_set = false;  // per process; the limit is the same on every device
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(gemv_kernel<kFmt, kNT>,
@@ -364,33 +413,20 @@ static cudaError_t launch_gemv_t(const GemvParams &p0, int nsplit, int sms, cuda
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    (void)sms;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((p.N + kGemvRows - 1) / kGemvRows), (unsigned)nsplit, 1);
+    cfg.gridDim = dim3((unsigned)((p.N + kGemvRows - 1) / kGemvRows), (unsigned)pl.nsplit, 1);
     cfg.blockDim = dim3(kGemvThreads, 1, 1);
-    cfg.dynamicSmemBytes = (size_t)L.total;
+    cfg.dynamicSmemBytes = (size_t)pl.smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = (unsigned)nsplit;
+    attr[0].val.clusterDim.y = (unsigned)pl.nsplit;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<kFmt, kNT>, p);
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<kFmt, kNT>, wmap, p);
 }
-
-// Split-K factor (cluster size along K) for an N x K problem.
-int gemv_split(int N, int K, int sms) {
-    const int tiles = (N + kGemvRows - 1) / kGemvRows;
-    const int nchunks = K / kGroup;
-    int s = 1;
-    while (s < 8 && tiles * s < 2 * sms && nchunks >= 4 * s) s *= 2;
-    return s;
-}
-
-// Activation window (in 256-weight chunks) staged in shared memory at once.
-constexpr int kGemvMaxWindow = 8;
 
 cudaError_t launch_gemv(int fmt, const void *W, const uint16_t *X, float *Y, int M, int N, int K,
                         int sms, cudaStream_t stream) {
@@ -403,13 +439,12 @@ cudaError_t launch_gemv(int fmt, const void *W, const uint16_t *X, float *Y, int
     p.K = K;
     p.nchunks = K / kGroup;
     p.row_bytes = (int64_t)p.nchunks * (fmt == 8 ? kQ8GroupBytes : kQ4Bytes);
-    const int nsplit = gemv_split(N, K, sms);
-    const int per = (p.nchunks + nsplit - 1) / nsplit;
-    p.stages = per < kGemvMaxStages ? per : kGemvMaxStages;
-    p.kr_max = (per < kGemvMaxWindow ? per : kGemvMaxWindow) * kGroup;
+    const GemvPlan pl = gemv_plan(fmt, M, N, K, sms);
+    p.stages = pl.stages;
+    p.kr_max = pl.kr_max;
     if (fmt == 8)
-        return M <= 8 ? launch_gemv_t<8, 1>(p, nsplit, sms, stream) : launch_gemv_t<8, 2>(p, nsplit, sms, stream);
-    return M <= 8 ? launch_gemv_t<4, 1>(p, nsplit, sms, stream) : launch_gemv_t<4, 2>(p, nsplit, sms, stream);
+        return M <= 8 ? launch_gemv_t<8, 1>(p, pl, stream) : launch_gemv_t<8, 2>(p, pl, stream);
+    return M <= 8 ? launch_gemv_t<4, 1>(p, pl, stream) : launch_gemv_t<4, 2>(p, pl, stream);
 }
 
 }  // namespace qmm
