@@ -1,19 +1,453 @@
-// gemm.cu -- prefill-shaped quantized matmul (M > 16).  Placeholder until the
-// tcgen05 kernel lands: reports "not supported".
+// gemm.cu -- prefill-shaped quantized matmul (M > 16 tokens) on the 5th-
+// generation tensor cores: Y[M x N] = X[M x K] * W^T, W packed Q8_0 / Q4_K.
+//
+// The mistral.rs documentation ("Quantization types") sends larger dense
+// batches to tiled matrix multiplication (section NVFP4) and describes FP8
+// W8A16 GEMMs that convert each weight tile to BF16 / F16 inside the GEMM
+// (section FP8).  This kernel does the same for the GGML block formats: the
+// packed weight tile is dequantized in shared memory and fed to tcgen05.mma.
+//
+// Operand precision.  The dequantized weights are rounded to binary16 (not
+// bf16): the relative error 2^-11 per weight keeps every output inside
+// 1e-3 * sum|w x| even for a one-hot activation row, which bf16's 2^-9 does
+// not.  tcgen05 kind::f16 needs both operands in one type, so the bf16
+// activations are converted to binary16 once per call (first kernel below)
+// into the caller's workspace.
+//
+// Tile: 128 weight rows (the MMA's M side, "swap AB") x 256 tokens (MMA N)
+// x 64 K per stage; the fp32 accumulator lives in 256 TMEM columns.
+//   warp 0      TMA producer: packed weights (one 128-row box per 256-weight
+//               group) and binary16 activation tiles (128B-swizzled boxes)
+//   warp 1      TMEM allocator and single-thread MMA issuer
+//   warps 2-9   dequantize packed weights into 128B-swizzled K-major f16
+//               A stages, then read the accumulator back (tcgen05.ld) and
+//               store Y.
+// Every wait is bounded (common.cuh); TMEM is always released.
 #include "common.cuh"
 
 namespace qmm {
 
+constexpr int kGemmBM = 128;        // weight rows per CTA (MMA M)
+constexpr int kGemmBN = 256;        // tokens per CTA (MMA N)
+constexpr int kGemmBK = 64;         // K per stage (one 128-byte swizzle atom of f16)
+constexpr int kGemmDeqWarps = 8;
+constexpr int kGemmThreads = (2 + kGemmDeqWarps) * 32;
+constexpr int kGemmStagesB = 3;     // activation stages (32 KB each)
+constexpr int kGemmStagesP = 2;     // packed weight groups
+constexpr int kGemmTmemCols = 256;
+
+__host__ __device__ constexpr int gemm_stages_a(int fmt) { return fmt == 8 ? 3 : 4; }
+__host__ __device__ constexpr int gemm_group_bytes(int fmt) { return fmt == 8 ? kQ8GroupBytes : kQ4Bytes; }
+
+struct GemmLayout {
+    int b, a, p, coef, bars, total;  // offsets from the 1024-aligned base
+};
+
+__host__ __device__ inline GemmLayout gemm_layout(int fmt) {
+    GemmLayout L;
+    int off = 0;
+    L.b = off;
+    off += kGemmStagesB * kGemmBN * kGemmBK * 2;
+    L.a = off;
+    off += gemm_stages_a(fmt) * kGemmBM * kGemmBK * 2;
+    L.p = off;
+    off += kGemmStagesP * kGemmBM * gemm_group_bytes(fmt);
+    L.coef = off;
+    off += fmt == 4 ? kGemmBM * 8 * 2 * 4 : 0;
+    off = (off + 15) & ~15;
+    L.bars = off;
+    off += 64 * 8;  // barriers + TMEM address slot
+    L.total = off + 1024;  // + alignment slack of the dynamic base
+    return L;
+}
+
+// ------------------------------------------------------------ tcgen05 / UMMA
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, both K-major, kind::f16.
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive (once) on an mbarrier when all previously issued tcgen05 ops of
+// this thread have completed.
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle,
+// 8-row core groups 1024 bytes apart (SBO), sm_100 descriptor version 1.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr >> 4) & 0x3FFFu);  // start address
+    d |= (uint64_t)1u << 16;                      // leading byte offset (unused with SW128)
+    d |= (uint64_t)(1024u >> 4) << 32;            // stride byte offset
+    d |= (uint64_t)1u << 46;                      // descriptor version
+    d |= (uint64_t)2u << 61;                      // SWIZZLE_128B
+    return d;
+}
+// Instruction descriptor of kind::f16: A = B = f16, D = f32, both K-major.
+__host__ __device__ constexpr uint32_t umma_idesc_f16(int m, int n) {
+    return (1u << 4)                       // D format f32
+           | (0u << 7) | (0u << 10)        // A, B format f16
+           | ((uint32_t)(n >> 3) << 17)    // N / 8
+           | ((uint32_t)(m >> 4) << 24);   // M / 16
+}
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+          "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+          "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+          "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void fence_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ----------------------------------------------------- activation conversion
+// X bf16 -> binary16 (round to nearest), 8 elements per thread.
+__global__ void __launch_bounds__(256) x_to_f16_kernel(const uint16_t *__restrict__ X,
+                                                       __half *__restrict__ Xh, int64_t n8) {
+    for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n8; i += (int64_t)gridDim.x * 256) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(X) + i);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const __half2 h = __floats2half2_rn(__uint_as_float(w[e] << 16),
+                                                __uint_as_float(w[e] & 0xFFFF0000u));
+            o[e] = *reinterpret_cast<const uint32_t *>(&h);
+        }
+        reinterpret_cast<uint4 *>(Xh)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+// --------------------------------------------------------- dequantization
+// Byte offset of element (row r, k) in a 128B-swizzled K-major f16 tile.
+__device__ __forceinline__ uint32_t sw128_chunk_off(int r, int chunk) {
+    return (uint32_t)(r * 128 + ((chunk ^ (r & 7)) << 4));
+}
+
+// Q8_0: 8 weights (k = 8c .. 8c+7 of k-step j) of packed row `prow`.
+__device__ __forceinline__ uint4 deq8_q8_0(const uint8_t *prow, int j, int c) {
+    const int b = 2 * j + (c >> 2);                 // block inside the 256-weight group
+    const int off = kQ8Bytes * b + 2 + 8 * (c & 3);  // first code byte (2-byte aligned)
+    const uint32_t *w = reinterpret_cast<const uint32_t *>(prow + (off & ~3));
+    const uint32_t sh = (uint32_t)(off & 3) * 8u;    // 0 or 16
+    const uint32_t w0 = __funnelshift_r(w[0], w[1], sh);
+    const uint32_t w1 = __funnelshift_r(w[1], w[2], sh);
+    const __half d = __ushort_as_half(*reinterpret_cast<const uint16_t *>(prow + kQ8Bytes * b));
+    const __half2 d2 = __halves2half2(d, d);
+    const __half2 bias = __floats2half2_rn(1152.0f, 1152.0f);
+    const uint32_t u0 = w0 ^ 0x80808080u, u1 = w1 ^ 0x80808080u;
+    uint32_t r[4] = {prmt(u0, 0x64646464u, 0x4140u), prmt(u0, 0x64646464u, 0x4342u),
+                     prmt(u1, 0x64646464u, 0x4140u), prmt(u1, 0x64646464u, 0x4342u)};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        __half2 h = *reinterpret_cast<__half2 *>(&r[e]);
+        h = __hmul2(__hsub2(h, bias), d2);  // q exact, then one rounding of d * q
+        r[e] = *reinterpret_cast<uint32_t *>(&h);
+    }
+    return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
+// Q4_K: 8 weights (k = 8c .. 8c+7 of k-step j = sub-blocks 2j, 2j+1).
+// coef[(r * 8 + sj) * 2 + {0,1}] = (S_j, Mn_j) of the row's superblock.
+__device__ __forceinline__ uint4 deq8_q4_k(const uint8_t *prow, const float *coefr, int j, int c) {
+    const int sj = 2 * j + (c >> 2);
+    const uint2 q = *reinterpret_cast<const uint2 *>(prow + 16 + 32 * j + 8 * (c & 3));
+    const int sh = (c >> 2) * 4;
+    const uint32_t n0 = (q.x >> sh) & 0x0F0F0F0Fu, n1 = (q.y >> sh) & 0x0F0F0F0Fu;
+    const float2 sm = *reinterpret_cast<const float2 *>(coefr + 2 * sj);
+    uint32_t r[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const uint32_t nw = e < 2 ? n0 : n1;
+        const int b0 = (2 * e) & 3;
+        const float q0 = __uint_as_float(prmt(nw, 0x4B000000u, 0x7440u + b0)) - 8388608.0f;
+        const float q1 = __uint_as_float(prmt(nw, 0x4B000000u, 0x7440u + b0 + 1)) - 8388608.0f;
+        const __half2 h = __floats2half2_rn(fmaf(sm.x, q0, -sm.y), fmaf(sm.x, q1, -sm.y));
+        r[e] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+    return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
+// ------------------------------------------------------------------ kernel
+struct GemmParams {
+    float *Y;
+    int M, N, K;
+};
+
+template <int kFmt>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
+            const GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    constexpr int kSA = gemm_stages_a(kFmt);
+    constexpr int kCB = gemm_group_bytes(kFmt);
+    constexpr uint32_t kBBytes = kGemmBN * kGemmBK * 2;
+    constexpr uint32_t kABytes = kGemmBM * kGemmBK * 2;
+    constexpr uint32_t kPBytes = kGemmBM * kCB;
+    const GemmLayout L = gemm_layout(kFmt);
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n0 = blockIdx.x * kGemmBM, m0 = blockIdx.y * kGemmBN;
+    const int ksteps = p.K / kGemmBK;
+    const int groups = p.K / kGroup;
+
+    const uint32_t bar = smem_addr(smem + L.bars);
+    // barrier slots
+    auto b_full = [&](int s) { return bar + 8u * s; };
+    auto b_empty = [&](int s) { return bar + 8u * (4 + s); };
+    auto a_full = [&](int s) { return bar + 8u * (8 + s); };
+    auto a_empty = [&](int s) { return bar + 8u * (12 + s); };
+    auto p_full = [&](int s) { return bar + 8u * (16 + s); };
+    auto p_empty = [&](int s) { return bar + 8u * (18 + s); };
+    const uint32_t acc_full = bar + 8u * 20;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.bars + 8 * 24);
+
+    if (tid == 0) {
+        for (int s = 0; s < kGemmStagesB; ++s) {
+            mbar_init(b_full(s), 1);
+            mbar_init(b_empty(s), 1);
+        }
+        for (int s = 0; s < kSA; ++s) {
+            mbar_init(a_full(s), kGemmDeqWarps);
+            mbar_init(a_empty(s), 1);
+        }
+        for (int s = 0; s < kGemmStagesP; ++s) {
+            mbar_init(p_full(s), 1);
+            mbar_init(p_empty(s), kGemmDeqWarps);
+        }
+        mbar_init(acc_full, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), kGemmTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wmap)) : "memory");
+            bool ok = true;
+            for (int g = 0; g < groups && ok; ++g) {
+                const int sp = g % kGemmStagesP;
+                if (g >= kGemmStagesP)
+                    ok = mbar_wait(p_empty(sp), ((g / kGemmStagesP) - 1) & 1, kErrGemmWait);
+                if (!ok) break;
+                mbar_arrive_expect_tx(p_full(sp), kPBytes);
+                tma_load_2d(smem_addr(smem + L.p + sp * kPBytes), &wmap, g * (kCB / 2), n0, p_full(sp));
+                for (int j = 0; j < 4 && ok; ++j) {
+                    const int ks = 4 * g + j;
+                    const int sb = ks % kGemmStagesB;
+                    if (ks >= kGemmStagesB)
+                        ok = mbar_wait(b_empty(sb), ((ks / kGemmStagesB) - 1) & 1, kErrGemmWait);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(b_full(sb), kBBytes);
+                    tma_load_2d(smem_addr(smem + L.b + sb * kBBytes), &xmap, ks * kGemmBK, m0, b_full(sb));
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = umma_idesc_f16(kGemmBM, kGemmBN);
+            bool ok = true;
+            for (int ks = 0; ks < ksteps && ok; ++ks) {
+                const int sa = ks % kSA, sb = ks % kGemmStagesB;
+                ok = mbar_wait(a_full(sa), (ks / kSA) & 1, kErrGemmWait) &&
+                     mbar_wait(b_full(sb), (ks / kGemmStagesB) & 1, kErrGemmWait);
+                if (!ok) break;
+                tc_fence_after();
+                const uint64_t ad = umma_desc_sw128(smem_addr(smem + L.a + sa * kABytes));
+                const uint64_t bd = umma_desc_sw128(smem_addr(smem + L.b + sb * kBBytes));
+#pragma unroll
+                for (int kk = 0; kk < kGemmBK / 16; ++kk)  // +32 bytes of K per MMA
+                    umma_f16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (ks | kk) != 0);
+                umma_commit(a_empty(sa));
+                umma_commit(b_empty(sb));
+            }
+            umma_commit(acc_full);  // also after an error: releases the epilogue
+        }
+    } else {
+        // ------------------------------------------------ dequantize, then epilogue
+        const int dw = warp - 2;              // 0..7
+        const int c = lane & 7;               // 16-byte chunk (8 k) of the 64-k step
+        const int rsub = lane >> 3;           // 0..3
+        float *coef = reinterpret_cast<float *>(smem + L.coef);
+        bool ok = true;
+        for (int g = 0; g < groups; ++g) {
+            const int sp = g % kGemmStagesP;
+            if (ok) ok = mbar_wait_warp(p_full(sp), (g / kGemmStagesP) & 1, kErrGemmWait);
+            const uint8_t *pst = smem + L.p + sp * kPBytes;
+            if constexpr (kFmt == 4) {
+                // (S_j, Mn_j) of the 8 sub-blocks of each row's superblock
+                if (ok && tid >= 64 && tid < 64 + kGemmBM) {
+                    const int r = tid - 64;
+                    const uint4 h = *reinterpret_cast<const uint4 *>(pst + r * kCB);
+                    const float dsc = __half2float(__ushort_as_half((unsigned short)(h.x & 0xFFFF)));
+                    const float dmn = __half2float(__ushort_as_half((unsigned short)(h.x >> 16)));
+                    const uint32_t sw[3] = {h.y, h.z, h.w};
+#pragma unroll
+                    for (int sj = 0; sj < 8; ++sj) {
+                        auto sb = [&](int k) { return (sw[k >> 2] >> (8 * (k & 3))) & 0xFFu; };
+                        uint32_t sc, mc;
+                        if (sj < 4) {
+                            sc = sb(sj) & 63u;
+                            mc = sb(sj + 4) & 63u;
+                        } else {
+                            sc = (sb(sj + 4) & 15u) | ((sb(sj - 4) >> 6) << 4);
+                            mc = (sb(sj + 4) >> 4) | ((sb(sj) >> 6) << 4);
+                        }
+                        coef[(r * 8 + sj) * 2] = dsc * (float)sc;
+                        coef[(r * 8 + sj) * 2 + 1] = dmn * (float)mc;
+                    }
+                }
+                named_bar_sync(1, kGemmDeqWarps * 32);
+            }
+            for (int j = 0; j < 4; ++j) {
+                const int ks = 4 * g + j;
+                const int sa = ks % kSA;
+                if (ok && ks >= kSA) ok = mbar_wait_warp(a_empty(sa), ((ks / kSA) - 1) & 1, kErrGemmWait);
+                uint8_t *ast = smem + L.a + sa * kABytes;
+                if (ok) {
+#pragma unroll
+                    for (int pass = 0; pass < kGemmBM / (4 * kGemmDeqWarps); ++pass) {
+                        const int r = pass * 4 * kGemmDeqWarps + 4 * dw + rsub;
+                        uint4 v;
+                        if constexpr (kFmt == 8)
+                            v = deq8_q8_0(pst + r * kCB, j, c);
+                        else
+                            v = deq8_q4_k(pst + r * kCB, coef + r * 16, j, c);
+                        *reinterpret_cast<uint4 *>(ast + sw128_chunk_off(r, c)) = v;
+                    }
+                }
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(a_full(sa));
+            }
+            if constexpr (kFmt == 4) named_bar_sync(1, kGemmDeqWarps * 32);  // coef reused next group
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_empty(sp));
+        }
+
+        // -------------------------------------------- epilogue: TMEM -> Y
+        mbar_wait_warp(acc_full, 0, kErrGemmWait);
+        tc_fence_after();
+        const int quarter = warp & 3;              // TMEM lanes 32*quarter .. +31
+        const int half = (warp - 2) >> 2;          // which 128 of the 256 columns
+        const int n = n0 + 32 * quarter + lane;
+#pragma unroll 1
+        for (int cb = 0; cb < kGemmBN / 2; cb += 32) {
+            const int col = half * (kGemmBN / 2) + cb;
+            uint32_t v[32];
+            tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)col, v);
+            if (n < p.N) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int m = m0 + col + i;
+                    if (m < p.M) p.Y[(int64_t)m * p.N + n] = __uint_as_float(v[i]);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, kGemmTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------- launcher
 size_t gemm_workspace_bytes(int fmt, int M, int N, int K) {
-    (void)fmt; (void)M; (void)N; (void)K;
-    return 0;
+    (void)fmt;
+    (void)N;
+    return (size_t)M * (size_t)K * 2;  // binary16 copy of X
+}
+
+template <int kFmt>
+static cudaError_t launch_gemm_t(const void *W, const uint16_t *X, float *Y, int M, int N, int K,
+                                 void *workspace, int sms, cudaStream_t stream) {
+    (void)sms;
+    __half *Xh = static_cast<__half *>(workspace);
+    const int64_t n8 = (int64_t)M * K / 8;
+    int cgrid = (int)((n8 + 255) / 256);
+    if (cgrid > 148 * 16) cgrid = 148 * 16;
+    x_to_f16_kernel<<<cgrid, 256, 0, stream>>>(X, Xh, n8);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    CUtensorMap xmap, wmap;
+    e = encode_tmap_2d(&xmap, Xh, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (uint64_t)K, (uint64_t)M,
+                       (uint64_t)K * 2, kGemmBK, kGemmBN, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (e != cudaSuccess) return e;
+    constexpr int kCB = gemm_group_bytes(kFmt);
+    const int64_t row_bytes = (int64_t)(K / kGroup) * kCB;
+    e = encode_tmap_2d(&wmap, W, CU_TENSOR_MAP_DATA_TYPE_UINT16, (uint64_t)(row_bytes / 2),
+                       (uint64_t)N, (uint64_t)row_bytes, kCB / 2, kGemmBM);
+    if (e != cudaSuccess) return e;
+
+    const GemmLayout L = gemm_layout(kFmt);
+    static bool attr_set = false;
+    if (!attr_set) {
+        e = cudaFuncSetAttribute(gemm_kernel<kFmt>, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    GemmParams p;
+    p.Y = Y;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    dim3 grid((unsigned)((N + kGemmBM - 1) / kGemmBM), (unsigned)((M + kGemmBN - 1) / kGemmBN), 1);
+    gemm_kernel<kFmt><<<grid, kGemmThreads, L.total, stream>>>(xmap, wmap, p);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_gemm(int fmt, const void *W, const uint16_t *X, float *Y, int M, int N, int K,
                         void *workspace, size_t workspace_bytes, int sms, cudaStream_t stream) {
-    (void)fmt; (void)W; (void)X; (void)Y; (void)M; (void)N; (void)K; (void)workspace;
-    (void)workspace_bytes; (void)sms; (void)stream;
-    return cudaErrorNotSupported;
+    if (workspace_bytes < gemm_workspace_bytes(fmt, M, N, K)) return cudaErrorInvalidValue;
+    if (fmt == 8) return launch_gemm_t<8>(W, X, Y, M, N, K, workspace, sms, stream);
+    return launch_gemm_t<4>(W, X, Y, M, N, K, workspace, sms, stream);
 }
 
 }  // namespace qmm

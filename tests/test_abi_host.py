@@ -105,6 +105,12 @@ def test_workspace_query(lib):
         for M in (1, 4, 16):  # decode shapes reduce in distributed shared memory
             assert q.qmm_matmul_workspace_bytes(fmt, M, 4096, 4096) == 0
         assert q.qmm_matmul_workspace_bytes(fmt, 512, 4096, 100) == 0  # invalid K
+        # prefill: a binary16 copy of the activations
+        assert q.qmm_matmul_workspace_bytes(fmt, 512, 4096, 4096) == 512 * 4096 * 2
+    L = lib
+    assert L.qmm_matmul(8, FAKE, FAKE, FAKE, 32, 64, 256, NULL, 0, S0) == q.QMM_ERR_WORKSPACE
+    assert L.qmm_matmul(4, FAKE, FAKE, FAKE, 32, 64, 256, FAKE, 100, S0) == q.QMM_ERR_WORKSPACE
+    assert L.qmm_matmul(4, FAKE, FAKE, FAKE, 32, 64, 256, MISALIGNED, 1 << 20, S0) == q.QMM_ERR_ALIGNMENT
 
 
 def test_missing_library_fails_loudly(tmp_path):

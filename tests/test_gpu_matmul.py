@@ -117,3 +117,45 @@ def test_activation_range(fmt):
     xb = inputs.bf16_bits(x.to(torch.bfloat16))
     Y, A = oracle.matmul(fmt, packed, xb, n, k)
     check_matmul(run(fmt, packed, xb, n), Y, A, "range")
+
+
+# ---------------------------------------------------------------- prefill GEMM
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("n,k", [(128, 256), (200, 512), (384, 1024), (130, 2304)])
+@pytest.mark.parametrize("m", [17, 64, 255, 256, 300])
+def test_prefill_small_full(fmt, n, k, m):
+    packed, xb = problem(fmt, n, k, m, 3000 + n + k + m)
+    Y, A = oracle.matmul(fmt, packed, xb, n, k)
+    check_matmul(run(fmt, packed, xb, n), Y, A, "fmt=%d n=%d k=%d m=%d" % (fmt, n, k, m))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("shape", inputs.PREFILL_SHAPES)
+@pytest.mark.parametrize("m", inputs.PREFILL_MS)
+def test_prefill_full_shapes_sampled(fmt, shape, m):
+    n, k = shape
+    si, mi = inputs.PREFILL_SHAPES.index(shape), inputs.PREFILL_MS.index(m)
+    w = inputs.weights(n, k, inputs.seed_for(4, si))
+    packed = oracle.quantize(fmt, inputs.bf16_bits(w))
+    xb = inputs.bf16_bits(inputs.activations(m, k, inputs.seed_for(4, si, mi)))
+    y = run(fmt, packed, xb, n).cpu()
+    ns = sample_rows(n, 40, 100 + si * 10 + mi)
+    Y, A = oracle.matmul_columns(fmt, packed, xb, k, ns)
+    check_matmul(y[:, torch.from_numpy(ns)], Y, A, "fmt=%d %s m=%d" % (fmt, shape, m))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_prefill_one_hot_and_determinism(fmt):
+    n, k = 256, 1024
+    packed, _ = problem(fmt, n, k, 1, 8)
+    cols = list(range(0, 1024, 17))[:40]
+    x = torch.zeros((len(cols), k), dtype=torch.bfloat16)
+    for i, c in enumerate(cols):
+        x[i, c] = 1.0
+    xb = inputs.bf16_bits(x)
+    Y, A = oracle.matmul(fmt, packed, xb, n, k)
+    y1 = run(fmt, packed, xb, n)
+    y2 = run(fmt, packed, xb, n)
+    check_matmul(y1, Y, A, "one-hot prefill")
+    assert torch.equal(y1, y2)
+    assert q.qmm_device_error_take() == 0
