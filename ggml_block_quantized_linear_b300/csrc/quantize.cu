@@ -9,17 +9,21 @@
 // Both formats are processed in groups of 256 consecutive weights of the
 // flattened row-major matrix (cols is a multiple of 256, so a group never
 // straddles two rows): 8 Q8_0 blocks -> 272 bytes, or one Q4_K superblock
-// -> 144 bytes.  One warp handles one group per iteration: every lane loads
-// 8 consecutive weights with 16-byte loads, block statistics are reduced
-// with warp shuffles, the packed group is assembled in shared memory and
-// written back with coalesced 16-byte stores.  The kernels are HBM-bound:
+// -> 144 bytes.  ISQ gives each lane one 32-weight (sub-)block, loaded with
+// 16-byte loads; Q4_K superblock statistics are reduced over 8 lanes with
+// shuffles; the packed output is assembled in shared memory and written
+// back with coalesced 16-byte stores.  Dequantization runs one warp per
+// 256-weight group.  The kernels are HBM-bound:
 // per weight they move 2 bytes in and 1.0625 (Q8_0) or 0.5625 (Q4_K) out.
 //
 // Bit-exactness: every floating-point step is an explicit IEEE single
 // operation (__fdiv_rn, __fadd_rn, __fsub_rn, __fmul_rn: no contraction),
 // codes use round-half-away (roundf), scales use binary16 round-to-nearest-
-// even (__float2half_rn).  Signed zeros cannot change a byte: the maxima
-// that feed a scale are forced to +0 when they are zero.
+// even (__float2half_rn).  The per-weight division of a code uses the
+// reciprocal of the block scale and falls back to the IEEE division only
+// next to a rounding tie (round_quotient), which gives the same codes.
+// Signed zeros cannot change a byte: the maxima that feed a scale are
+// forced to +0 when they are zero.
 #include "common.cuh"
 
 namespace qmm {
@@ -49,45 +53,83 @@ __device__ __forceinline__ float clamp_f(float v, float lo, float hi) {
     return v < lo ? lo : (v > hi ? hi : v);
 }
 
+// roundf(x / D) for D > 0, bit-identical to roundf(__fdiv_rn(x, D)), from
+// the correctly rounded reciprocal r = 1/D.  t = x * r (rounded) is within
+// 1.5 * 2^-23 * |x/D| of the correctly rounded quotient; roundf only jumps at
+// half-integers, so the nearest integer k of t is the answer unless t lies
+// within 2^-14 of a half-integer (|t| * 2^-21 < 2^-14 while |t| <= 128),
+// where the exact division decides.  Callers clamp the result to a range
+// inside [-128, 128]: beyond it, both ways clamp to the same code.
+__device__ __forceinline__ float round_quotient(float x, float D, float r) {
+    const float t = __fmul_rn(x, r);
+    const float k = rintf(t);
+    if (fabsf(__fsub_rn(t, k)) >= 0.49993896484375f)  // 0.5 - 2^-14
+        return roundf(__fdiv_rn(x, D));
+    return k;
+}
+
+// Byte of an integral float in [-128, 127] (two's complement): adding
+// 1.5 * 2^23 moves the integer into the low mantissa bits.
+__device__ __forceinline__ uint32_t int_byte(float v) {
+    return __float_as_uint(__fadd_rn(v, 12582912.0f)) & 0xFFu;
+}
+
+template <bool kSrcF32>
+__device__ __forceinline__ void load32(const void *src, int64_t elem, float (&x)[32]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float v[8];
+        load8<kSrcF32>(src, elem + 8 * i, v);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[8 * i + e] = v[e];
+    }
+}
+
 // ------------------------------------------------------------------ Q8_0
+// One lane quantizes one 32-weight block; a warp covers 32 consecutive
+// blocks (1024 weights, 1088 packed bytes) per iteration, assembled in
+// shared memory and stored with coalesced 16-byte writes.
 template <bool kSrcF32>
 __global__ void __launch_bounds__(kQuantThreads)
-quantize_q8_0_kernel(const void *__restrict__ src, uint8_t *__restrict__ dst, int64_t ngroups) {
-    __shared__ __align__(16) uint8_t stage[kQuantWarps][kQ8GroupBytes];
+quantize_q8_0_kernel(const void *__restrict__ src, uint8_t *__restrict__ dst, int64_t nblocks) {
+    __shared__ __align__(16) uint8_t stage[kQuantWarps][32 * kQ8Bytes];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int blk = lane >> 2, part = lane & 3;
     uint8_t *st = stage[warp];
     const int64_t nwarps = (int64_t)gridDim.x * kQuantWarps;
-    for (int64_t g = (int64_t)blockIdx.x * kQuantWarps + warp; g < ngroups; g += nwarps) {
-        float x[8];
-        load8<kSrcF32>(src, g * kGroup + lane * 8, x);
-        float amax = 0.0f;
+    for (int64_t b0 = ((int64_t)blockIdx.x * kQuantWarps + warp) * 32; b0 < nblocks; b0 += nwarps * 32) {
+        const int64_t blk = b0 + lane;
+        const int nvalid = (int)min((int64_t)32, nblocks - b0);  // a multiple of 8
+        if (blk < nblocks) {
+            float x[32];
+            load32<kSrcF32>(src, blk * kQ8Weights, x);
+            float amax = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        const float d = __fdiv_rn(amax, 127.0f);
-        const __half dh = __float2half_rn(d);
-        const float df = __half2float(dh);
-        uint32_t packed[2] = {0u, 0u};
-        if (df != 0.0f) {
+            for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
+            const __half dh = __float2half_rn(__fdiv_rn(amax, 127.0f));
+            const float df = __half2float(dh);
+            uint32_t w[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) w[i] = 0u;
+            if (df != 0.0f) {
+                const float r = __frcp_rn(df);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float q = clamp_f(round_quotient(x[i], df, r), -127.0f, 127.0f);
+                    w[i >> 2] |= int_byte(q) << (8 * (i & 3));
+                }
+            }
+            uint16_t *o = reinterpret_cast<uint16_t *>(st + kQ8Bytes * lane);
+            o[0] = __half_as_ushort(dh);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const float q = clamp_f(roundf(__fdiv_rn(x[i], df)), -127.0f, 127.0f);
-                packed[i >> 2] |= (uint32_t)((uint8_t)(int8_t)(int)q) << (8 * (i & 3));
+                o[1 + 2 * i] = (uint16_t)w[i];
+                o[2 + 2 * i] = (uint16_t)(w[i] >> 16);
             }
         }
-        // 8 codes at byte 34*blk + 2 + 8*part (2-byte aligned)
-        uint16_t *q16 = reinterpret_cast<uint16_t *>(st + kQ8Bytes * blk + 2 + 8 * part);
-        q16[0] = (uint16_t)packed[0];
-        q16[1] = (uint16_t)(packed[0] >> 16);
-        q16[2] = (uint16_t)packed[1];
-        q16[3] = (uint16_t)(packed[1] >> 16);
-        if (part == 0) *reinterpret_cast<uint16_t *>(st + kQ8Bytes * blk) = __half_as_ushort(dh);
         __syncwarp();
-        if (lane < kQ8GroupBytes / 16)
-            reinterpret_cast<uint4 *>(dst + g * kQ8GroupBytes)[lane] =
-                reinterpret_cast<const uint4 *>(st)[lane];
+        const int nvec = nvalid * kQ8Bytes / 16;
+        uint4 *out = reinterpret_cast<uint4 *>(dst + b0 * kQ8Bytes);
+        for (int v = lane; v < nvec; v += 32) out[v] = reinterpret_cast<const uint4 *>(st)[v];
         __syncwarp();
     }
 }
@@ -122,33 +164,39 @@ dequantize_q8_0_kernel(const uint8_t *__restrict__ src, float *__restrict__ dst,
 }
 
 // ------------------------------------------------------------------ Q4_K
+// ------------------------------------------------------------------ Q4_K
+// One lane quantizes one 32-weight sub-block; 8 lanes make a superblock and
+// a warp covers 4 superblocks (1024 weights, 576 packed bytes) per
+// iteration.
 template <bool kSrcF32>
 __global__ void __launch_bounds__(kQuantThreads)
-quantize_q4_k_kernel(const void *__restrict__ src, uint8_t *__restrict__ dst, int64_t ngroups) {
-    __shared__ __align__(16) uint8_t stage[kQuantWarps][kQ4Bytes];
+quantize_q4_k_kernel(const void *__restrict__ src, uint8_t *__restrict__ dst, int64_t nsuper) {
+    __shared__ __align__(16) uint8_t stage[kQuantWarps][4 * kQ4Bytes];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int sub = lane >> 2, part = lane & 3;  // sub-block j, 8-weight slice
-    uint8_t *st = stage[warp];
+    const int sj = lane & 7, sbl = lane >> 3;  // sub-block j, superblock in the warp tile
+    uint8_t *st = stage[warp] + sbl * kQ4Bytes;
     const int64_t nwarps = (int64_t)gridDim.x * kQuantWarps;
-    for (int64_t g = (int64_t)blockIdx.x * kQuantWarps + warp; g < ngroups; g += nwarps) {
-        float x[8];
-        load8<kSrcF32>(src, g * kGroup + lane * 8, x);
+    for (int64_t s0 = ((int64_t)blockIdx.x * kQuantWarps + warp) * 4; s0 < nsuper; s0 += nwarps * 4) {
+        const int64_t sb = s0 + sbl;
+        const bool valid = sb < nsuper;  // uniform over each group of 8 lanes
+        const int nvalid = (int)min((int64_t)4, nsuper - s0);
+        float x[32];
+        if (valid) load32<kSrcF32>(src, sb * kQ4Weights + sj * 32, x);
+        else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) x[i] = 0.0f;
+        }
         float mx = x[0], mn = 0.0f;  // max_i x_i and min(0, min_i x_i)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < 32; ++i) {
             mx = fmaxf(mx, x[i]);
             mn = fminf(mn, x[i]);
-        }
-#pragma unroll
-        for (int o = 1; o <= 2; o <<= 1) {
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
         }
         const float s = __fdiv_rn(__fsub_rn(mx, mn), 15.0f);
         const float m = __fsub_rn(0.0f, mn);
         float smax = s, mmax = m;
 #pragma unroll
-        for (int o = 4; o <= 16; o <<= 1) {
+        for (int o = 1; o <= 4; o <<= 1) {
             smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o));
             mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, o));
         }
@@ -161,47 +209,45 @@ quantize_q4_k_kernel(const void *__restrict__ src, uint8_t *__restrict__ dst, in
         const int mc = dminf > 0.0f ? (int)clamp_f(roundf(__fdiv_rn(m, dminf)), 0.0f, 63.0f) : 0;
         const float S = __fmul_rn(df, (float)sc);
         const float Mn = __fmul_rn(dminf, (float)mc);
-        uint32_t w[2] = {0u, 0u};
-        if (S > 0.0f) {
+        uint32_t w[8];  // 4-bit codes, one per byte
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float q = clamp_f(roundf(__fdiv_rn(__fadd_rn(x[i], Mn), S)), 0.0f, 15.0f);
-                w[i >> 2] |= (uint32_t)(int)q << (8 * (i & 3));
+        for (int i = 0; i < 8; ++i) w[i] = 0u;
+        if (S > 0.0f) {
+            const float r = __frcp_rn(S);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float q = clamp_f(round_quotient(__fadd_rn(x[i], Mn), S, r), 0.0f, 15.0f);
+                w[i >> 2] |= int_byte(q) << (8 * (i & 3));
             }
         }
         // sub-block 2c (low nibbles) and 2c+1 (high nibbles) share chunk c
-        const uint32_t h0 = __shfl_xor_sync(0xffffffffu, w[0], 4);
-        const uint32_t h1 = __shfl_xor_sync(0xffffffffu, w[1], 4);
-        if ((sub & 1) == 0) {
-            uint2 v = make_uint2(w[0] | (h0 << 4), w[1] | (h1 << 4));
-            *reinterpret_cast<uint2 *>(st + 16 + 32 * (sub >> 1) + 8 * part) = v;
-        }
-        // gather the eight (sc, mc) pairs into lane 0 and pack the header
-        uint32_t code = (uint32_t)sc | ((uint32_t)mc << 8);
-        uint32_t codes[8];
+        uint32_t hw[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) codes[j] = __shfl_sync(0xffffffffu, code, 4 * j);
-        if (lane == 0) {
-            uint8_t sb[12];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t scj = codes[j] & 0xFF, mcj = codes[j] >> 8;
-                const uint32_t sch = codes[j + 4] & 0xFF, mch = codes[j + 4] >> 8;
-                sb[j] = (uint8_t)(scj | ((sch >> 4) << 6));
-                sb[j + 4] = (uint8_t)(mcj | ((mch >> 4) << 6));
-                sb[j + 8] = (uint8_t)((sch & 15) | ((mch & 15) << 4));
+        for (int i = 0; i < 8; ++i) hw[i] = __shfl_xor_sync(0xffffffffu, w[i], 1);
+        // scale bytes: j < 4 writes s[j], s[j+4], s[j+8] with the codes of j+4
+        const int sc4 = __shfl_down_sync(0xffffffffu, sc, 4);
+        const int mc4 = __shfl_down_sync(0xffffffffu, mc, 4);
+        if (valid) {
+            if ((sj & 1) == 0) {
+                uint4 *o = reinterpret_cast<uint4 *>(st + 16 + 32 * (sj >> 1));
+                o[0] = make_uint4(w[0] | (hw[0] << 4), w[1] | (hw[1] << 4), w[2] | (hw[2] << 4),
+                                  w[3] | (hw[3] << 4));
+                o[1] = make_uint4(w[4] | (hw[4] << 4), w[5] | (hw[5] << 4), w[6] | (hw[6] << 4),
+                                  w[7] | (hw[7] << 4));
             }
-            uint4 hdr;
-            hdr.x = (uint32_t)__half_as_ushort(dh) | ((uint32_t)__half_as_ushort(dminh) << 16);
-            hdr.y = sb[0] | (sb[1] << 8) | (sb[2] << 16) | ((uint32_t)sb[3] << 24);
-            hdr.z = sb[4] | (sb[5] << 8) | (sb[6] << 16) | ((uint32_t)sb[7] << 24);
-            hdr.w = sb[8] | (sb[9] << 8) | (sb[10] << 16) | ((uint32_t)sb[11] << 24);
-            *reinterpret_cast<uint4 *>(st) = hdr;
+            if (sj < 4) {
+                st[4 + sj] = (uint8_t)(sc | ((sc4 >> 4) << 6));
+                st[8 + sj] = (uint8_t)(mc | ((mc4 >> 4) << 6));
+                st[12 + sj] = (uint8_t)((sc4 & 15) | ((mc4 & 15) << 4));
+            }
+            if (sj == 0)
+                *reinterpret_cast<uint32_t *>(st) =
+                    (uint32_t)__half_as_ushort(dh) | ((uint32_t)__half_as_ushort(dminh) << 16);
         }
         __syncwarp();
-        if (lane < kQ4Bytes / 16)
-            reinterpret_cast<uint4 *>(dst + g * kQ4Bytes)[lane] =
-                reinterpret_cast<const uint4 *>(st)[lane];
+        const int nvec = nvalid * kQ4Bytes / 16;
+        uint4 *out = reinterpret_cast<uint4 *>(dst + s0 * kQ4Bytes);
+        for (int v = lane; v < nvec; v += 32) out[v] = reinterpret_cast<const uint4 *>(stage[warp])[v];
         __syncwarp();
     }
 }
@@ -253,28 +299,30 @@ dequantize_q4_k_kernel(const uint8_t *__restrict__ src, float *__restrict__ dst,
 }
 
 // ------------------------------------------------------------- launchers
-static int grid_for(int64_t ngroups, int sms) {
-    int64_t want = (ngroups + kQuantWarps - 1) / kQuantWarps;
+static int grid_for(int64_t items, int per_cta, int sms) {
+    int64_t want = (items + per_cta - 1) / per_cta;
     int64_t cap = (int64_t)sms * 8;  // 8 resident CTAs of 256 threads per SM
     return (int)(want < cap ? (want > 0 ? want : 1) : cap);
 }
 
 cudaError_t launch_quantize(int fmt, int src_f32, const void *src, void *dst, int64_t nweights,
                             int sms, cudaStream_t stream) {
-    const int64_t ngroups = nweights / kGroup;
-    if (ngroups == 0) return cudaSuccess;
-    const int grid = grid_for(ngroups, sms);
+    if (nweights == 0) return cudaSuccess;
     uint8_t *d = static_cast<uint8_t *>(dst);
     if (fmt == 8) {
+        const int64_t nblocks = nweights / kQ8Weights;
+        const int grid = grid_for(nblocks, 32 * kQuantWarps, sms);
         if (src_f32)
-            quantize_q8_0_kernel<true><<<grid, kQuantThreads, 0, stream>>>(src, d, ngroups);
+            quantize_q8_0_kernel<true><<<grid, kQuantThreads, 0, stream>>>(src, d, nblocks);
         else
-            quantize_q8_0_kernel<false><<<grid, kQuantThreads, 0, stream>>>(src, d, ngroups);
+            quantize_q8_0_kernel<false><<<grid, kQuantThreads, 0, stream>>>(src, d, nblocks);
     } else {
+        const int64_t nsuper = nweights / kQ4Weights;
+        const int grid = grid_for(nsuper, 4 * kQuantWarps, sms);
         if (src_f32)
-            quantize_q4_k_kernel<true><<<grid, kQuantThreads, 0, stream>>>(src, d, ngroups);
+            quantize_q4_k_kernel<true><<<grid, kQuantThreads, 0, stream>>>(src, d, nsuper);
         else
-            quantize_q4_k_kernel<false><<<grid, kQuantThreads, 0, stream>>>(src, d, ngroups);
+            quantize_q4_k_kernel<false><<<grid, kQuantThreads, 0, stream>>>(src, d, nsuper);
     }
     return cudaGetLastError();
 }
@@ -283,7 +331,7 @@ cudaError_t launch_dequantize(int fmt, const void *src, float *dst, int64_t nwei
                               cudaStream_t stream) {
     const int64_t ngroups = nweights / kGroup;
     if (ngroups == 0) return cudaSuccess;
-    const int grid = grid_for(ngroups, sms);
+    const int grid = grid_for(ngroups, kQuantWarps, sms);
     const uint8_t *s = static_cast<const uint8_t *>(src);
     if (fmt == 8)
         dequantize_q8_0_kernel<<<grid, kQuantThreads, 0, stream>>>(s, dst, ngroups);

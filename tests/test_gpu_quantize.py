@@ -76,6 +76,19 @@ def edge_cases():
     ties[:, ::32] = 127 * 2.0 ** -7
     cases["ties"] = torch.from_numpy(ties)
     cases["large"] = torch.from_numpy(rng.normal(0, 1000, (4, 512)).astype(np.float32))
+    # one float32 ulp either side of the half-steps: the reciprocal shortcut
+    # of the quantizer must hand these to the exact division
+    near = ties.copy()
+    near[0] = np.nextafter(near[0], np.float32(np.inf))
+    near[1] = np.nextafter(near[1], np.float32(-np.inf))
+    near[2] = np.nextafter(np.nextafter(near[2], np.float32(np.inf)), np.float32(np.inf))
+    near[:, ::32] = 127 * 2.0 ** -7
+    cases["near_ties"] = torch.from_numpy(near.astype(np.float32))
+    q4 = np.zeros((4, 512), dtype=np.float32)  # Q4_K grid: min 0, 15 steps of 2^-6
+    q4[:, :] = ((np.arange(512) % 32) / 2.0) * 2.0 ** -6
+    q4[1] = np.nextafter(q4[1], np.float32(np.inf))
+    q4[2] = np.nextafter(q4[2], np.float32(-np.inf))
+    cases["q4_half_steps"] = torch.from_numpy(q4)
     return cases
 
 
