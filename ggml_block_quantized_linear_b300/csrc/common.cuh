@@ -122,6 +122,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// Prefetch a 2-D box of a tensor into L2 (no shared-memory destination).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 // Host: encode a 2-D tiled tensor map (row-major [dim1][dim0] of `dtype`,
 // row pitch `stride1_bytes`, box [box1][box0], no swizzle, zero fill out of
 // bounds).  The driver function is looked up once through the runtime.

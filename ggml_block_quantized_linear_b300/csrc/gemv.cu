@@ -15,17 +15,18 @@
 //    bytes) per row per stage, as ONE 2-D tensor-map TMA copy per stage
 //    (cp.async.bulk.tensor) into a ring of shared-memory stages guarded by
 //    mbarriers.  Rows past N are zero-filled by the TMA unit.
-//  * Four consumer warps (16 rows each) run warp-level tensor-core MMAs
-//    (m16n8k16, f16 inputs, fp32 accumulation) with the weight rows as the
-//    M side and the (padded) tokens as N.  The MMA operands are the integer
-//    codes, which binary16 holds exactly: an int8 code becomes 1152 + q and
-//    a 4-bit code 1024 + q (or 1024 + 16 q for a high nibble) through one
-//    PRMT / LOP3 that places the byte in the mantissa of a binary16 1024.
-//    The offsets and the per-block scales are applied in fp32 after each
-//    32-weight block:  sum_k w x = a * R - b * sum_k x,  with R the MMA
-//    result of the block, a the block scale (d, or S_j, S_j / 16) and
-//    b the offset term (1152 d, or 1024 S_j + Mn_j, 64 S_j + Mn_j).
-//    sum_k x per block and token comes from the staged activations.
+//  * Eight consumer warps run warp-level tensor-core MMAs: warp w takes the
+//    16 rows 16 * (w % 4) .. + 15 and one half of every 256-weight chunk
+//    (blocks 0-3 or 4-7; Q4_K sub-blocks 0-3 or 4-7), so that twice as many
+//    warps hide latency; the two halves are added in shared memory.  The
+//    MMAs are m16n8k16 (f16 inputs, fp32 accumulation) with the weight rows
+//    as the M side and the (padded) tokens as N.  The MMA operands are the
+//    integer codes, which binary16 holds exactly: one PRMT / LOP3 places a
+//    code under a binary16 exponent (1152 + q, 1024 + q or 1024 + 16 q for a
+//    high nibble) and one HSUB2 / HFMA2 removes the offset exactly.  The
+//    scales are applied in fp32 after each 32-weight block, R being the MMA
+//    result of the block:  Q8_0  d * R;  Q4_K  S_j * R - Mn_j * sum_k x,
+//    with sum_k x per sub-block and token from the staged activations.
 //  * The activations of the CTA's K range are converted once to binary16
 //    (round to nearest) in shared memory, each group of 4 stored in the
 //    order (0, 2, 1, 3) so that one 16-byte load yields both B fragments.
@@ -33,8 +34,10 @@
 
 namespace qmm {
 
-constexpr int kGemvWarps = 4;                       // consumer warps
-constexpr int kGemvRows = 16 * kGemvWarps;          // weight rows per CTA
+constexpr int kGemvRowGroups = 4;                   // 16-row groups per CTA
+constexpr int kGemvKHalves = 2;                     // consumer warps per row group
+constexpr int kGemvWarps = kGemvRowGroups * kGemvKHalves;  // consumer warps
+constexpr int kGemvRows = 16 * kGemvRowGroups;      // weight rows per CTA
 constexpr int kGemvThreads = (kGemvWarps + 1) * 32; // + one producer warp
 constexpr int kGemvMaxStages = 4;
 
@@ -66,9 +69,9 @@ __host__ __device__ inline GemvLayout gemv_layout(int fmt, int nt, int M, int st
     L.xs = off;
     off += (kr_max / 32) * mt * 4;
     L.coef = off;
-    off += (fmt == 4 ? kGemvWarps * 16 * 16 * 4 : 0);
+    off += (fmt == 4 ? kGemvWarps * 16 * 8 * 4 : 0);
     L.ypart = off;
-    off += kGemvRows * mt * 4;
+    off += kGemvKHalves * kGemvRows * mt * 4;
     off = (off + 15) & ~15;
     L.bars = off;
     off += 2 * stages * 8;
@@ -103,6 +106,22 @@ __device__ __forceinline__ void load_q8_codes(const uint8_t *p, uint32_t &w0, ui
 // u under a binary16 exponent of 1024.  Lanes take positions (0,2) or (1,3).
 __device__ __forceinline__ uint32_t q8_pair02(uint32_t u) { return prmt(u, 0x64646464u, 0x4240u); }
 __device__ __forceinline__ uint32_t q8_pair13(uint32_t u) { return prmt(u, 0x64646464u, 0x4341u); }
+// (1152 + q) - 1152 = q, exact in binary16.  The MMA then multiplies the
+// exact codes: no large offset enters the fp32 sums (an offset left in would
+// cost ~2^-24 * 1152 * d * |sum x| of accuracy).
+__device__ __forceinline__ uint32_t hsub_bits(uint32_t v, uint32_t c) {
+    __half2 r = __hsub2(*reinterpret_cast<const __half2 *>(&v), *reinterpret_cast<const __half2 *>(&c));
+    return *reinterpret_cast<uint32_t *>(&r);
+}
+__device__ __forceinline__ uint32_t q8_exact(uint32_t v) { return hsub_bits(v, 0x64806480u); }
+// 4-bit codes: (1024 + q) - 1024 = q and (1024 + 16 q) / 16 - 64 = q, exact.
+__device__ __forceinline__ uint32_t q4_lo_exact(uint32_t v) { return hsub_bits(v, 0x64006400u); }
+__device__ __forceinline__ uint32_t q4_hi_exact(uint32_t v) {
+    const uint32_t s16 = 0x2C002C00u, m64 = 0xD400D400u;  // 1/16 and -64
+    __half2 r = __hfma2(*reinterpret_cast<const __half2 *>(&v), *reinterpret_cast<const __half2 *>(&s16),
+                        *reinterpret_cast<const __half2 *>(&m64));
+    return *reinterpret_cast<uint32_t *>(&r);
+}
 
 // 16-byte B-fragment load of token row (g + 8 nt); tokens >= M are zero.
 __device__ __forceinline__ uint4 x_frag(const __half *p, bool valid) {
@@ -122,40 +141,44 @@ __device__ __forceinline__ void q8_block(const uint8_t *r0, const uint8_t *r1, c
     load_q8_codes<kMod8>(r0 + kOff + 8 * t, a0, a1);
     load_q8_codes<kMod8>(r1 + kOff + 8 * t, b0, b1);
     a0 ^= 0x80808080u; a1 ^= 0x80808080u; b0 ^= 0x80808080u; b1 ^= 0x80808080u;
-    const uint32_t A0[4] = {q8_pair02(a0), q8_pair02(b0), q8_pair13(a0), q8_pair13(b0)};
-    const uint32_t A1[4] = {q8_pair02(a1), q8_pair02(b1), q8_pair13(a1), q8_pair13(b1)};
+    const uint32_t A0[4] = {q8_exact(q8_pair02(a0)), q8_exact(q8_pair02(b0)),
+                            q8_exact(q8_pair13(a0)), q8_exact(q8_pair13(b0))};
+    const uint32_t A1[4] = {q8_exact(q8_pair02(a1)), q8_exact(q8_pair02(b1)),
+                            q8_exact(q8_pair13(a1)), q8_exact(q8_pair13(b1))};
 #pragma unroll
     for (int nt = 0; nt < kNT; ++nt) {
         const uint4 xv = x_frag(xrow + nt * 8 * xstride + kQ8Weights * kB + 8 * t, nt * 8 < gvalid);
         float c[4] = {0.f, 0.f, 0.f, 0.f};
         mma_f16_16816(c, A0, xv.x, xv.y);
         mma_f16_16816(c, A1, xv.z, xv.w);
-        const float2 s = *reinterpret_cast<const float2 *>(xs + blk * (8 * kNT) + nt * 8 + 2 * t);
-        acc[nt][0] = fmaf(d0, fmaf(-1152.0f, s.x, c[0]), acc[nt][0]);
-        acc[nt][1] = fmaf(d0, fmaf(-1152.0f, s.y, c[1]), acc[nt][1]);
-        acc[nt][2] = fmaf(d1, fmaf(-1152.0f, s.x, c[2]), acc[nt][2]);
-        acc[nt][3] = fmaf(d1, fmaf(-1152.0f, s.y, c[3]), acc[nt][3]);
+        acc[nt][0] = fmaf(d0, c[0], acc[nt][0]);
+        acc[nt][1] = fmaf(d0, c[1], acc[nt][1]);
+        acc[nt][2] = fmaf(d1, c[2], acc[nt][2]);
+        acc[nt][3] = fmaf(d1, c[3], acc[nt][3]);
     }
 }
 
 template <int kNT>
-__device__ __forceinline__ void q4k_chunk(const uint8_t *base, const uint8_t *r0, const uint8_t *r1,
-                                          const __half *xr, int xstride, const float *xs, int li,
-                                          float *cw, int lane, int g, int t, int gvalid,
-                                          float (&acc)[kNT][4]) {
+__device__ __forceinline__ void q4k_half(const uint8_t *base, const uint8_t *r0, const uint8_t *r1,
+                                         const __half *xr, int xstride, const float *xs, int li,
+                                         float *cw, int lane, int g, int t, int gvalid, int kh,
+                                         float (&acc)[kNT][4]) {
     constexpr int kSlot = kQ4Bytes;
     constexpr int kMT = 8 * kNT;
-    // per-row coefficients (a_j, b_j) of the 8 sub-blocks; lane (row =
-    // lane / 2) decodes sub-blocks 4 * (lane & 1) .. + 3 of its row
+    // per-row coefficients (a_j, b_j) of this half's 4 sub-blocks; lane
+    // (row = lane / 2) decodes sub-blocks 4 kh + 2 (lane & 1) + {0, 1}
     {
-        const int rr = lane >> 1, half = lane & 1;
+        const int rr = lane >> 1;
         const uint4 h = *reinterpret_cast<const uint4 *>(base + rr * kSlot);
         const float dsc = h2f_bits(h.x), dmn = h2f_bits(h.x >> 16);
-        const uint32_t sw[3] = {h.y, h.z, h.w};
-        auto sbyte = [&](int k) { return (sw[k >> 2] >> (8 * (k & 3))) & 0xFFu; };
+        auto sbyte = [&](int k) {  // scale byte k (selects, no local-memory array)
+            const uint32_t w = k < 4 ? h.y : (k < 8 ? h.z : h.w);
+            return (w >> (8 * (k & 3))) & 0xFFu;
+        };
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-            const int j = 4 * half + jj;
+        for (int jj = 0; jj < 2; ++jj) {
+            const int jl = 2 * (lane & 1) + jj;  // 0..3 inside the half
+            const int j = 4 * kh + jl;
             uint32_t sc, mc;
             if (j < 4) {
                 sc = sbyte(j) & 63u;
@@ -164,29 +187,26 @@ __device__ __forceinline__ void q4k_chunk(const uint8_t *base, const uint8_t *r0
                 sc = (sbyte(j + 4) & 15u) | ((sbyte(j - 4) >> 6) << 4);
                 mc = (sbyte(j + 4) >> 4) | ((sbyte(j) >> 6) << 4);
             }
-            const float S = dsc * (float)sc, Mn = dmn * (float)mc;
-            const bool hi = (j & 1) != 0;
-            cw[rr * 16 + 2 * j] = hi ? S * 0.0625f : S;
-            cw[rr * 16 + 2 * j + 1] = fmaf(hi ? 64.0f : 1024.0f, S, Mn);
+            cw[rr * 8 + 2 * jl] = dsc * (float)sc;       // S_j
+            cw[rr * 8 + 2 * jl + 1] = -(dmn * (float)mc);  // -Mn_j
         }
     }
     __syncwarp();
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * kh + cc;  // 64-weight chunk: sub-blocks 2c (low) and 2c+1 (high)
         const uint2 qa = *reinterpret_cast<const uint2 *>(r0 + 16 + 32 * c + 8 * t);
         const uint2 qb = *reinterpret_cast<const uint2 *>(r1 + 16 + 32 * c + 8 * t);
-        const float4 ca = *reinterpret_cast<const float4 *>(cw + g * 16 + 4 * c);
-        const float4 cb = *reinterpret_cast<const float4 *>(cw + (g + 8) * 16 + 4 * c);
+        const float4 ca = *reinterpret_cast<const float4 *>(cw + g * 8 + 4 * cc);
+        const float4 cb = *reinterpret_cast<const float4 *>(cw + (g + 8) * 8 + 4 * cc);
         const uint32_t M16 = 0x64006400u;
         const uint32_t qa0s = qa.x >> 8, qa1s = qa.y >> 8, qb0s = qb.x >> 8, qb1s = qb.y >> 8;
-        const uint32_t L0[4] = {and_or(qa.x, 0x000F000Fu, M16), and_or(qb.x, 0x000F000Fu, M16),
-                                and_or(qa0s, 0x000F000Fu, M16), and_or(qb0s, 0x000F000Fu, M16)};
-        const uint32_t L1[4] = {and_or(qa.y, 0x000F000Fu, M16), and_or(qb.y, 0x000F000Fu, M16),
-                                and_or(qa1s, 0x000F000Fu, M16), and_or(qb1s, 0x000F000Fu, M16)};
-        const uint32_t H0[4] = {and_or(qa.x, 0x00F000F0u, M16), and_or(qb.x, 0x00F000F0u, M16),
-                                and_or(qa0s, 0x00F000F0u, M16), and_or(qb0s, 0x00F000F0u, M16)};
-        const uint32_t H1[4] = {and_or(qa.y, 0x00F000F0u, M16), and_or(qb.y, 0x00F000F0u, M16),
-                                and_or(qa1s, 0x00F000F0u, M16), and_or(qb1s, 0x00F000F0u, M16)};
+        auto lo = [&](uint32_t w) { return q4_lo_exact(and_or(w, 0x000F000Fu, M16)); };
+        auto hi = [&](uint32_t w) { return q4_hi_exact(and_or(w, 0x00F000F0u, M16)); };
+        const uint32_t L0[4] = {lo(qa.x), lo(qb.x), lo(qa0s), lo(qb0s)};
+        const uint32_t L1[4] = {lo(qa.y), lo(qb.y), lo(qa1s), lo(qb1s)};
+        const uint32_t H0[4] = {hi(qa.x), hi(qb.x), hi(qa0s), hi(qb0s)};
+        const uint32_t H1[4] = {hi(qa.y), hi(qb.y), hi(qa1s), hi(qb1s)};
         const int blo = li * 8 + 2 * c;
 #pragma unroll
         for (int nt = 0; nt < kNT; ++nt) {
@@ -200,10 +220,11 @@ __device__ __forceinline__ void q4k_chunk(const uint8_t *base, const uint8_t *r0
             mma_f16_16816(chh, H1, xhv.z, xhv.w);
             const float2 sl = *reinterpret_cast<const float2 *>(xs + blo * kMT + nt * 8 + 2 * t);
             const float2 sh = *reinterpret_cast<const float2 *>(xs + (blo + 1) * kMT + nt * 8 + 2 * t);
-            acc[nt][0] += fmaf(ca.x, cl[0], -ca.y * sl.x) + fmaf(ca.z, chh[0], -ca.w * sh.x);
-            acc[nt][1] += fmaf(ca.x, cl[1], -ca.y * sl.y) + fmaf(ca.z, chh[1], -ca.w * sh.y);
-            acc[nt][2] += fmaf(cb.x, cl[2], -cb.y * sl.x) + fmaf(cb.z, chh[2], -cb.w * sh.x);
-            acc[nt][3] += fmaf(cb.x, cl[3], -cb.y * sl.y) + fmaf(cb.z, chh[3], -cb.w * sh.y);
+            // S_lo R_lo + S_hi R_hi - Mn_lo Xs_lo - Mn_hi Xs_hi (coefficients hold -Mn)
+            acc[nt][0] = fmaf(ca.w, sh.x, fmaf(ca.y, sl.x, fmaf(ca.z, chh[0], fmaf(ca.x, cl[0], acc[nt][0]))));
+            acc[nt][1] = fmaf(ca.w, sh.y, fmaf(ca.y, sl.y, fmaf(ca.z, chh[1], fmaf(ca.x, cl[1], acc[nt][1]))));
+            acc[nt][2] = fmaf(cb.w, sh.x, fmaf(cb.y, sl.x, fmaf(cb.z, chh[2], fmaf(cb.x, cl[2], acc[nt][2]))));
+            acc[nt][3] = fmaf(cb.w, sh.y, fmaf(cb.y, sl.y, fmaf(cb.z, chh[3], fmaf(cb.x, cl[3], acc[nt][3]))));
         }
     }
     __syncwarp();
@@ -243,11 +264,24 @@ gemv_kernel(const __grid_constant__ CUtensorMap wmap, const GemvParams p) {
     }
     // block sums of padding tokens (m >= M) stay zero for the whole kernel
     for (int idx = tid; idx < (p.kr_max / 32) * kMT; idx += kGemvThreads) xs[idx] = 0.f;
+    if (warp == kGemvWarps && lane == 0) {
+        // descriptor fetch and an L2 prefetch of the first weight stages:
+        // safe before the dependency wait below (L2 stays coherent with the
+        // previous kernel's writes; nothing lands in shared memory yet)
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wmap)) : "memory");
+        for (int i = 0; i < nloc && i < 2 * p.stages; ++i)
+            tma_prefetch_l2_2d(&wmap, (c_begin + i) * (kCB / 2), row0);
+    }
     __syncthreads();
+    // Programmatic dependent launch: everything above overlaps the tail of
+    // the previous kernel in the stream; no shared-memory copy, activation
+    // read or output write happens before that kernel has completed and
+    // flushed.  The next kernel may start its own prologue now.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == kGemvWarps) {
         // ---------------- producer: one 2-D TMA copy of the row tile per chunk
-        if (lane == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wmap)) : "memory");
         for (int i = 0; i < nloc; ++i) {
             const int s = i % p.stages;
             if (i >= p.stages &&
@@ -269,7 +303,8 @@ gemv_kernel(const __grid_constant__ CUtensorMap wmap, const GemvParams p) {
             acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
         const __half *xrow = xh + g * xstride;  // token g (+ 8 nt); read only if < M
         const int gvalid = p.M - g;             // token g + 8 nt is real iff 8 nt < gvalid
-        float *cw = coef + warp * 16 * 16;
+        const int rgrp = warp % kGemvRowGroups, kh = warp / kGemvRowGroups;
+        float *cw = coef + warp * 16 * 8;
         const int win = p.kr_max / kGroup;  // chunks per activation window
         // `ok` is warp-uniform; after a timed-out wait the warp skips its
         // remaining waits and MMAs but still takes every named barrier.
@@ -316,32 +351,36 @@ gemv_kernel(const __grid_constant__ CUtensorMap wmap, const GemvParams p) {
                 const int s = i % p.stages;
                 if (ok) ok = mbar_wait_warp(full_bar(s), (i / p.stages) & 1, kErrGemvFullWait);
                 if (!ok) continue;
-                const uint8_t *base = ring + (s * kGemvRows + 16 * warp) * kSlot;
+                const uint8_t *base = ring + (s * kGemvRows + 16 * rgrp) * kSlot;
                 const uint8_t *r0 = base + g * kSlot;
                 const uint8_t *r1 = base + (g + 8) * kSlot;
                 const __half *xr = xrow + li * kGroup;
                 if constexpr (kFmt == 8) {
-                    q8_block<0, kNT>(r0, r1, xr, xstride, xs, li * 8 + 0, t, gvalid, acc);
-                    q8_block<1, kNT>(r0, r1, xr, xstride, xs, li * 8 + 1, t, gvalid, acc);
-                    q8_block<2, kNT>(r0, r1, xr, xstride, xs, li * 8 + 2, t, gvalid, acc);
-                    q8_block<3, kNT>(r0, r1, xr, xstride, xs, li * 8 + 3, t, gvalid, acc);
-                    q8_block<4, kNT>(r0, r1, xr, xstride, xs, li * 8 + 4, t, gvalid, acc);
-                    q8_block<5, kNT>(r0, r1, xr, xstride, xs, li * 8 + 5, t, gvalid, acc);
-                    q8_block<6, kNT>(r0, r1, xr, xstride, xs, li * 8 + 6, t, gvalid, acc);
-                    q8_block<7, kNT>(r0, r1, xr, xstride, xs, li * 8 + 7, t, gvalid, acc);
+                    if (kh == 0) {
+                        q8_block<0, kNT>(r0, r1, xr, xstride, xs, li * 8 + 0, t, gvalid, acc);
+                        q8_block<1, kNT>(r0, r1, xr, xstride, xs, li * 8 + 1, t, gvalid, acc);
+                        q8_block<2, kNT>(r0, r1, xr, xstride, xs, li * 8 + 2, t, gvalid, acc);
+                        q8_block<3, kNT>(r0, r1, xr, xstride, xs, li * 8 + 3, t, gvalid, acc);
+                    } else {
+                        q8_block<4, kNT>(r0, r1, xr, xstride, xs, li * 8 + 4, t, gvalid, acc);
+                        q8_block<5, kNT>(r0, r1, xr, xstride, xs, li * 8 + 5, t, gvalid, acc);
+                        q8_block<6, kNT>(r0, r1, xr, xstride, xs, li * 8 + 6, t, gvalid, acc);
+                        q8_block<7, kNT>(r0, r1, xr, xstride, xs, li * 8 + 7, t, gvalid, acc);
+                    }
                 } else {
-                    q4k_chunk<kNT>(base, r0, r1, xr, xstride, xs, li, cw, lane, g, t, gvalid, acc);
+                    q4k_half<kNT>(base, r0, r1, xr, xstride, xs, li, cw, lane, g, t, gvalid, kh, acc);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty_bar(s));
             }
         }
-        // partial sums of this CTA: ypart[row][token]
-        const int rg = 16 * warp + g;
+        // partial sums of this CTA and K half: ypart[kh][row][token]
+        const int rg = 16 * rgrp + g;
+        float *yp = ypart + kh * kGemvRows * kMT;
 #pragma unroll
         for (int nt = 0; nt < kNT; ++nt) {
-            *reinterpret_cast<float2 *>(ypart + rg * kMT + nt * 8 + 2 * t) = make_float2(acc[nt][0], acc[nt][1]);
-            *reinterpret_cast<float2 *>(ypart + (rg + 8) * kMT + nt * 8 + 2 * t) =
+            *reinterpret_cast<float2 *>(yp + rg * kMT + nt * 8 + 2 * t) = make_float2(acc[nt][0], acc[nt][1]);
+            *reinterpret_cast<float2 *>(yp + (rg + 8) * kMT + nt * 8 + 2 * t) =
                 make_float2(acc[nt][2], acc[nt][3]);
         }
     }
@@ -352,9 +391,11 @@ gemv_kernel(const __grid_constant__ CUtensorMap wmap, const GemvParams p) {
     for (int idx = tid; idx < rpr * kMT; idx += kGemvThreads) {
         const int r = (int)rank * rpr + idx / kMT, m = idx % kMT;
         if (m < p.M && row0 + r < p.N) {
-            const uint32_t a = smem_addr(ypart + r * kMT + m);
+            const uint32_t a0 = smem_addr(ypart + r * kMT + m);
+            const uint32_t a1 = smem_addr(ypart + (kGemvRows + r) * kMT + m);
             float sum = 0.f;
-            for (uint32_t q = 0; q < nsplit; ++q) sum += ld_dsmem_f32(map_to_rank(a, q));
+            for (uint32_t q = 0; q < nsplit; ++q)
+                sum += ld_dsmem_f32(map_to_rank(a0, q)) + ld_dsmem_f32(map_to_rank(a1, q));
             p.Y[(int64_t)m * p.N + row0 + r] = sum;
         }
     }
@@ -364,8 +405,20 @@ gemv_kernel(const __grid_constant__ CUtensorMap wmap, const GemvParams p) {
 // ------------------------------------------------------------- launcher
 // Activation window (in 256-weight chunks) staged in shared memory at once,
 // and ring depth, per format / token tile.
+#ifndef QMM_GEMV_STAGES_Q8
+#define QMM_GEMV_STAGES_Q8 3
+#endif
+#ifndef QMM_GEMV_STAGES_Q4
+#define QMM_GEMV_STAGES_Q4 4
+#endif
+#ifndef QMM_GEMV_WAVE_PCT  // grid size allowed, in % of one wave of resident CTAs
+#define QMM_GEMV_WAVE_PCT 100
+#endif
+#ifndef QMM_GEMV_PDL
+#define QMM_GEMV_PDL 1
+#endif
 static int gemv_window(int nt) { return nt == 1 ? 8 : 4; }
-static int gemv_stages(int fmt) { return fmt == 8 ? 3 : 4; }
+static int gemv_stages(int fmt) { return fmt == 8 ? QMM_GEMV_STAGES_Q8 : QMM_GEMV_STAGES_Q4; }
 
 struct GemvPlan {
     int nsplit, stages, kr_max, smem;
@@ -390,7 +443,7 @@ static GemvPlan gemv_plan(int fmt, int M, int N, int K, int sms) {
         const int by_smem = (228 * 1024) / (pl.smem + 1024);
         const int by_warps = 64 / (kGemvThreads / 32);
         const int per_sm = by_smem < by_warps ? by_smem : by_warps;
-        if (s == 1 || tiles * s <= sms * per_sm) best = pl;
+        if (s == 1 || tiles * s * 100 <= sms * per_sm * QMM_GEMV_WAVE_PCT) best = pl;
         else break;
     }
     return best;
@@ -418,13 +471,15 @@ static cudaError_t launch_gemv_t(const GemvParams &p, const GemvPlan &pl, cudaSt
     cfg.blockDim = dim3(kGemvThreads, 1, 1);
     cfg.dynamicSmemBytes = (size_t)pl.smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 1;
     attr[0].val.clusterDim.y = (unsigned)pl.nsplit;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = QMM_GEMV_PDL;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, gemv_kernel<kFmt, kNT>, wmap, p);
 }
 
