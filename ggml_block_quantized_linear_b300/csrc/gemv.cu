@@ -21,12 +21,14 @@
 //    warps hide latency; the two halves are added in shared memory.  The
 //    MMAs are m16n8k16 (f16 inputs, fp32 accumulation) with the weight rows
 //    as the M side and the (padded) tokens as N.  The MMA operands are the
-//    integer codes, which binary16 holds exactly: one PRMT / LOP3 places a
-//    code under a binary16 exponent (1152 + q, 1024 + q or 1024 + 16 q for a
-//    high nibble) and one HSUB2 / HFMA2 removes the offset exactly.  The
-//    scales are applied in fp32 after each 32-weight block, R being the MMA
-//    result of the block:  Q8_0  d * R;  Q4_K  S_j * R - Mn_j * sum_k x,
-//    with sum_k x per sub-block and token from the staged activations.
+//    integer codes, which binary16 holds exactly: an int8 code goes through
+//    one PRMT under a binary16 exponent (1152 + q) and one HSUB2 back to q;
+//    a masked pair of 4-bit codes already is a pair of binary16 subnormals
+//    (q * 2^-24, or q * 2^-20 for a high nibble).  The scales are applied in
+//    fp32 after each 32-weight block, R being the MMA result of the block:
+//    Q8_0  d * R;  Q4_K  S_j * R - Mn_j * sum_k x  (the power of two of the
+//    subnormal folded into S_j), sum_k x per sub-block and token coming from
+//    the staged activations.
 //  * The activations of the CTA's K range are converted once to binary16
 //    (round to nearest) in shared memory, each group of 4 stored in the
 //    order (0, 2, 1, 3) so that one 16-byte load yields both B fragments.
@@ -114,14 +116,6 @@ __device__ __forceinline__ uint32_t hsub_bits(uint32_t v, uint32_t c) {
     return *reinterpret_cast<uint32_t *>(&r);
 }
 __device__ __forceinline__ uint32_t q8_exact(uint32_t v) { return hsub_bits(v, 0x64806480u); }
-// 4-bit codes: (1024 + q) - 1024 = q and (1024 + 16 q) / 16 - 64 = q, exact.
-__device__ __forceinline__ uint32_t q4_lo_exact(uint32_t v) { return hsub_bits(v, 0x64006400u); }
-__device__ __forceinline__ uint32_t q4_hi_exact(uint32_t v) {
-    const uint32_t s16 = 0x2C002C00u, m64 = 0xD400D400u;  // 1/16 and -64
-    __half2 r = __hfma2(*reinterpret_cast<const __half2 *>(&v), *reinterpret_cast<const __half2 *>(&s16),
-                        *reinterpret_cast<const __half2 *>(&m64));
-    return *reinterpret_cast<uint32_t *>(&r);
-}
 
 // 16-byte B-fragment load of token row (g + 8 nt); tokens >= M are zero.
 __device__ __forceinline__ uint4 x_frag(const __half *p, bool valid) {
@@ -187,8 +181,9 @@ __device__ __forceinline__ void q4k_half(const uint8_t *base, const uint8_t *r0,
                 sc = (sbyte(j + 4) & 15u) | ((sbyte(j - 4) >> 6) << 4);
                 mc = (sbyte(j + 4) >> 4) | ((sbyte(j) >> 6) << 4);
             }
-            cw[rr * 8 + 2 * jl] = dsc * (float)sc;       // S_j
-            cw[rr * 8 + 2 * jl + 1] = -(dmn * (float)mc);  // -Mn_j
+            // S_j * 2^24 (low nibble: sub-block even) or S_j * 2^20 (high), -Mn_j
+            cw[rr * 8 + 2 * jl] = dsc * (float)sc * ((j & 1) ? 1048576.0f : 16777216.0f);
+            cw[rr * 8 + 2 * jl + 1] = -(dmn * (float)mc);
         }
     }
     __syncwarp();
@@ -199,10 +194,12 @@ __device__ __forceinline__ void q4k_half(const uint8_t *base, const uint8_t *r0,
         const uint2 qb = *reinterpret_cast<const uint2 *>(r1 + 16 + 32 * c + 8 * t);
         const float4 ca = *reinterpret_cast<const float4 *>(cw + g * 8 + 4 * cc);
         const float4 cb = *reinterpret_cast<const float4 *>(cw + (g + 8) * 8 + 4 * cc);
-        const uint32_t M16 = 0x64006400u;
         const uint32_t qa0s = qa.x >> 8, qa1s = qa.y >> 8, qb0s = qb.x >> 8, qb1s = qb.y >> 8;
-        auto lo = [&](uint32_t w) { return q4_lo_exact(and_or(w, 0x000F000Fu, M16)); };
-        auto hi = [&](uint32_t w) { return q4_hi_exact(and_or(w, 0x00F000F0u, M16)); };
+        // a masked nibble pair IS a pair of binary16 subnormals: q * 2^-24 (low
+        // nibble) and q * 2^-20 (high nibble), exact; the MMA sums q x exactly
+        // scaled, and 2^24 / 2^20 are folded into S_j
+        auto lo = [&](uint32_t w) { return w & 0x000F000Fu; };
+        auto hi = [&](uint32_t w) { return w & 0x00F000F0u; };
         const uint32_t L0[4] = {lo(qa.x), lo(qb.x), lo(qa0s), lo(qb0s)};
         const uint32_t L1[4] = {lo(qa.y), lo(qb.y), lo(qa1s), lo(qb1s)};
         const uint32_t H0[4] = {hi(qa.x), hi(qb.x), hi(qa0s), hi(qb0s)};

@@ -15,6 +15,8 @@ cudaError_t launch_dequantize(int fmt, const void *src, float *dst, int64_t nwei
                               cudaStream_t stream);
 cudaError_t launch_gemv(int fmt, const void *W, const uint16_t *X, float *Y, int M, int N, int K,
                         int sms, cudaStream_t stream);
+cudaError_t launch_gemv_rows(int fmt, const void *W, const uint16_t *X, float *Y, int M, int N,
+                             int K, int sms, cudaStream_t stream);
 cudaError_t launch_gemm(int fmt, const void *W, const uint16_t *X, float *Y, int M, int N, int K,
                         void *workspace, size_t workspace_bytes, int sms, cudaStream_t stream);
 size_t gemm_workspace_bytes(int fmt, int M, int N, int K);
@@ -35,6 +37,19 @@ static int sm_count() {
         cached[dev] = n;
     }
     return cached[dev];
+}
+
+#ifndef QMM_ROWS_MAX_M
+#define QMM_ROWS_MAX_M 8
+#endif
+#ifndef QMM_ROWS_MIN_CTAS_PER_SM  // in 1/4 CTA per SM
+#define QMM_ROWS_MIN_CTAS_PER_SM 4
+#endif
+// Decode kernel choice: 16-row CTAs over the whole K (no cluster) when the
+// tokens are few and the rows alone give every SM enough CTAs; otherwise the
+// 64-row tile with a cluster split-K.
+static bool use_rows_kernel(int M, int N, int sms) {
+    return M <= QMM_ROWS_MAX_M && (int64_t)((N + 15) / 16) * 4 >= (int64_t)sms * QMM_ROWS_MIN_CTAS_PER_SM;
 }
 
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -99,9 +114,13 @@ qmm_status qmm_matmul(qmm_format fmt, const void *W_packed, const uint16_t *X_bf
     if (W_packed == nullptr || X_bf16 == nullptr || Y == nullptr) return QMM_ERR_INVALID_ARG;
     if (!aligned16(W_packed) || !aligned16(X_bf16) || !aligned16(Y)) return QMM_ERR_ALIGNMENT;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (M <= kMaxDecodeM)
+    if (M <= kMaxDecodeM) {
+        if (use_rows_kernel((int)M, (int)N, sm_count()))
+            return from_cuda(launch_gemv_rows((int)fmt, W_packed, X_bf16, Y, (int)M, (int)N, (int)K,
+                                              sm_count(), s));
         return from_cuda(launch_gemv((int)fmt, W_packed, X_bf16, Y, (int)M, (int)N, (int)K,
                                      sm_count(), s));
+    }
     const size_t need = gemm_workspace_bytes((int)fmt, (int)M, (int)N, (int)K);
     if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return QMM_ERR_WORKSPACE;
     if (need > 0 && !aligned16(workspace)) return QMM_ERR_ALIGNMENT;

@@ -3,4 +3,5 @@
 #include "qmm_api.cu"
 #include "quantize.cu"
 #include "gemv.cu"
+#include "gemv_rows.cu"
 #include "gemm.cu"
