@@ -5,3 +5,4 @@
 #include "gemv.cu"
 #include "gemv_rows.cu"
 #include "gemm.cu"
+#include "static_scratch.cu"

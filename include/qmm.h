@@ -127,6 +127,29 @@ QMM_API qmm_status qmm_matmul(qmm_format fmt, const void *W_packed, const uint16
                       int64_t M, int64_t N, int64_t K, void *workspace, size_t workspace_bytes,
                       qmm_stream_t stream);
 
+/* Prefill matmul (M > 16) that allocates nothing, for callers that cannot
+ * allocate device memory: code handed only raw tensor pointers by a host
+ * framework, engines whose pool owns all device memory, loops that must not
+ * call cudaMalloc because it can synchronise the device.  It computes what
+ * qmm_matmul computes, with the same kernels, but its scratch (the binary16
+ * copy of X) lives in a fixed 64 MiB device array inside this library, held
+ * by every GPU that loads the library until the process exits.  The pages
+ * describe no counterpart of this call; it is an interface convenience.
+ *  - Requires qmm_matmul_workspace_bytes(fmt, M, N, K) <= 64 MiB (that is,
+ *    M * K <= 32 Mi); larger problems return QMM_ERR_WORKSPACE and launch
+ *    nothing.  M <= 16 returns QMM_ERR_UNSUPPORTED: the decode path needs no
+ *    scratch, call qmm_matmul with a NULL workspace.
+ *  - The first call on a device looks up the array's device address with
+ *    that device current (cudaGetSymbolAddress); make that first call before
+ *    any stream capture.
+ *  - All calls share the one array: calls whose executions overlap on the
+ *    GPU (different streams, or different host threads on one device) race
+ *    on it.  Serialise them, e.g. on one stream.  Nothing in the array needs
+ *    to start at zero. */
+QMM_API qmm_status qmm_matmul_prefill_static(qmm_format fmt, const void *W_packed,
+                                             const uint16_t *X_bf16, float *Y, int64_t M,
+                                             int64_t N, int64_t K, qmm_stream_t stream);
+
 /* Static description of a status code (never NULL). */
 QMM_API const char *qmm_status_string(qmm_status s);
 
