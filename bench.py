@@ -75,8 +75,9 @@ def kernel_source_hash():
 
 
 def load_traffic():
-    """Per-launch DRAM traffic measured by ncu (profiles/dram_traffic.txt),
-    valid only for the kernel sources it was measured on."""
+    """DRAM bytes per weight measured by ncu for each kernel family
+    (profiles/dram_traffic.txt, lines `family=bytes_per_weight`), valid only
+    for the kernel sources they were measured on (`source_hash=`)."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     out = {}
     if not os.path.exists(p):
@@ -217,13 +218,14 @@ class Workload:
                 for w, o in zip(self.w_bf16, self.isq_out[f]):
                     q.qmm_quantize(f, w, out=o)
         nw = sum(n * k for n, k in shapes)
-        S.append(("isq", isq, 8, sum(nw * (2 + bw[f]) for f in self.fmts), 0.0, "quantize"))
+        S.append(("isq", isq, 8, sum(nw * (2 + bw[f]) for f in self.fmts), 0.0, "quantize", 2 * nw))
 
         def deq():
             for f in self.fmts:
                 for (n, k), p, o in zip(shapes, self.packed[f], self.deq_out):
                     q.qmm_dequantize(f, p, n, k, out=o)
-        S.append(("dequant", deq, 8, sum(nw * (bw[f] + 4) for f in self.fmts), 0.0, "dequantize"))
+        S.append(("dequant", deq, 8, sum(nw * (bw[f] + 4) for f in self.fmts), 0.0, "dequantize",
+                  2 * nw))
 
         for m in inputs.DECODE_MS:
             def gemv(m=m):
@@ -232,7 +234,7 @@ class Workload:
                         q.qmm_matmul(f, p, x, n, out=y)
             wbytes = sum(nw * bw[f] for f in self.fmts)
             io = 2 * sum((2 * m * k + 4 * m * n) for n, k in shapes)
-            S.append(("gemv_m%d" % m, gemv, 8, wbytes + io, 2.0 * 2 * m * nw, "gemv"))
+            S.append(("gemv_m%d" % m, gemv, 8, wbytes + io, 2.0 * 2 * m * nw, "gemv", 2 * nw))
 
         if self.gemm_ok:
             pshapes = inputs.PREFILL_SHAPES
@@ -244,7 +246,9 @@ class Workload:
                                 q.qmm_matmul(f, self.packed[f][si], self.x[m][si], n,
                                              out=self.y[m][f][si])
                 fl = 2 * 2.0 * m * sum(n * k for n, k in pshapes)
-                S.append(("gemm_m%d" % m, gemm, 6, 0, fl, "gemm"))
+                # each prefill call launches two kernels: X -> binary16, then the GEMM
+                S.append(("gemm_m%d" % m, gemm, 12, 0, fl, "gemm",
+                          2 * sum(n * k for n, k in pshapes)))
 
         if self.model is not None:
             mw = sum(n * k for _, n, k in inputs.MODEL_LINEARS) * inputs.MODEL_LAYERS
@@ -255,7 +259,7 @@ class Workload:
                     for w, p in zip(self.model["w"], self.model["packed"][f]):
                         q.qmm_quantize(f, w, out=p)
             S.append(("model_isq", model_isq, 2 * nl, sum(mw * (2 + bw[f]) for f in self.fmts),
-                      0.0, "quantize"))
+                      0.0, "quantize", 2 * mw))
             for f in self.fmts:
                 def model_decode(f=f):
                     for (_, n, k), p, x, y in zip(inputs.MODEL_LINEARS * inputs.MODEL_LAYERS,
@@ -263,7 +267,7 @@ class Workload:
                                                   self.model["y"]):
                         q.qmm_matmul(f, p, x, n, out=y)
                 name = "model_decode_" + ("q8_0" if f == q.QMM_Q8_0 else "q4_k")
-                S.append((name, model_decode, nl, mw * bw[f], 2.0 * mw, "gemv"))
+                S.append((name, model_decode, nl, mw * bw[f], 2.0 * mw, "gemv", mw))
         return S
 
 
@@ -517,7 +521,7 @@ def main(argv=None):
 
     rows = {}
     fam_time = {}
-    for name, _, launches, nbytes, flops, fam in stages:
+    for name, _, launches, nbytes, flops, fam, _nw in stages:
         t = med[name] * 1e-3
         r = {"ms": round(med[name], 4), "launches": launches}
         if nbytes:
@@ -544,13 +548,16 @@ def main(argv=None):
                     "peak_source": peak_kind + " bf16 burst (f16 same nominal rate)",
                     "launches": launches}
         nb = sum(s[3] for s in sel)
+        nw = sum(s[6] for s in sel)
         peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
         ach = nb / t / 1e9
-        tr = traffic.get(fam)
+        bpw = traffic.get(fam)  # measured DRAM bytes per weight (one ncu capture)
+        tr = bpw * nw / launches if bpw else None  # scaled to the average launch here
         return {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(ach / peak, 4),
-                "traffic": tr, "traffic_ratio": round(tr / (nb / launches), 3) if tr else None,
-                "peak_source": peak_kind + " copy bandwidth", "launches": launches}
+                "traffic": round(tr) if tr else None,
+                "traffic_ratio": round(tr / (nb / launches), 3) if tr else None,
+                "peak_source": peak_kind + " copy bandwidth (burst)", "launches": launches}
 
     dominant = max(fam_time, key=fam_time.get)
     rooflines = {fam: roofline_for(fam) for fam in fam_time}
