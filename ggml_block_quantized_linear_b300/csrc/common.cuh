@@ -63,18 +63,31 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
 }
-// Suspend-time hint of one try_wait: the thread sleeps until the phase
-// completes or this many nanoseconds pass, instead of spinning.
-constexpr uint32_t kTryWaitHintNs = 20000;
+#ifndef QMM_TRYWAIT_HINT_NS
+#define QMM_TRYWAIT_HINT_NS 0
+#endif
+// One mbarrier.try_wait: the hardware may suspend the thread for a short,
+// system-dependent time (or up to an explicit hint, when one is compiled in)
+// until the phase completes.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
+#if QMM_TRYWAIT_HINT_NS > 0
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(kTryWaitHintNs)
+        : "r"(bar), "r"(parity), "r"(QMM_TRYWAIT_HINT_NS)
         : "memory");
+#else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+#endif
     return ok != 0;
 }
 // Bounded wait for the phase with the given parity to complete.  Returns
@@ -119,6 +132,18 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
         "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// 2-D tiled tensor copy global -> shared, multicast to the CTAs of the
+// cluster in ctaMask: the box lands at the same shared-memory offset in each
+// of them and completes `bytes` on the mbarrier at the same offset in each.
+__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                                      uint32_t bar, uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster "
+        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(cta_mask)
         : "memory");
 }
 

@@ -15,13 +15,18 @@
 // into the caller's workspace.
 //
 // Tile: 128 weight rows (the MMA's M side, "swap AB") x 256 tokens (MMA N)
-// x 64 K per stage; the fp32 accumulator lives in 256 TMEM columns.
-//   warp 0      TMA producer: packed weights (one 128-row box per 256-weight
-//               group) and binary16 activation tiles (128B-swizzled boxes)
-//   warp 1      TMEM allocator and single-thread MMA issuer
-//   warps 2-9   dequantize packed weights into 128B-swizzled K-major f16
-//               A stages, then read the accumulator back (tcgen05.ld) and
-//               store Y.
+// x 64 K per stage; persistent CTAs (one per SM) walk the tiles, and two fp32
+// accumulators of 256 TMEM columns alternate between consecutive tiles.
+//   warp 0       TMA producer of the binary16 activation tiles (128B-swizzled
+//                boxes, multicast to the CTAs of the cluster)
+//   warp 1       TMEM allocator and single-thread MMA issuer
+//   warps 2-17   dequantize packed weights into 128B-swizzled K-major f16
+//                A stages
+//   warps 18-21  epilogue: read an accumulator back (tcgen05.ld) and store
+//                Y while the next tile's main loop runs
+//   warp 22      TMA producer of the packed weights (separate from warp 0 so
+//                that the dequantizing warps never wait behind activation
+//                stages)
 // Every wait is bounded (common.cuh); TMEM is always released.
 #include "common.cuh"
 
@@ -30,13 +35,34 @@ namespace qmm {
 constexpr int kGemmBM = 128;        // weight rows per CTA (MMA M)
 constexpr int kGemmBN = 256;        // tokens per CTA (MMA N)
 constexpr int kGemmBK = 64;         // K per stage (one 128-byte swizzle atom of f16)
-constexpr int kGemmDeqWarps = 8;
-constexpr int kGemmThreads = (2 + kGemmDeqWarps) * 32;
-constexpr int kGemmStagesB = 3;     // activation stages (32 KB each)
+#ifndef QMM_GEMM_DEQ_WARPS
+#define QMM_GEMM_DEQ_WARPS 16
+#endif
+constexpr int kGemmDeqWarps = QMM_GEMM_DEQ_WARPS;  // 8 or 16 (128 rows / (4 rows x warps) passes)
+constexpr int kGemmEpiWarps = 4;
+// warps: 0 activation producer, 1 MMA, then the dequantizing warps, the
+// epilogue warps and the packed-weight producer
+constexpr int kGemmWarpPackedTma = 2 + kGemmDeqWarps + kGemmEpiWarps;
+constexpr int kGemmThreads = (kGemmWarpPackedTma + 1) * 32;
+#ifndef QMM_GEMM_STAGES_B_Q4
+#define QMM_GEMM_STAGES_B_Q4 4
+#endif
+#ifndef QMM_GEMM_STAGES_A_Q4
+#define QMM_GEMM_STAGES_A_Q4 3
+#endif
 constexpr int kGemmStagesP = 2;     // packed weight groups
-constexpr int kGemmTmemCols = 256;
+constexpr int kGemmTmemCols = 512;  // two 256-column fp32 accumulators
+#ifndef QMM_GEMM_CLUSTER
+#define QMM_GEMM_CLUSTER 2
+#endif
+// CTAs per cluster: they compute neighbouring weight tiles against the same
+// token tile, and each TMA-loads 1/kGemmCluster of every activation stage and
+// multicasts it to all of them (activation traffic from L2 / kGemmCluster).
+constexpr int kGemmCluster = QMM_GEMM_CLUSTER;
 
-__host__ __device__ constexpr int gemm_stages_a(int fmt) { return fmt == 8 ? 3 : 4; }
+// activation stages (32 KB each) and dequantized-weight stages (16 KB each)
+__host__ __device__ constexpr int gemm_stages_b(int fmt) { return fmt == 8 ? 3 : QMM_GEMM_STAGES_B_Q4; }
+__host__ __device__ constexpr int gemm_stages_a(int fmt) { return fmt == 8 ? 3 : QMM_GEMM_STAGES_A_Q4; }
 __host__ __device__ constexpr int gemm_group_bytes(int fmt) { return fmt == 8 ? kQ8GroupBytes : kQ4Bytes; }
 
 struct GemmLayout {
@@ -47,7 +73,7 @@ __host__ __device__ inline GemmLayout gemm_layout(int fmt) {
     GemmLayout L;
     int off = 0;
     L.b = off;
-    off += kGemmStagesB * kGemmBN * kGemmBK * 2;
+    off += gemm_stages_b(fmt) * kGemmBN * kGemmBK * 2;
     L.a = off;
     off += gemm_stages_a(fmt) * kGemmBM * kGemmBK * 2;
     L.p = off;
@@ -95,6 +121,14 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint6
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+// The same, arriving on the mbarrier at this offset in every CTA of ctaMask.
+__device__ __forceinline__ void umma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+        "[%0], %1;" ::"r"(bar),
+        "h"(cta_mask)
         : "memory");
 }
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle,
@@ -208,12 +242,18 @@ struct GemmParams {
     int M, N, K;
 };
 
+// Persistent: CTA b computes the output tiles b, b + gridDim.x, ... (weight
+// tile index fastest).  Every ring index (packed groups, activation stages,
+// A stages) runs on across tiles, and the two TMEM accumulators alternate
+// between tiles, so the epilogue of one tile overlaps the main loop of the
+// next.
 template <int kFmt>
 __global__ void __launch_bounds__(kGemmThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
             const GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     constexpr int kSA = gemm_stages_a(kFmt);
+    constexpr int kGemmStagesB = gemm_stages_b(kFmt);
     constexpr int kCB = gemm_group_bytes(kFmt);
     constexpr uint32_t kBBytes = kGemmBN * kGemmBK * 2;
     constexpr uint32_t kABytes = kGemmBM * kGemmBK * 2;
@@ -221,25 +261,36 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
     const GemmLayout L = gemm_layout(kFmt);
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int n0 = blockIdx.x * kGemmBM, m0 = blockIdx.y * kGemmBN;
+    // work unit = (group of kGemmCluster neighbouring weight tiles, token tile);
+    // cluster c takes units c, c + nclusters, ...; its CTA of rank r takes
+    // weight tile kGemmCluster * group + r of each unit (past N: all zero)
+    const int crank = kGemmCluster > 1 ? (int)cluster_ctarank() : 0;
+    const int cid = (int)blockIdx.x / kGemmCluster, nclusters = (int)gridDim.x / kGemmCluster;
+    const int tiles_n = (p.N + kGemmBM - 1) / kGemmBM;
+    const int ngroups_n = (tiles_n + kGemmCluster - 1) / kGemmCluster;
+    const int units = ngroups_n * ((p.M + kGemmBN - 1) / kGemmBN);
+    const int my_tiles = units > cid ? (units - 1 - cid) / nclusters + 1 : 0;
+    auto tile_n0 = [&](int lt) { return (((cid + lt * nclusters) % ngroups_n) * kGemmCluster + crank) * kGemmBM; };
+    auto tile_m0 = [&](int lt) { return ((cid + lt * nclusters) / ngroups_n) * kGemmBN; };
+    constexpr uint16_t kAllCtas = (uint16_t)((1u << kGemmCluster) - 1);
     const int ksteps = p.K / kGemmBK;
     const int groups = p.K / kGroup;
 
     const uint32_t bar = smem_addr(smem + L.bars);
-    // barrier slots
     auto b_full = [&](int s) { return bar + 8u * s; };
     auto b_empty = [&](int s) { return bar + 8u * (4 + s); };
     auto a_full = [&](int s) { return bar + 8u * (8 + s); };
     auto a_empty = [&](int s) { return bar + 8u * (12 + s); };
     auto p_full = [&](int s) { return bar + 8u * (16 + s); };
     auto p_empty = [&](int s) { return bar + 8u * (18 + s); };
-    const uint32_t acc_full = bar + 8u * 20;
+    auto acc_full = [&](int b) { return bar + 8u * (20 + b); };
+    auto acc_empty = [&](int b) { return bar + 8u * (22 + b); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.bars + 8 * 24);
 
     if (tid == 0) {
         for (int s = 0; s < kGemmStagesB; ++s) {
             mbar_init(b_full(s), 1);
-            mbar_init(b_empty(s), 1);
+            mbar_init(b_empty(s), kGemmCluster);  // every CTA's MMA releases every copy
         }
         for (int s = 0; s < kSA; ++s) {
             mbar_init(a_full(s), kGemmDeqWarps);
@@ -249,7 +300,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
             mbar_init(p_full(s), 1);
             mbar_init(p_empty(s), kGemmDeqWarps);
         }
-        mbar_init(acc_full, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(acc_full(b), 1);
+            mbar_init(acc_empty(b), kGemmEpiWarps);
+        }
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -257,31 +311,51 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
         tmem_relinquish();
     }
     tc_fence_before();
-    __syncthreads();
+    // peers multicast into this CTA's stages and arrive on its barriers: all
+    // barriers of the cluster are initialised before anyone proceeds
+    if (kGemmCluster > 1) cluster_sync_all(); else __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        // ------------------------------------------------ TMA producer
+        // ------------------------------------------------ activation TMA producer
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
+            bool ok = true;
+            int ki = 0;  // running activation-stage counter
+            for (int lt = 0; lt < my_tiles && ok; ++lt) {
+                const int m0 = tile_m0(lt);
+                for (int ks = 0; ks < ksteps && ok; ++ks, ++ki) {
+                    const int sb = ki % kGemmStagesB;
+                    if (ki >= kGemmStagesB)
+                        ok = mbar_wait(b_empty(sb), ((ki / kGemmStagesB) - 1) & 1, kErrGemmWait);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(b_full(sb), kBBytes);  // all slices, from every CTA
+                    constexpr uint32_t kSlice = kBBytes / kGemmCluster;
+                    const uint32_t dst = smem_addr(smem + L.b + sb * kBBytes + crank * kSlice);
+                    const int y0 = m0 + crank * (kGemmBN / kGemmCluster);
+                    if (kGemmCluster > 1)
+                        tma_load_2d_multicast(dst, &xmap, ks * kGemmBK, y0, b_full(sb), kAllCtas);
+                    else
+                        tma_load_2d(dst, &xmap, ks * kGemmBK, y0, b_full(sb));
+                }
+            }
+        }
+    } else if (warp == kGemmWarpPackedTma) {
+        // ------------------------------------------------ packed-weight TMA producer
+        if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wmap)) : "memory");
             bool ok = true;
-            for (int g = 0; g < groups && ok; ++g) {
-                const int sp = g % kGemmStagesP;
-                if (g >= kGemmStagesP)
-                    ok = mbar_wait(p_empty(sp), ((g / kGemmStagesP) - 1) & 1, kErrGemmWait);
-                if (!ok) break;
-                mbar_arrive_expect_tx(p_full(sp), kPBytes);
-                tma_load_2d(smem_addr(smem + L.p + sp * kPBytes), &wmap, g * (kCB / 2), n0, p_full(sp));
-                for (int j = 0; j < 4 && ok; ++j) {
-                    const int ks = 4 * g + j;
-                    const int sb = ks % kGemmStagesB;
-                    if (ks >= kGemmStagesB)
-                        ok = mbar_wait(b_empty(sb), ((ks / kGemmStagesB) - 1) & 1, kErrGemmWait);
+            int gi = 0;  // running packed-group counter
+            for (int lt = 0; lt < my_tiles && ok; ++lt) {
+                const int n0 = tile_n0(lt);
+                for (int g = 0; g < groups && ok; ++g, ++gi) {
+                    const int sp = gi % kGemmStagesP;
+                    if (gi >= kGemmStagesP)
+                        ok = mbar_wait(p_empty(sp), ((gi / kGemmStagesP) - 1) & 1, kErrGemmWait);
                     if (!ok) break;
-                    mbar_arrive_expect_tx(b_full(sb), kBBytes);
-                    tma_load_2d(smem_addr(smem + L.b + sb * kBBytes), &xmap, ks * kGemmBK, m0, b_full(sb));
+                    mbar_arrive_expect_tx(p_full(sp), kPBytes);
+                    tma_load_2d(smem_addr(smem + L.p + sp * kPBytes), &wmap, g * (kCB / 2), n0, p_full(sp));
                 }
             }
         }
@@ -290,106 +364,125 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
         if (lane == 0) {
             constexpr uint32_t idesc = umma_idesc_f16(kGemmBM, kGemmBN);
             bool ok = true;
-            for (int ks = 0; ks < ksteps && ok; ++ks) {
-                const int sa = ks % kSA, sb = ks % kGemmStagesB;
-                ok = mbar_wait(a_full(sa), (ks / kSA) & 1, kErrGemmWait) &&
-                     mbar_wait(b_full(sb), (ks / kGemmStagesB) & 1, kErrGemmWait);
-                if (!ok) break;
-                tc_fence_after();
-                const uint64_t ad = umma_desc_sw128(smem_addr(smem + L.a + sa * kABytes));
-                const uint64_t bd = umma_desc_sw128(smem_addr(smem + L.b + sb * kBBytes));
+            int ki = 0;  // running k-step counter (A and activation rings)
+            for (int lt = 0; lt < my_tiles; ++lt) {
+                const int buf = lt & 1, use = lt >> 1;
+                const uint32_t dacc = tmem + (uint32_t)(buf * kGemmBN);
+                if (ok && use > 0) ok = mbar_wait(acc_empty(buf), (use - 1) & 1, kErrGemmWait);
+                for (int ks = 0; ks < ksteps && ok; ++ks, ++ki) {
+                    const int sa = ki % kSA, sb = ki % kGemmStagesB;
+                    ok = mbar_wait(a_full(sa), (ki / kSA) & 1, kErrGemmWait) &&
+                         mbar_wait(b_full(sb), (ki / kGemmStagesB) & 1, kErrGemmWait);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint64_t ad = umma_desc_sw128(smem_addr(smem + L.a + sa * kABytes));
+                    const uint64_t bd = umma_desc_sw128(smem_addr(smem + L.b + sb * kBBytes));
 #pragma unroll
-                for (int kk = 0; kk < kGemmBK / 16; ++kk)  // +32 bytes of K per MMA
-                    umma_f16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (ks | kk) != 0);
-                umma_commit(a_empty(sa));
-                umma_commit(b_empty(sb));
+                    for (int kk = 0; kk < kGemmBK / 16; ++kk)  // +32 bytes of K per MMA
+                        umma_f16(dacc, ad + 2 * kk, bd + 2 * kk, idesc, (ks | kk) != 0);
+                    umma_commit(a_empty(sa));
+                    if (kGemmCluster > 1) umma_commit_multicast(b_empty(sb), kAllCtas);
+                    else umma_commit(b_empty(sb));
+                }
+                umma_commit(acc_full(buf));  // also after an error: releases the epilogue
             }
-            umma_commit(acc_full);  // also after an error: releases the epilogue
         }
-    } else {
-        // ------------------------------------------------ dequantize, then epilogue
-        const int dw = warp - 2;              // 0..7
+    } else if (warp < 2 + kGemmDeqWarps) {
+        // ------------------------------------------------ dequantize packed tiles
+        const int dw = warp - 2;              // 0 .. kGemmDeqWarps - 1
         const int c = lane & 7;               // 16-byte chunk (8 k) of the 64-k step
         const int rsub = lane >> 3;           // 0..3
         float *coef = reinterpret_cast<float *>(smem + L.coef);
         bool ok = true;
-        for (int g = 0; g < groups; ++g) {
-            const int sp = g % kGemmStagesP;
-            if (ok) ok = mbar_wait_warp(p_full(sp), (g / kGemmStagesP) & 1, kErrGemmWait);
-            const uint8_t *pst = smem + L.p + sp * kPBytes;
-            if constexpr (kFmt == 4) {
-                // (S_j, Mn_j) of the 8 sub-blocks of each row's superblock
-                if (ok && tid >= 64 && tid < 64 + kGemmBM) {
-                    const int r = tid - 64;
-                    const uint4 h = *reinterpret_cast<const uint4 *>(pst + r * kCB);
-                    const float dsc = __half2float(__ushort_as_half((unsigned short)(h.x & 0xFFFF)));
-                    const float dmn = __half2float(__ushort_as_half((unsigned short)(h.x >> 16)));
-                    const uint32_t sw[3] = {h.y, h.z, h.w};
+        int gi = 0, ki = 0;
+        for (int lt = 0; lt < my_tiles; ++lt) {
+            for (int g = 0; g < groups; ++g, ++gi) {
+                const int sp = gi % kGemmStagesP;
+                if (ok) ok = mbar_wait_warp(p_full(sp), (gi / kGemmStagesP) & 1, kErrGemmWait);
+                const uint8_t *pst = smem + L.p + sp * kPBytes;
+                if constexpr (kFmt == 4) {
+                    // (S_j, Mn_j) of the 8 sub-blocks of each row's superblock
+                    if (ok && tid >= 64 && tid < 64 + kGemmBM) {
+                        const int r = tid - 64;
+                        const uint4 h = *reinterpret_cast<const uint4 *>(pst + r * kCB);
+                        const float dsc = __half2float(__ushort_as_half((unsigned short)(h.x & 0xFFFF)));
+                        const float dmn = __half2float(__ushort_as_half((unsigned short)(h.x >> 16)));
+                        const uint32_t sw[3] = {h.y, h.z, h.w};
 #pragma unroll
-                    for (int sj = 0; sj < 8; ++sj) {
-                        auto sb = [&](int k) { return (sw[k >> 2] >> (8 * (k & 3))) & 0xFFu; };
-                        uint32_t sc, mc;
-                        if (sj < 4) {
-                            sc = sb(sj) & 63u;
-                            mc = sb(sj + 4) & 63u;
-                        } else {
-                            sc = (sb(sj + 4) & 15u) | ((sb(sj - 4) >> 6) << 4);
-                            mc = (sb(sj + 4) >> 4) | ((sb(sj) >> 6) << 4);
+                        for (int sj = 0; sj < 8; ++sj) {
+                            auto sb = [&](int k) { return (sw[k >> 2] >> (8 * (k & 3))) & 0xFFu; };
+                            uint32_t sc, mc;
+                            if (sj < 4) {
+                                sc = sb(sj) & 63u;
+                                mc = sb(sj + 4) & 63u;
+                            } else {
+                                sc = (sb(sj + 4) & 15u) | ((sb(sj - 4) >> 6) << 4);
+                                mc = (sb(sj + 4) >> 4) | ((sb(sj) >> 6) << 4);
+                            }
+                            coef[(r * 8 + sj) * 2] = dsc * (float)sc;
+                            coef[(r * 8 + sj) * 2 + 1] = dmn * (float)mc;
                         }
-                        coef[(r * 8 + sj) * 2] = dsc * (float)sc;
-                        coef[(r * 8 + sj) * 2 + 1] = dmn * (float)mc;
                     }
+                    named_bar_sync(1, kGemmDeqWarps * 32);
                 }
-                named_bar_sync(1, kGemmDeqWarps * 32);
-            }
-            for (int j = 0; j < 4; ++j) {
-                const int ks = 4 * g + j;
-                const int sa = ks % kSA;
-                if (ok && ks >= kSA) ok = mbar_wait_warp(a_empty(sa), ((ks / kSA) - 1) & 1, kErrGemmWait);
-                uint8_t *ast = smem + L.a + sa * kABytes;
-                if (ok) {
+                for (int j = 0; j < 4; ++j, ++ki) {
+                    const int sa = ki % kSA;
+                    if (ok && ki >= kSA) ok = mbar_wait_warp(a_empty(sa), ((ki / kSA) - 1) & 1, kErrGemmWait);
+                    uint8_t *ast = smem + L.a + sa * kABytes;
+                    if (ok) {
 #pragma unroll
-                    for (int pass = 0; pass < kGemmBM / (4 * kGemmDeqWarps); ++pass) {
-                        const int r = pass * 4 * kGemmDeqWarps + 4 * dw + rsub;
-                        uint4 v;
-                        if constexpr (kFmt == 8)
-                            v = deq8_q8_0(pst + r * kCB, j, c);
-                        else
-                            v = deq8_q4_k(pst + r * kCB, coef + r * 16, j, c);
-                        *reinterpret_cast<uint4 *>(ast + sw128_chunk_off(r, c)) = v;
+                        for (int pass = 0; pass < kGemmBM / (4 * kGemmDeqWarps); ++pass) {
+                            const int r = pass * 4 * kGemmDeqWarps + 4 * dw + rsub;
+                            uint4 v;
+                            if constexpr (kFmt == 8)
+                                v = deq8_q8_0(pst + r * kCB, j, c);
+                            else
+                                v = deq8_q4_k(pst + r * kCB, coef + r * 16, j, c);
+                            *reinterpret_cast<uint4 *>(ast + sw128_chunk_off(r, c)) = v;
+                        }
                     }
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(a_full(sa));
                 }
-                fence_async_smem();
+                if constexpr (kFmt == 4) named_bar_sync(1, kGemmDeqWarps * 32);  // coef reused next group
                 __syncwarp();
-                if (lane == 0) mbar_arrive(a_full(sa));
+                if (lane == 0) mbar_arrive(p_empty(sp));
             }
-            if constexpr (kFmt == 4) named_bar_sync(1, kGemmDeqWarps * 32);  // coef reused next group
-            __syncwarp();
-            if (lane == 0) mbar_arrive(p_empty(sp));
         }
-
-        // -------------------------------------------- epilogue: TMEM -> Y
-        mbar_wait_warp(acc_full, 0, kErrGemmWait);
-        tc_fence_after();
-        const int quarter = warp & 3;              // TMEM lanes 32*quarter .. +31
-        const int half = (warp - 2) >> 2;          // which 128 of the 256 columns
-        const int n = n0 + 32 * quarter + lane;
+    } else {
+        // ------------------------------------------------ epilogue: TMEM -> Y
+        const int quarter = warp & 3;  // this warp may read TMEM lanes 32*quarter .. +31
+        bool ok = true;
+        for (int lt = 0; lt < my_tiles; ++lt) {
+            const int buf = lt & 1, use = lt >> 1;
+            const int n0 = tile_n0(lt), m0 = tile_m0(lt);
+            if (ok) ok = mbar_wait_warp(acc_full(buf), use & 1, kErrGemmWait);
+            tc_fence_after();
+            const int n = n0 + 32 * quarter + lane;
+            if (ok) {
 #pragma unroll 1
-        for (int cb = 0; cb < kGemmBN / 2; cb += 32) {
-            const int col = half * (kGemmBN / 2) + cb;
-            uint32_t v[32];
-            tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)col, v);
-            if (n < p.N) {
+                for (int col = 0; col < kGemmBN; col += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(buf * kGemmBN + col), v);
+                    if (n < p.N) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int m = m0 + col + i;
-                    if (m < p.M) p.Y[(int64_t)m * p.N + n] = __uint_as_float(v[i]);
+                        for (int i = 0; i < 32; ++i) {
+                            const int m = m0 + col + i;
+                            if (m < p.M) p.Y[(int64_t)m * p.N + n] = __uint_as_float(v[i]);
+                        }
+                    }
                 }
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty(buf));
         }
     }
     tc_fence_before();
-    __syncthreads();
+    // no CTA leaves while a peer may still multicast into it or arrive on its
+    // barriers (every arrival precedes the peer's last accumulator commit)
+    if (kGemmCluster > 1) cluster_sync_all(); else __syncthreads();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
@@ -407,7 +500,6 @@ size_t gemm_workspace_bytes(int fmt, int M, int N, int K) {
 template <int kFmt>
 static cudaError_t launch_gemm_t(const void *W, const uint16_t *X, float *Y, int M, int N, int K,
                                  void *workspace, int sms, cudaStream_t stream) {
-    (void)sms;
     __half *Xh = static_cast<__half *>(workspace);
     const int64_t n8 = (int64_t)M * K / 8;
     int cgrid = (int)((n8 + 255) / 256);
@@ -418,7 +510,7 @@ static cudaError_t launch_gemm_t(const void *W, const uint16_t *X, float *Y, int
 
     CUtensorMap xmap, wmap;
     e = encode_tmap_2d(&xmap, Xh, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (uint64_t)K, (uint64_t)M,
-                       (uint64_t)K * 2, kGemmBK, kGemmBN, CU_TENSOR_MAP_SWIZZLE_128B);
+                       (uint64_t)K * 2, kGemmBK, kGemmBN / kGemmCluster, CU_TENSOR_MAP_SWIZZLE_128B);
     if (e != cudaSuccess) return e;
     constexpr int kCB = gemm_group_bytes(kFmt);
     const int64_t row_bytes = (int64_t)(K / kGroup) * kCB;
@@ -438,9 +530,23 @@ static cudaError_t launch_gemm_t(const void *W, const uint16_t *X, float *Y, int
     p.M = M;
     p.N = N;
     p.K = K;
-    dim3 grid((unsigned)((N + kGemmBM - 1) / kGemmBM), (unsigned)((M + kGemmBN - 1) / kGemmBN), 1);
-    gemm_kernel<kFmt><<<grid, kGemmThreads, L.total, stream>>>(xmap, wmap, p);
-    return cudaGetLastError();
+    const int tiles_n = (N + kGemmBM - 1) / kGemmBM;
+    const int units = ((tiles_n + kGemmCluster - 1) / kGemmCluster) * ((M + kGemmBN - 1) / kGemmBN);
+    int nclusters = sms / kGemmCluster;  // one persistent CTA per SM
+    if (units < nclusters) nclusters = units;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(nclusters * kGemmCluster), 1, 1);
+    cfg.blockDim = dim3(kGemmThreads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)L.total;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)kGemmCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<kFmt>, xmap, wmap, p);
 }
 
 cudaError_t launch_gemm(int fmt, const void *W, const uint16_t *X, float *Y, int M, int N, int K,
