@@ -73,6 +73,14 @@ __device__ __forceinline__ float round_quotient(float x, float D, float r) {
 __device__ __forceinline__ uint32_t int_byte(float v) {
     return __float_as_uint(__fadd_rn(v, 12582912.0f)) & 0xFFu;
 }
+// Four integral floats in [-128, 127] -> one word of bytes (v0 lowest).
+__device__ __forceinline__ uint32_t pack4_bytes(float v0, float v1, float v2, float v3) {
+    const uint32_t a = __float_as_uint(__fadd_rn(v0, 12582912.0f));
+    const uint32_t b = __float_as_uint(__fadd_rn(v1, 12582912.0f));
+    const uint32_t c = __float_as_uint(__fadd_rn(v2, 12582912.0f));
+    const uint32_t d = __float_as_uint(__fadd_rn(v3, 12582912.0f));
+    return prmt(prmt(a, b, 0x0040u), prmt(c, d, 0x0040u), 0x5410u);
+}
 
 template <bool kSrcF32>
 __device__ __forceinline__ void load32(const void *src, int64_t elem, float (&x)[32]) {
@@ -110,7 +118,15 @@ quantize_q8_0_kernel(const void *__restrict__ src, uint8_t *__restrict__ dst, in
             uint32_t w[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) w[i] = 0u;
-            if (df != 0.0f) {
+            if (df >= 6.103515625e-05f) {
+                // normal binary16 scale: |x / d16| <= 127 (1 + 2^-11) < 127.5,
+                // so round(x / d16) never needs the clamp
+                const float r = __frcp_rn(df);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    w[i] = pack4_bytes(round_quotient(x[4 * i], df, r), round_quotient(x[4 * i + 1], df, r),
+                                       round_quotient(x[4 * i + 2], df, r), round_quotient(x[4 * i + 3], df, r));
+            } else if (df != 0.0f) {  // subnormal scale: the quotient may pass 127.5
                 const float r = __frcp_rn(df);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
@@ -214,11 +230,10 @@ quantize_q4_k_kernel(const void *__restrict__ src, uint8_t *__restrict__ dst, in
         for (int i = 0; i < 8; ++i) w[i] = 0u;
         if (S > 0.0f) {
             const float r = __frcp_rn(S);
+            auto code = [&](int i) { return clamp_f(round_quotient(__fadd_rn(x[i], Mn), S, r), 0.0f, 15.0f); };
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float q = clamp_f(round_quotient(__fadd_rn(x[i], Mn), S, r), 0.0f, 15.0f);
-                w[i >> 2] |= int_byte(q) << (8 * (i & 3));
-            }
+            for (int i = 0; i < 8; ++i)
+                w[i] = pack4_bytes(code(4 * i), code(4 * i + 1), code(4 * i + 2), code(4 * i + 3));
         }
         // sub-block 2c (low nibbles) and 2c+1 (high nibbles) share chunk c
         uint32_t hw[8];
