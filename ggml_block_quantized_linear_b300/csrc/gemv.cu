@@ -153,17 +153,16 @@ __device__ __forceinline__ void q8_block(const uint8_t *r0, const uint8_t *r1, c
 }
 
 template <int kNT>
-__device__ __forceinline__ void q4k_half(const uint8_t *base, const uint8_t *r0, const uint8_t *r1,
+__device__ __forceinline__ void q4k_half(const uint8_t *base, int rstride, const uint8_t *r0, const uint8_t *r1,
                                          const __half *xr, int xstride, const float *xs, int li,
                                          float *cw, int lane, int g, int t, int gvalid, int kh,
                                          float (&acc)[kNT][4]) {
-    constexpr int kSlot = kQ4Bytes;
     constexpr int kMT = 8 * kNT;
     // per-row coefficients (a_j, b_j) of this half's 4 sub-blocks; lane
     // (row = lane / 2) decodes sub-blocks 4 kh + 2 (lane & 1) + {0, 1}
     {
         const int rr = lane >> 1;
-        const uint4 h = *reinterpret_cast<const uint4 *>(base + rr * kSlot);
+        const uint4 h = *reinterpret_cast<const uint4 *>(base + rr * rstride);
         const float dsc = h2f_bits(h.x), dmn = h2f_bits(h.x >> 16);
         auto sbyte = [&](int k) {  // scale byte k (selects, no local-memory array)
             const uint32_t w = k < 4 ? h.y : (k < 8 ? h.z : h.w);
@@ -365,7 +364,7 @@ gemv_kernel(const __grid_constant__ CUtensorMap wmap, const GemvParams p) {
                         q8_block<7, kNT>(r0, r1, xr, xstride, xs, li * 8 + 7, t, gvalid, acc);
                     }
                 } else {
-                    q4k_half<kNT>(base, r0, r1, xr, xstride, xs, li, cw, lane, g, t, gvalid, kh, acc);
+                    q4k_half<kNT>(base, kSlot, r0, r1, xr, xstride, xs, li, cw, lane, g, t, gvalid, kh, acc);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty_bar(s));

@@ -1,44 +1,68 @@
 // gemv_rows.cu -- decode matmul for M <= 8 tokens without thread-block
-// clusters: one CTA owns 16 weight rows over the whole K.
+// clusters: persistent CTAs, each owning whole 16-row tiles over all of K.
 //
-// Each CTA streams its tile with one 2-D tensor-map TMA copy (16 rows x 256
-// weights) per chunk into a deep ring (up to 16 / 32 stages), and eight
-// consumer warps take the chunks round-robin (chunk i -> warp i % 8).  The per-chunk arithmetic is the
-// one of gemv.cu (exact integer codes on m16n8k16 tensor-core MMAs, scales in
-// fp32 per 32-weight block).  The eight warps' partial sums are added in
-// shared memory in warp order, so the result is deterministic; there is no
-// cluster barrier, no distributed shared memory and no workspace.  Used when
-// the row count alone fills the GPU's SMs and the activations are few enough
-// (M <= 8) to restage cheaply per CTA.
+// CTA b takes the row tiles b, b + G, b + 2G, ... (G = grid size, at most
+// the number of CTAs resident on the GPU at once), so the weight stream of a
+// CTA runs on from one tile into the next without a CTA launch, a ring
+// refill or an activation restage in between.
+//  * Producer warp (one thread): first the activations (bf16, one 1-D bulk
+//    copy per token row), then one 2-D tensor-map TMA copy per stage of
+//    16 rows x 2 chunks of 256 weights (8.5 KB Q8_0, 4.5 KB Q4_K).  In shared
+//    memory a stage row is 544 / 288 bytes long, which puts the 8 rows read by
+//    one 64-bit load of a warp on distinct banks.
+//  * Eight consumer warps: chunk i of a tile goes to warp i mod 8, so the two
+//    chunks of a stage go to the warp pair (2p, 2p + 1), p = stage mod 4.
+//    Every pair has its own sub-ring of stages, so a stage is only ever
+//    reused by the warps that consumed it (an mbarrier parity wait cannot
+//    tell phase k from k + 2).  The activations are converted in place to
+//    binary16 once per CTA (when all of K fits; otherwise once per tile and
+//    window of K).  Per chunk: exact integer codes on m16n8k16 tensor-core
+//    MMAs, scales in fp32 per 32-weight block (see gemv.cu).
+//  * Reducer warp: at the end of a tile each consumer warp leaves its
+//    partial sums in a double-buffered shared array and moves on; the reducer
+//    adds the eight partials in warp order (deterministic) and stores the
+//    tile's outputs.  There is no cluster and no workspace.
+// Used when the row tiles alone fill the GPU's SMs and the activations are
+// few (M <= 8).
+#include <atomic>
+#include <mutex>
+
 #include "common.cuh"
 
 namespace qmm {
 
 constexpr int kRowsR = 16;
-constexpr int kWarpsR = 8;
-constexpr int kThreadsR = (kWarpsR + 1) * 32;
+constexpr int kWarpsR = 8;  // consumer warps
+constexpr int kPairsR = kWarpsR / 2;
+constexpr int kProdWarpR = kWarpsR, kRedWarpR = kWarpsR + 1;
+constexpr int kThreadsR = (kWarpsR + 2) * 32;
+constexpr int kYBufsR = 2;
+constexpr int kCoefStrideR = 20;  // floats per row of a warp's Q4_K coefficient table (padded)
+// Activations held in shared memory at once: M * window chunks <= 128
+// (64 KB of binary16).
+constexpr int kRowsXChunkBudget = 128;
 
 struct RowsLayout {
     int ring, xh, xs, coef, ypart, bars, total;
 };
 
-__host__ __device__ inline RowsLayout rows_layout(int fmt, int M, int stages, int win) {
-    const int slot = fmt == 8 ? kQ8GroupBytes : kQ4Bytes;
+__host__ __device__ inline RowsLayout rows_layout(int fmt, int M, int dpp, int win) {
+    const int cb = fmt == 8 ? kQ8GroupBytes : kQ4Bytes;
     RowsLayout L;
     int off = 0;
     L.ring = off;
-    off += stages * kRowsR * slot;
+    off += kPairsR * dpp * kRowsR * 2 * cb;  // a stage: 16 rows x 2 chunks (multiple of 128 bytes)
     L.xh = off;
-    off += M * (win * kGroup + 32) * 2;
+    off += M * (win * kGroup + 32) * 2;       // token rows, 32 halves of padding between them
     L.xs = off;
-    off += fmt == 4 ? win * 8 * 8 * 4 : 0;
+    off += fmt == 4 ? win * 8 * 8 * 4 : 0;    // Q4_K: sum of x per 32-block and token
     L.coef = off;
-    off += fmt == 4 ? kWarpsR * 16 * 8 * 4 : 0;
+    off += fmt == 4 ? kWarpsR * kRowsR * kCoefStrideR * 4 : 0;
     L.ypart = off;
-    off += kWarpsR * kRowsR * 8 * 4;
+    off += kYBufsR * kWarpsR * kRowsR * M * 4;
     off = (off + 15) & ~15;
     L.bars = off;
-    off += 2 * stages * 8;
+    off += (2 * kPairsR * dpp + 2 + 2 * kYBufsR) * 8;
     L.total = off;
     return L;
 }
@@ -48,19 +72,25 @@ struct RowsParams {
     const uint16_t *X;
     int M, N, K;
     int nchunks;  // K / 256
-    int stages;   // ring depth
-    int win;      // activation window in chunks (a multiple of 8, or nchunks)
+    int ntiles;   // ceil(N / 16)
+    int dpp;      // ring stages per warp pair
+    int win;      // activation window in chunks: nchunks, or a multiple of 8
 };
 
+// Convert the raw bf16 activations of a window, landed by TMA at xh (token m
+// at xh + m * xstride), in place to binary16 (round to nearest), each group
+// of 4 stored in the order (0, 2, 1, 3) so that one 16-byte load yields both
+// B fragments of an MMA; Q4_K also sums each 32-weight block per token.
 template <int kFmt>
-__device__ __forceinline__ void rows_stage_x(const RowsParams &p, __half *xh, float *xs, int xstride,
-                                             int w0, int wn, int tid) {
+__device__ __forceinline__ void rows_convert_x(int M, __half *xh, float *xs, int xstride, int wn,
+                                               int tid) {
     constexpr int kMT = 8;
-    const int ngr = (wn * kGroup) / 8;
-    const int kw = w0 * kGroup;
-    for (int idx = tid; idx < p.M * ngr; idx += kWarpsR * 32) {
-        const int m = idx / ngr, kg = idx - m * ngr;
-        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p.X + (int64_t)m * p.K + kw + 8 * kg));
+    const int ngr = (wn * kGroup) / 8;  // 8-element groups per token
+    int m = 0, kg = tid;
+    while (kg >= ngr && m < M) { kg -= ngr; ++m; }
+    for (; m < M;) {
+        uint4 *p = reinterpret_cast<uint4 *>(xh + m * xstride + 8 * kg);
+        const uint4 v = *p;
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
         float f[8];
 #pragma unroll
@@ -77,8 +107,9 @@ __device__ __forceinline__ void rows_stage_x(const RowsParams &p, __half *xh, fl
         o.y = *reinterpret_cast<const uint32_t *>(&h13);
         o.z = *reinterpret_cast<const uint32_t *>(&h46);
         o.w = *reinterpret_cast<const uint32_t *>(&h57);
-        *reinterpret_cast<uint4 *>(xh + m * xstride + 8 * kg) = o;
+        *p = o;
         if constexpr (kFmt == 4) {
+            // lanes 4j .. 4j + 3 hold one 32-weight block (ngr is a multiple of 32)
             const float2 s02 = __half22float2(h02), s13 = __half22float2(h13);
             const float2 s46 = __half22float2(h46), s57 = __half22float2(h57);
             float sum = ((s02.x + s13.x) + (s02.y + s13.y)) + ((s46.x + s57.x) + (s46.y + s57.y));
@@ -86,185 +117,426 @@ __device__ __forceinline__ void rows_stage_x(const RowsParams &p, __half *xh, fl
             sum += __shfl_xor_sync(0xffffffffu, sum, 2);
             if ((kg & 3) == 0) xs[(kg >> 2) * kMT + m] = sum;
         }
+        kg += kWarpsR * 32;
+        while (kg >= ngr && m < M) { kg -= ngr; ++m; }
     }
 }
 
-// One CTA per 16-row tile.  Chunk i of the tile goes to stage i % stages
-// and to consumer warp i % 8.
+// 8 code bytes at shared address p with p mod 8 == kMod8, as two words,
+// using 8-byte loads where the alignment allows.
+template <int kMod8>
+__device__ __forceinline__ void rq8_codes(const uint8_t *p, uint32_t &w0, uint32_t &w1) {
+    if constexpr (kMod8 == 0) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(p);
+        w0 = v.x;
+        w1 = v.y;
+    } else if constexpr (kMod8 == 4) {
+        w0 = *reinterpret_cast<const uint32_t *>(p);
+        w1 = *reinterpret_cast<const uint32_t *>(p + 4);
+    } else if constexpr (kMod8 == 2) {  // bytes 2..9 of [p - 2, p + 14)
+        const uint2 a = *reinterpret_cast<const uint2 *>(p - 2);
+        const uint2 b = *reinterpret_cast<const uint2 *>(p + 6);
+        w0 = __byte_perm(a.x, a.y, 0x5432);
+        w1 = __byte_perm(a.y, b.x, 0x5432);
+    } else {  // 6: bytes 2..9 of [p - 2, p + 10)
+        const uint32_t a = *reinterpret_cast<const uint32_t *>(p - 2);
+        const uint2 b = *reinterpret_cast<const uint2 *>(p + 2);
+        w0 = __byte_perm(a, b.x, 0x5432);
+        w1 = __byte_perm(b.x, b.y, 0x5432);
+    }
+}
+
+// One Q8_0 block (32 weights) of rows g and g + 8 (row bases r0, r1, 16-byte
+// aligned) against token g's binary16 activations at xb (if xvalid).
+template <int kB>
+__device__ __forceinline__ void rq8_block(const uint8_t *r0, const uint8_t *r1, const __half *xb, int t,
+                                          bool xvalid, float (&acc)[4]) {
+    constexpr int kOff = kQ8Bytes * kB + 2;
+    constexpr int kMod8 = kOff % 8;
+    const float d0 = h2f_bits(*reinterpret_cast<const uint16_t *>(r0 + kQ8Bytes * kB));
+    const float d1 = h2f_bits(*reinterpret_cast<const uint16_t *>(r1 + kQ8Bytes * kB));
+    uint32_t a0, a1, b0, b1;
+    rq8_codes<kMod8>(r0 + kOff + 8 * t, a0, a1);
+    rq8_codes<kMod8>(r1 + kOff + 8 * t, b0, b1);
+    a0 ^= 0x80808080u; a1 ^= 0x80808080u; b0 ^= 0x80808080u; b1 ^= 0x80808080u;
+    const uint32_t A0[4] = {q8_exact(q8_pair02(a0)), q8_exact(q8_pair02(b0)),
+                            q8_exact(q8_pair13(a0)), q8_exact(q8_pair13(b0))};
+    const uint32_t A1[4] = {q8_exact(q8_pair02(a1)), q8_exact(q8_pair02(b1)),
+                            q8_exact(q8_pair13(a1)), q8_exact(q8_pair13(b1))};
+    const uint4 xv = x_frag(xb + kQ8Weights * kB + 8 * t, xvalid);
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_f16_16816(c, A0, xv.x, xv.y);
+    mma_f16_16816(c, A1, xv.z, xv.w);
+    acc[0] = fmaf(d0, c[0], acc[0]);
+    acc[1] = fmaf(d0, c[1], acc[1]);
+    acc[2] = fmaf(d1, c[2], acc[2]);
+    acc[3] = fmaf(d1, c[3], acc[3]);
+}
+
+// Q4_K scale/min decode of one chunk (16 rows x 8 sub-blocks): lane r + 16 h
+// decodes row r, sub-blocks 4h .. 4h + 3, with word-parallel unpacking of the
+// 6-bit fields; writes (S_j * 2^24 or S_j * 2^20, -Mn_j) pairs to cw.
+__device__ __forceinline__ void rq4_coefs(const uint8_t *row0, int pitch, float *cw, int lane) {
+    const int r = lane & 15, h = lane >> 4;
+    const uint4 hd = *reinterpret_cast<const uint4 *>(row0 + r * pitch);
+    const float d = h2f_bits(hd.x), dmin = h2f_bits(hd.x >> 16);
+    const uint32_t sc = h ? ((hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u)) : (hd.y & 0x3F3F3F3Fu);
+    const uint32_t mc = h ? (((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u)) : (hd.z & 0x3F3F3F3Fu);
+    // byte b -> 2^23 + b as a float, then one fma: (2^23 + b) * s - 2^23 * s = b * s, exact
+    const float dlo = d * 16777216.0f, dhi = d * 1048576.0f;  // even / odd sub-block (low / high nibble)
+    float o[8];
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+        const float fs = __uint_as_float(__byte_perm(sc, 0x4B000000u, 0x7540 + jj));
+        const float fm = __uint_as_float(__byte_perm(mc, 0x4B000000u, 0x7540 + jj));
+        const float ds = (jj & 1) ? dhi : dlo;
+        o[2 * jj] = fmaf(fs, ds, -8388608.0f * ds);
+        o[2 * jj + 1] = fmaf(fm, -dmin, 8388608.0f * dmin);
+    }
+    float4 *dst = reinterpret_cast<float4 *>(cw + r * kCoefStrideR + 8 * h);
+    dst[0] = make_float4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+}
+
+// 64 weights (sub-blocks 2c, 2c + 1) of rows g and g + 8 of a Q4_K chunk.
+template <int kC>
+__device__ __forceinline__ void rq4_group(const uint8_t *r0, const uint8_t *r1, const __half *xb,
+                                          const float *xsb, const float *cw, int g, int t, bool xvalid,
+                                          float (&acc)[4]) {
+    const uint2 qa = *reinterpret_cast<const uint2 *>(r0 + 16 + 32 * kC + 8 * t);
+    const uint2 qb = *reinterpret_cast<const uint2 *>(r1 + 16 + 32 * kC + 8 * t);
+    const float4 ca = *reinterpret_cast<const float4 *>(cw + g * kCoefStrideR + 4 * kC);
+    const float4 cb = *reinterpret_cast<const float4 *>(cw + (g + 8) * kCoefStrideR + 4 * kC);
+    const uint32_t qa0s = qa.x >> 8, qa1s = qa.y >> 8, qb0s = qb.x >> 8, qb1s = qb.y >> 8;
+    // masked nibble pairs are binary16 subnormals: q * 2^-24 (low), q * 2^-20 (high)
+    const uint32_t L0[4] = {qa.x & 0x000F000Fu, qb.x & 0x000F000Fu, qa0s & 0x000F000Fu, qb0s & 0x000F000Fu};
+    const uint32_t L1[4] = {qa.y & 0x000F000Fu, qb.y & 0x000F000Fu, qa1s & 0x000F000Fu, qb1s & 0x000F000Fu};
+    const uint32_t H0[4] = {qa.x & 0x00F000F0u, qb.x & 0x00F000F0u, qa0s & 0x00F000F0u, qb0s & 0x00F000F0u};
+    const uint32_t H1[4] = {qa.y & 0x00F000F0u, qb.y & 0x00F000F0u, qa1s & 0x00F000F0u, qb1s & 0x00F000F0u};
+    const __half *xq = xb + 64 * kC + 8 * t;
+    const uint4 xl = x_frag(xq, xvalid);
+    const uint4 xhv = x_frag(xq + 32, xvalid);
+    float cl[4] = {0.f, 0.f, 0.f, 0.f}, chh[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_f16_16816(cl, L0, xl.x, xl.y);
+    mma_f16_16816(cl, L1, xl.z, xl.w);
+    mma_f16_16816(chh, H0, xhv.x, xhv.y);
+    mma_f16_16816(chh, H1, xhv.z, xhv.w);
+    const float2 sl = *reinterpret_cast<const float2 *>(xsb + (2 * kC) * 8 + 2 * t);
+    const float2 sh = *reinterpret_cast<const float2 *>(xsb + (2 * kC + 1) * 8 + 2 * t);
+    acc[0] = fmaf(ca.w, sh.x, fmaf(ca.y, sl.x, fmaf(ca.z, chh[0], fmaf(ca.x, cl[0], acc[0]))));
+    acc[1] = fmaf(ca.w, sh.y, fmaf(ca.y, sl.y, fmaf(ca.z, chh[1], fmaf(ca.x, cl[1], acc[1]))));
+    acc[2] = fmaf(cb.w, sh.x, fmaf(cb.y, sl.x, fmaf(cb.z, chh[2], fmaf(cb.x, cl[2], acc[2]))));
+    acc[3] = fmaf(cb.w, sh.y, fmaf(cb.y, sl.y, fmaf(cb.z, chh[3], fmaf(cb.x, cl[3], acc[3]))));
+}
+
 template <int kFmt>
-__global__ void __launch_bounds__(kThreadsR)
+__global__ void __launch_bounds__(kThreadsR, 3)
 gemv_rows_kernel(const __grid_constant__ CUtensorMap wmap, const RowsParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int kCB = kFmt == 8 ? kQ8GroupBytes : kQ4Bytes;
-    constexpr int kNT = 1;
-    constexpr int kMT = 8;
+    constexpr int kPitch = 2 * kCB;               // stage row: two chunks
+    constexpr int kStage = kRowsR * kPitch;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int row0 = blockIdx.x * kRowsR;
-    const int nch = p.nchunks;
-    const int xstride = p.win * kGroup + 32;
-    const RowsLayout L = rows_layout(kFmt, p.M, p.stages, p.win);
+    const int nch = p.nchunks, dpp = p.dpp, win = p.win, M = p.M;
+    const bool resident = win >= nch;  // activations staged once per CTA
+    const int xstride = win * kGroup + 32;
+    const RowsLayout L = rows_layout(kFmt, M, dpp, win);
     uint8_t *ring = smem + L.ring;
     __half *xh = reinterpret_cast<__half *>(smem + L.xh);
     float *xs = reinterpret_cast<float *>(smem + L.xs);
-    float *coef = reinterpret_cast<float *>(smem + L.coef);
     float *ypart = reinterpret_cast<float *>(smem + L.ypart);
+    const int nst = kPairsR * dpp;
     const uint32_t bar0 = smem_addr(smem + L.bars);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (p.stages + s); };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (nst + s); };
+    const uint32_t xfull = bar0 + 16u * nst, xempty = xfull + 8u;
+    const uint32_t yfull0 = xempty + 8u, yempty0 = yfull0 + 8u * kYBufsR;
 
     if (tid == 0) {
-        for (int s = 0; s < p.stages; ++s) {
+        for (int s = 0; s < nst; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
+            mbar_init(empty_bar(s), 2);
+        }
+        mbar_init(xfull, 1);
+        mbar_init(xempty, kWarpsR);
+        for (int b = 0; b < kYBufsR; ++b) {
+            mbar_init(yfull0 + 8u * b, kWarpsR);
+            mbar_init(yempty0 + 8u * b, 1);
         }
         fence_mbar_init();
     }
+    // block sums of padding tokens (m >= M) stay zero for the whole kernel
     if constexpr (kFmt == 4)
-        for (int idx = tid; idx < p.win * 8 * kMT; idx += kThreadsR) xs[idx] = 0.f;
-    if (warp == kWarpsR && lane == 0) {
-        // descriptor fetch and L2 prefetch of the first stages (safe before
-        // the dependency wait: nothing lands in shared memory)
+        for (int idx = tid; idx < win * 8 * 8; idx += kThreadsR) xs[idx] = 0.f;
+    if (warp == kProdWarpR && lane == 0) {
+        // descriptor fetch and L2 prefetch of the first tile's leading stages
+        // (safe before the dependency wait: nothing lands in shared memory)
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wmap)) : "memory");
-        for (int i = 0; i < nch && i < p.stages; ++i) tma_prefetch_l2_2d(&wmap, i * (kCB / 2), row0);
+        for (int j = 0; 2 * j < nch && j < nst; ++j)
+            tma_prefetch_l2_2d(&wmap, 2 * j * (kCB / 8), (int)blockIdx.x * kRowsR);
     }
     __syncthreads();
     // programmatic dependent launch: see gemv.cu
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-    if (warp == kWarpsR) {
-        // ---------------- producer
+    if (warp == kProdWarpR) {
+        // ---------------- producer (one thread)
         if (lane == 0) {
-            for (int i = 0; i < nch; ++i) {
-                const int s = i % p.stages;
-                if (i >= p.stages && !mbar_wait(empty_bar(s), ((i / p.stages) - 1) & 1, kErrGemvEmptyWait))
-                    break;  // bug path: consumers then time out on their full barriers
-                mbar_arrive_expect_tx(full_bar(s), (uint32_t)(kRowsR * kCB));
-                tma_load_2d(smem_addr(ring + s * kRowsR * kCB), &wmap, i * (kCB / 2), row0, full_bar(s));
+            bool ok = true;
+            int xseq = 0;
+            int dpos[kPairsR] = {0, 0, 0, 0}, ph[kPairsR] = {0, 0, 0, 0};
+            bool lap[kPairsR] = {false, false, false, false};  // slot used before
+            for (int tile = blockIdx.x; ok && tile < p.ntiles; tile += gridDim.x) {
+                const int row0 = tile * kRowsR;
+                for (int w0 = 0; ok && w0 < nch; w0 += win) {
+                    const int wn = min(win, nch - w0);
+                    if (!resident || xseq == 0) {
+                        // the previous window must be fully read before it is overwritten
+                        if (xseq > 0 && !mbar_wait(xempty, (xseq - 1) & 1, kErrGemvEmptyWait)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(xfull, (uint32_t)(M * wn * kGroup * 2));
+                        for (int m = 0; m < M; ++m)
+                            bulk_g2s(smem_addr(xh + m * xstride), p.X + (int64_t)m * p.K + w0 * kGroup,
+                                     (uint32_t)(wn * kGroup * 2), xfull);
+                        ++xseq;
+                    }
+                    const int j_end = (w0 + wn + 1) / 2;  // stages of the tile up to this window's end
+                    for (int j0 = w0 / 2; ok && j0 < j_end; j0 += kPairsR) {
+#pragma unroll
+                        for (int pp = 0; pp < kPairsR; ++pp) {
+                            if (ok && j0 + pp < j_end) {
+                                const int s = pp + kPairsR * dpos[pp];
+                                if (lap[pp] && !mbar_wait(empty_bar(s), ph[pp] ^ 1, kErrGemvEmptyWait)) {
+                                    ok = false;  // bug path: consumers then time out on their full barriers
+                                } else {
+                                    // a box may run past K (zero filled); its bytes all count
+                                    mbar_arrive_expect_tx(full_bar(s), (uint32_t)kStage);
+                                    tma_load_2d(smem_addr(ring + s * kStage), &wmap, 2 * (j0 + pp) * (kCB / 8),
+                                                row0, full_bar(s));
+                                    if (++dpos[pp] == dpp) {
+                                        dpos[pp] = 0;
+                                        ph[pp] ^= 1;
+                                        lap[pp] = true;
+                                    }
+                                }
+                            }
+                        }
+                    }
+                }
             }
+        }
+    } else if (warp == kRedWarpR) {
+        // ---------------- reducer: fixed-order sum of the eight partials of a tile
+        bool ok = true;
+        int u = 0;
+        for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x, ++u) {
+            const int b = u & (kYBufsR - 1);
+            const uint32_t yf = yfull0 + 8u * b, ye = yempty0 + 8u * b;
+            if (ok) ok = mbar_wait_warp(yf, (u / kYBufsR) & 1, kErrGemvFullWait);
+            if (!ok) continue;
+            const float *yb = ypart + b * (kWarpsR * kRowsR * M);
+            const int row0 = tile * kRowsR;
+            for (int idx = lane; idx < kRowsR * M; idx += 32) {
+                const int r = idx / M, m = idx - r * M;
+                if (row0 + r < p.N) {
+                    float sum = 0.f;
+#pragma unroll
+                    for (int w = 0; w < kWarpsR; ++w) sum += yb[(w * kRowsR + r) * M + m];
+                    p.Y[(int64_t)m * p.N + row0 + r] = sum;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(ye);
         }
     } else {
-        // ---------------- consumers: warp w takes chunks w, w + 8, ...
+        // ---------------- consumers: warp w takes chunks w, w + 8, ... of every tile
         const int g = lane >> 2, t = lane & 3;
-        float acc[kNT][4] = {{0.f, 0.f, 0.f, 0.f}};
+        const int pr = warp >> 1, hb = warp & 1;
         const __half *xrow = xh + g * xstride;
-        const int gvalid = p.M - g;
-        float *cw = coef + warp * 16 * 8;
+        const bool xvalid = g < M;
+        float *cw = reinterpret_cast<float *>(smem + L.coef) + warp * kRowsR * kCoefStrideR;
         bool ok = true;  // warp-uniform, see gemv.cu
-        for (int w0 = 0; w0 < nch; w0 += p.win) {
-            const int wn = min(p.win, nch - w0);
-            if (w0 > 0) named_bar_sync(1, kWarpsR * 32);
-            rows_stage_x<kFmt>(p, xh, xs, xstride, w0, wn, tid);
-            named_bar_sync(1, kWarpsR * 32);
-            for (int i = w0 + warp; i < w0 + wn; i += kWarpsR) {
-                const int s = i % p.stages, li = i - w0;
-                if (ok) ok = mbar_wait_warp(full_bar(s), (i / p.stages) & 1, kErrGemvFullWait);
-                if (!ok) continue;
-                const uint8_t *base = ring + s * kRowsR * kCB;
-                const uint8_t *r0 = base + g * kCB;
-                const uint8_t *r1 = base + (g + 8) * kCB;
-                const __half *xr = xrow + li * kGroup;
-                if constexpr (kFmt == 8) {
-                    q8_block<0, kNT>(r0, r1, xr, xstride, xs, li * 8 + 0, t, gvalid, acc);
-                    q8_block<1, kNT>(r0, r1, xr, xstride, xs, li * 8 + 1, t, gvalid, acc);
-                    q8_block<2, kNT>(r0, r1, xr, xstride, xs, li * 8 + 2, t, gvalid, acc);
-                    q8_block<3, kNT>(r0, r1, xr, xstride, xs, li * 8 + 3, t, gvalid, acc);
-                    q8_block<4, kNT>(r0, r1, xr, xstride, xs, li * 8 + 4, t, gvalid, acc);
-                    q8_block<5, kNT>(r0, r1, xr, xstride, xs, li * 8 + 5, t, gvalid, acc);
-                    q8_block<6, kNT>(r0, r1, xr, xstride, xs, li * 8 + 6, t, gvalid, acc);
-                    q8_block<7, kNT>(r0, r1, xr, xstride, xs, li * 8 + 7, t, gvalid, acc);
-                } else {
-                    q4k_half<kNT>(base, r0, r1, xr, xstride, xs, li, cw, lane, g, t, gvalid, 0, acc);
-                    q4k_half<kNT>(base, r0, r1, xr, xstride, xs, li, cw, lane, g, t, gvalid, 1, acc);
+        int dpos = 0, ph = 0, xseq = 0, u = 0;
+        for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x, ++u) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int w0 = 0; w0 < nch; w0 += win) {
+                const int wn = min(win, nch - w0);
+                if (!resident || xseq == 0) {
+                    if (ok) ok = mbar_wait_warp(xfull, xseq & 1, kErrGemvFullWait);
+                    if (ok) rows_convert_x<kFmt>(M, xh, xs, xstride, wn, tid);
+                    named_bar_sync(1, kWarpsR * 32);
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(empty_bar(s));
+                const int j_end = (w0 + wn + 1) / 2;
+                for (int j = w0 / 2 + pr; j < j_end; j += kPairsR) {
+                    const int s = pr + kPairsR * dpos;
+                    // both warps of the pair wait for the data before releasing
+                    // the stage, also when this warp's chunk is past K
+                    if (ok) ok = mbar_wait_warp(full_bar(s), ph, kErrGemvFullWait);
+                    const int i = 2 * j + hb;
+                    if (ok && i < w0 + wn) {
+                        const int li = i - w0;
+                        const uint8_t *cbase = ring + s * kStage + hb * kCB;  // row r at cbase + r * kPitch
+                        const uint8_t *r0 = cbase + g * kPitch;
+                        const uint8_t *r1 = cbase + (g + 8) * kPitch;
+                        const __half *xb = xrow + li * kGroup;
+                        if constexpr (kFmt == 8) {
+                            rq8_block<0>(r0, r1, xb, t, xvalid, acc);
+                            rq8_block<1>(r0, r1, xb, t, xvalid, acc);
+                            rq8_block<2>(r0, r1, xb, t, xvalid, acc);
+                            rq8_block<3>(r0, r1, xb, t, xvalid, acc);
+                            rq8_block<4>(r0, r1, xb, t, xvalid, acc);
+                            rq8_block<5>(r0, r1, xb, t, xvalid, acc);
+                            rq8_block<6>(r0, r1, xb, t, xvalid, acc);
+                            rq8_block<7>(r0, r1, xb, t, xvalid, acc);
+                        } else {
+                            rq4_coefs(cbase, kPitch, cw, lane);
+                            __syncwarp();
+                            const float *xsb = xs + li * 8 * 8;
+                            rq4_group<0>(r0, r1, xb, xsb, cw, g, t, xvalid, acc);
+                            rq4_group<1>(r0, r1, xb, xsb, cw, g, t, xvalid, acc);
+                            rq4_group<2>(r0, r1, xb, xsb, cw, g, t, xvalid, acc);
+                            rq4_group<3>(r0, r1, xb, xsb, cw, g, t, xvalid, acc);
+                        }
+                    }
+                    __syncwarp();
+                    if (ok && lane == 0) mbar_arrive(empty_bar(s));
+                    if (++dpos == dpp) {
+                        dpos = 0;
+                        ph ^= 1;
+                    }
+                }
+                if (!resident) {
+                    // this warp is done with the window's activations
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(xempty);
+                }
+                ++xseq;
             }
-        }
-        float *yp = ypart + warp * kRowsR * kMT;
-        *reinterpret_cast<float2 *>(yp + g * kMT + 2 * t) = make_float2(acc[0][0], acc[0][1]);
-        *reinterpret_cast<float2 *>(yp + (g + 8) * kMT + 2 * t) = make_float2(acc[0][2], acc[0][3]);
-        named_bar_sync(1, kWarpsR * 32);
-        // fixed-order sum of the eight warps' partials
-        for (int idx = tid; idx < kRowsR * p.M; idx += kWarpsR * 32) {
-            const int r = idx / p.M, m = idx - r * p.M;
-            if (row0 + r < p.N) {
-                float sum = 0.f;
-#pragma unroll
-                for (int w = 0; w < kWarpsR; ++w) sum += ypart[(w * kRowsR + r) * kMT + m];
-                p.Y[(int64_t)m * p.N + row0 + r] = sum;
+            // hand the tile's partial sums to the reducer
+            const int b = u & (kYBufsR - 1);
+            if (ok && u >= kYBufsR)
+                ok = mbar_wait_warp(yempty0 + 8u * b, ((u / kYBufsR) - 1) & 1, kErrGemvEmptyWait);
+            float *yp = ypart + (b * kWarpsR + warp) * kRowsR * M;
+            if (2 * t < M) {
+                yp[g * M + 2 * t] = acc[0];
+                yp[(g + 8) * M + 2 * t] = acc[2];
             }
+            if (2 * t + 1 < M) {
+                yp[g * M + 2 * t + 1] = acc[1];
+                yp[(g + 8) * M + 2 * t + 1] = acc[3];
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(yfull0 + 8u * b);
         }
     }
-}
-
-#ifndef QMM_ROWS_CARVEOUT  // preferred shared-memory carveout in %, -1 = driver default
-#define QMM_ROWS_CARVEOUT -1
-#endif
-#ifndef QMM_ROWS_MAX_STAGES_Q8
-#define QMM_ROWS_MAX_STAGES_Q8 16
-#endif
-#ifndef QMM_ROWS_MAX_STAGES_Q4
-#define QMM_ROWS_MAX_STAGES_Q4 32
-#endif
-
-// Ring depth.  Chunk i goes to warp i % 8 and stage i % stages; a stage may
-// only be reused by the warp that used it before (an mbarrier parity wait
-// cannot tell phase k from phase k + 2), so the depth is a multiple of 8:
-// 16 (Q8_0) or 32 (Q4_K), lowered (to at least 8) until the grid fits one
-// wave of resident CTAs; one CTA per tile (a persistent loop over tiles
-// measured slower on the decode shapes).
-bool gemv_rows_plan(int fmt, int M, int N, int K, int sms, RowsParams &p, int &smem, int &grid) {
-    const int nch = K / kGroup;
-    const int ntiles = (N + kRowsR - 1) / kRowsR;
-    // window: all of K while M * K <= 64 chunks of binary16 (32 KB), else the
-    // largest multiple of 8 chunks within that budget (at least 8)
-    int win = nch;
-    if (M * nch > 64) {
-        win = (64 / M) / 8 * 8;
-        if (win < 8) win = 8;
-    }
-    int st = fmt == 8 ? QMM_ROWS_MAX_STAGES_Q8 : QMM_ROWS_MAX_STAGES_Q4;
-    while (true) {
-        const int sm = rows_layout(fmt, M, st, win).total;
-        const int by_smem = (227 * 1024) / (sm + 1024);
-        const int by_warps = 64 / (kThreadsR / 32);
-        const int per_sm = by_smem < by_warps ? by_smem : by_warps;
-        if (st <= 8 || ntiles <= sms * per_sm) break;
-        st -= 8;
-    }
-    p.stages = st;
-    p.win = win;
-    smem = rows_layout(fmt, M, st, win).total;
-    grid = ntiles;
-    return true;
 }
 
 template <int kFmt>
-static cudaError_t launch_rows_t(const void *W, const RowsParams &p, int smem, int grid,
-                                 cudaStream_t stream) {
+static cudaError_t rows_set_attrs(int dev) {
+    static std::atomic<uint64_t> done{0};  // one bit per device: the attribute is per context
+    const uint64_t bit = 1ull << (dev & 63);
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(gemv_rows_kernel<kFmt>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
+
+// Resident CTAs per SM for a given dynamic shared-memory size (registers,
+// threads and shared memory all counted by the runtime).
+template <int kFmt>
+static int rows_occupancy(int smem) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemv_rows_kernel<kFmt>, kThreadsR,
+                                                      (size_t)smem) != cudaSuccess)
+        return 1;
+    return n < 1 ? 1 : n;
+}
+
+#ifndef QMM_ROWS_FORCE_DPP  // 0: chosen by the plan
+#define QMM_ROWS_FORCE_DPP 0
+#endif
+#ifndef QMM_ROWS_MAX_DPP
+#define QMM_ROWS_MAX_DPP 4
+#endif
+
+struct RowsPlan {
+    int dev, M, K, dpp, win, smem, occ;
+};
+
+// Plan for (M, K): activation window (all of K when M * chunks fits the
+// budget), then the sub-ring depth per warp pair with the most weight bytes
+// in flight per SM (resident CTAs x ring bytes), preferring more resident
+// CTAs on ties.
+template <int kFmt>
+static RowsPlan rows_plan_compute(int dev, int M, int K) {
     constexpr int kCB = kFmt == 8 ? kQ8GroupBytes : kQ4Bytes;
+    const int nch = K / kGroup;
+    int win = nch;
+    if (M * nch > kRowsXChunkBudget) {
+        win = (kRowsXChunkBudget / M) / 8 * 8;
+        if (win < 8) win = 8;
+    }
+    RowsPlan best{dev, M, K, 0, win, 0, 0};
+    long best_bytes = -1;
+    for (int d = 1; d <= QMM_ROWS_MAX_DPP; ++d) {
+        if (QMM_ROWS_FORCE_DPP > 0 && d != QMM_ROWS_FORCE_DPP) continue;
+        const int sm = rows_layout(kFmt, M, d, win).total;
+        if (sm > 227 * 1024) break;
+        const int occ = rows_occupancy<kFmt>(sm);
+        const long bytes = (long)occ * kPairsR * d * kRowsR * 2 * kCB;
+        if (bytes > best_bytes || (bytes == best_bytes && occ > best.occ)) {
+            best_bytes = bytes;
+            best = RowsPlan{dev, M, K, d, win, sm, occ};
+        }
+    }
+    return best;
+}
+
+// The plan depends on (device, M, K) only; it is computed once (the
+// occupancy queries cost host time) and kept in a small table.
+template <int kFmt>
+static RowsPlan rows_plan(int dev, int M, int K) {
+    static std::mutex mu;
+    static RowsPlan table[64];
+    static int count = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < count; ++i)
+        if (table[i].dev == dev && table[i].M == M && table[i].K == K) return table[i];
+    const RowsPlan pl = rows_plan_compute<kFmt>(dev, M, K);
+    table[count < 64 ? count++ : (int)(((unsigned)M * 31u + (unsigned)K) % 64u)] = pl;
+    return pl;
+}
+
+template <int kFmt>
+static cudaError_t launch_rows_t(const void *W, RowsParams &p, int sms, cudaStream_t stream) {
+    constexpr int kCB = kFmt == 8 ? kQ8GroupBytes : kQ4Bytes;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = rows_set_attrs<kFmt>(dev);
+    if (e != cudaSuccess) return e;
+    const RowsPlan pl = rows_plan<kFmt>(dev, p.M, p.K);
+    if (pl.dpp == 0) return cudaErrorInvalidConfiguration;  // no plan fits shared memory
+    p.nchunks = p.K / kGroup;
+    p.ntiles = (p.N + kRowsR - 1) / kRowsR;
+    p.dpp = pl.dpp;
+    p.win = pl.win;
+    const long cap = (long)sms * pl.occ;
+    const int grid = (int)(p.ntiles < cap ? p.ntiles : cap);
+    // the matrix as 8-byte elements; a box is 16 rows x 2 chunks
     const int64_t row_bytes = (int64_t)p.nchunks * kCB;
     CUtensorMap wmap;
-    cudaError_t e = encode_tmap_2d(&wmap, W, CU_TENSOR_MAP_DATA_TYPE_UINT16, (uint64_t)(row_bytes / 2),
-                                   (uint64_t)p.N, (uint64_t)row_bytes, kCB / 2, kRowsR);
+    e = encode_tmap_2d(&wmap, W, CU_TENSOR_MAP_DATA_TYPE_UINT64, (uint64_t)(row_bytes / 8),
+                       (uint64_t)p.N, (uint64_t)row_bytes, (uint32_t)(2 * kCB / 8), kRowsR);
     if (e != cudaSuccess) return e;
-    static bool attr_set = false;
-    if (!attr_set) {
-        e = cudaFuncSetAttribute(gemv_rows_kernel<kFmt>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 227 * 1024);
-        if (e != cudaSuccess) return e;
-#if QMM_ROWS_CARVEOUT >= 0
-        e = cudaFuncSetAttribute(gemv_rows_kernel<kFmt>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 QMM_ROWS_CARVEOUT);
-        if (e != cudaSuccess) return e;
-#endif
-        attr_set = true;
-    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
     cfg.blockDim = dim3(kThreadsR, 1, 1);
-    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.dynamicSmemBytes = (size_t)pl.smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -282,11 +554,7 @@ cudaError_t launch_gemv_rows(int fmt, const void *W, const uint16_t *X, float *Y
     p.M = M;
     p.N = N;
     p.K = K;
-    p.nchunks = K / kGroup;
-    int smem = 0, grid = 1;
-    gemv_rows_plan(fmt, M, N, K, sms, p, smem, grid);
-    return fmt == 8 ? launch_rows_t<8>(W, p, smem, grid, stream)
-                    : launch_rows_t<4>(W, p, smem, grid, stream);
+    return fmt == 8 ? launch_rows_t<8>(W, p, sms, stream) : launch_rows_t<4>(W, p, sms, stream);
 }
 
 }  // namespace qmm

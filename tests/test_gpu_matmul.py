@@ -39,6 +39,20 @@ def test_decode_small_full(fmt, n, k, m):
     check_matmul(run(fmt, packed, xb, n), Y, A, "fmt=%d n=%d k=%d m=%d" % (fmt, n, k, m))
 
 
+# Shapes with at least one 16-row tile per SM take the persistent row-tile
+# kernel (M <= 8): one chunk per tile (seven idle consumer warps), a chunk
+# count that is not a multiple of 8, more tiles than resident CTAs (CTAs
+# loop over tiles), activations too many to hold at once (windows of K, with
+# a one-chunk last window), and a ragged last tile.
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("n,k,m", [(2369, 256, 1), (2369, 256, 8), (9999, 1280, 2), (9999, 1280, 8),
+                                   (3000, 4352, 5), (3000, 4352, 8), (12000, 4352, 8), (10000, 2304, 3)])
+def test_decode_row_tiles_full(fmt, n, k, m):
+    packed, xb = problem(fmt, n, k, m, 2000 + n + k + m)
+    Y, A = oracle.matmul(fmt, packed, xb, n, k)
+    check_matmul(run(fmt, packed, xb, n), Y, A, "fmt=%d n=%d k=%d m=%d" % (fmt, n, k, m))
+
+
 @pytest.mark.parametrize("fmt", FMTS)
 def test_tiny_linear_config(fmt):
     # fp32 W 256 x 512 quantized, X bf16 1 x 512
