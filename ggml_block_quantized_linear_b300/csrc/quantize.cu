@@ -60,11 +60,22 @@ __device__ __forceinline__ float clamp_f(float v, float lo, float hi) {
 // within 2^-14 of a half-integer (|t| * 2^-21 < 2^-14 while |t| <= 128),
 // where the exact division decides.  Callers clamp the result to a range
 // inside [-128, 128]: beyond it, both ways clamp to the same code.
+//
+// The block quantizers apply this per block: every code takes the fast
+// path, the largest |t - k| of the block is kept, and only a block where it
+// reaches 0.5 - 2^-14 (a possible tie) is recomputed with exact divisions --
+// one branch per block instead of one per weight.
+constexpr float kTieGuard = 0.49993896484375f;  // 0.5 - 2^-14
+__device__ __forceinline__ float rint_quotient(float x, float r, float &dev) {
+    const float t = __fmul_rn(x, r);
+    const float k = rintf(t);
+    dev = fmaxf(dev, fabsf(__fsub_rn(t, k)));
+    return k;
+}
 __device__ __forceinline__ float round_quotient(float x, float D, float r) {
     const float t = __fmul_rn(x, r);
     const float k = rintf(t);
-    if (fabsf(__fsub_rn(t, k)) >= 0.49993896484375f)  // 0.5 - 2^-14
-        return roundf(__fdiv_rn(x, D));
+    if (fabsf(__fsub_rn(t, k)) >= kTieGuard) return roundf(__fdiv_rn(x, D));
     return k;
 }
 
@@ -122,10 +133,17 @@ quantize_q8_0_kernel(const void *__restrict__ src, uint8_t *__restrict__ dst, in
                 // normal binary16 scale: |x / d16| <= 127 (1 + 2^-11) < 127.5,
                 // so round(x / d16) never needs the clamp
                 const float r = __frcp_rn(df);
+                float dev = 0.0f;
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
-                    w[i] = pack4_bytes(round_quotient(x[4 * i], df, r), round_quotient(x[4 * i + 1], df, r),
-                                       round_quotient(x[4 * i + 2], df, r), round_quotient(x[4 * i + 3], df, r));
+                    w[i] = pack4_bytes(rint_quotient(x[4 * i], r, dev), rint_quotient(x[4 * i + 1], r, dev),
+                                       rint_quotient(x[4 * i + 2], r, dev), rint_quotient(x[4 * i + 3], r, dev));
+                if (dev >= kTieGuard) {  // a possible tie: exact divisions for the block
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        w[i] = pack4_bytes(roundf(__fdiv_rn(x[4 * i], df)), roundf(__fdiv_rn(x[4 * i + 1], df)),
+                                           roundf(__fdiv_rn(x[4 * i + 2], df)), roundf(__fdiv_rn(x[4 * i + 3], df)));
+                }
             } else if (df != 0.0f) {  // subnormal scale: the quotient may pass 127.5
                 const float r = __frcp_rn(df);
 #pragma unroll
@@ -184,8 +202,11 @@ dequantize_q8_0_kernel(const uint8_t *__restrict__ src, float *__restrict__ dst,
 // One lane quantizes one 32-weight sub-block; 8 lanes make a superblock and
 // a warp covers 4 superblocks (1024 weights, 576 packed bytes) per
 // iteration.
+#ifndef QMM_Q4_QUANT_MIN_BLOCKS  // resident CTAs per SM the register budget must allow
+#define QMM_Q4_QUANT_MIN_BLOCKS 4
+#endif
 template <bool kSrcF32>
-__global__ void __launch_bounds__(kQuantThreads)
+__global__ void __launch_bounds__(kQuantThreads, QMM_Q4_QUANT_MIN_BLOCKS)
 quantize_q4_k_kernel(const void *__restrict__ src, uint8_t *__restrict__ dst, int64_t nsuper) {
     __shared__ __align__(16) uint8_t stage[kQuantWarps][4 * kQ4Bytes];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -230,10 +251,17 @@ quantize_q4_k_kernel(const void *__restrict__ src, uint8_t *__restrict__ dst, in
         for (int i = 0; i < 8; ++i) w[i] = 0u;
         if (S > 0.0f) {
             const float r = __frcp_rn(S);
-            auto code = [&](int i) { return clamp_f(round_quotient(__fadd_rn(x[i], Mn), S, r), 0.0f, 15.0f); };
+            float dev = 0.0f;
+            auto code = [&](int i) { return clamp_f(rint_quotient(__fadd_rn(x[i], Mn), r, dev), 0.0f, 15.0f); };
 #pragma unroll
             for (int i = 0; i < 8; ++i)
                 w[i] = pack4_bytes(code(4 * i), code(4 * i + 1), code(4 * i + 2), code(4 * i + 3));
+            if (dev >= kTieGuard) {  // a possible tie: exact divisions for the sub-block
+                auto exact = [&](int i) { return clamp_f(roundf(__fdiv_rn(__fadd_rn(x[i], Mn), S)), 0.0f, 15.0f); };
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    w[i] = pack4_bytes(exact(4 * i), exact(4 * i + 1), exact(4 * i + 2), exact(4 * i + 3));
+            }
         }
         // sub-block 2c (low nibbles) and 2c+1 (high nibbles) share chunk c
         uint32_t hw[8];
