@@ -155,6 +155,16 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int x
                  : "memory");
 }
 
+// Prefetch `bytes` (a multiple of 16) of global memory at a 16-byte-aligned
+// address into L2.  Safe before a programmatic-dependency wait: L2 is the
+// point of coherence, so a later write by the previous kernel updates the
+// prefetched lines.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)),
+                 "r"(bytes)
+                 : "memory");
+}
+
 // Host: encode a 2-D tiled tensor map (row-major [dim1][dim0] of `dtype`,
 // row pitch `stride1_bytes`, box [box1][box0], no swizzle, zero fill out of
 // bounds).  The driver function is looked up once through the runtime.

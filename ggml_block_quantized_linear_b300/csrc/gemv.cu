@@ -267,6 +267,9 @@ gemv_kernel(const __grid_constant__ CUtensorMap wmap, const GemvParams p) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wmap)) : "memory");
         for (int i = 0; i < nloc && i < 2 * p.stages; ++i)
             tma_prefetch_l2_2d(&wmap, (c_begin + i) * (kCB / 2), row0);
+        // and of this CTA's first activation window
+        const int wk = min(p.kr_max, nloc * kGroup);
+        for (int m = 0; m < p.M; ++m) bulk_prefetch_l2(p.X + (int64_t)m * p.K + kbase, (uint32_t)(wk * 2));
     }
     __syncthreads();
     // Programmatic dependent launch: everything above overlaps the tail of

@@ -274,6 +274,9 @@ gemv_rows_kernel(const __grid_constant__ CUtensorMap wmap, const RowsParams p) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wmap)) : "memory");
         for (int j = 0; 2 * j < nch && j < nst; ++j)
             tma_prefetch_l2_2d(&wmap, 2 * j * (kCB / 8), (int)blockIdx.x * kRowsR);
+        // and of the first activation window, which gates every consumer
+        for (int m = 0; m < M; ++m)
+            bulk_prefetch_l2(p.X + (int64_t)m * p.K, (uint32_t)(min(win, nch) * kGroup * 2));
     }
     __syncthreads();
     // programmatic dependent launch: see gemv.cu
