@@ -218,16 +218,48 @@ quantize_q4_k_kernel(const void *__restrict__ src, uint8_t *__restrict__ dst, in
         const bool valid = sb < nsuper;  // uniform over each group of 8 lanes
         const int nvalid = (int)min((int64_t)4, nsuper - s0);
         float x[32];
-        if (valid) load32<kSrcF32>(src, sb * kQ4Weights + sj * 32, x);
-        else {
+        float mx, mn;  // max_i x_i and min(0, min_i x_i)
+        if constexpr (kSrcF32) {
+            if (valid) load32<kSrcF32>(src, sb * kQ4Weights + sj * 32, x);
+            else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) x[i] = 0.0f;
-        }
-        float mx = x[0], mn = 0.0f;  // max_i x_i and min(0, min_i x_i)
+                for (int i = 0; i < 32; ++i) x[i] = 0.0f;
+            }
+            mx = x[0];
+            mn = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            mx = fmaxf(mx, x[i]);
-            mn = fminf(mn, x[i]);
+            for (int i = 0; i < 32; ++i) {
+                mx = fmaxf(mx, x[i]);
+                mn = fminf(mn, x[i]);
+            }
+        } else {
+            // bf16 source: the extremes on packed pairs (exact, NaN-skipping
+            // like fmaxf / fminf), then the conversion to fp32
+            uint32_t raw[16];
+            const uint4 *src4 = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(src) +
+                                                                sb * kQ4Weights + sj * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint4 v = valid ? __ldg(src4 + i) : make_uint4(0u, 0u, 0u, 0u);
+                raw[4 * i] = v.x;
+                raw[4 * i + 1] = v.y;
+                raw[4 * i + 2] = v.z;
+                raw[4 * i + 3] = v.w;
+            }
+            __nv_bfloat162 vmax = *reinterpret_cast<const __nv_bfloat162 *>(&raw[0]), vmin = vmax;
+#pragma unroll
+            for (int i = 1; i < 16; ++i) {
+                const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162 *>(&raw[i]);
+                vmax = __hmax2(vmax, v);
+                vmin = __hmin2(vmin, v);
+            }
+            mx = fmaxf(__low2float(vmax), __high2float(vmax));
+            mn = fminf(0.0f, fminf(__low2float(vmin), __high2float(vmin)));
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                x[2 * i] = __uint_as_float(raw[i] << 16);
+                x[2 * i + 1] = __uint_as_float(raw[i] & 0xFFFF0000u);
+            }
         }
         const float s = __fdiv_rn(__fsub_rn(mx, mn), 15.0f);
         const float m = __fsub_rn(0.0f, mn);
