@@ -59,6 +59,9 @@ constexpr int kGemmTmemCols = 512;  // two 256-column fp32 accumulators
 // token tile, and each TMA-loads 1/kGemmCluster of every activation stage and
 // multicasts it to all of them (activation traffic from L2 / kGemmCluster).
 constexpr int kGemmCluster = QMM_GEMM_CLUSTER;
+#ifndef QMM_GEMM_SPLIT_K  // 1: split K in two for under-filled grids
+#define QMM_GEMM_SPLIT_K 1
+#endif
 
 // activation stages (32 KB each) and dequantized-weight stages (16 KB each)
 __host__ __device__ constexpr int gemm_stages_b(int fmt) { return fmt == 8 ? 3 : QMM_GEMM_STAGES_B_Q4; }
@@ -170,8 +173,15 @@ __device__ __forceinline__ void fence_async_smem() {
 
 // ----------------------------------------------------- activation conversion
 // X bf16 -> binary16 (round to nearest), 8 elements per thread.
+// With a K split, the same launch also zeroes Y (ny floats; 0 otherwise),
+// which the split GEMM then accumulates into.
 __global__ void __launch_bounds__(256) x_to_f16_kernel(const uint16_t *__restrict__ X,
-                                                       __half *__restrict__ Xh, int64_t n8) {
+                                                       __half *__restrict__ Xh, int64_t n8,
+                                                       float *__restrict__ Yz, int64_t ny) {
+    const int64_t y4 = ny / 4;  // Y is 16-byte aligned
+    for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < y4; i += (int64_t)gridDim.x * 256)
+        reinterpret_cast<float4 *>(Yz)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (blockIdx.x == 0 && threadIdx.x < ny - 4 * y4) Yz[4 * y4 + threadIdx.x] = 0.f;
     for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n8; i += (int64_t)gridDim.x * 256) {
         const uint4 v = __ldg(reinterpret_cast<const uint4 *>(X) + i);
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -240,6 +250,7 @@ __device__ __forceinline__ uint4 deq8_q4_k(const uint8_t *prow, const float *coe
 struct GemmParams {
     float *Y;
     int M, N, K;
+    int ksplit;  // 1, or 2: each output tile is two units (K halves) added into a zeroed Y
 };
 
 // Persistent: CTA b computes the output tiles b, b + gridDim.x, ... (weight
@@ -268,13 +279,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
     const int cid = (int)blockIdx.x / kGemmCluster, nclusters = (int)gridDim.x / kGemmCluster;
     const int tiles_n = (p.N + kGemmBM - 1) / kGemmBM;
     const int ngroups_n = (tiles_n + kGemmCluster - 1) / kGemmCluster;
-    const int units = ngroups_n * ((p.M + kGemmBN - 1) / kGemmBN);
+    // unit u = ((token tile * ngroups_n + weight group) * ksplit + K part)
+    const int ksplit = p.ksplit;
+    const int units = ngroups_n * ((p.M + kGemmBN - 1) / kGemmBN) * ksplit;
     const int my_tiles = units > cid ? (units - 1 - cid) / nclusters + 1 : 0;
-    auto tile_n0 = [&](int lt) { return (((cid + lt * nclusters) % ngroups_n) * kGemmCluster + crank) * kGemmBM; };
-    auto tile_m0 = [&](int lt) { return ((cid + lt * nclusters) / ngroups_n) * kGemmBN; };
+    auto tile_base = [&](int lt) { return (cid + lt * nclusters) / ksplit; };
+    auto tile_n0 = [&](int lt) { return ((tile_base(lt) % ngroups_n) * kGemmCluster + crank) * kGemmBM; };
+    auto tile_m0 = [&](int lt) { return (tile_base(lt) / ngroups_n) * kGemmBN; };
+    auto kpart = [&](int lt) { return (cid + lt * nclusters) % ksplit; };
     constexpr uint16_t kAllCtas = (uint16_t)((1u << kGemmCluster) - 1);
-    const int ksteps = p.K / kGemmBK;
-    const int groups = p.K / kGroup;
+    const int ksteps = p.K / kGemmBK / ksplit;  // k-steps and packed groups of one unit
+    const int groups = p.K / kGroup / ksplit;
 
     const uint32_t bar = smem_addr(smem + L.bars);
     auto b_full = [&](int s) { return bar + 8u * s; };
@@ -324,7 +339,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
             bool ok = true;
             int ki = 0;  // running activation-stage counter
             for (int lt = 0; lt < my_tiles && ok; ++lt) {
-                const int m0 = tile_m0(lt);
+                const int m0 = tile_m0(lt), kbase = kpart(lt) * ksteps;
                 for (int ks = 0; ks < ksteps && ok; ++ks, ++ki) {
                     const int sb = ki % kGemmStagesB;
                     if (ki >= kGemmStagesB)
@@ -335,9 +350,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
                     const uint32_t dst = smem_addr(smem + L.b + sb * kBBytes + crank * kSlice);
                     const int y0 = m0 + crank * (kGemmBN / kGemmCluster);
                     if (kGemmCluster > 1)
-                        tma_load_2d_multicast(dst, &xmap, ks * kGemmBK, y0, b_full(sb), kAllCtas);
+                        tma_load_2d_multicast(dst, &xmap, (kbase + ks) * kGemmBK, y0, b_full(sb), kAllCtas);
                     else
-                        tma_load_2d(dst, &xmap, ks * kGemmBK, y0, b_full(sb));
+                        tma_load_2d(dst, &xmap, (kbase + ks) * kGemmBK, y0, b_full(sb));
                 }
             }
         }
@@ -348,14 +363,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
             bool ok = true;
             int gi = 0;  // running packed-group counter
             for (int lt = 0; lt < my_tiles && ok; ++lt) {
-                const int n0 = tile_n0(lt);
+                const int n0 = tile_n0(lt), gbase = kpart(lt) * groups;
                 for (int g = 0; g < groups && ok; ++g, ++gi) {
                     const int sp = gi % kGemmStagesP;
                     if (gi >= kGemmStagesP)
                         ok = mbar_wait(p_empty(sp), ((gi / kGemmStagesP) - 1) & 1, kErrGemmWait);
                     if (!ok) break;
                     mbar_arrive_expect_tx(p_full(sp), kPBytes);
-                    tma_load_2d(smem_addr(smem + L.p + sp * kPBytes), &wmap, g * (kCB / 2), n0, p_full(sp));
+                    tma_load_2d(smem_addr(smem + L.p + sp * kPBytes), &wmap, (gbase + g) * (kCB / 2), n0,
+                                p_full(sp));
                 }
             }
         }
@@ -466,10 +482,20 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
                     uint32_t v[32];
                     tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(buf * kGemmBN + col), v);
                     if (n < p.N) {
+                        if (ksplit == 1) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const int m = m0 + col + i;
-                            if (m < p.M) p.Y[(int64_t)m * p.N + n] = __uint_as_float(v[i]);
+                            for (int i = 0; i < 32; ++i) {
+                                const int m = m0 + col + i;
+                                if (m < p.M) p.Y[(int64_t)m * p.N + n] = __uint_as_float(v[i]);
+                            }
+                        } else {
+                            // two halves added onto 0 in either order give the same
+                            // float (addition commutes), so the result is deterministic
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                const int m = m0 + col + i;
+                                if (m < p.M) atomicAdd(p.Y + (int64_t)m * p.N + n, __uint_as_float(v[i]));
+                            }
                         }
                     }
                 }
@@ -501,10 +527,23 @@ template <int kFmt>
 static cudaError_t launch_gemm_t(const void *W, const uint16_t *X, float *Y, int M, int N, int K,
                                  void *workspace, int sms, cudaStream_t stream) {
     __half *Xh = static_cast<__half *>(workspace);
+    // K split: when the output tiles fill under about half of the persistent
+    // clusters, two units per tile (K halves) fill twice as many SMs
+    const int tiles_n = (N + kGemmBM - 1) / kGemmBM;
+    const int units1 = ((tiles_n + kGemmCluster - 1) / kGemmCluster) * ((M + kGemmBN - 1) / kGemmBN);
+    const int slots = sms / kGemmCluster;
+    auto occupancy = [&](int u) {
+        const int waves = (u + slots - 1) / slots;
+        return (double)u / ((double)waves * slots);
+    };
+    const int ksplit = (QMM_GEMM_SPLIT_K && (K / kGroup) % 2 == 0 && occupancy(2 * units1) > occupancy(units1) + 0.2)
+                           ? 2 : 1;
     const int64_t n8 = (int64_t)M * K / 8;
-    int cgrid = (int)((n8 + 255) / 256);
+    const int64_t ny = ksplit > 1 ? (int64_t)M * N : 0;  // Y is zeroed for the split-K sum
+    const int64_t work = n8 > ny / 4 ? n8 : ny / 4;
+    int cgrid = (int)((work + 255) / 256);
     if (cgrid > 148 * 16) cgrid = 148 * 16;
-    x_to_f16_kernel<<<cgrid, 256, 0, stream>>>(X, Xh, n8);
+    x_to_f16_kernel<<<cgrid, 256, 0, stream>>>(X, Xh, n8, Y, ny);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
@@ -530,9 +569,9 @@ static cudaError_t launch_gemm_t(const void *W, const uint16_t *X, float *Y, int
     p.M = M;
     p.N = N;
     p.K = K;
-    const int tiles_n = (N + kGemmBM - 1) / kGemmBM;
-    const int units = ((tiles_n + kGemmCluster - 1) / kGemmCluster) * ((M + kGemmBN - 1) / kGemmBN);
-    int nclusters = sms / kGemmCluster;  // one persistent CTA per SM
+    p.ksplit = ksplit;
+    const int units = units1 * ksplit;
+    int nclusters = slots;  // one persistent CTA per SM
     if (units < nclusters) nclusters = units;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(nclusters * kGemmCluster), 1, 1);

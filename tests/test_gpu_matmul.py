@@ -137,6 +137,19 @@ def test_activation_range(fmt):
 
 
 # ---------------------------------------------------------------- prefill GEMM
+# Output grids filling under half of the SMs split K in two (each output
+# tile is two units added into a zeroed Y): 16 and 20 weight tiles x 2-3
+# token tiles; the last also has a Y size that is not a multiple of 4.
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("n,k,m", [(2048, 512, 513), (2560, 1024, 257), (2047, 512, 301)])
+def test_prefill_split_k_full(fmt, n, k, m):
+    packed, xb = problem(fmt, n, k, m, 3000 + n + k + m)
+    Y, A = oracle.matmul(fmt, packed, xb, n, k)
+    y = run(fmt, packed, xb, n)
+    check_matmul(y, Y, A, "fmt=%d n=%d k=%d m=%d" % (fmt, n, k, m))
+    assert torch.equal(y, run(fmt, packed, xb, n))  # the two halves add in either order
+
+
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("n,k", [(128, 256), (200, 512), (384, 1024), (130, 2304)])
 @pytest.mark.parametrize("m", [17, 64, 255, 256, 300])
