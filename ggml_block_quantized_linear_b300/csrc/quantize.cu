@@ -19,9 +19,11 @@
 // Bit-exactness: every floating-point step is an explicit IEEE single
 // operation (__fdiv_rn, __fadd_rn, __fsub_rn, __fmul_rn: no contraction),
 // codes use round-half-away (roundf), scales use binary16 round-to-nearest-
-// even (__float2half_rn).  The per-weight division of a code uses the
-// reciprocal of the block scale and falls back to the IEEE division only
-// next to a rounding tie (round_quotient), which gives the same codes.
+// even (__float2half_rn).  Divisions by the constants 15, 63, 127 use an
+// FMA-corrected product that equals the IEEE quotient (div_const); a
+// quotient that is only rounded to an integer (a weight code, a 6-bit scale
+// code) uses an approximate reciprocal and falls back to the IEEE division
+// only next to a rounding tie (round_quotient), which gives the same codes.
 // Signed zeros cannot change a byte: the maxima that feed a scale are
 // forced to +0 when they are zero.
 #include "common.cuh"
@@ -54,17 +56,38 @@ __device__ __forceinline__ float clamp_f(float v, float lo, float hi) {
 }
 
 // roundf(x / D) for D > 0, bit-identical to roundf(__fdiv_rn(x, D)), from
-// the correctly rounded reciprocal r = 1/D.  t = x * r (rounded) is within
-// 1.5 * 2^-23 * |x/D| of the correctly rounded quotient; roundf only jumps at
+// a reciprocal r of D within 1 ulp (the hardware approximation rcp_approx).
+// t = x * r (rounded) is within (2^-23 + 2^-24) |Q| of Q = x / D, and the
+// correctly rounded quotient within 2^-24 |Q|; roundf only jumps at
 // half-integers, so the nearest integer k of t is the answer unless t lies
-// within 2^-14 of a half-integer (|t| * 2^-21 < 2^-14 while |t| <= 128),
-// where the exact division decides.  Callers clamp the result to a range
-// inside [-128, 128]: beyond it, both ways clamp to the same code.
+// within 4 * 2^-24 * 128 < 2^-14 of a half-integer (|Q| <= 128), where the
+// exact division decides.  Callers clamp the result to a range inside
+// [-128, 128]: beyond it, both ways clamp to the same code.
 //
 // The block quantizers apply this per block: every code takes the fast
 // path, the largest |t - k| of the block is kept, and only a block where it
 // reaches 0.5 - 2^-14 (a possible tie) is recomputed with exact divisions --
 // one branch per block instead of one per weight.
+__device__ __forceinline__ float rcp_approx(float d) {
+    float r;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(d));
+    return r;
+}
+
+// x / c for a constant c > 0 and x >= 0, correctly rounded: Markstein's
+// correction of the product with the rounded reciprocal r = RN(1/c)
+// (P. Markstein, IBM J. Res. Dev. 34(1), 1990): q0 = x r, e = x - c q0
+// (exact by fma), q = q0 + e r rounded once.  Checked bit for bit against
+// the IEEE division for every non-negative finite float and c = 15, 63, 127.
+template <int kC>
+__device__ __forceinline__ float div_const(float x) {
+    constexpr float c = (float)kC;
+    constexpr float r = 1.0f / (float)kC;
+    const float q0 = __fmul_rn(x, r);
+    const float q = __fmaf_rn(__fmaf_rn(-q0, c, x), r, q0);
+    return isinf(q0) ? q0 : q;  // x = inf: the residual would be inf - inf
+}
+
 constexpr float kTieGuard = 0.49993896484375f;  // 0.5 - 2^-14
 __device__ __forceinline__ float rint_quotient(float x, float r, float &dev) {
     const float t = __fmul_rn(x, r);
@@ -124,7 +147,7 @@ quantize_q8_0_kernel(const void *__restrict__ src, uint8_t *__restrict__ dst, in
             float amax = 0.0f;
 #pragma unroll
             for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
-            const __half dh = __float2half_rn(__fdiv_rn(amax, 127.0f));
+            const __half dh = __float2half_rn(div_const<127>(amax));
             const float df = __half2float(dh);
             uint32_t w[8];
 #pragma unroll
@@ -132,7 +155,7 @@ quantize_q8_0_kernel(const void *__restrict__ src, uint8_t *__restrict__ dst, in
             if (df >= 6.103515625e-05f) {
                 // normal binary16 scale: |x / d16| <= 127 (1 + 2^-11) < 127.5,
                 // so round(x / d16) never needs the clamp
-                const float r = __frcp_rn(df);
+                const float r = rcp_approx(df);
                 float dev = 0.0f;
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
@@ -145,7 +168,7 @@ quantize_q8_0_kernel(const void *__restrict__ src, uint8_t *__restrict__ dst, in
                                            roundf(__fdiv_rn(x[4 * i + 2], df)), roundf(__fdiv_rn(x[4 * i + 3], df)));
                 }
             } else if (df != 0.0f) {  // subnormal scale: the quotient may pass 127.5
-                const float r = __frcp_rn(df);
+                const float r = rcp_approx(df);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const float q = clamp_f(round_quotient(x[i], df, r), -127.0f, 127.0f);
@@ -261,7 +284,7 @@ quantize_q4_k_kernel(const void *__restrict__ src, uint8_t *__restrict__ dst, in
                 x[2 * i + 1] = __uint_as_float(raw[i] & 0xFFFF0000u);
             }
         }
-        const float s = __fdiv_rn(__fsub_rn(mx, mn), 15.0f);
+        const float s = div_const<15>(__fsub_rn(mx, mn));
         const float m = __fsub_rn(0.0f, mn);
         float smax = s, mmax = m;
 #pragma unroll
@@ -271,18 +294,27 @@ quantize_q4_k_kernel(const void *__restrict__ src, uint8_t *__restrict__ dst, in
         }
         smax = smax > 0.0f ? smax : 0.0f;
         mmax = mmax > 0.0f ? mmax : 0.0f;
-        const __half dh = __float2half_rn(__fdiv_rn(smax, 63.0f));
-        const __half dminh = __float2half_rn(__fdiv_rn(mmax, 63.0f));
+        const __half dh = __float2half_rn(div_const<63>(smax));
+        const __half dminh = __float2half_rn(div_const<63>(mmax));
         const float df = __half2float(dh), dminf = __half2float(dminh);
-        const int sc = df > 0.0f ? (int)clamp_f(roundf(__fdiv_rn(s, df)), 0.0f, 63.0f) : 0;
-        const int mc = dminf > 0.0f ? (int)clamp_f(roundf(__fdiv_rn(m, dminf)), 0.0f, 63.0f) : 0;
+        // 6-bit codes of the scale and the min: s / d16 and m / dmin16 are at
+        // most ~64, so the reciprocal quotient with the tie check applies
+        float tsc = 0.0f, tmc = 0.0f, sdev = 0.0f;
+        if (df > 0.0f) tsc = rint_quotient(s, rcp_approx(df), sdev);
+        if (dminf > 0.0f) tmc = rint_quotient(m, rcp_approx(dminf), sdev);
+        if (sdev >= kTieGuard) {
+            tsc = df > 0.0f ? roundf(__fdiv_rn(s, df)) : 0.0f;
+            tmc = dminf > 0.0f ? roundf(__fdiv_rn(m, dminf)) : 0.0f;
+        }
+        const int sc = (int)clamp_f(tsc, 0.0f, 63.0f);
+        const int mc = (int)clamp_f(tmc, 0.0f, 63.0f);
         const float S = __fmul_rn(df, (float)sc);
         const float Mn = __fmul_rn(dminf, (float)mc);
         uint32_t w[8];  // 4-bit codes, one per byte
 #pragma unroll
         for (int i = 0; i < 8; ++i) w[i] = 0u;
         if (S > 0.0f) {
-            const float r = __frcp_rn(S);
+            const float r = rcp_approx(S);
             float dev = 0.0f;
             auto code = [&](int i) { return clamp_f(rint_quotient(__fadd_rn(x[i], Mn), r, dev), 0.0f, 15.0f); };
 #pragma unroll
