@@ -11,6 +11,8 @@
 #include <cudaTypedefs.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace qmm {
 
 // Block geometry of the two formats (see include/qmm.h for the layouts).
@@ -163,6 +165,20 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)),
                  "r"(bytes)
                  : "memory");
+}
+
+// Host: raise a kernel's dynamic shared-memory limit once per device (the
+// attribute belongs to the current context, so each device needs its own
+// call); `done` is the caller's per-kernel bitmask of devices already set.
+inline cudaError_t set_smem_limit_once(const void *kernel, int bytes, std::atomic<uint64_t> &done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
 }
 
 // Host: encode a 2-D tiled tensor map (row-major [dim1][dim0] of `dtype`,

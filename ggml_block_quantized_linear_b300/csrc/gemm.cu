@@ -558,12 +558,9 @@ static cudaError_t launch_gemm_t(const void *W, const uint16_t *X, float *Y, int
     if (e != cudaSuccess) return e;
 
     const GemmLayout L = gemm_layout(kFmt);
-    static bool attr_set = false;
-    if (!attr_set) {
-        e = cudaFuncSetAttribute(gemm_kernel<kFmt>, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static std::atomic<uint64_t> attr_done{0};
+    e = set_smem_limit_once(reinterpret_cast<const void *>(gemm_kernel<kFmt>), L.total, attr_done);
+    if (e != cudaSuccess) return e;
     GemmParams p;
     p.Y = Y;
     p.M = M;

@@ -458,13 +458,10 @@ static cudaError_t launch_gemv_t(const GemvParams &p, const GemvPlan &pl, cudaSt
                                     (uint64_t)(p.row_bytes / 2), (uint64_t)p.N,
                                     (uint64_t)p.row_bytes, kCB / 2, kGemvRows);
     if (te != cudaSuccess) return te;
-    static bool attr_set = false;  // per process; the limit is the same on every device
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(gemv_kernel<kFmt, kNT>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static std::atomic<uint64_t> attr_done{0};
+    cudaError_t e = set_smem_limit_once(reinterpret_cast<const void *>(gemv_kernel<kFmt, kNT>), 227 * 1024,
+                                        attr_done);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((p.N + kGemvRows - 1) / kGemvRows), (unsigned)pl.nsplit, 1);
     cfg.blockDim = dim3(kGemvThreads, 1, 1);

@@ -438,14 +438,9 @@ gemv_rows_kernel(const __grid_constant__ CUtensorMap wmap, const RowsParams p) {
 }
 
 template <int kFmt>
-static cudaError_t rows_set_attrs(int dev) {
-    static std::atomic<uint64_t> done{0};  // one bit per device: the attribute is per context
-    const uint64_t bit = 1ull << (dev & 63);
-    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(gemv_rows_kernel<kFmt>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
-    return e;
+static cudaError_t rows_set_attrs() {
+    static std::atomic<uint64_t> done{0};
+    return set_smem_limit_once(reinterpret_cast<const void *>(gemv_rows_kernel<kFmt>), 227 * 1024, done);
 }
 
 // Resident CTAs per SM for a given dynamic shared-memory size (registers,
@@ -520,7 +515,7 @@ static cudaError_t launch_rows_t(const void *W, RowsParams &p, int sms, cudaStre
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    e = rows_set_attrs<kFmt>(dev);
+    e = rows_set_attrs<kFmt>();
     if (e != cudaSuccess) return e;
     const RowsPlan pl = rows_plan<kFmt>(dev, p.M, p.K);
     if (pl.dpp == 0) return cudaErrorInvalidConfiguration;  // no plan fits shared memory
