@@ -416,7 +416,10 @@ gemv_kernel(const __grid_constant__ CUtensorMap wmap, const GemvParams p) {
 #ifndef QMM_GEMV_PDL
 #define QMM_GEMV_PDL 1
 #endif
-static int gemv_window(int nt) { return nt == 1 ? 8 : 4; }
+#ifndef QMM_GEMV_WINDOW_NT2  // activation window in chunks with 9..16 tokens
+#define QMM_GEMV_WINDOW_NT2 4
+#endif
+static int gemv_window(int nt) { return nt == 1 ? 8 : QMM_GEMV_WINDOW_NT2; }
 static int gemv_stages(int fmt) { return fmt == 8 ? QMM_GEMV_STAGES_Q8 : QMM_GEMV_STAGES_Q4; }
 
 struct GemvPlan {

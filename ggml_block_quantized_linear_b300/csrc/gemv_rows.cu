@@ -38,9 +38,12 @@ constexpr int kProdWarpR = kWarpsR, kRedWarpR = kWarpsR + 1;
 constexpr int kThreadsR = (kWarpsR + 2) * 32;
 constexpr int kYBufsR = 2;
 constexpr int kCoefStrideR = 20;  // floats per row of a warp's Q4_K coefficient table (padded)
-// Activations held in shared memory at once: M * window chunks <= 128
-// (64 KB of binary16).
-constexpr int kRowsXChunkBudget = 128;
+// Activations held in shared memory at once: M * window chunks <= 256
+// (128 KB of binary16; one CTA per SM then, but no per-tile restaging).
+#ifndef QMM_ROWS_X_BUDGET
+#define QMM_ROWS_X_BUDGET 256
+#endif
+constexpr int kRowsXChunkBudget = QMM_ROWS_X_BUDGET;
 
 struct RowsLayout {
     int ring, xh, xs, coef, ypart, bars, total;

@@ -44,12 +44,13 @@ def test_decode_small_full(fmt, n, k, m):
 # count that is not a multiple of 8, more tiles than resident CTAs (CTAs
 # loop over tiles), activations too many to hold at once (windows of K, with
 # a one-chunk last window), and a ragged last tile; odd and even chunk
-# counts (the 2-chunk copies then end on a half-filled or a full box), 18
-# chunks in windows of 16 + 2.
+# counts (the 2-chunk copies then end on a half-filled or a full box).
+# Windows (M * chunks > 256): 34 chunks in 32 + 2, 33 in 32 + 1, 56 in 48 + 8.
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("n,k,m", [(2369, 256, 1), (2369, 256, 8), (9999, 1280, 2), (9999, 1280, 8),
                                    (3000, 4352, 5), (3000, 4352, 8), (12000, 4352, 8), (10000, 2304, 3),
-                                   (2369, 512, 1), (10000, 2560, 3), (3000, 4608, 8), (12000, 4608, 1)])
+                                   (2369, 512, 1), (10000, 2560, 3), (3000, 4608, 8), (12000, 4608, 1),
+                                   (2400, 8704, 8), (2500, 8448, 8), (2400, 14336, 5)])
 def test_decode_row_tiles_full(fmt, n, k, m):
     packed, xb = problem(fmt, n, k, m, 2000 + n + k + m)
     Y, A = oracle.matmul(fmt, packed, xb, n, k)
