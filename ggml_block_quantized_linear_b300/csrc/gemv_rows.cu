@@ -1,4 +1,4 @@
-// gemv_rows.cu -- decode matmul for M <= 8 tokens without thread-block
+// gemv_rows.cu -- decode matmul for M <= 16 tokens without thread-block
 // clusters: persistent CTAs, each owning whole 16-row tiles over all of K.
 //
 // CTA b takes the row tiles b, b + G, b + 2G, ... (G = grid size, at most
@@ -22,8 +22,8 @@
 //    partial sums in a double-buffered shared array and moves on; the reducer
 //    adds the eight partials in warp order (deterministic) and stores the
 //    tile's outputs.  There is no cluster and no workspace.
-// Used when the row tiles alone fill the GPU's SMs and the activations are
-// few (M <= 8).
+// Used when the row tiles alone fill the GPU's SMs; up to 16 tokens (one or
+// two 8-token column tiles of the MMA).
 #include <atomic>
 #include <mutex>
 
@@ -49,7 +49,8 @@ struct RowsLayout {
     int ring, xh, xs, coef, ypart, bars, total;
 };
 
-__host__ __device__ inline RowsLayout rows_layout(int fmt, int M, int dpp, int win) {
+// mt = 8 * (token tiles): the stride of the Q4_K block sums per 32-block.
+__host__ __device__ inline RowsLayout rows_layout(int fmt, int M, int dpp, int win, int mt) {
     const int cb = fmt == 8 ? kQ8GroupBytes : kQ4Bytes;
     RowsLayout L;
     int off = 0;
@@ -58,7 +59,7 @@ __host__ __device__ inline RowsLayout rows_layout(int fmt, int M, int dpp, int w
     L.xh = off;
     off += M * (win * kGroup + 32) * 2;       // token rows, 32 halves of padding between them
     L.xs = off;
-    off += fmt == 4 ? win * 8 * 8 * 4 : 0;    // Q4_K: sum of x per 32-block and token
+    off += fmt == 4 ? win * 8 * mt * 4 : 0;   // Q4_K: sum of x per 32-block and token
     L.coef = off;
     off += fmt == 4 ? kWarpsR * kRowsR * kCoefStrideR * 4 : 0;
     L.ypart = off;
@@ -84,10 +85,9 @@ struct RowsParams {
 // at xh + m * xstride), in place to binary16 (round to nearest), each group
 // of 4 stored in the order (0, 2, 1, 3) so that one 16-byte load yields both
 // B fragments of an MMA; Q4_K also sums each 32-weight block per token.
-template <int kFmt>
+template <int kFmt, int kMT>
 __device__ __forceinline__ void rows_convert_x(int M, __half *xh, float *xs, int xstride, int wn,
                                                int tid) {
-    constexpr int kMT = 8;
     const int ngr = (wn * kGroup) / 8;  // 8-element groups per token
     int m = 0, kg = tid;
     while (kg >= ngr && m < M) { kg -= ngr; ++m; }
@@ -150,10 +150,11 @@ __device__ __forceinline__ void rq8_codes(const uint8_t *p, uint32_t &w0, uint32
 }
 
 // One Q8_0 block (32 weights) of rows g and g + 8 (row bases r0, r1, 16-byte
-// aligned) against token g's binary16 activations at xb (if xvalid).
-template <int kB>
-__device__ __forceinline__ void rq8_block(const uint8_t *r0, const uint8_t *r1, const __half *xb, int t,
-                                          bool xvalid, float (&acc)[4]) {
+// aligned) against tokens g + 8 nt (nt < kNT) at xb + nt * 8 * xstride,
+// present when v0 (nt = 0) / v1 (nt = 1).
+template <int kB, int kNT>
+__device__ __forceinline__ void rq8_block(const uint8_t *r0, const uint8_t *r1, const __half *xb, int xstride,
+                                          int t, bool v0, bool v1, float (&acc)[kNT][4]) {
     constexpr int kOff = kQ8Bytes * kB + 2;
     constexpr int kMod8 = kOff % 8;
     const float d0 = h2f_bits(*reinterpret_cast<const uint16_t *>(r0 + kQ8Bytes * kB));
@@ -166,14 +167,17 @@ __device__ __forceinline__ void rq8_block(const uint8_t *r0, const uint8_t *r1, 
                             q8_exact(q8_pair13(a0)), q8_exact(q8_pair13(b0))};
     const uint32_t A1[4] = {q8_exact(q8_pair02(a1)), q8_exact(q8_pair02(b1)),
                             q8_exact(q8_pair13(a1)), q8_exact(q8_pair13(b1))};
-    const uint4 xv = x_frag(xb + kQ8Weights * kB + 8 * t, xvalid);
-    float c[4] = {0.f, 0.f, 0.f, 0.f};
-    mma_f16_16816(c, A0, xv.x, xv.y);
-    mma_f16_16816(c, A1, xv.z, xv.w);
-    acc[0] = fmaf(d0, c[0], acc[0]);
-    acc[1] = fmaf(d0, c[1], acc[1]);
-    acc[2] = fmaf(d1, c[2], acc[2]);
-    acc[3] = fmaf(d1, c[3], acc[3]);
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt) {
+        const uint4 xv = x_frag(xb + nt * 8 * xstride + kQ8Weights * kB + 8 * t, nt == 0 ? v0 : v1);
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_f16_16816(c, A0, xv.x, xv.y);
+        mma_f16_16816(c, A1, xv.z, xv.w);
+        acc[nt][0] = fmaf(d0, c[0], acc[nt][0]);
+        acc[nt][1] = fmaf(d0, c[1], acc[nt][1]);
+        acc[nt][2] = fmaf(d1, c[2], acc[nt][2]);
+        acc[nt][3] = fmaf(d1, c[3], acc[nt][3]);
+    }
 }
 
 // Q4_K scale/min decode of one chunk (16 rows x 8 sub-blocks): lane r + 16 h
@@ -201,11 +205,13 @@ __device__ __forceinline__ void rq4_coefs(const uint8_t *row0, int pitch, float 
     dst[1] = make_float4(o[4], o[5], o[6], o[7]);
 }
 
-// 64 weights (sub-blocks 2c, 2c + 1) of rows g and g + 8 of a Q4_K chunk.
-template <int kC>
-__device__ __forceinline__ void rq4_group(const uint8_t *r0, const uint8_t *r1, const __half *xb,
-                                          const float *xsb, const float *cw, int g, int t, bool xvalid,
-                                          float (&acc)[4]) {
+// 64 weights (sub-blocks 2c, 2c + 1) of rows g and g + 8 of a Q4_K chunk;
+// xsb: the chunk's block sums, stride 8 kNT per 32-block.
+template <int kC, int kNT>
+__device__ __forceinline__ void rq4_group(const uint8_t *r0, const uint8_t *r1, const __half *xb, int xstride,
+                                          const float *xsb, const float *cw, int g, int t, bool v0, bool v1,
+                                          float (&acc)[kNT][4]) {
+    constexpr int kMT = 8 * kNT;
     const uint2 qa = *reinterpret_cast<const uint2 *>(r0 + 16 + 32 * kC + 8 * t);
     const uint2 qb = *reinterpret_cast<const uint2 *>(r1 + 16 + 32 * kC + 8 * t);
     const float4 ca = *reinterpret_cast<const float4 *>(cw + g * kCoefStrideR + 4 * kC);
@@ -216,24 +222,29 @@ __device__ __forceinline__ void rq4_group(const uint8_t *r0, const uint8_t *r1, 
     const uint32_t L1[4] = {qa.y & 0x000F000Fu, qb.y & 0x000F000Fu, qa1s & 0x000F000Fu, qb1s & 0x000F000Fu};
     const uint32_t H0[4] = {qa.x & 0x00F000F0u, qb.x & 0x00F000F0u, qa0s & 0x00F000F0u, qb0s & 0x00F000F0u};
     const uint32_t H1[4] = {qa.y & 0x00F000F0u, qb.y & 0x00F000F0u, qa1s & 0x00F000F0u, qb1s & 0x00F000F0u};
-    const __half *xq = xb + 64 * kC + 8 * t;
-    const uint4 xl = x_frag(xq, xvalid);
-    const uint4 xhv = x_frag(xq + 32, xvalid);
-    float cl[4] = {0.f, 0.f, 0.f, 0.f}, chh[4] = {0.f, 0.f, 0.f, 0.f};
-    mma_f16_16816(cl, L0, xl.x, xl.y);
-    mma_f16_16816(cl, L1, xl.z, xl.w);
-    mma_f16_16816(chh, H0, xhv.x, xhv.y);
-    mma_f16_16816(chh, H1, xhv.z, xhv.w);
-    const float2 sl = *reinterpret_cast<const float2 *>(xsb + (2 * kC) * 8 + 2 * t);
-    const float2 sh = *reinterpret_cast<const float2 *>(xsb + (2 * kC + 1) * 8 + 2 * t);
-    acc[0] = fmaf(ca.w, sh.x, fmaf(ca.y, sl.x, fmaf(ca.z, chh[0], fmaf(ca.x, cl[0], acc[0]))));
-    acc[1] = fmaf(ca.w, sh.y, fmaf(ca.y, sl.y, fmaf(ca.z, chh[1], fmaf(ca.x, cl[1], acc[1]))));
-    acc[2] = fmaf(cb.w, sh.x, fmaf(cb.y, sl.x, fmaf(cb.z, chh[2], fmaf(cb.x, cl[2], acc[2]))));
-    acc[3] = fmaf(cb.w, sh.y, fmaf(cb.y, sl.y, fmaf(cb.z, chh[3], fmaf(cb.x, cl[3], acc[3]))));
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt) {
+        const __half *xq = xb + nt * 8 * xstride + 64 * kC + 8 * t;
+        const uint4 xl = x_frag(xq, nt == 0 ? v0 : v1);
+        const uint4 xhv = x_frag(xq + 32, nt == 0 ? v0 : v1);
+        float cl[4] = {0.f, 0.f, 0.f, 0.f}, chh[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_f16_16816(cl, L0, xl.x, xl.y);
+        mma_f16_16816(cl, L1, xl.z, xl.w);
+        mma_f16_16816(chh, H0, xhv.x, xhv.y);
+        mma_f16_16816(chh, H1, xhv.z, xhv.w);
+        const float2 sl = *reinterpret_cast<const float2 *>(xsb + (2 * kC) * kMT + nt * 8 + 2 * t);
+        const float2 sh = *reinterpret_cast<const float2 *>(xsb + (2 * kC + 1) * kMT + nt * 8 + 2 * t);
+        acc[nt][0] = fmaf(ca.w, sh.x, fmaf(ca.y, sl.x, fmaf(ca.z, chh[0], fmaf(ca.x, cl[0], acc[nt][0]))));
+        acc[nt][1] = fmaf(ca.w, sh.y, fmaf(ca.y, sl.y, fmaf(ca.z, chh[1], fmaf(ca.x, cl[1], acc[nt][1]))));
+        acc[nt][2] = fmaf(cb.w, sh.x, fmaf(cb.y, sl.x, fmaf(cb.z, chh[2], fmaf(cb.x, cl[2], acc[nt][2]))));
+        acc[nt][3] = fmaf(cb.w, sh.y, fmaf(cb.y, sl.y, fmaf(cb.z, chh[3], fmaf(cb.x, cl[3], acc[nt][3]))));
+    }
 }
 
-template <int kFmt>
-__global__ void __launch_bounds__(kThreadsR, 3)
+// kNT token tiles of 8 (M <= 8 kNT); two tiles double the accumulators, so
+// their register budget allows two CTAs per SM instead of three.
+template <int kFmt, int kNT>
+__global__ void __launch_bounds__(kThreadsR, kNT == 1 ? 3 : 2)
 gemv_rows_kernel(const __grid_constant__ CUtensorMap wmap, const RowsParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int kCB = kFmt == 8 ? kQ8GroupBytes : kQ4Bytes;
@@ -243,7 +254,7 @@ gemv_rows_kernel(const __grid_constant__ CUtensorMap wmap, const RowsParams p) {
     const int nch = p.nchunks, dpp = p.dpp, win = p.win, M = p.M;
     const bool resident = win >= nch;  // activations staged once per CTA
     const int xstride = win * kGroup + 32;
-    const RowsLayout L = rows_layout(kFmt, M, dpp, win);
+    const RowsLayout L = rows_layout(kFmt, M, dpp, win, 8 * kNT);
     uint8_t *ring = smem + L.ring;
     __half *xh = reinterpret_cast<__half *>(smem + L.xh);
     float *xs = reinterpret_cast<float *>(smem + L.xs);
@@ -269,8 +280,9 @@ gemv_rows_kernel(const __grid_constant__ CUtensorMap wmap, const RowsParams p) {
         fence_mbar_init();
     }
     // block sums of padding tokens (m >= M) stay zero for the whole kernel
+    constexpr int kMT = 8 * kNT;
     if constexpr (kFmt == 4)
-        for (int idx = tid; idx < win * 8 * 8; idx += kThreadsR) xs[idx] = 0.f;
+        for (int idx = tid; idx < win * 8 * kMT; idx += kThreadsR) xs[idx] = 0.f;
     if (warp == kProdWarpR && lane == 0) {
         // descriptor fetch and L2 prefetch of the first tile's leading stages
         // (safe before the dependency wait: nothing lands in shared memory)
@@ -362,17 +374,17 @@ gemv_rows_kernel(const __grid_constant__ CUtensorMap wmap, const RowsParams p) {
         const int g = lane >> 2, t = lane & 3;
         const int pr = warp >> 1, hb = warp & 1;
         const __half *xrow = xh + g * xstride;
-        const bool xvalid = g < M;
+        const bool v0 = g < M, v1 = g + 8 < M;  // tokens g and g + 8 are real
         float *cw = reinterpret_cast<float *>(smem + L.coef) + warp * kRowsR * kCoefStrideR;
         bool ok = true;  // warp-uniform, see gemv.cu
         int dpos = 0, ph = 0, xseq = 0, u = 0;
         for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x, ++u) {
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            float acc[kNT][4] = {};
             for (int w0 = 0; w0 < nch; w0 += win) {
                 const int wn = min(win, nch - w0);
                 if (!resident || xseq == 0) {
                     if (ok) ok = mbar_wait_warp(xfull, xseq & 1, kErrGemvFullWait);
-                    if (ok) rows_convert_x<kFmt>(M, xh, xs, xstride, wn, tid);
+                    if (ok) rows_convert_x<kFmt, kMT>(M, xh, xs, xstride, wn, tid);
                     named_bar_sync(1, kWarpsR * 32);
                 }
                 const int j_end = (w0 + wn + 1) / 2;
@@ -389,22 +401,22 @@ gemv_rows_kernel(const __grid_constant__ CUtensorMap wmap, const RowsParams p) {
                         const uint8_t *r1 = cbase + (g + 8) * kPitch;
                         const __half *xb = xrow + li * kGroup;
                         if constexpr (kFmt == 8) {
-                            rq8_block<0>(r0, r1, xb, t, xvalid, acc);
-                            rq8_block<1>(r0, r1, xb, t, xvalid, acc);
-                            rq8_block<2>(r0, r1, xb, t, xvalid, acc);
-                            rq8_block<3>(r0, r1, xb, t, xvalid, acc);
-                            rq8_block<4>(r0, r1, xb, t, xvalid, acc);
-                            rq8_block<5>(r0, r1, xb, t, xvalid, acc);
-                            rq8_block<6>(r0, r1, xb, t, xvalid, acc);
-                            rq8_block<7>(r0, r1, xb, t, xvalid, acc);
+                            rq8_block<0, kNT>(r0, r1, xb, xstride, t, v0, v1, acc);
+                            rq8_block<1, kNT>(r0, r1, xb, xstride, t, v0, v1, acc);
+                            rq8_block<2, kNT>(r0, r1, xb, xstride, t, v0, v1, acc);
+                            rq8_block<3, kNT>(r0, r1, xb, xstride, t, v0, v1, acc);
+                            rq8_block<4, kNT>(r0, r1, xb, xstride, t, v0, v1, acc);
+                            rq8_block<5, kNT>(r0, r1, xb, xstride, t, v0, v1, acc);
+                            rq8_block<6, kNT>(r0, r1, xb, xstride, t, v0, v1, acc);
+                            rq8_block<7, kNT>(r0, r1, xb, xstride, t, v0, v1, acc);
                         } else {
                             rq4_coefs(cbase, kPitch, cw, lane);
                             __syncwarp();
-                            const float *xsb = xs + li * 8 * 8;
-                            rq4_group<0>(r0, r1, xb, xsb, cw, g, t, xvalid, acc);
-                            rq4_group<1>(r0, r1, xb, xsb, cw, g, t, xvalid, acc);
-                            rq4_group<2>(r0, r1, xb, xsb, cw, g, t, xvalid, acc);
-                            rq4_group<3>(r0, r1, xb, xsb, cw, g, t, xvalid, acc);
+                            const float *xsb = xs + li * 8 * kMT;
+                            rq4_group<0, kNT>(r0, r1, xb, xstride, xsb, cw, g, t, v0, v1, acc);
+                            rq4_group<1, kNT>(r0, r1, xb, xstride, xsb, cw, g, t, v0, v1, acc);
+                            rq4_group<2, kNT>(r0, r1, xb, xstride, xsb, cw, g, t, v0, v1, acc);
+                            rq4_group<3, kNT>(r0, r1, xb, xstride, xsb, cw, g, t, v0, v1, acc);
                         }
                     }
                     __syncwarp();
@@ -426,13 +438,17 @@ gemv_rows_kernel(const __grid_constant__ CUtensorMap wmap, const RowsParams p) {
             if (ok && u >= kYBufsR)
                 ok = mbar_wait_warp(yempty0 + 8u * b, ((u / kYBufsR) - 1) & 1, kErrGemvEmptyWait);
             float *yp = ypart + (b * kWarpsR + warp) * kRowsR * M;
-            if (2 * t < M) {
-                yp[g * M + 2 * t] = acc[0];
-                yp[(g + 8) * M + 2 * t] = acc[2];
-            }
-            if (2 * t + 1 < M) {
-                yp[g * M + 2 * t + 1] = acc[1];
-                yp[(g + 8) * M + 2 * t + 1] = acc[3];
+#pragma unroll
+            for (int nt = 0; nt < kNT; ++nt) {
+                const int m0 = 8 * nt + 2 * t;
+                if (m0 < M) {
+                    yp[g * M + m0] = acc[nt][0];
+                    yp[(g + 8) * M + m0] = acc[nt][2];
+                }
+                if (m0 + 1 < M) {
+                    yp[g * M + m0 + 1] = acc[nt][1];
+                    yp[(g + 8) * M + m0 + 1] = acc[nt][3];
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(yfull0 + 8u * b);
@@ -440,18 +456,18 @@ gemv_rows_kernel(const __grid_constant__ CUtensorMap wmap, const RowsParams p) {
     }
 }
 
-template <int kFmt>
+template <int kFmt, int kNT>
 static cudaError_t rows_set_attrs() {
     static std::atomic<uint64_t> done{0};
-    return set_smem_limit_once(reinterpret_cast<const void *>(gemv_rows_kernel<kFmt>), 227 * 1024, done);
+    return set_smem_limit_once(reinterpret_cast<const void *>(gemv_rows_kernel<kFmt, kNT>), 227 * 1024, done);
 }
 
 // Resident CTAs per SM for a given dynamic shared-memory size (registers,
 // threads and shared memory all counted by the runtime).
-template <int kFmt>
+template <int kFmt, int kNT>
 static int rows_occupancy(int smem) {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemv_rows_kernel<kFmt>, kThreadsR,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemv_rows_kernel<kFmt, kNT>, kThreadsR,
                                                       (size_t)smem) != cudaSuccess)
         return 1;
     return n < 1 ? 1 : n;
@@ -472,7 +488,7 @@ struct RowsPlan {
 // budget), then the sub-ring depth per warp pair with the most weight bytes
 // in flight per SM (resident CTAs x ring bytes), preferring more resident
 // CTAs on ties.
-template <int kFmt>
+template <int kFmt, int kNT>
 static RowsPlan rows_plan_compute(int dev, int M, int K) {
     constexpr int kCB = kFmt == 8 ? kQ8GroupBytes : kQ4Bytes;
     const int nch = K / kGroup;
@@ -485,9 +501,9 @@ static RowsPlan rows_plan_compute(int dev, int M, int K) {
     long best_bytes = -1;
     for (int d = 1; d <= QMM_ROWS_MAX_DPP; ++d) {
         if (QMM_ROWS_FORCE_DPP > 0 && d != QMM_ROWS_FORCE_DPP) continue;
-        const int sm = rows_layout(kFmt, M, d, win).total;
+        const int sm = rows_layout(kFmt, M, d, win, 8 * kNT).total;
         if (sm > 227 * 1024) break;
-        const int occ = rows_occupancy<kFmt>(sm);
+        const int occ = rows_occupancy<kFmt, kNT>(sm);
         const long bytes = (long)occ * kPairsR * d * kRowsR * 2 * kCB;
         if (bytes > best_bytes || (bytes == best_bytes && occ > best.occ)) {
             best_bytes = bytes;
@@ -499,7 +515,7 @@ static RowsPlan rows_plan_compute(int dev, int M, int K) {
 
 // The plan depends on (device, M, K) only; it is computed once (the
 // occupancy queries cost host time) and kept in a small table.
-template <int kFmt>
+template <int kFmt, int kNT>
 static RowsPlan rows_plan(int dev, int M, int K) {
     static std::mutex mu;
     static RowsPlan table[64];
@@ -507,20 +523,20 @@ static RowsPlan rows_plan(int dev, int M, int K) {
     std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < count; ++i)
         if (table[i].dev == dev && table[i].M == M && table[i].K == K) return table[i];
-    const RowsPlan pl = rows_plan_compute<kFmt>(dev, M, K);
+    const RowsPlan pl = rows_plan_compute<kFmt, kNT>(dev, M, K);
     table[count < 64 ? count++ : (int)(((unsigned)M * 31u + (unsigned)K) % 64u)] = pl;
     return pl;
 }
 
-template <int kFmt>
+template <int kFmt, int kNT>
 static cudaError_t launch_rows_t(const void *W, RowsParams &p, int sms, cudaStream_t stream) {
     constexpr int kCB = kFmt == 8 ? kQ8GroupBytes : kQ4Bytes;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    e = rows_set_attrs<kFmt>();
+    e = rows_set_attrs<kFmt, kNT>();
     if (e != cudaSuccess) return e;
-    const RowsPlan pl = rows_plan<kFmt>(dev, p.M, p.K);
+    const RowsPlan pl = rows_plan<kFmt, kNT>(dev, p.M, p.K);
     if (pl.dpp == 0) return cudaErrorInvalidConfiguration;  // no plan fits shared memory
     p.nchunks = p.K / kGroup;
     p.ntiles = (p.N + kRowsR - 1) / kRowsR;
@@ -544,7 +560,7 @@ static cudaError_t launch_rows_t(const void *W, RowsParams &p, int sms, cudaStre
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_rows_kernel<kFmt>, wmap, p);
+    return cudaLaunchKernelEx(&cfg, gemv_rows_kernel<kFmt, kNT>, wmap, p);
 }
 
 cudaError_t launch_gemv_rows(int fmt, const void *W, const uint16_t *X, float *Y, int M, int N, int K,
@@ -555,7 +571,9 @@ cudaError_t launch_gemv_rows(int fmt, const void *W, const uint16_t *X, float *Y
     p.M = M;
     p.N = N;
     p.K = K;
-    return fmt == 8 ? launch_rows_t<8>(W, p, sms, stream) : launch_rows_t<4>(W, p, sms, stream);
+    if (M > 8)
+        return fmt == 8 ? launch_rows_t<8, 2>(W, p, sms, stream) : launch_rows_t<4, 2>(W, p, sms, stream);
+    return fmt == 8 ? launch_rows_t<8, 1>(W, p, sms, stream) : launch_rows_t<4, 1>(W, p, sms, stream);
 }
 
 }  // namespace qmm

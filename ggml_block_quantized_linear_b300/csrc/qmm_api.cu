@@ -40,7 +40,7 @@ static int sm_count() {
 }
 
 #ifndef QMM_ROWS_MAX_M
-#define QMM_ROWS_MAX_M 8
+#define QMM_ROWS_MAX_M 16
 #endif
 #ifndef QMM_ROWS_MIN_CTAS_PER_SM  // in 1/4 CTA per SM
 #define QMM_ROWS_MIN_CTAS_PER_SM 4
@@ -48,8 +48,13 @@ static int sm_count() {
 // Decode kernel choice: 16-row CTAs over the whole K (no cluster) when the
 // tokens are few and the rows alone give every SM enough CTAs; otherwise the
 // 64-row tile with a cluster split-K.
-static bool use_rows_kernel(int M, int N, int sms) {
-    return M <= QMM_ROWS_MAX_M && (int64_t)((N + 15) / 16) * 4 >= (int64_t)sms * QMM_ROWS_MIN_CTAS_PER_SM;
+// The persistent row-tile kernel when its 16-row tiles fill the SMs; with
+// more than 8 tokens only while the activations stay resident in shared
+// memory (M * K / 256 <= 256: restaging 16 token rows per tile costs more
+// than the cluster kernel's windows).
+static bool use_rows_kernel(int M, int N, int K, int sms) {
+    if (M > QMM_ROWS_MAX_M || (M > 8 && (int64_t)M * (K / 256) > 256)) return false;
+    return (int64_t)((N + 15) / 16) * 4 >= (int64_t)sms * QMM_ROWS_MIN_CTAS_PER_SM;
 }
 
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -115,7 +120,7 @@ qmm_status qmm_matmul(qmm_format fmt, const void *W_packed, const uint16_t *X_bf
     if (!aligned16(W_packed) || !aligned16(X_bf16) || !aligned16(Y)) return QMM_ERR_ALIGNMENT;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (M <= kMaxDecodeM) {
-        if (use_rows_kernel((int)M, (int)N, sm_count()))
+        if (use_rows_kernel((int)M, (int)N, (int)K, sm_count()))
             return from_cuda(launch_gemv_rows((int)fmt, W_packed, X_bf16, Y, (int)M, (int)N, (int)K,
                                               sm_count(), s));
         return from_cuda(launch_gemv((int)fmt, W_packed, X_bf16, Y, (int)M, (int)N, (int)K,

@@ -40,7 +40,7 @@ def test_decode_small_full(fmt, n, k, m):
 
 
 # Shapes with at least one 16-row tile per SM take the persistent row-tile
-# kernel (M <= 8): one chunk per tile (seven idle consumer warps), a chunk
+# kernel (M <= 16, one or two 8-token MMA column tiles): one chunk per tile (seven idle consumer warps), a chunk
 # count that is not a multiple of 8, more tiles than resident CTAs (CTAs
 # loop over tiles), activations too many to hold at once (windows of K, with
 # a one-chunk last window), and a ragged last tile; odd and even chunk
@@ -50,7 +50,9 @@ def test_decode_small_full(fmt, n, k, m):
 @pytest.mark.parametrize("n,k,m", [(2369, 256, 1), (2369, 256, 8), (9999, 1280, 2), (9999, 1280, 8),
                                    (3000, 4352, 5), (3000, 4352, 8), (12000, 4352, 8), (10000, 2304, 3),
                                    (2369, 512, 1), (10000, 2560, 3), (3000, 4608, 8), (12000, 4608, 1),
-                                   (2400, 8704, 8), (2500, 8448, 8), (2400, 14336, 5)])
+                                   (2400, 8704, 8), (2500, 8448, 8), (2400, 14336, 5),
+                                   (2369, 256, 16), (9999, 1280, 12), (3000, 4608, 16), (2400, 4096, 9),
+                                   (12000, 2304, 16)])
 def test_decode_row_tiles_full(fmt, n, k, m):
     packed, xb = problem(fmt, n, k, m, 2000 + n + k + m)
     Y, A = oracle.matmul(fmt, packed, xb, n, k)
