@@ -22,8 +22,10 @@
 //    partial sums in a double-buffered shared array and moves on; the reducer
 //    adds the eight partials in warp order (deterministic) and stores the
 //    tile's outputs.  There is no cluster and no workspace.
-// Used when the row tiles alone fill the GPU's SMs; up to 16 tokens (one or
-// two 8-token column tiles of the MMA).
+// Used when the row tiles alone fill the GPU's SMs, for up to 8 tokens (one
+// 8-token MMA column tile) or, while up to 128 KB of activations stay
+// resident, up to 16 (two tiles).  The ring depth and the activation window
+// are planned per (M, K) from the resident CTAs per SM.
 #include <atomic>
 #include <mutex>
 
