@@ -46,13 +46,15 @@ def test_decode_small_full(fmt, n, k, m):
 # a one-chunk last window), and a ragged last tile; odd and even chunk
 # counts (the 2-chunk copies then end on a half-filled or a full box).
 # Windows (M * chunks > 256): 34 chunks in 32 + 2, 33 in 32 + 1, 56 in 48 + 8.
+# With 1-2 tokens the kernel also takes grids of a quarter of the SMs
+# (38 and 63 tiles, ragged).
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("n,k,m", [(2369, 256, 1), (2369, 256, 8), (9999, 1280, 2), (9999, 1280, 8),
                                    (3000, 4352, 5), (3000, 4352, 8), (12000, 4352, 8), (10000, 2304, 3),
                                    (2369, 512, 1), (10000, 2560, 3), (3000, 4608, 8), (12000, 4608, 1),
                                    (2400, 8704, 8), (2500, 8448, 8), (2400, 14336, 5),
                                    (2369, 256, 16), (9999, 1280, 12), (3000, 4608, 16), (2400, 4096, 9),
-                                   (12000, 2304, 16)])
+                                   (12000, 2304, 16), (600, 2304, 2), (1000, 4096, 1)])
 def test_decode_row_tiles_full(fmt, n, k, m):
     packed, xb = problem(fmt, n, k, m, 2000 + n + k + m)
     Y, A = oracle.matmul(fmt, packed, xb, n, k)
