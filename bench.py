@@ -64,39 +64,51 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash():
+# Source files that define each kernel family: a DRAM-traffic figure measured by
+# ncu stays valid while these files are unchanged.
+FAMILY_SOURCES = {
+    "quantize": ("common.cuh", "quantize.cu"),
+    "dequantize": ("common.cuh", "quantize.cu"),
+    "gemv": ("common.cuh", "gemv.cu", "gemv_rows.cu"),
+    "gemm": ("common.cuh", "gemm.cu"),
+}
+
+
+def kernel_source_hash(names=None):
+    """sha256 prefix over the CUDA sources `names` (default: every .cu/.cuh)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "ggml_block_quantized_linear_b300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            h.update(name.encode())
-            h.update(open(os.path.join(csrc, name), "rb").read())
+    if names is None:
+        names = [n for n in os.listdir(csrc) if n.endswith((".cu", ".cuh"))]
+    for name in sorted(names):
+        h.update(name.encode())
+        h.update(open(os.path.join(csrc, name), "rb").read())
     return h.hexdigest()[:16]
 
 
 def load_traffic():
     """DRAM bytes per weight measured by ncu for each kernel family
-    (profiles/dram_traffic.txt, lines `family=bytes_per_weight`), valid only
-    for the kernel sources they were measured on (`source_hash=`)."""
+    (profiles/dram_traffic.txt, lines `family=bytes_per_weight source_hash`).
+    A figure is used only while the family's sources hash to the value it was
+    measured on."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     out = {}
     if not os.path.exists(p):
         return out
-    src_hash = None
     for line in open(p):
-        line = line.strip()
-        if not line or line.startswith("#"):
+        line = line.split("#", 1)[0].strip()
+        if not line:
             continue
         k, _, v = line.partition("=")
-        if k.strip() == "source_hash":
-            src_hash = v.strip()
-        else:
-            try:
-                out[k.strip()] = float(v)
-            except ValueError:
-                pass
-    if src_hash != kernel_source_hash():
-        return {}
+        k, parts = k.strip(), v.split()
+        if k not in FAMILY_SOURCES or len(parts) != 2:
+            continue
+        try:
+            bpw = float(parts[0])
+        except ValueError:
+            continue
+        if parts[1] == kernel_source_hash(FAMILY_SOURCES[k]):
+            out[k] = bpw
     return out
 
 
