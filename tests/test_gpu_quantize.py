@@ -89,7 +89,50 @@ def edge_cases():
     q4[1] = np.nextafter(q4[1], np.float32(np.inf))
     q4[2] = np.nextafter(q4[2], np.float32(-np.inf))
     cases["q4_half_steps"] = torch.from_numpy(q4)
+    cases["q8_near_ties_scaled"] = torch.from_numpy(q8_near_ties_scaled(rng))
+    cases["q4_near_ties_scaled"] = torch.from_numpy(q4_near_ties_scaled(rng))
     return cases
+
+
+def _nudge(v, steps):
+    """v moved by `steps` float32 ulps (elementwise, signed)."""
+    v = v.astype(np.float32).copy()
+    for s in range(int(np.abs(steps).max())):
+        up = steps > s
+        dn = -steps > s
+        v[up] = np.nextafter(v[up], np.float32(np.inf))
+        v[dn] = np.nextafter(v[dn], np.float32(-np.inf))
+    return v
+
+
+def q8_near_ties_scaled(rng, rows=16, cols=512):
+    """Q8_0 blocks whose scale is a known binary16 value D (amax = 127 D, so
+    amax / 127 = D exactly) and whose other weights lie a few float32 ulps
+    from the half-steps (k + 1/2) D: quotients just inside and outside the
+    tie guard of the reciprocal shortcut, with D not a power of two."""
+    nb = rows * cols // 32
+    D = np.ldexp(1.0 + rng.integers(0, 1024, nb) / 1024.0, rng.integers(-10, 4, nb)).astype(np.float32)
+    k = rng.integers(-127, 127, (nb, 32)).astype(np.float32)
+    x = _nudge((k + 0.5) * D[:, None], rng.integers(-12, 13, (nb, 32)))
+    x[:, 0] = 127.0 * D
+    return x.reshape(rows, cols)
+
+
+def q4_near_ties_scaled(rng, rows=16, cols=512):
+    """Q4_K superblocks with non-negative weights (so the min terms vanish),
+    a known superblock scale D (sub-block 0 spans 15 * 63 D) and sub-block
+    scale codes c_j (sub-block j spans 15 c_j D), so S_j = c_j D exactly;
+    the other weights lie a few float32 ulps from (k + 1/2) S_j."""
+    ns = rows * cols // 256
+    D = np.ldexp(1.0 + rng.integers(0, 32, ns) / 32.0, rng.integers(-12, 2, ns)).astype(np.float32)
+    c = rng.integers(1, 64, (ns, 8)).astype(np.float32)
+    c[:, 0] = 63.0
+    S = c * D[:, None]
+    k = rng.integers(0, 15, (ns, 8, 32)).astype(np.float32)
+    x = _nudge((k + 0.5) * S[:, :, None], rng.integers(-12, 13, (ns, 8, 32)))
+    x[:, :, 0] = 15.0 * S
+    x[:, :, 1] = 0.0
+    return x.reshape(rows, cols)
 
 
 @pytest.mark.parametrize("fmt", FMTS)
