@@ -52,6 +52,10 @@ constexpr int kGemmThreads = (kGemmWarpPackedTma + 1) * 32;
 #endif
 constexpr int kGemmStagesP = 2;     // packed weight groups
 constexpr int kGemmTmemCols = 512;  // two 256-column fp32 accumulators
+// Q4_K (S_j, Mn_j) table: 16 floats per weight row, padded to 18 so that the
+// rows a warp reads together (2 apart) fall in different banks
+constexpr int kGemmCoefStride = 18;
+static_assert((kGemmBM / (4 * kGemmDeqWarps)) % 2 == 0, "dequantization passes come in even / odd row pairs");
 #ifndef QMM_GEMM_CLUSTER
 #define QMM_GEMM_CLUSTER 2
 #endif
@@ -82,7 +86,7 @@ __host__ __device__ inline GemmLayout gemm_layout(int fmt) {
     L.p = off;
     off += kGemmStagesP * kGemmBM * gemm_group_bytes(fmt);
     L.coef = off;
-    off += fmt == 4 ? kGemmBM * 8 * 2 * 4 : 0;
+    off += fmt == 4 ? kGemmBM * kGemmCoefStride * 4 : 0;
     off = (off + 15) & ~15;
     L.bars = off;
     off += 64 * 8;  // barriers + TMEM address slot
@@ -226,7 +230,7 @@ __device__ __forceinline__ uint4 deq8_q8_0(const uint8_t *prow, int j, int c) {
 }
 
 // Q4_K: 8 weights (k = 8c .. 8c+7 of k-step j = sub-blocks 2j, 2j+1).
-// coef[(r * 8 + sj) * 2 + {0,1}] = (S_j, Mn_j) of the row's superblock.
+// coefr[2 sj + {0,1}] = (S_j, Mn_j) of the row's superblock.
 __device__ __forceinline__ uint4 deq8_q4_k(const uint8_t *prow, const float *coefr, int j, int c) {
     const int sj = 2 * j + (c >> 2);
     const uint2 q = *reinterpret_cast<const uint2 *>(prow + 16 + 32 * j + 8 * (c & 3));
@@ -435,8 +439,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
                                 sc = (sb(sj + 4) & 15u) | ((sb(sj - 4) >> 6) << 4);
                                 mc = (sb(sj + 4) >> 4) | ((sb(sj) >> 6) << 4);
                             }
-                            coef[(r * 8 + sj) * 2] = dsc * (float)sc;
-                            coef[(r * 8 + sj) * 2 + 1] = dmn * (float)mc;
+                            coef[r * kGemmCoefStride + 2 * sj] = dsc * (float)sc;
+                            coef[r * kGemmCoefStride + 2 * sj + 1] = dmn * (float)mc;
                         }
                     }
                     named_bar_sync(1, kGemmDeqWarps * 32);
@@ -448,12 +452,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
                     if (ok) {
 #pragma unroll
                         for (int pass = 0; pass < kGemmBM / (4 * kGemmDeqWarps); ++pass) {
-                            const int r = pass * 4 * kGemmDeqWarps + 4 * dw + rsub;
+                            // warp dw owns 8-row blocks; one pass takes their even
+                            // rows, the next the odd ones: with packed row pitches of
+                            // 4 banks mod 32 (272 and 144 bytes), rows 2 apart keep the
+                            // code loads of the 32 lanes free of bank conflicts
+                            const int r = (pass >> 1) * 8 * kGemmDeqWarps + 8 * dw + 2 * rsub + (pass & 1);
                             uint4 v;
                             if constexpr (kFmt == 8)
                                 v = deq8_q8_0(pst + r * kCB, j, c);
                             else
-                                v = deq8_q4_k(pst + r * kCB, coef + r * 16, j, c);
+                                v = deq8_q4_k(pst + r * kCB, coef + r * kGemmCoefStride, j, c);
                             *reinterpret_cast<uint4 *>(ast + sw128_chunk_off(r, c)) = v;
                         }
                     }
