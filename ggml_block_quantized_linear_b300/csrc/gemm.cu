@@ -237,14 +237,21 @@ __device__ __forceinline__ uint4 deq8_q4_k(const uint8_t *prow, const float *coe
     const int sh = (c >> 2) * 4;
     const uint32_t n0 = (q.x >> sh) & 0x0F0F0F0Fu, n1 = (q.y >> sh) & 0x0F0F0F0Fu;
     const float2 sm = *reinterpret_cast<const float2 *>(coefr + 2 * sj);
+    // q (exact, from 2^23 + q) and S q - Mn with one rounding, two weights
+    // per packed fp32 instruction
+    const uint64_t s2 = f2_pack(sm.x, sm.x), nm2 = f2_pack(-sm.y, -sm.y);
+    const uint64_t k2 = f2_pack(-8388608.0f, -8388608.0f);
     uint32_t r[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
         const uint32_t nw = e < 2 ? n0 : n1;
         const int b0 = (2 * e) & 3;
-        const float q0 = __uint_as_float(prmt(nw, 0x4B000000u, 0x7440u + b0)) - 8388608.0f;
-        const float q1 = __uint_as_float(prmt(nw, 0x4B000000u, 0x7440u + b0 + 1)) - 8388608.0f;
-        const __half2 h = __floats2half2_rn(fmaf(sm.x, q0, -sm.y), fmaf(sm.x, q1, -sm.y));
+        const uint64_t qq = f2_add(f2_pack(__uint_as_float(prmt(nw, 0x4B000000u, 0x7440u + b0)),
+                                           __uint_as_float(prmt(nw, 0x4B000000u, 0x7440u + b0 + 1))),
+                                   k2);
+        float v0, v1;
+        f2_unpack(f2_fma(s2, qq, nm2), v0, v1);
+        const __half2 h = __floats2half2_rn(v0, v1);
         r[e] = *reinterpret_cast<const uint32_t *>(&h);
     }
     return make_uint4(r[0], r[1], r[2], r[3]);

@@ -98,32 +98,6 @@ __device__ __forceinline__ float round_div(float x, float D) {
     return fabsf(d) >= kTieGuard ? tie_code(x, D, k, d) : k;
 }
 
-// Pairs of fp32 values in one 64-bit register: sm_100-family GPUs issue
-// add / sub / fma on .f32x2 operands once for both lanes, each lane rounded
-// exactly like the scalar instruction (IEEE, round to nearest even).
-__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-    return r;
-}
 // bf16 pair (low half first) -> fp32 pair
 __device__ __forceinline__ uint64_t f2_from_bf16x2(uint32_t w) {
     return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
