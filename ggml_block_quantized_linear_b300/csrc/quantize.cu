@@ -222,14 +222,25 @@ quantize_q8_0_kernel(const void *__restrict__ src, uint8_t *__restrict__ dst, in
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint8_t *st = stage[warp];
     const int64_t nwarps = (int64_t)gridDim.x * kQuantWarps;
-    for (int64_t b0 = ((int64_t)blockIdx.x * kQuantWarps + warp) * 32; b0 < nblocks; b0 += nwarps * 32) {
+    // bf16 sources: the next iteration's weights are loaded before this
+    // one's are used (fp32 sources have no registers to spare for that)
+    const int64_t step = nwarps * 32;
+    int64_t b0 = ((int64_t)blockIdx.x * kQuantWarps + warp) * 32;
+    Lane32<kSrcF32> Ln;
+    if (!kSrcF32 && b0 + lane < nblocks) Ln.load(src, (b0 + lane) * kQ8Weights, true);
+    for (; b0 < nblocks; b0 += step) {
         const int64_t blk = b0 + lane;
         const int nvalid = (int)min((int64_t)32, nblocks - b0);  // a multiple of 8
         float df = 0.0f, r = 0.0f;
         bool normal = true, tie = false;
+        Lane32<kSrcF32> L;
+        if constexpr (kSrcF32) {
+            if (blk < nblocks) L.load(src, blk * kQ8Weights, true);
+        } else {
+            L = Ln;
+            if (blk + step < nblocks) Ln.load(src, (blk + step) * kQ8Weights, true);
+        }
         if (blk < nblocks) {
-            Lane32<kSrcF32> L;
-            L.load(src, blk * kQ8Weights, true);
             float mx, mn;
             L.extremes(mx, mn);
             float amax = fmaxf(mx, -mn);
@@ -328,22 +339,33 @@ dequantize_q8_0_kernel(const uint8_t *__restrict__ src, float *__restrict__ dst,
 // a warp covers 4 superblocks (1024 weights, 576 packed bytes) per
 // iteration.
 #ifndef QMM_Q4_QUANT_MIN_BLOCKS  // resident CTAs per SM the register budget must allow
-#define QMM_Q4_QUANT_MIN_BLOCKS 4
+#define QMM_Q4_QUANT_MIN_BLOCKS 3
 #endif
 template <bool kSrcF32>
-__global__ void __launch_bounds__(kQuantThreads, kSrcF32 ? 3 : QMM_Q4_QUANT_MIN_BLOCKS)
+__global__ void __launch_bounds__(kQuantThreads, QMM_Q4_QUANT_MIN_BLOCKS)
 quantize_q4_k_kernel(const void *__restrict__ src, uint8_t *__restrict__ dst, int64_t nsuper) {
     __shared__ __align__(16) uint8_t stage[kQuantWarps][4 * kQ4Bytes];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int sj = lane & 7, sbl = lane >> 3;  // sub-block j, superblock in the warp tile
     uint8_t *st = stage[warp] + sbl * kQ4Bytes;
     const int64_t nwarps = (int64_t)gridDim.x * kQuantWarps;
-    for (int64_t s0 = ((int64_t)blockIdx.x * kQuantWarps + warp) * 4; s0 < nsuper; s0 += nwarps * 4) {
+    // bf16 sources: the next iteration's weights are loaded before this
+    // one's are used (fp32 sources have no registers to spare for that)
+    const int64_t step = nwarps * 4;
+    int64_t s0 = ((int64_t)blockIdx.x * kQuantWarps + warp) * 4;
+    Lane32<kSrcF32> Ln;
+    if (!kSrcF32) Ln.load(src, (s0 + sbl) * kQ4Weights + sj * 32, s0 + sbl < nsuper);
+    for (; s0 < nsuper; s0 += step) {
         const int64_t sb = s0 + sbl;
         const bool valid = sb < nsuper;  // uniform over each group of 8 lanes
         const int nvalid = (int)min((int64_t)4, nsuper - s0);
         Lane32<kSrcF32> L;
-        L.load(src, sb * kQ4Weights + sj * 32, valid);
+        if constexpr (kSrcF32) {
+            L.load(src, sb * kQ4Weights + sj * 32, valid);
+        } else {
+            L = Ln;
+            Ln.load(src, (sb + step) * kQ4Weights + sj * 32, sb + step < nsuper);
+        }
         float mx, mn;  // max_i x_i and min(0, min_i x_i)
         L.extremes(mx, mn);
         mn = fminf(0.0f, mn);
@@ -459,10 +481,15 @@ dequantize_q4_k_kernel(const uint8_t *__restrict__ src, float *__restrict__ dst,
     const int sub = lane >> 2, part = lane & 3;
     uint8_t *st = stage[warp];
     const int64_t nwarps = (int64_t)gridDim.x * kQuantWarps;
-    for (int64_t g = (int64_t)blockIdx.x * kQuantWarps + warp; g < ngroups; g += nwarps) {
-        if (lane < kQ4Bytes / 16)
-            reinterpret_cast<uint4 *>(st)[lane] =
-                __ldg(reinterpret_cast<const uint4 *>(src + g * kQ4Bytes) + lane);
+    // the next group's bytes are loaded before this one is converted
+    constexpr int kVec = kQ4Bytes / 16;
+    int64_t g = (int64_t)blockIdx.x * kQuantWarps + warp;
+    uint4 nx = make_uint4(0u, 0u, 0u, 0u);
+    if (g < ngroups && lane < kVec) nx = __ldg(reinterpret_cast<const uint4 *>(src + g * kQ4Bytes) + lane);
+    for (; g < ngroups; g += nwarps) {
+        if (lane < kVec) reinterpret_cast<uint4 *>(st)[lane] = nx;
+        if (g + nwarps < ngroups && lane < kVec)
+            nx = __ldg(reinterpret_cast<const uint4 *>(src + (g + nwarps) * kQ4Bytes) + lane);
         __syncwarp();
         const uint32_t dd = *reinterpret_cast<const uint32_t *>(st);
         const float df = __half2float(__ushort_as_half((uint16_t)(dd & 0xFFFF)));
