@@ -116,10 +116,14 @@ QMM_API qmm_status qmm_dequantize(qmm_format fmt, const void *src_packed, float 
 QMM_API size_t qmm_matmul_workspace_bytes(qmm_format fmt, int64_t M, int64_t N, int64_t K);
 
 /* Y[M x N] (fp32, row-major) = X[M x K] (bf16 bit patterns, row-major) times
- * the transpose of the packed weights W[N x K].  M <= 16 runs the decode
- * kernel (split-K over a thread-block cluster, reduced in distributed shared
- * memory in a fixed order: deterministic).  Larger M runs the prefill kernel
- * (tcgen05 tensor cores, TMEM accumulators).  Accuracy: per element
+ * the transpose of the packed weights W[N x K].  M <= 16 runs a decode
+ * kernel: persistent CTAs over 16-row tiles when the tiles fill the GPU
+ * (each tile's partial sums added in a fixed order), otherwise split-K over
+ * a thread-block cluster reduced in distributed shared memory in a fixed
+ * order; both are deterministic.  Larger M runs the prefill kernel (tcgen05
+ * tensor cores, TMEM accumulators; with K split in two when the output tiles
+ * fill under half the SMs, the two halves add onto a zeroed Y, which is
+ * still deterministic).  Accuracy: per element
  * |y - y_exact| <= 1e-3 * sum_k |w^_k x_k| + 1e-6, where w^ are the
  * dequantized weights.  `workspace` must hold
  * qmm_matmul_workspace_bytes(fmt, M, N, K) bytes (or be NULL when that is 0). */
