@@ -281,7 +281,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
     constexpr uint32_t kABytes = kGemmBM * kGemmBK * 2;
     constexpr uint32_t kPBytes = kGemmBM * kCB;
     const GemmLayout L = gemm_layout(kFmt);
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned base for the 128B-swizzled stages, kept as an offset
+    // into the shared array so that every access compiles to LDS / STS
+    // (an address rounded through an integer would be a generic pointer)
+    uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // work unit = (group of kGemmCluster neighbouring weight tiles, token tile);
     // cluster c takes units c, c + nclusters, ...; its CTA of rank r takes
