@@ -86,12 +86,12 @@ def kernel_source_hash(names=None):
     return h.hexdigest()[:16]
 
 
-def load_traffic():
+def load_traffic(path=None):
     """DRAM bytes per weight measured by ncu for each kernel family
     (profiles/dram_traffic.txt, lines `family=bytes_per_weight source_hash`).
     A figure is used only while the family's sources hash to the value it was
     measured on."""
-    p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    p = path or os.path.join(ROOT, "profiles", "dram_traffic.txt")
     out = {}
     if not os.path.exists(p):
         return out
