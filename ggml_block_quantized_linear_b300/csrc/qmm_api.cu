@@ -1,6 +1,7 @@
 // qmm_api.cu -- the C ABI declared in include/qmm.h: argument checks on the
 // host, kernel selection and launch.  Nothing here allocates or synchronises
 // (except qmm_device_error_take, which is documented to synchronise).
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 
@@ -25,18 +26,20 @@ constexpr int kMaxDecodeM = 16;
 // Largest dimension accepted (keeps every 32-bit index in the kernels exact).
 constexpr int64_t kMaxDim = (int64_t)1 << 30;
 
+// SMs of the current device, looked up once per device (calls may come
+// from several host threads: the cache is atomic).
 static int sm_count() {
-    static int cached[64] = {0};
+    static std::atomic<int> cached[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 148;
     if (dev < 0 || dev >= 64) return 148;
-    if (cached[dev] == 0) {
-        int n = 0;
+    int n = cached[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
             n = 148;
-        cached[dev] = n;
+        cached[dev].store(n, std::memory_order_relaxed);
     }
-    return cached[dev];
+    return n;
 }
 
 #ifndef QMM_ROWS_MAX_M
