@@ -482,6 +482,22 @@ def workload_config():
             "accumulate": "f32", "graphs": "each stage captured as one CUDA graph"}
 
 
+# ------------------------------------------------------------- ranks (N > 1)
+def max_over_ranks(dist, ms_step, med, names, device):
+    """The step time and each stage's median time, as the maximum over the
+    ranks of the process group (every rank times the same per-GPU work)."""
+    import torch
+    vals = torch.tensor([ms_step] + [med[n] for n in names], device=device, dtype=torch.float64)
+    dist.all_reduce(vals, op=dist.ReduceOp.MAX)
+    return float(vals[0]), {**med, **{n: float(vals[i + 1]) for i, n in enumerate(names)}}
+
+
+def whole_job_gbps(bytes_per_rank, world, ms):
+    """Whole-job throughput: the bytes all ranks processed over the slowest
+    rank's time (weak scaling: the per-rank work is fixed)."""
+    return bytes_per_rank * world / (ms * 1e-3) / 1e9
+
+
 # --------------------------------------------------------------------- main
 def main(argv=None):
     ap = argparse.ArgumentParser()
@@ -543,17 +559,13 @@ def main(argv=None):
     med = {n: statistics.median(v) for n, v in per.items()}
     ms_step = statistics.median(step_ms)
     if world > 1:
-        vals = torch.tensor([ms_step] + [med[n] for n, *_ in stages], device=dev, dtype=torch.float64)
-        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-        ms_step = float(vals[0])
-        for i, (n, *_) in enumerate(stages):
-            med[n] = float(vals[i + 1])
+        ms_step, med = max_over_ranks(dist, ms_step, med, [n for n, *_ in stages], dev)
 
     peaks, peak_kind = load_peaks()
     traffic = load_traffic()
     info = {s[0]: s for s in stages}
     wbytes_m1 = sum(p.numel() for f in wl.fmts for p in wl.packed[f])
-    value = wbytes_m1 * world / (med["gemv_m1"] * 1e-3) / 1e9
+    value = whole_job_gbps(wbytes_m1, world, med["gemv_m1"])
 
     rows = {}
     fam_time = {}
