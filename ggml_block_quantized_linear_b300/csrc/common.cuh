@@ -29,11 +29,14 @@ constexpr int kQ8GroupBytes = 272;
 // ran out (see qmm_device_error_take).  The library is one translation unit
 // (qmm_lib.cu), so this is its only definition.
 __device__ int g_device_error = 0;
+// The codes match qmm_device_error in include/qmm.h.
 enum DeviceError : int {
     kErrNone = 0,
     kErrGemvFullWait = 101,
     kErrGemvEmptyWait = 102,
     kErrGemmWait = 201,
+    kErrSelftestTimeout = 901,
+    kErrSelftestUnexpected = 902,
 };
 
 __device__ __forceinline__ void record_error(int code) { atomicCAS(&g_device_error, 0, code); }
@@ -93,17 +96,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 // Bounded wait for the phase with the given parity to complete.  Returns
-// false (after recording `err`) if it has not completed within the limit.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int err) {
+// false (after recording `err`) if it has not completed within limit_ns.
+__device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity, int err, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t i = 0;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 255u && global_timer_ns() - t0 > kWaitLimitNs) {
+        if ((i & 255u) == 255u && global_timer_ns() - t0 > limit_ns) {
             record_error(err);
             return false;
         }
     }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int err) {
+    return mbar_wait_limit(bar, parity, err, kWaitLimitNs);
 }
 
 // mbar_wait by a whole warp, with a warp-uniform answer (true only if every
@@ -134,18 +140,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
         "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-
-// 2-D tiled tensor copy global -> shared, multicast to the CTAs of the
-// cluster in ctaMask: the box lands at the same shared-memory offset in each
-// of them and completes `bytes` on the mbarrier at the same offset in each.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap *map, int x, int y,
-                                                      uint32_t bar, uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster "
-        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(cta_mask)
         : "memory");
 }
 

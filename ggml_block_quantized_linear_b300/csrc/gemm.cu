@@ -18,7 +18,7 @@
 // x 64 K per stage; persistent CTAs (one per SM) walk the tiles, and two fp32
 // accumulators of 256 TMEM columns alternate between consecutive tiles.
 //   warp 0       TMA producer of the binary16 activation tiles (128B-swizzled
-//                boxes, multicast to the CTAs of the cluster)
+//                boxes, each CTA loading its own)
 //   warp 1       TMEM allocator and single-thread MMA issuer
 //   warps 2-17   dequantize packed weights into 128B-swizzled K-major f16
 //                A stages
@@ -56,13 +56,6 @@ constexpr int kGemmTmemCols = 512;  // two 256-column fp32 accumulators
 // rows a warp reads together (2 apart) fall in different banks
 constexpr int kGemmCoefStride = 18;
 static_assert((kGemmBM / (4 * kGemmDeqWarps)) % 2 == 0, "dequantization passes come in even / odd row pairs");
-#ifndef QMM_GEMM_CLUSTER
-#define QMM_GEMM_CLUSTER 2
-#endif
-// CTAs per cluster: they compute neighbouring weight tiles against the same
-// token tile, and each TMA-loads 1/kGemmCluster of every activation stage and
-// multicasts it to all of them (activation traffic from L2 / kGemmCluster).
-constexpr int kGemmCluster = QMM_GEMM_CLUSTER;
 #ifndef QMM_GEMM_SPLIT_K  // 1: split K in two for under-filled grids
 #define QMM_GEMM_SPLIT_K 1
 #endif
@@ -130,14 +123,6 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
         : "memory");
 }
-// The same, arriving on the mbarrier at this offset in every CTA of ctaMask.
-__device__ __forceinline__ void umma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
-        "[%0], %1;" ::"r"(bar),
-        "h"(cta_mask)
-        : "memory");
-}
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle,
 // 8-row core groups 1024 bytes apart (SBO), sm_100 descriptor version 1.
 __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_addr) {
@@ -179,7 +164,7 @@ __device__ __forceinline__ void fence_async_smem() {
 // X bf16 -> binary16 (round to nearest), 8 elements per thread.
 // With a K split, the same launch also zeroes Y (ny floats; 0 otherwise),
 // which the split GEMM then accumulates into.
-__global__ void __launch_bounds__(256) x_to_f16_kernel(const uint16_t *__restrict__ X,
+__global__ void __launch_bounds__(256) qmm_x_to_f16_kernel(const uint16_t *__restrict__ X,
                                                        __half *__restrict__ Xh, int64_t n8,
                                                        float *__restrict__ Yz, int64_t ny) {
     const int64_t y4 = ny / 4;  // Y is 16-byte aligned
@@ -271,7 +256,7 @@ struct GemmParams {
 // next.
 template <int kFmt>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
+qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
             const GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     constexpr int kSA = gemm_stages_a(kFmt);
@@ -286,22 +271,19 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
     // (an address rounded through an integer would be a generic pointer)
     uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // work unit = (group of kGemmCluster neighbouring weight tiles, token tile);
-    // cluster c takes units c, c + nclusters, ...; its CTA of rank r takes
-    // weight tile kGemmCluster * group + r of each unit (past N: all zero)
-    const int crank = kGemmCluster > 1 ? (int)cluster_ctarank() : 0;
-    const int cid = (int)blockIdx.x / kGemmCluster, nclusters = (int)gridDim.x / kGemmCluster;
+    // work unit u = ((token tile * tiles_n + weight tile) * ksplit + K part);
+    // CTA b takes units b, b + gridDim.x, ...  Consecutive CTAs run
+    // neighbouring weight tiles against the same token tile, so an
+    // activation tile is read from DRAM about once and then from L2.
+    const int cid = (int)blockIdx.x, nctas = (int)gridDim.x;
     const int tiles_n = (p.N + kGemmBM - 1) / kGemmBM;
-    const int ngroups_n = (tiles_n + kGemmCluster - 1) / kGemmCluster;
-    // unit u = ((token tile * ngroups_n + weight group) * ksplit + K part)
     const int ksplit = p.ksplit;
-    const int units = ngroups_n * ((p.M + kGemmBN - 1) / kGemmBN) * ksplit;
-    const int my_tiles = units > cid ? (units - 1 - cid) / nclusters + 1 : 0;
-    auto tile_base = [&](int lt) { return (cid + lt * nclusters) / ksplit; };
-    auto tile_n0 = [&](int lt) { return ((tile_base(lt) % ngroups_n) * kGemmCluster + crank) * kGemmBM; };
-    auto tile_m0 = [&](int lt) { return (tile_base(lt) / ngroups_n) * kGemmBN; };
-    auto kpart = [&](int lt) { return (cid + lt * nclusters) % ksplit; };
-    constexpr uint16_t kAllCtas = (uint16_t)((1u << kGemmCluster) - 1);
+    const int units = tiles_n * ((p.M + kGemmBN - 1) / kGemmBN) * ksplit;
+    const int my_tiles = units > cid ? (units - 1 - cid) / nctas + 1 : 0;
+    auto tile_base = [&](int lt) { return (cid + lt * nctas) / ksplit; };
+    auto tile_n0 = [&](int lt) { return (tile_base(lt) % tiles_n) * kGemmBM; };
+    auto tile_m0 = [&](int lt) { return (tile_base(lt) / tiles_n) * kGemmBN; };
+    auto kpart = [&](int lt) { return (cid + lt * nctas) % ksplit; };
     const int ksteps = p.K / kGemmBK / ksplit;  // k-steps and packed groups of one unit
     const int groups = p.K / kGroup / ksplit;
 
@@ -319,7 +301,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
     if (tid == 0) {
         for (int s = 0; s < kGemmStagesB; ++s) {
             mbar_init(b_full(s), 1);
-            mbar_init(b_empty(s), kGemmCluster);  // every CTA's MMA releases every copy
+            mbar_init(b_empty(s), 1);
         }
         for (int s = 0; s < kSA; ++s) {
             mbar_init(a_full(s), kGemmDeqWarps);
@@ -340,9 +322,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
         tmem_relinquish();
     }
     tc_fence_before();
-    // peers multicast into this CTA's stages and arrive on its barriers: all
-    // barriers of the cluster are initialised before anyone proceeds
-    if (kGemmCluster > 1) cluster_sync_all(); else __syncthreads();
+    __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
@@ -359,14 +339,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
                     if (ki >= kGemmStagesB)
                         ok = mbar_wait(b_empty(sb), ((ki / kGemmStagesB) - 1) & 1, kErrGemmWait);
                     if (!ok) break;
-                    mbar_arrive_expect_tx(b_full(sb), kBBytes);  // all slices, from every CTA
-                    constexpr uint32_t kSlice = kBBytes / kGemmCluster;
-                    const uint32_t dst = smem_addr(smem + L.b + sb * kBBytes + crank * kSlice);
-                    const int y0 = m0 + crank * (kGemmBN / kGemmCluster);
-                    if (kGemmCluster > 1)
-                        tma_load_2d_multicast(dst, &xmap, (kbase + ks) * kGemmBK, y0, b_full(sb), kAllCtas);
-                    else
-                        tma_load_2d(dst, &xmap, (kbase + ks) * kGemmBK, y0, b_full(sb));
+                    mbar_arrive_expect_tx(b_full(sb), kBBytes);
+                    tma_load_2d(smem_addr(smem + L.b + sb * kBBytes), &xmap, (kbase + ks) * kGemmBK, m0,
+                                b_full(sb));
                 }
             }
         }
@@ -411,8 +386,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
                     for (int kk = 0; kk < kGemmBK / 16; ++kk)  // +32 bytes of K per MMA
                         umma_f16(dacc, ad + 2 * kk, bd + 2 * kk, idesc, (ks | kk) != 0);
                     umma_commit(a_empty(sa));
-                    if (kGemmCluster > 1) umma_commit_multicast(b_empty(sb), kAllCtas);
-                    else umma_commit(b_empty(sb));
+                    umma_commit(b_empty(sb));
                 }
                 umma_commit(acc_full(buf));  // also after an error: releases the epilogue
             }
@@ -524,9 +498,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
         }
     }
     tc_fence_before();
-    // no CTA leaves while a peer may still multicast into it or arrive on its
-    // barriers (every arrival precedes the peer's last accumulator commit)
-    if (kGemmCluster > 1) cluster_sync_all(); else __syncthreads();
+    __syncthreads();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
@@ -546,10 +518,10 @@ static cudaError_t launch_gemm_t(const void *W, const uint16_t *X, float *Y, int
                                  void *workspace, int sms, cudaStream_t stream) {
     __half *Xh = static_cast<__half *>(workspace);
     // K split: when the output tiles fill under about half of the persistent
-    // clusters, two units per tile (K halves) fill twice as many SMs
+    // CTAs, two units per tile (K halves) fill twice as many SMs
     const int tiles_n = (N + kGemmBM - 1) / kGemmBM;
-    const int units1 = ((tiles_n + kGemmCluster - 1) / kGemmCluster) * ((M + kGemmBN - 1) / kGemmBN);
-    const int slots = sms / kGemmCluster;
+    const int units1 = tiles_n * ((M + kGemmBN - 1) / kGemmBN);
+    const int slots = sms;
     auto occupancy = [&](int u) {
         const int waves = (u + slots - 1) / slots;
         return (double)u / ((double)waves * slots);
@@ -561,13 +533,13 @@ static cudaError_t launch_gemm_t(const void *W, const uint16_t *X, float *Y, int
     const int64_t work = n8 > ny / 4 ? n8 : ny / 4;
     int cgrid = (int)((work + 255) / 256);
     if (cgrid > 148 * 16) cgrid = 148 * 16;
-    x_to_f16_kernel<<<cgrid, 256, 0, stream>>>(X, Xh, n8, Y, ny);
+    qmm_x_to_f16_kernel<<<cgrid, 256, 0, stream>>>(X, Xh, n8, Y, ny);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
     CUtensorMap xmap, wmap;
     e = encode_tmap_2d(&xmap, Xh, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (uint64_t)K, (uint64_t)M,
-                       (uint64_t)K * 2, kGemmBK, kGemmBN / kGemmCluster, CU_TENSOR_MAP_SWIZZLE_128B);
+                       (uint64_t)K * 2, kGemmBK, kGemmBN, CU_TENSOR_MAP_SWIZZLE_128B);
     if (e != cudaSuccess) return e;
     constexpr int kCB = gemm_group_bytes(kFmt);
     const int64_t row_bytes = (int64_t)(K / kGroup) * kCB;
@@ -577,7 +549,7 @@ static cudaError_t launch_gemm_t(const void *W, const uint16_t *X, float *Y, int
 
     const GemmLayout L = gemm_layout(kFmt);
     static std::atomic<uint64_t> attr_done{0};
-    e = set_smem_limit_once(reinterpret_cast<const void *>(gemm_kernel<kFmt>), L.total, attr_done);
+    e = set_smem_limit_once(reinterpret_cast<const void *>(qmm_gemm_kernel<kFmt>), L.total, attr_done);
     if (e != cudaSuccess) return e;
     GemmParams p;
     p.Y = Y;
@@ -586,21 +558,9 @@ static cudaError_t launch_gemm_t(const void *W, const uint16_t *X, float *Y, int
     p.K = K;
     p.ksplit = ksplit;
     const int units = units1 * ksplit;
-    int nclusters = slots;  // one persistent CTA per SM
-    if (units < nclusters) nclusters = units;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(nclusters * kGemmCluster), 1, 1);
-    cfg.blockDim = dim3(kGemmThreads, 1, 1);
-    cfg.dynamicSmemBytes = (size_t)L.total;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)kGemmCluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_kernel<kFmt>, xmap, wmap, p);
+    const int grid = units < slots ? units : slots;  // one persistent CTA per SM
+    qmm_gemm_kernel<kFmt><<<grid, kGemmThreads, (size_t)L.total, stream>>>(xmap, wmap, p);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_gemm(int fmt, const void *W, const uint16_t *X, float *Y, int M, int N, int K,
