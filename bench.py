@@ -210,11 +210,11 @@ class Workload:
         self.model = {"w": [], "packed": {f: [] for f in self.fmts}, "x": [], "y": []}
         for layer in range(inputs.MODEL_LAYERS):
             for li, (name, n, k) in enumerate(inputs.MODEL_LINEARS):
-                w = inputs.weights(n, k, 50000 + 10 * layer + li, device=self.dev)
+                w = inputs.weights(n, k, inputs.model_weight_seed(layer, li), device=self.dev)
                 self.model["w"].append(w)
                 for f in self.fmts:
                     self.model["packed"][f].append(q.qmm_quantize(f, w))
-                self.model["x"].append(inputs.activations(1, k, 60000 + 10 * layer + li,
+                self.model["x"].append(inputs.activations(1, k, inputs.model_activation_seed(layer, li),
                                                           device=self.dev))
                 self.model["y"].append(torch.empty((1, n), dtype=torch.float32, device=self.dev))
 
@@ -307,7 +307,10 @@ def time_graphs(torch, graphs, steps, warmup, dev):
 
 
 def parity_check(wl):
-    """Sampled parity of the benchmarked kernels against the CPU oracle."""
+    """Sampled parity of the benchmarked kernels against the CPU oracle: the
+    decode-shaped linears (packed bytes of 64 rows; outputs of 4 rows at
+    M = 1, 16 and 2048) and the last layer of the model (packed bytes and
+    M = 1 outputs of 6 rows of each of its 7 linears, both formats)."""
     import numpy as np
     import oracle
     q, inputs = wl.q, wl.inputs
@@ -325,6 +328,25 @@ def parity_check(wl):
                 y = wl.y[m][f][si][:, ns].double().cpu().numpy()
                 r = float((np.abs(y - Y) / (1e-3 * A + 1e-6)).max())
                 worst = max(worst, r)
+    if wl.model is not None:
+        # the last model layer: its 7 linears, packed bytes and M = 1 outputs
+        # on a row sample, both formats
+        torch = wl.torch
+        layer = inputs.MODEL_LAYERS - 1
+        for li, (_, n, k) in enumerate(inputs.MODEL_LINEARS):
+            j = layer * len(inputs.MODEL_LINEARS) + li
+            rows = np.array(sorted({0, 1, n // 3, n // 2, n - 2, n - 1}), dtype=np.int64)
+            ridx = torch.from_numpy(rows).to(wl.dev)
+            wb = inputs.bf16_bits(wl.model["w"][j][ridx])
+            xb = inputs.bf16_bits(wl.model["x"][j])
+            for f in wl.fmts:
+                want = oracle.quantize(f, wb)
+                packed = wl.model["packed"][f][j]
+                if not np.array_equal(packed[ridx].cpu().numpy(), want):
+                    return "FAIL: model packed bytes differ (fmt %d linear %d)" % (f, j)
+                y = q.qmm_matmul(f, packed, wl.model["x"][j], n)[:, ridx].double().cpu().numpy()
+                Y, A = oracle.matmul(f, want, xb, rows.size, k)
+                worst = max(worst, float((np.abs(y - Y) / (1e-3 * A + 1e-6)).max()))
     return "ok (max err/bound %.3f)" % worst if worst <= 1.0 else "FAIL (max err/bound %.3f)" % worst
 
 

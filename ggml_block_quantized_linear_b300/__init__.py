@@ -74,6 +74,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
         L.qmm_device_error_take.restype = ctypes.c_int
         L.qmm_version.argtypes = []
         L.qmm_version.restype = ctypes.c_char_p
+        L.qmm_selftest_bounded_wait.argtypes = [i64, vp]
+        L.qmm_selftest_bounded_wait.restype = ctypes.c_int
+        L.qmm_matmul_prefill_static.argtypes = [ctypes.c_int, vp, vp, vp, i64, i64, i64, vp]
+        L.qmm_matmul_prefill_static.restype = ctypes.c_int
         if path is None:
             _lib = L
         return L
@@ -112,6 +116,15 @@ def qmm_matmul_workspace_bytes(fmt: int, M: int, N: int, K: int) -> int:
 
 def qmm_device_error_take() -> int:
     return int(load().qmm_device_error_take())
+
+
+QMM_DEVERR_SELFTEST_TIMEOUT = 901
+
+
+def qmm_selftest_bounded_wait(limit_ns: int, stream=None) -> None:
+    """Launch the bounded-wait self-test kernel (see include/qmm.h)."""
+    _check("qmm_selftest_bounded_wait",
+           load().qmm_selftest_bounded_wait(int(limit_ns), _stream_ptr(stream)))
 
 
 def qmm_quantize(fmt: int, src, out=None, stream=None):

@@ -228,7 +228,7 @@ __device__ __forceinline__ void q4k_half(const uint8_t *base, int rstride, const
 
 template <int kFmt, int kNT>
 __global__ void __launch_bounds__(kGemvThreads)
-gemv_kernel(const __grid_constant__ CUtensorMap wmap, const GemvParams p) {
+qmm_gemv_cluster_kernel(const __grid_constant__ CUtensorMap wmap, const GemvParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int kCB = kFmt == 8 ? kQ8GroupBytes : kQ4Bytes;  // bytes per row per chunk
     constexpr int kSlot = kCB;
@@ -462,7 +462,7 @@ static cudaError_t launch_gemv_t(const GemvParams &p, const GemvPlan &pl, cudaSt
                                     (uint64_t)p.row_bytes, kCB / 2, kGemvRows);
     if (te != cudaSuccess) return te;
     static std::atomic<uint64_t> attr_done{0};
-    cudaError_t e = set_smem_limit_once(reinterpret_cast<const void *>(gemv_kernel<kFmt, kNT>), 227 * 1024,
+    cudaError_t e = set_smem_limit_once(reinterpret_cast<const void *>(qmm_gemv_cluster_kernel<kFmt, kNT>), 227 * 1024,
                                         attr_done);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -479,7 +479,7 @@ static cudaError_t launch_gemv_t(const GemvParams &p, const GemvPlan &pl, cudaSt
     attr[1].val.programmaticStreamSerializationAllowed = QMM_GEMV_PDL;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<kFmt, kNT>, wmap, p);
+    return cudaLaunchKernelEx(&cfg, qmm_gemv_cluster_kernel<kFmt, kNT>, wmap, p);
 }
 
 cudaError_t launch_gemv(int fmt, const void *W, const uint16_t *X, float *Y, int M, int N, int K,

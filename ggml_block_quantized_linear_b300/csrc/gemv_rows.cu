@@ -247,7 +247,7 @@ __device__ __forceinline__ void rq4_group(const uint8_t *r0, const uint8_t *r1, 
 // their register budget allows two CTAs per SM instead of three.
 template <int kFmt, int kNT>
 __global__ void __launch_bounds__(kThreadsR, kNT == 1 ? 3 : 2)
-gemv_rows_kernel(const __grid_constant__ CUtensorMap wmap, const RowsParams p) {
+qmm_gemv_rows_kernel(const __grid_constant__ CUtensorMap wmap, const RowsParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int kCB = kFmt == 8 ? kQ8GroupBytes : kQ4Bytes;
     constexpr int kPitch = 2 * kCB;               // stage row: two chunks
@@ -461,7 +461,7 @@ gemv_rows_kernel(const __grid_constant__ CUtensorMap wmap, const RowsParams p) {
 template <int kFmt, int kNT>
 static cudaError_t rows_set_attrs() {
     static std::atomic<uint64_t> done{0};
-    return set_smem_limit_once(reinterpret_cast<const void *>(gemv_rows_kernel<kFmt, kNT>), 227 * 1024, done);
+    return set_smem_limit_once(reinterpret_cast<const void *>(qmm_gemv_rows_kernel<kFmt, kNT>), 227 * 1024, done);
 }
 
 // Resident CTAs per SM for a given dynamic shared-memory size (registers,
@@ -469,7 +469,7 @@ static cudaError_t rows_set_attrs() {
 template <int kFmt, int kNT>
 static int rows_occupancy(int smem) {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemv_rows_kernel<kFmt, kNT>, kThreadsR,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, qmm_gemv_rows_kernel<kFmt, kNT>, kThreadsR,
                                                       (size_t)smem) != cudaSuccess)
         return 1;
     return n < 1 ? 1 : n;
@@ -562,7 +562,7 @@ static cudaError_t launch_rows_t(const void *W, RowsParams &p, int sms, cudaStre
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_rows_kernel<kFmt, kNT>, wmap, p);
+    return cudaLaunchKernelEx(&cfg, qmm_gemv_rows_kernel<kFmt, kNT>, wmap, p);
 }
 
 cudaError_t launch_gemv_rows(int fmt, const void *W, const uint16_t *X, float *Y, int M, int N, int K,

@@ -69,6 +69,26 @@ static bool known_fmt(qmm_format f) { return f == QMM_Q8_0 || f == QMM_Q4_K; }
 
 static qmm_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA; }
 
+// Self-test of the bounded-wait path that every kernel's mbarrier waits use:
+// one warp waits on a barrier that has completed (must succeed) and then on
+// one that nothing ever arrives on (must give up after limit_ns, record
+// kErrSelftestTimeout and return).  No copy is in flight, nothing faults.
+__global__ void __launch_bounds__(32) qmm_selftest_wait_kernel(uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bars[2];
+    const uint32_t done = smem_addr(&bars[0]), never = smem_addr(&bars[1]);
+    if (threadIdx.x == 0) {
+        mbar_init(done, 1);
+        mbar_init(never, 1);
+        fence_mbar_init();
+        mbar_arrive(done);  // completes phase 0 of `done`
+    }
+    __syncwarp();
+    if (threadIdx.x == 0) {
+        if (mbar_wait_limit(done, 0, kErrSelftestUnexpected, limit_ns))
+            mbar_wait_limit(never, 0, kErrSelftestTimeout, limit_ns);
+    }
+}
+
 }  // namespace qmm
 
 using namespace qmm;
@@ -165,6 +185,12 @@ int qmm_device_error_take(void) {
     return v;
 }
 
-const char *qmm_version(void) { return "qmm 0.1.0 sm_103a"; }
+qmm_status qmm_selftest_bounded_wait(int64_t limit_ns, qmm_stream_t stream) {
+    if (limit_ns <= 0 || limit_ns > 100000000) return QMM_ERR_INVALID_ARG;
+    qmm_selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>((uint64_t)limit_ns);
+    return from_cuda(cudaGetLastError());
+}
+
+const char *qmm_version(void) { return "qmm 0.2.0 sm_103a"; }
 
 }  // extern "C"

@@ -217,7 +217,7 @@ template <> struct Lane32<false> {
 // shared memory and stored with coalesced 16-byte writes.
 template <bool kSrcF32>
 __global__ void __launch_bounds__(kQuantThreads, kSrcF32 ? 3 : 4)
-quantize_q8_0_kernel(const void *__restrict__ src, uint8_t *__restrict__ dst, int64_t nblocks) {
+qmm_quantize_q8_0_kernel(const void *__restrict__ src, uint8_t *__restrict__ dst, int64_t nblocks) {
     __shared__ __align__(16) uint8_t stage[kQuantWarps][32 * kQ8Bytes];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint8_t *st = stage[warp];
@@ -306,7 +306,7 @@ quantize_q8_0_kernel(const void *__restrict__ src, uint8_t *__restrict__ dst, in
 }
 
 __global__ void __launch_bounds__(kQuantThreads)
-dequantize_q8_0_kernel(const uint8_t *__restrict__ src, float *__restrict__ dst, int64_t ngroups) {
+qmm_dequantize_q8_0_kernel(const uint8_t *__restrict__ src, float *__restrict__ dst, int64_t ngroups) {
     __shared__ __align__(16) uint8_t stage[kQuantWarps][kQ8GroupBytes];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int blk = lane >> 2, part = lane & 3;
@@ -343,7 +343,7 @@ dequantize_q8_0_kernel(const uint8_t *__restrict__ src, float *__restrict__ dst,
 #endif
 template <bool kSrcF32>
 __global__ void __launch_bounds__(kQuantThreads, QMM_Q4_QUANT_MIN_BLOCKS)
-quantize_q4_k_kernel(const void *__restrict__ src, uint8_t *__restrict__ dst, int64_t nsuper) {
+qmm_quantize_q4_k_kernel(const void *__restrict__ src, uint8_t *__restrict__ dst, int64_t nsuper) {
     __shared__ __align__(16) uint8_t stage[kQuantWarps][4 * kQ4Bytes];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int sj = lane & 7, sbl = lane >> 3;  // sub-block j, superblock in the warp tile
@@ -475,7 +475,7 @@ __device__ __forceinline__ void q4k_codes(const uint8_t *s, int j, int &sc, int 
 }
 
 __global__ void __launch_bounds__(kQuantThreads)
-dequantize_q4_k_kernel(const uint8_t *__restrict__ src, float *__restrict__ dst, int64_t ngroups) {
+qmm_dequantize_q4_k_kernel(const uint8_t *__restrict__ src, float *__restrict__ dst, int64_t ngroups) {
     __shared__ __align__(16) uint8_t stage[kQuantWarps][kQ4Bytes];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int sub = lane >> 2, part = lane & 3;
@@ -529,16 +529,16 @@ cudaError_t launch_quantize(int fmt, int src_f32, const void *src, void *dst, in
         const int64_t nblocks = nweights / kQ8Weights;
         const int grid = grid_for(nblocks, 32 * kQuantWarps, sms);
         if (src_f32)
-            quantize_q8_0_kernel<true><<<grid, kQuantThreads, 0, stream>>>(src, d, nblocks);
+            qmm_quantize_q8_0_kernel<true><<<grid, kQuantThreads, 0, stream>>>(src, d, nblocks);
         else
-            quantize_q8_0_kernel<false><<<grid, kQuantThreads, 0, stream>>>(src, d, nblocks);
+            qmm_quantize_q8_0_kernel<false><<<grid, kQuantThreads, 0, stream>>>(src, d, nblocks);
     } else {
         const int64_t nsuper = nweights / kQ4Weights;
         const int grid = grid_for(nsuper, 4 * kQuantWarps, sms);
         if (src_f32)
-            quantize_q4_k_kernel<true><<<grid, kQuantThreads, 0, stream>>>(src, d, nsuper);
+            qmm_quantize_q4_k_kernel<true><<<grid, kQuantThreads, 0, stream>>>(src, d, nsuper);
         else
-            quantize_q4_k_kernel<false><<<grid, kQuantThreads, 0, stream>>>(src, d, nsuper);
+            qmm_quantize_q4_k_kernel<false><<<grid, kQuantThreads, 0, stream>>>(src, d, nsuper);
     }
     return cudaGetLastError();
 }
@@ -550,9 +550,9 @@ cudaError_t launch_dequantize(int fmt, const void *src, float *dst, int64_t nwei
     const int grid = grid_for(ngroups, kQuantWarps, sms);
     const uint8_t *s = static_cast<const uint8_t *>(src);
     if (fmt == 8)
-        dequantize_q8_0_kernel<<<grid, kQuantThreads, 0, stream>>>(s, dst, ngroups);
+        qmm_dequantize_q8_0_kernel<<<grid, kQuantThreads, 0, stream>>>(s, dst, ngroups);
     else
-        dequantize_q4_k_kernel<<<grid, kQuantThreads, 0, stream>>>(s, dst, ngroups);
+        qmm_dequantize_q4_k_kernel<<<grid, kQuantThreads, 0, stream>>>(s, dst, ngroups);
     return cudaGetLastError();
 }
 

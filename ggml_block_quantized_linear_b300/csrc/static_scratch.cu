@@ -10,8 +10,6 @@
 // synchronise the device.  This entry point runs the same kernels with the
 // scratch in a fixed, file-scope device array instead, so it allocates
 // nothing at call time.
-#include <mutex>
-
 #include "common.cuh"
 #include "qmm.h"
 
@@ -22,26 +20,14 @@ namespace qmm {
 constexpr size_t kStaticScratchBytes = (size_t)64 << 20;
 static __device__ __align__(256) uint8_t g_prefill_scratch[kStaticScratchBytes];
 
-// Device address of g_prefill_scratch, looked up once per device with that
-// device current (in host code the symbol is only a host-side stand-in).
+// Device address of g_prefill_scratch in the current device's context (in
+// host code the symbol is only a host-side stand-in).  It is looked up on
+// every call, not cached: after a device reset the module is loaded again
+// and the array may move.
 static void *static_scratch_for_current_device(cudaError_t *err) {
-    static std::mutex mu;
-    static void *addr[64] = {nullptr};
-    int dev = 0;
-    *err = cudaGetDevice(&dev);
-    if (*err != cudaSuccess) return nullptr;
-    if (dev < 0 || dev >= 64) {
-        *err = cudaErrorInvalidDevice;
-        return nullptr;
-    }
-    std::lock_guard<std::mutex> lock(mu);
-    if (addr[dev] == nullptr) {
-        void *p = nullptr;
-        *err = cudaGetSymbolAddress(&p, g_prefill_scratch);
-        if (*err != cudaSuccess) return nullptr;
-        addr[dev] = p;
-    }
-    return addr[dev];
+    void *p = nullptr;
+    *err = cudaGetSymbolAddress(&p, g_prefill_scratch);
+    return *err == cudaSuccess ? p : nullptr;
 }
 
 }  // namespace qmm

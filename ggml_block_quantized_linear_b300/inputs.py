@@ -42,6 +42,15 @@ def seed_for(config: int, shape_index: int = 0, m_index: int = 0) -> int:
     return 1000 * config + 10 * shape_index + m_index
 
 
+def model_weight_seed(layer: int, linear_index: int) -> int:
+    """Seed of linear ``linear_index`` (MODEL_LINEARS order) of model layer ``layer``."""
+    return 50000 + 10 * layer + linear_index
+
+
+def model_activation_seed(layer: int, linear_index: int) -> int:
+    return 60000 + 10 * layer + linear_index
+
+
 def weights(n: int, k: int, seed: int, device="cpu", fp32: bool = False) -> torch.Tensor:
     """W[n x k]: N(0, 0.02) with 0.1 % outliers x20; bf16 unless ``fp32``."""
     g = torch.Generator(device=device)

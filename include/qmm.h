@@ -48,9 +48,8 @@
  *    reported by the CUDA runtime maps to QMM_ERR_CUDA.  Faults during the
  *    asynchronous execution surface at the caller's next synchronisation.
  *  - NaN or infinite inputs give unspecified (but memory-safe) results.
- *  - qmm_matmul converts the bf16 activations to binary16 for the tensor
- *    cores: |x| must stay below 65504, and activations below 2^-14 in
- *    magnitude keep an absolute precision of 2^-25.
+ *  - qmm_matmul feeds binary16 operands to the tensor cores (see its
+ *    declaration for the exact accuracy contract): |x| must stay below 65504.
  *  - No C++ exception crosses this interface.
  */
 #ifndef QMM_H
@@ -105,9 +104,13 @@ QMM_API size_t qmm_packed_bytes(qmm_format fmt, int64_t rows, int64_t cols);
 QMM_API qmm_status qmm_quantize(qmm_format fmt, qmm_src_dtype st, const void *src, void *dst_packed,
                         int64_t rows, int64_t cols, qmm_stream_t stream);
 
-/* dst[rows x cols] (fp32) = the exactly dequantized weights of src_packed.
- * Every value is exact except the single rounding of Q4_K's final
- * subtraction.  One kernel launch. */
+/* dst[rows x cols] (fp32) = the dequantized weights of src_packed: Q8_0
+ * d * q, Q4_K (d*sc_j) * q - dmin*mc_j (formulas above).  The pages fix only
+ * what the formats are (mistral.rs "Quantization types", tables "Q*K family"
+ * and "Legacy GGML types"); the values are those of the layouts above.  Every
+ * value is exact except the single rounding of Q4_K's final subtraction.
+ * src_packed: qmm_packed_bytes(fmt, rows, cols) bytes; dst: rows * cols fp32.
+ * One kernel launch. */
 QMM_API qmm_status qmm_dequantize(qmm_format fmt, const void *src_packed, float *dst, int64_t rows,
                           int64_t cols, qmm_stream_t stream);
 
@@ -116,17 +119,30 @@ QMM_API qmm_status qmm_dequantize(qmm_format fmt, const void *src_packed, float 
 QMM_API size_t qmm_matmul_workspace_bytes(qmm_format fmt, int64_t M, int64_t N, int64_t K);
 
 /* Y[M x N] (fp32, row-major) = X[M x K] (bf16 bit patterns, row-major) times
- * the transpose of the packed weights W[N x K].  M <= 16 runs a decode
- * kernel: persistent CTAs over 16-row tiles when the tiles fill the GPU
- * (each tile's partial sums added in a fixed order), otherwise split-K over
- * a thread-block cluster reduced in distributed shared memory in a fixed
- * order; both are deterministic.  Larger M runs the prefill kernel (tcgen05
- * tensor cores, TMEM accumulators; with K split in two when the output tiles
- * fill under half the SMs, the two halves add onto a zeroed Y, which is
- * still deterministic).  Accuracy: per element
- * |y - y_exact| <= 1e-3 * sum_k |w^_k x_k| + 1e-6, where w^ are the
- * dequantized weights.  `workspace` must hold
- * qmm_matmul_workspace_bytes(fmt, M, N, K) bytes (or be NULL when that is 0). */
+ * the transpose of the packed weights W[N x K] (qmm_packed_bytes(fmt, N, K)
+ * bytes).  The split follows mistral.rs "Quantization types", section
+ * "NVFP4" (a dedicated matrix-vector kernel for small decode batches, tiled
+ * matrix multiplication for larger ones), and the large-batch kernel converts
+ * each weight tile inside the GEMM as that page's section "FP8" describes for
+ * W8A16.  M <= 16 runs a decode kernel: persistent CTAs over 16-row tiles
+ * when the tiles fill the GPU (each tile's partial sums added in a fixed
+ * order), otherwise split-K over a thread-block cluster reduced in
+ * distributed shared memory in a fixed order; both are deterministic.
+ * Larger M runs the prefill kernel (tcgen05 tensor cores, TMEM accumulators;
+ * with K split in two when the output tiles fill under half the SMs, the two
+ * halves add onto a zeroed Y, which is still deterministic).
+ *
+ * Accuracy, per element, with w^ the dequantized weights:
+ *   |y - y_exact| <= 1e-3 * sum_k |w^_k x_k| + 1e-6 + 2^-25 * T,
+ * where T = sum over k of |x_k| for the weights with |w^_k| < 2^-14 (prefill
+ * path, M > 16, only) plus |w^_k| for the activations with |x_k| < 2^-14 (both
+ * paths).  Both paths round each activation to binary16 once, and the prefill
+ * path also rounds each dequantized weight to binary16 once: a relative error
+ * of at most 2^-11 for values in binary16's normal range, an absolute error
+ * of at most 2^-25 below it.  T is 0 when no such values occur; for the
+ * synthetic weights and activations of the tests it is negligible.
+ * `workspace` must hold qmm_matmul_workspace_bytes(fmt, M, N, K) bytes (or be
+ * NULL when that is 0); it is only read and written by this call's kernels. */
 QMM_API qmm_status qmm_matmul(qmm_format fmt, const void *W_packed, const uint16_t *X_bf16, float *Y,
                       int64_t M, int64_t N, int64_t K, void *workspace, size_t workspace_bytes,
                       qmm_stream_t stream);
@@ -143,9 +159,10 @@ QMM_API qmm_status qmm_matmul(qmm_format fmt, const void *W_packed, const uint16
  *    M * K <= 32 Mi); larger problems return QMM_ERR_WORKSPACE and launch
  *    nothing.  M <= 16 returns QMM_ERR_UNSUPPORTED: the decode path needs no
  *    scratch, call qmm_matmul with a NULL workspace.
- *  - The first call on a device looks up the array's device address with
- *    that device current (cudaGetSymbolAddress); make that first call before
- *    any stream capture.
+ *  - Every call looks up the array's address in the current device's
+ *    context (cudaGetSymbolAddress), so it stays valid after a device reset.
+ *    The first call on a device may load the library's device code: make
+ *    that first call before any stream capture.
  *  - All calls share the one array: calls whose executions overlap on the
  *    GPU (different streams, or different host threads on one device) race
  *    on it.  Serialise them, e.g. on one stream.  Nothing in the array needs
@@ -157,14 +174,34 @@ QMM_API qmm_status qmm_matmul_prefill_static(qmm_format fmt, const void *W_packe
 /* Static description of a status code (never NULL). */
 QMM_API const char *qmm_status_string(qmm_status s);
 
+/* Codes a kernel records in the device error word (qmm_device_error_take). */
+typedef enum {
+    QMM_DEVERR_NONE = 0,
+    QMM_DEVERR_GEMV_FULL_WAIT = 101,   /* decode: waited too long for a stage */
+    QMM_DEVERR_GEMV_EMPTY_WAIT = 102,  /* decode: waited too long for a free slot */
+    QMM_DEVERR_GEMM_WAIT = 201,        /* prefill: a pipeline wait ran out */
+    QMM_DEVERR_SELFTEST_TIMEOUT = 901, /* qmm_selftest_bounded_wait: expected */
+    QMM_DEVERR_SELFTEST_UNEXPECTED = 902
+} qmm_device_error;
+
 /* Kernels never trap.  A wait inside a kernel that exceeds its time limit
  * (about two seconds; it can only happen through a bug) makes the kernel
- * record a nonzero code in a device word and return early.  This call
- * synchronises the current device, returns that code (0 = none) and clears
- * it. */
+ * record a nonzero code (qmm_device_error; the first one recorded is kept) in
+ * a device word and return early.  This call synchronises the current device,
+ * returns that code (0 = none) and clears it; -1 if the synchronisation or
+ * the copy of the word failed. */
 QMM_API int qmm_device_error_take(void);
 
-/* Library version, e.g. "qmm 0.1.0 sm_103a". */
+/* Diagnostic (no counterpart on the pages): runs the bounded-wait path that
+ * every kernel's pipeline waits use, on one warp: a wait on a completed
+ * barrier (must succeed) and then one on a barrier that nothing arrives on,
+ * which must give up after limit_ns nanoseconds (1 .. 1e8), record
+ * QMM_DEVERR_SELFTEST_TIMEOUT and return.  Nothing faults and no copy is in
+ * flight.  The next qmm_device_error_take() then returns 901 and the device
+ * stays usable.  Returns QMM_ERR_INVALID_ARG for a limit out of range. */
+QMM_API qmm_status qmm_selftest_bounded_wait(int64_t limit_ns, qmm_stream_t stream);
+
+/* Library version, e.g. "qmm 0.2.0 sm_103a". */
 QMM_API const char *qmm_version(void);
 
 #ifdef __cplusplus

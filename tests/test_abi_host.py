@@ -113,6 +113,21 @@ def test_workspace_query(lib):
     assert L.qmm_matmul(4, FAKE, FAKE, FAKE, 32, 64, 256, MISALIGNED, 1 << 20, S0) == q.QMM_ERR_ALIGNMENT
 
 
+def test_selftest_limit_checked_on_the_host(lib):
+    for bad in (0, -5, 100000001):
+        assert lib.qmm_selftest_bounded_wait(bad, S0) == q.QMM_ERR_INVALID_ARG
+
+
+def test_static_prefill_argument_errors(lib):
+    f = lib.qmm_matmul_prefill_static
+    # M * K * 2 bytes of scratch beyond the fixed 64 MiB array
+    assert f(8, FAKE, FAKE, FAKE, 4096, 64, 16384 + 256, S0) == q.QMM_ERR_WORKSPACE
+    assert f(8, FAKE, FAKE, FAKE, 16, 64, 256, S0) == q.QMM_ERR_UNSUPPORTED
+    assert f(4, FAKE, FAKE, FAKE, 32, 64, 300, S0) == q.QMM_ERR_SHAPE
+    assert f(4, NULL, FAKE, FAKE, 32, 64, 256, S0) == q.QMM_ERR_INVALID_ARG
+    assert f(4, FAKE, MISALIGNED, FAKE, 32, 64, 256, S0) == q.QMM_ERR_ALIGNMENT
+
+
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError):
         q.load(str(tmp_path / "nope.so"))
