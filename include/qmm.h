@@ -142,7 +142,8 @@ QMM_API size_t qmm_matmul_workspace_bytes(qmm_format fmt, int64_t M, int64_t N, 
  * of at most 2^-25 below it.  T is 0 when no such values occur; for the
  * synthetic weights and activations of the tests it is negligible.
  * `workspace` must hold qmm_matmul_workspace_bytes(fmt, M, N, K) bytes (or be
- * NULL when that is 0); it is only read and written by this call's kernels. */
+ * NULL when that is 0): the prefill path keeps the binary16 copy of X there.
+ * It is only read and written by this call's kernels. */
 QMM_API qmm_status qmm_matmul(qmm_format fmt, const void *W_packed, const uint16_t *X_bf16, float *Y,
                       int64_t M, int64_t N, int64_t K, void *workspace, size_t workspace_bytes,
                       qmm_stream_t stream);
