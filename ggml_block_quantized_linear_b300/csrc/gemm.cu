@@ -14,9 +14,18 @@
 // activations are converted to binary16 once per call (first kernel below)
 // into the caller's workspace.
 //
-// Tile: 128 weight rows (the MMA's M side, "swap AB") x 256 tokens (MMA N)
-// x 64 K per stage; persistent CTAs (one per SM) walk the tiles, and two fp32
-// accumulators of 256 TMEM columns alternate between consecutive tiles.
+// Tile: 128 weight rows (the MMA's M side, "swap AB") x BN tokens (MMA N:
+// 32, 64, 128 or 256, the smallest that holds M up to 128, else 256) x 64 K
+// per stage; persistent CTAs (one per SM) walk the work units, and two fp32
+// accumulators of BN TMEM columns alternate between consecutive units.
+// When the output tiles are fewer than the SMs, K is split into parts (a
+// unit is one part of one tile).  256-token tiles: at most two parts, both
+// added onto a Y zeroed by the conversion launch (two additions onto zero
+// commute, so the result does not depend on their order).  Smaller tiles:
+// up to 8 parts; each part stores its partial tile in the workspace and takes
+// a ticket, and the last part of a tile to arrive adds all parts in part
+// order and writes Y.  Both are deterministic and nothing ever waits for
+// another CTA.
 //   warp 0       TMA producer of the binary16 activation tiles (128B-swizzled
 //                boxes, each CTA loading its own)
 //   warp 1       TMEM allocator and single-thread MMA issuer
@@ -33,7 +42,6 @@
 namespace qmm {
 
 constexpr int kGemmBM = 128;        // weight rows per CTA (MMA M)
-constexpr int kGemmBN = 256;        // tokens per CTA (MMA N)
 constexpr int kGemmBK = 64;         // K per stage (one 128-byte swizzle atom of f16)
 #ifndef QMM_GEMM_DEQ_WARPS
 #define QMM_GEMM_DEQ_WARPS 16
@@ -51,16 +59,14 @@ constexpr int kGemmThreads = (kGemmWarpPackedTma + 1) * 32;
 #define QMM_GEMM_STAGES_A_Q4 3
 #endif
 constexpr int kGemmStagesP = 2;     // packed weight groups
-constexpr int kGemmTmemCols = 512;  // two 256-column fp32 accumulators
+// two BN-column fp32 accumulators (a power of two, at least 32 columns)
+__host__ __device__ constexpr int gemm_tmem_cols(int bn) { return 2 * bn < 32 ? 32 : 2 * bn; }
 // Q4_K (S_j, Mn_j) table: 16 floats per weight row, padded to 18 so that the
 // rows a warp reads together (2 apart) fall in different banks
 constexpr int kGemmCoefStride = 18;
 static_assert((kGemmBM / (4 * kGemmDeqWarps)) % 2 == 0, "dequantization passes come in even / odd row pairs");
-#ifndef QMM_GEMM_SPLIT_K  // 1: split K in two for under-filled grids
-#define QMM_GEMM_SPLIT_K 1
-#endif
 
-// activation stages (32 KB each) and dequantized-weight stages (16 KB each)
+// activation stages (BN x 128 bytes each) and dequantized-weight stages (16 KB each)
 __host__ __device__ constexpr int gemm_stages_b(int fmt) { return fmt == 8 ? 3 : QMM_GEMM_STAGES_B_Q4; }
 __host__ __device__ constexpr int gemm_stages_a(int fmt) { return fmt == 8 ? 3 : QMM_GEMM_STAGES_A_Q4; }
 __host__ __device__ constexpr int gemm_group_bytes(int fmt) { return fmt == 8 ? kQ8GroupBytes : kQ4Bytes; }
@@ -69,11 +75,11 @@ struct GemmLayout {
     int b, a, p, coef, bars, total;  // offsets from the 1024-aligned base
 };
 
-__host__ __device__ inline GemmLayout gemm_layout(int fmt) {
+__host__ __device__ inline GemmLayout gemm_layout(int fmt, int bn) {
     GemmLayout L;
     int off = 0;
     L.b = off;
-    off += gemm_stages_b(fmt) * kGemmBN * kGemmBK * 2;
+    off += gemm_stages_b(fmt) * bn * kGemmBK * 2;
     L.a = off;
     off += gemm_stages_a(fmt) * kGemmBM * kGemmBK * 2;
     L.p = off;
@@ -82,7 +88,7 @@ __host__ __device__ inline GemmLayout gemm_layout(int fmt) {
     off += fmt == 4 ? kGemmBM * kGemmCoefStride * 4 : 0;
     off = (off + 15) & ~15;
     L.bars = off;
-    off += 64 * 8;  // barriers + TMEM address slot
+    off += 64 * 8;  // barriers, TMEM address slot, last-part flag
     L.total = off + 1024;  // + alignment slack of the dynamic base
     return L;
 }
@@ -161,12 +167,14 @@ __device__ __forceinline__ void fence_async_smem() {
 }
 
 // ----------------------------------------------------- activation conversion
-// X bf16 -> binary16 (round to nearest), 8 elements per thread.
-// With a K split, the same launch also zeroes Y (ny floats; 0 otherwise),
-// which the split GEMM then accumulates into.
+// X bf16 -> binary16 (round to nearest), 8 elements per thread.  With a K
+// split, the same launch also clears the tiles' tickets (nt words) or zeroes
+// Y (ny floats) for the parts to add onto.
 __global__ void __launch_bounds__(256) qmm_x_to_f16_kernel(const uint16_t *__restrict__ X,
-                                                       __half *__restrict__ Xh, int64_t n8,
-                                                       float *__restrict__ Yz, int64_t ny) {
+                                                           __half *__restrict__ Xh, int64_t n8,
+                                                           int *__restrict__ tickets, int nt,
+                                                           float *__restrict__ Yz, int64_t ny) {
+    for (int i = blockIdx.x * 256 + threadIdx.x; i < nt; i += gridDim.x * 256) tickets[i] = 0;
     const int64_t y4 = ny / 4;  // Y is 16-byte aligned
     for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < y4; i += (int64_t)gridDim.x * 256)
         reinterpret_cast<float4 *>(Yz)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -245,8 +253,11 @@ __device__ __forceinline__ uint4 deq8_q4_k(const uint8_t *prow, const float *coe
 // ------------------------------------------------------------------ kernel
 struct GemmParams {
     float *Y;
+    float *partials;  // ticket mode: [tile][part][128 rows][BN columns] fp32
+    int *tickets;     // ticket mode: parts of each tile done so far (cleared by the conversion launch)
     int M, N, K;
-    int ksplit;  // 1, or 2: each output tile is two units (K halves) added into a zeroed Y
+    int ksplit;       // K parts per output tile
+    int tickets_mode; // 1: partial tiles + tickets; 0: (ksplit 2) add onto a zeroed Y
 };
 
 // Persistent: CTA b computes the output tiles b, b + gridDim.x, ... (weight
@@ -254,18 +265,19 @@ struct GemmParams {
 // A stages) runs on across tiles, and the two TMEM accumulators alternate
 // between tiles, so the epilogue of one tile overlaps the main loop of the
 // next.
-template <int kFmt>
+template <int kFmt, int kBN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
 qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
-            const GemmParams p) {
+                const GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     constexpr int kSA = gemm_stages_a(kFmt);
     constexpr int kGemmStagesB = gemm_stages_b(kFmt);
     constexpr int kCB = gemm_group_bytes(kFmt);
-    constexpr uint32_t kBBytes = kGemmBN * kGemmBK * 2;
+    constexpr uint32_t kBBytes = kBN * kGemmBK * 2;
+    constexpr int kTmemCols = gemm_tmem_cols(kBN);
     constexpr uint32_t kABytes = kGemmBM * kGemmBK * 2;
     constexpr uint32_t kPBytes = kGemmBM * kCB;
-    const GemmLayout L = gemm_layout(kFmt);
+    const GemmLayout L = gemm_layout(kFmt, kBN);
     // 1024-byte aligned base for the 128B-swizzled stages, kept as an offset
     // into the shared array so that every access compiles to LDS / STS
     // (an address rounded through an integer would be a generic pointer)
@@ -278,14 +290,16 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
     const int cid = (int)blockIdx.x, nctas = (int)gridDim.x;
     const int tiles_n = (p.N + kGemmBM - 1) / kGemmBM;
     const int ksplit = p.ksplit;
-    const int units = tiles_n * ((p.M + kGemmBN - 1) / kGemmBN) * ksplit;
+    const int units = tiles_n * ((p.M + kBN - 1) / kBN) * ksplit;
     const int my_tiles = units > cid ? (units - 1 - cid) / nctas + 1 : 0;
     auto tile_base = [&](int lt) { return (cid + lt * nctas) / ksplit; };
     auto tile_n0 = [&](int lt) { return (tile_base(lt) % tiles_n) * kGemmBM; };
-    auto tile_m0 = [&](int lt) { return (tile_base(lt) / tiles_n) * kGemmBN; };
+    auto tile_m0 = [&](int lt) { return (tile_base(lt) / tiles_n) * kBN; };
     auto kpart = [&](int lt) { return (cid + lt * nctas) % ksplit; };
-    const int ksteps = p.K / kGemmBK / ksplit;  // k-steps and packed groups of one unit
-    const int groups = p.K / kGroup / ksplit;
+    // packed groups [kg0, kg1) of the unit's K part (parts differ by at most one group)
+    const int gtot = p.K / kGroup;
+    auto kg0 = [&](int lt) { return (int)((int64_t)gtot * kpart(lt) / ksplit); };
+    auto kg1 = [&](int lt) { return (int)((int64_t)gtot * (kpart(lt) + 1) / ksplit); };
 
     const uint32_t bar = smem_addr(smem + L.bars);
     auto b_full = [&](int s) { return bar + 8u * s; };
@@ -297,6 +311,7 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
     auto acc_full = [&](int b) { return bar + 8u * (20 + b); };
     auto acc_empty = [&](int b) { return bar + 8u * (22 + b); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.bars + 8 * 24);
+    volatile int *last_slot = reinterpret_cast<volatile int *>(smem + L.bars + 8 * 25);
 
     if (tid == 0) {
         for (int s = 0; s < kGemmStagesB; ++s) {
@@ -318,7 +333,7 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(smem_addr(tmem_slot), kGemmTmemCols);
+        tmem_alloc(smem_addr(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -333,7 +348,7 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
             bool ok = true;
             int ki = 0;  // running activation-stage counter
             for (int lt = 0; lt < my_tiles && ok; ++lt) {
-                const int m0 = tile_m0(lt), kbase = kpart(lt) * ksteps;
+                const int m0 = tile_m0(lt), kbase = 4 * kg0(lt), ksteps = 4 * (kg1(lt) - kg0(lt));
                 for (int ks = 0; ks < ksteps && ok; ++ks, ++ki) {
                     const int sb = ki % kGemmStagesB;
                     if (ki >= kGemmStagesB)
@@ -352,7 +367,7 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
             bool ok = true;
             int gi = 0;  // running packed-group counter
             for (int lt = 0; lt < my_tiles && ok; ++lt) {
-                const int n0 = tile_n0(lt), gbase = kpart(lt) * groups;
+                const int n0 = tile_n0(lt), gbase = kg0(lt), groups = kg1(lt) - kg0(lt);
                 for (int g = 0; g < groups && ok; ++g, ++gi) {
                     const int sp = gi % kGemmStagesP;
                     if (gi >= kGemmStagesP)
@@ -367,12 +382,13 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = umma_idesc_f16(kGemmBM, kGemmBN);
+            constexpr uint32_t idesc = umma_idesc_f16(kGemmBM, kBN);
             bool ok = true;
             int ki = 0;  // running k-step counter (A and activation rings)
             for (int lt = 0; lt < my_tiles; ++lt) {
                 const int buf = lt & 1, use = lt >> 1;
-                const uint32_t dacc = tmem + (uint32_t)(buf * kGemmBN);
+                const int ksteps = 4 * (kg1(lt) - kg0(lt));
+                const uint32_t dacc = tmem + (uint32_t)(buf * kBN);
                 if (ok && use > 0) ok = mbar_wait(acc_empty(buf), (use - 1) & 1, kErrGemmWait);
                 for (int ks = 0; ks < ksteps && ok; ++ks, ++ki) {
                     const int sa = ki % kSA, sb = ki % kGemmStagesB;
@@ -400,7 +416,7 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
         bool ok = true;
         int gi = 0, ki = 0;
         for (int lt = 0; lt < my_tiles; ++lt) {
-            for (int g = 0; g < groups; ++g, ++gi) {
+            for (int g = kg0(lt); g < kg1(lt); ++g, ++gi) {
                 const int sp = gi % kGemmStagesP;
                 if (ok) ok = mbar_wait_warp(p_full(sp), (gi / kGemmStagesP) & 1, kErrGemmWait);
                 const uint8_t *pst = smem + L.p + sp * kPBytes;
@@ -461,40 +477,91 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
     } else {
         // ------------------------------------------------ epilogue: TMEM -> Y
         const int quarter = warp & 3;  // this warp may read TMEM lanes 32*quarter .. +31
+        const int r = 32 * quarter + lane;  // weight row within the tile
+        const int etid = tid - 32 * (2 + kGemmDeqWarps);  // 0 .. 127
         bool ok = true;
         for (int lt = 0; lt < my_tiles; ++lt) {
             const int buf = lt & 1, use = lt >> 1;
             const int n0 = tile_n0(lt), m0 = tile_m0(lt);
             if (ok) ok = mbar_wait_warp(acc_full(buf), use & 1, kErrGemmWait);
             tc_fence_after();
-            const int n = n0 + 32 * quarter + lane;
+            const int n = n0 + r;
+            const int tile = tile_base(lt);
+            float *pw = p.partials + ((int64_t)tile * ksplit + kpart(lt)) * (kBN * kGemmBM);
             if (ok) {
 #pragma unroll 1
-                for (int col = 0; col < kGemmBN; col += 32) {
+                for (int col = 0; col < kBN; col += 32) {
                     uint32_t v[32];
-                    tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(buf * kGemmBN + col), v);
-                    if (n < p.N) {
-                        if (ksplit == 1) {
+                    tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(buf * kBN + col), v);
+                    if (!p.tickets_mode) {
+                        if (n < p.N) {
 #pragma unroll
                             for (int i = 0; i < 32; ++i) {
                                 const int m = m0 + col + i;
-                                if (m < p.M) p.Y[(int64_t)m * p.N + n] = __uint_as_float(v[i]);
-                            }
-                        } else {
-                            // two halves added onto 0 in either order give the same
-                            // float (addition commutes), so the result is deterministic
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) {
-                                const int m = m0 + col + i;
-                                if (m < p.M) atomicAdd(p.Y + (int64_t)m * p.N + n, __uint_as_float(v[i]));
+                                if (m >= p.M) continue;
+                                if (ksplit == 1) p.Y[(int64_t)m * p.N + n] = __uint_as_float(v[i]);
+                                else atomicAdd(p.Y + (int64_t)m * p.N + n, __uint_as_float(v[i]));
                             }
                         }
+                    } else {
+                        // this part's sums, row-major (one row's BN columns contiguous)
+                        float4 *pr = reinterpret_cast<float4 *>(pw + r * kBN + col);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            pr[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                                __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
                     }
                 }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_empty(buf));
+            if (p.tickets_mode) {
+                // ticket: the last part of the tile to finish adds all parts in order
+                __threadfence();
+                named_bar_sync(2, kGemmEpiWarps * 32);
+                if (etid == 0) *last_slot = atomicAdd(p.tickets + tile, 1) == ksplit - 1;
+                named_bar_sync(2, kGemmEpiWarps * 32);
+                if (*last_slot && ok && n < p.N) {
+                    __threadfence();
+                    const float *pt = p.partials + (int64_t)tile * ksplit * (kBN * kGemmBM) + r * kBN;
+#pragma unroll 1
+                    for (int col = 0; col < kBN; col += 16) {
+                        // 4 float4 of two parts in flight before their sums
+                        float4 acc[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        for (int q0 = 0; q0 < ksplit; q0 += 2) {
+                            const float4 *a = reinterpret_cast<const float4 *>(pt + (int64_t)q0 * (kBN * kGemmBM) + col);
+                            const float4 *b = reinterpret_cast<const float4 *>(pt + (int64_t)(q0 + 1) * (kBN * kGemmBM) + col);
+                            const bool two = q0 + 1 < ksplit;
+                            float4 va[4], vb[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                va[i] = __ldcg(a + i);
+                                vb[i] = two ? __ldcg(b + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                            }
+                            // parts in order: acc + part q0, then + part q0 + 1
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                acc[i].x += va[i].x; acc[i].y += va[i].y; acc[i].z += va[i].z; acc[i].w += va[i].w;
+                                if (two) {
+                                    acc[i].x += vb[i].x; acc[i].y += vb[i].y; acc[i].z += vb[i].z; acc[i].w += vb[i].w;
+                                }
+                            }
+                        }
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float o[4] = {acc[i].x, acc[i].y, acc[i].z, acc[i].w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int m = m0 + col + 4 * i + e;
+                                if (m < p.M) p.Y[(int64_t)m * p.N + n] = o[e];
+                            }
+                        }
+                    }
+                }
+            }
         }
     }
     tc_fence_before();
@@ -502,44 +569,88 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem, kGemmTmemCols);
+        tmem_dealloc(tmem, kTmemCols);
     }
 }
 
 // ---------------------------------------------------------------- launcher
-size_t gemm_workspace_bytes(int fmt, int M, int N, int K) {
-    (void)fmt;
-    (void)N;
-    return (size_t)M * (size_t)K * 2;  // binary16 copy of X
+// Token tile and K split of a problem.  BN: the smallest of 32 / 64 / 128
+// that holds M, else 256.  K parts: as many as fill the SMs with one unit
+// each when the output tiles alone do not (at most one part per packed
+// group of K).
+#ifndef QMM_GEMM_MAX_PARTS  // K parts per tile for token tiles below 256
+#define QMM_GEMM_MAX_PARTS 8
+#endif
+struct GemmPlan {
+    int bn, ksplit, tiles, tickets;
+};
+static GemmPlan gemm_plan(int M, int N, int K, int sms) {
+    GemmPlan pl;
+    pl.bn = M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+    pl.tiles = ((N + kGemmBM - 1) / kGemmBM) * ((M + pl.bn - 1) / pl.bn);
+    const int groups = K / kGroup;
+    if (pl.bn == 256) {
+        // two K halves when the tiles fill under about half of the SMs
+        auto occupancy = [&](int u) {
+            const int waves = (u + sms - 1) / sms;
+            return (double)u / ((double)waves * sms);
+        };
+        pl.ksplit = (groups % 2 == 0 && occupancy(2 * pl.tiles) > occupancy(pl.tiles) + 0.2) ? 2 : 1;
+        pl.tickets = 0;
+    } else {
+        int ks = sms / pl.tiles;
+        if (ks > groups) ks = groups;
+        if (ks > QMM_GEMM_MAX_PARTS) ks = QMM_GEMM_MAX_PARTS;
+        pl.ksplit = ks < 1 ? 1 : ks;
+        pl.tickets = pl.ksplit > 1;
+    }
+    return pl;
 }
 
-template <int kFmt>
+// Workspace: the binary16 copy of X, then (with a K split) the partial tiles
+// and one ticket word per tile, each region 256-byte aligned.
+struct GemmWorkspace {
+    size_t xh, partials, tickets, total;
+};
+static GemmWorkspace gemm_workspace(int M, int N, int K, int sms) {
+    const GemmPlan pl = gemm_plan(M, N, K, sms);
+    auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
+    GemmWorkspace w;
+    w.xh = 0;
+    w.partials = up((size_t)M * (size_t)K * 2);
+    const size_t pbytes = pl.tickets ? (size_t)pl.tiles * pl.ksplit * pl.bn * kGemmBM * 4 : 0;
+    w.tickets = up(w.partials + pbytes);
+    w.total = w.tickets + (pl.tickets ? up((size_t)pl.tiles * 4) : 0);
+    return w;
+}
+
+size_t gemm_workspace_bytes(int fmt, int M, int N, int K, int sms) {
+    (void)fmt;
+    return gemm_workspace(M, N, K, sms).total;
+}
+
+template <int kFmt, int kBN>
 static cudaError_t launch_gemm_t(const void *W, const uint16_t *X, float *Y, int M, int N, int K,
                                  void *workspace, int sms, cudaStream_t stream) {
-    __half *Xh = static_cast<__half *>(workspace);
-    // K split: when the output tiles fill under about half of the persistent
-    // CTAs, two units per tile (K halves) fill twice as many SMs
-    const int tiles_n = (N + kGemmBM - 1) / kGemmBM;
-    const int units1 = tiles_n * ((M + kGemmBN - 1) / kGemmBN);
-    const int slots = sms;
-    auto occupancy = [&](int u) {
-        const int waves = (u + slots - 1) / slots;
-        return (double)u / ((double)waves * slots);
-    };
-    const int ksplit = (QMM_GEMM_SPLIT_K && (K / kGroup) % 2 == 0 && occupancy(2 * units1) > occupancy(units1) + 0.2)
-                           ? 2 : 1;
+    const GemmPlan pl = gemm_plan(M, N, K, sms);
+    const GemmWorkspace ws = gemm_workspace(M, N, K, sms);
+    uint8_t *wb = static_cast<uint8_t *>(workspace);
+    __half *Xh = reinterpret_cast<__half *>(wb + ws.xh);
+    const int nt = pl.tickets ? pl.tiles : 0;
+    const int64_t ny = (!pl.tickets && pl.ksplit > 1) ? (int64_t)M * N : 0;  // Y to add the halves onto
     const int64_t n8 = (int64_t)M * K / 8;
-    const int64_t ny = ksplit > 1 ? (int64_t)M * N : 0;  // Y is zeroed for the split-K sum
     const int64_t work = n8 > ny / 4 ? n8 : ny / 4;
     int cgrid = (int)((work + 255) / 256);
     if (cgrid > 148 * 16) cgrid = 148 * 16;
-    qmm_x_to_f16_kernel<<<cgrid, 256, 0, stream>>>(X, Xh, n8, Y, ny);
+    if (cgrid < 1) cgrid = 1;
+    qmm_x_to_f16_kernel<<<cgrid, 256, 0, stream>>>(X, Xh, n8, reinterpret_cast<int *>(wb + ws.tickets), nt,
+                                                   Y, ny);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
     CUtensorMap xmap, wmap;
     e = encode_tmap_2d(&xmap, Xh, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (uint64_t)K, (uint64_t)M,
-                       (uint64_t)K * 2, kGemmBK, kGemmBN, CU_TENSOR_MAP_SWIZZLE_128B);
+                       (uint64_t)K * 2, kGemmBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B);
     if (e != cudaSuccess) return e;
     constexpr int kCB = gemm_group_bytes(kFmt);
     const int64_t row_bytes = (int64_t)(K / kGroup) * kCB;
@@ -547,27 +658,41 @@ static cudaError_t launch_gemm_t(const void *W, const uint16_t *X, float *Y, int
                        (uint64_t)N, (uint64_t)row_bytes, kCB / 2, kGemmBM);
     if (e != cudaSuccess) return e;
 
-    const GemmLayout L = gemm_layout(kFmt);
+    const GemmLayout L = gemm_layout(kFmt, kBN);
     static std::atomic<uint64_t> attr_done{0};
-    e = set_smem_limit_once(reinterpret_cast<const void *>(qmm_gemm_kernel<kFmt>), L.total, attr_done);
+    e = set_smem_limit_once(reinterpret_cast<const void *>(qmm_gemm_kernel<kFmt, kBN>), L.total, attr_done);
     if (e != cudaSuccess) return e;
     GemmParams p;
     p.Y = Y;
+    p.partials = reinterpret_cast<float *>(wb + ws.partials);
+    p.tickets = reinterpret_cast<int *>(wb + ws.tickets);
     p.M = M;
     p.N = N;
     p.K = K;
-    p.ksplit = ksplit;
-    const int units = units1 * ksplit;
-    const int grid = units < slots ? units : slots;  // one persistent CTA per SM
-    qmm_gemm_kernel<kFmt><<<grid, kGemmThreads, (size_t)L.total, stream>>>(xmap, wmap, p);
+    p.ksplit = pl.ksplit;
+    p.tickets_mode = pl.tickets;
+    const int units = pl.tiles * pl.ksplit;
+    const int grid = units < sms ? units : sms;  // one persistent CTA per SM
+    qmm_gemm_kernel<kFmt, kBN><<<grid, kGemmThreads, (size_t)L.total, stream>>>(xmap, wmap, p);
     return cudaGetLastError();
+}
+
+template <int kFmt>
+static cudaError_t launch_gemm_f(const void *W, const uint16_t *X, float *Y, int M, int N, int K,
+                                 void *workspace, int sms, cudaStream_t stream) {
+    switch (gemm_plan(M, N, K, sms).bn) {
+    case 32: return launch_gemm_t<kFmt, 32>(W, X, Y, M, N, K, workspace, sms, stream);
+    case 64: return launch_gemm_t<kFmt, 64>(W, X, Y, M, N, K, workspace, sms, stream);
+    case 128: return launch_gemm_t<kFmt, 128>(W, X, Y, M, N, K, workspace, sms, stream);
+    default: return launch_gemm_t<kFmt, 256>(W, X, Y, M, N, K, workspace, sms, stream);
+    }
 }
 
 cudaError_t launch_gemm(int fmt, const void *W, const uint16_t *X, float *Y, int M, int N, int K,
                         void *workspace, size_t workspace_bytes, int sms, cudaStream_t stream) {
-    if (workspace_bytes < gemm_workspace_bytes(fmt, M, N, K)) return cudaErrorInvalidValue;
-    if (fmt == 8) return launch_gemm_t<8>(W, X, Y, M, N, K, workspace, sms, stream);
-    return launch_gemm_t<4>(W, X, Y, M, N, K, workspace, sms, stream);
+    if (workspace_bytes < gemm_workspace_bytes(fmt, M, N, K, sms)) return cudaErrorInvalidValue;
+    if (fmt == 8) return launch_gemm_f<8>(W, X, Y, M, N, K, workspace, sms, stream);
+    return launch_gemm_f<4>(W, X, Y, M, N, K, workspace, sms, stream);
 }
 
 }  // namespace qmm

@@ -20,7 +20,7 @@ cudaError_t launch_gemv_rows(int fmt, const void *W, const uint16_t *X, float *Y
                              int K, int sms, cudaStream_t stream);
 cudaError_t launch_gemm(int fmt, const void *W, const uint16_t *X, float *Y, int M, int N, int K,
                         void *workspace, size_t workspace_bytes, int sms, cudaStream_t stream);
-size_t gemm_workspace_bytes(int fmt, int M, int N, int K);
+size_t gemm_workspace_bytes(int fmt, int M, int N, int K, int sms);
 
 constexpr int kMaxDecodeM = 16;
 // Largest dimension accepted (keeps every 32-bit index in the kernels exact).
@@ -132,7 +132,7 @@ size_t qmm_matmul_workspace_bytes(qmm_format fmt, int64_t M, int64_t N, int64_t 
     if (!known_fmt(fmt) || M <= kMaxDecodeM || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim ||
         K > kMaxDim || K % kGroup != 0)
         return 0;
-    return gemm_workspace_bytes((int)fmt, (int)M, (int)N, (int)K);
+    return gemm_workspace_bytes((int)fmt, (int)M, (int)N, (int)K, sm_count());
 }
 
 qmm_status qmm_matmul(qmm_format fmt, const void *W_packed, const uint16_t *X_bf16, float *Y,
@@ -153,7 +153,7 @@ qmm_status qmm_matmul(qmm_format fmt, const void *W_packed, const uint16_t *X_bf
         return from_cuda(launch_gemv((int)fmt, W_packed, X_bf16, Y, (int)M, (int)N, (int)K,
                                      sm_count(), s));
     }
-    const size_t need = gemm_workspace_bytes((int)fmt, (int)M, (int)N, (int)K);
+    const size_t need = gemm_workspace_bytes((int)fmt, (int)M, (int)N, (int)K, sm_count());
     if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return QMM_ERR_WORKSPACE;
     if (need > 0 && !aligned16(workspace)) return QMM_ERR_ALIGNMENT;
     return from_cuda(launch_gemm((int)fmt, W_packed, X_bf16, Y, (int)M, (int)N, (int)K, workspace,

@@ -45,7 +45,7 @@ extern "C" qmm_status qmm_matmul_prefill_static(qmm_format fmt, const void *W_pa
     if (M <= kMaxDecodeM) return QMM_ERR_UNSUPPORTED;  // decode needs no scratch: use qmm_matmul
     if (W_packed == nullptr || X_bf16 == nullptr || Y == nullptr) return QMM_ERR_INVALID_ARG;
     if (!aligned16(W_packed) || !aligned16(X_bf16) || !aligned16(Y)) return QMM_ERR_ALIGNMENT;
-    const size_t need = gemm_workspace_bytes((int)fmt, (int)M, (int)N, (int)K);
+    const size_t need = gemm_workspace_bytes((int)fmt, (int)M, (int)N, (int)K, sm_count());
     if (need > kStaticScratchBytes) return QMM_ERR_WORKSPACE;
     cudaError_t e = cudaSuccess;
     void *scratch = static_scratch_for_current_device(&e);

@@ -128,9 +128,11 @@ QMM_API size_t qmm_matmul_workspace_bytes(qmm_format fmt, int64_t M, int64_t N, 
  * when the tiles fill the GPU (each tile's partial sums added in a fixed
  * order), otherwise split-K over a thread-block cluster reduced in
  * distributed shared memory in a fixed order; both are deterministic.
- * Larger M runs the prefill kernel (tcgen05 tensor cores, TMEM accumulators;
- * with K split in two when the output tiles fill under half the SMs, the two
- * halves add onto a zeroed Y, which is still deterministic).
+ * Larger M runs the tiled kernel (tcgen05 tensor cores, TMEM accumulators):
+ * token tiles of 32, 64, 128 or 256 (the smallest of 32 / 64 / 128 that holds
+ * M, else 256); when the output tiles are fewer than the SMs, K is split into
+ * parts whose partial tiles the last part to finish adds in part order, so
+ * the result is still deterministic.
  *
  * Accuracy, per element, with w^ the dequantized weights:
  *   |y - y_exact| <= 1e-3 * sum_k |w^_k x_k| + 1e-6 + 2^-25 * T,
@@ -142,8 +144,10 @@ QMM_API size_t qmm_matmul_workspace_bytes(qmm_format fmt, int64_t M, int64_t N, 
  * of at most 2^-25 below it.  T is 0 when no such values occur; for the
  * synthetic weights and activations of the tests it is negligible.
  * `workspace` must hold qmm_matmul_workspace_bytes(fmt, M, N, K) bytes (or be
- * NULL when that is 0): the prefill path keeps the binary16 copy of X there.
- * It is only read and written by this call's kernels. */
+ * NULL when that is 0): the tiled path keeps the binary16 copy of X there
+ * and, with a K split, the partial tiles and their tickets (cleared by the
+ * call itself).  The size depends on the current device's SM count.  It is
+ * only read and written by this call's kernels. */
 QMM_API qmm_status qmm_matmul(qmm_format fmt, const void *W_packed, const uint16_t *X_bf16, float *Y,
                       int64_t M, int64_t N, int64_t K, void *workspace, size_t workspace_bytes,
                       qmm_stream_t stream);
@@ -153,12 +157,13 @@ QMM_API qmm_status qmm_matmul(qmm_format fmt, const void *W_packed, const uint16
  * framework, engines whose pool owns all device memory, loops that must not
  * call cudaMalloc because it can synchronise the device.  It computes what
  * qmm_matmul computes, with the same kernels, but its scratch (the binary16
- * copy of X) lives in a fixed 64 MiB device array inside this library, held
- * by every GPU that loads the library until the process exits.  The pages
+ * copy of X and, with a K split, the partial tiles) lives in a fixed 64 MiB
+ * device array inside this library, held by every GPU that loads the library
+ * until the process exits.  The pages
  * describe no counterpart of this call; it is an interface convenience.
- *  - Requires qmm_matmul_workspace_bytes(fmt, M, N, K) <= 64 MiB (that is,
- *    M * K <= 32 Mi); larger problems return QMM_ERR_WORKSPACE and launch
- *    nothing.  M <= 16 returns QMM_ERR_UNSUPPORTED: the decode path needs no
+ *  - Requires qmm_matmul_workspace_bytes(fmt, M, N, K) <= 64 MiB (M * K
+ *    somewhat below 32 Mi); larger problems return QMM_ERR_WORKSPACE and
+ *    launch nothing.  M <= 16 returns QMM_ERR_UNSUPPORTED: the decode path needs no
  *    scratch, call qmm_matmul with a NULL workspace.
  *  - Every call looks up the array's address in the current device's
  *    context (cudaGetSymbolAddress), so it stays valid after a device reset.

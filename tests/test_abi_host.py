@@ -105,8 +105,15 @@ def test_workspace_query(lib):
         for M in (1, 4, 16):  # decode shapes reduce in distributed shared memory
             assert q.qmm_matmul_workspace_bytes(fmt, M, 4096, 4096) == 0
         assert q.qmm_matmul_workspace_bytes(fmt, 512, 4096, 100) == 0  # invalid K
-        # prefill: a binary16 copy of the activations
+        # tiled path (148 SMs when no GPU is visible): a binary16 copy of the
+        # activations; with a K split of tiles under 256 tokens, the partial
+        # tiles and one ticket per tile follow (256-byte aligned regions)
+        # 512 x 4096: 256-token tiles, K halves added onto a zeroed Y
         assert q.qmm_matmul_workspace_bytes(fmt, 512, 4096, 4096) == 512 * 4096 * 2
+        # 2048 x 14336: 112 x 8 tiles fill the SMs, no split
+        assert q.qmm_matmul_workspace_bytes(fmt, 2048, 14336, 4096) == 2048 * 4096 * 2
+        # 32 tokens: a 32-token tile; 8 weight tiles, K in min(16, 148 // 8, 8) = 8 parts
+        assert q.qmm_matmul_workspace_bytes(fmt, 32, 1024, 4096) == 32 * 4096 * 2 + 8 * 8 * 32 * 128 * 4 + 256
     L = lib
     assert L.qmm_matmul(8, FAKE, FAKE, FAKE, 32, 64, 256, NULL, 0, S0) == q.QMM_ERR_WORKSPACE
     assert L.qmm_matmul(4, FAKE, FAKE, FAKE, 32, 64, 256, FAKE, 100, S0) == q.QMM_ERR_WORKSPACE

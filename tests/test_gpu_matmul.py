@@ -142,9 +142,10 @@ def test_activation_range(fmt):
 
 
 # ---------------------------------------------------------------- prefill GEMM
-# Output grids filling under half of the SMs split K in two (each output
-# tile is two units added into a zeroed Y): 16 and 20 weight tiles x 2-3
-# token tiles; the last also has a Y size that is not a multiple of 4.
+# Output grids filling under half of the SMs split K (each output tile is a
+# few units whose partial tiles the last one to finish adds in order): 16 and
+# 20 weight tiles x 2-3 token tiles; the last also has a Y size that is not a
+# multiple of 4.
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("n,k,m", [(2048, 512, 513), (2560, 1024, 257), (2047, 512, 301)])
 def test_prefill_split_k_full(fmt, n, k, m):
@@ -152,7 +153,7 @@ def test_prefill_split_k_full(fmt, n, k, m):
     Y, A = oracle.matmul(fmt, packed, xb, n, k)
     y = run(fmt, packed, xb, n)
     check_matmul(y, Y, A, "fmt=%d n=%d k=%d m=%d" % (fmt, n, k, m))
-    assert torch.equal(y, run(fmt, packed, xb, n))  # the two halves add in either order
+    assert torch.equal(y, run(fmt, packed, xb, n))  # parts added in a fixed order
 
 
 @pytest.mark.parametrize("fmt", FMTS)
@@ -162,6 +163,38 @@ def test_prefill_small_full(fmt, n, k, m):
     packed, xb = problem(fmt, n, k, m, 3000 + n + k + m)
     Y, A = oracle.matmul(fmt, packed, xb, n, k)
     check_matmul(run(fmt, packed, xb, n), Y, A, "fmt=%d n=%d k=%d m=%d" % (fmt, n, k, m))
+
+
+# Mid-size batches (continuous batching, 17 <= M < 256): the token tile is
+# 32, 64, 128 or 256 (the smallest of 32 / 64 / 128 holding M, else 256) and
+# K is split into as many parts as fill the SMs (up to one part per 256-wide
+# group), the last part of each tile adding all parts in order.  Tile
+# boundaries (32 / 33, 64 / 65, 128 / 129), one-group parts, uneven parts
+# (groups not a multiple of the part count) and ragged N.
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("n,k", [(128, 256), (300, 1280), (1024, 4096), (130, 2304)])
+@pytest.mark.parametrize("m", [17, 32, 33, 64, 65, 100, 128, 129, 200])
+def test_mid_batch_full(fmt, n, k, m):
+    packed, xb = problem(fmt, n, k, m, 4000 + n + k + m)
+    Y, A = oracle.matmul(fmt, packed, xb, n, k)
+    y = run(fmt, packed, xb, n)
+    check_matmul(y, Y, A, "fmt=%d n=%d k=%d m=%d" % (fmt, n, k, m))
+    assert torch.equal(y, run(fmt, packed, xb, n))  # same parts, same order
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("shape", inputs.DECODE_SHAPES)
+@pytest.mark.parametrize("m", [17, 32, 64, 128])
+def test_mid_batch_decode_shapes_sampled(fmt, shape, m):
+    n, k = shape
+    si = inputs.DECODE_SHAPES.index(shape)
+    w = inputs.weights(n, k, inputs.seed_for(6, si))
+    packed = oracle.quantize(fmt, inputs.bf16_bits(w))
+    xb = inputs.bf16_bits(inputs.activations(m, k, inputs.seed_for(6, si, m)))
+    y = run(fmt, packed, xb, n).cpu()
+    ns = sample_rows(n, 40, 200 + si * 10 + m)
+    Y, A = oracle.matmul_columns(fmt, packed, xb, k, ns)
+    check_matmul(y[:, torch.from_numpy(ns)], Y, A, "fmt=%d %s m=%d" % (fmt, shape, m))
 
 
 @pytest.mark.parametrize("fmt", FMTS)
