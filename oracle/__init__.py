@@ -20,6 +20,7 @@ import numpy as np
 
 Q8_0 = 8
 Q4_K = 4
+Q6_K = 6
 SRC_BF16 = 0
 SRC_F32 = 1
 
@@ -30,7 +31,7 @@ _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-BLOCK = {Q8_0: (32, 34), Q4_K: (256, 144)}
+BLOCK = {Q8_0: (32, 34), Q4_K: (256, 144), Q6_K: (256, 210)}
 
 
 def build(force: bool = False) -> str:
@@ -70,6 +71,9 @@ def lib() -> ctypes.CDLL:
             L.orc_matmul.restype = ctypes.c_int
             L.orc_matmul_columns.argtypes = [ctypes.c_int, vp, vp, i64, i64, vp, i64, vp, vp]
             L.orc_matmul_columns.restype = ctypes.c_int
+            L.orc_gather.argtypes = [ctypes.c_int, vp, i64, i64, vp, i64, vp]
+            L.orc_gather.restype = ctypes.c_int
+            L.orc_q6_k_position.argtypes = [ctypes.c_int, vp]
             L.orc_q4_k_pack_scales.argtypes = [vp, vp, vp]
             L.orc_q4_k_unpack_scales.argtypes = [vp, vp, vp]
             L.orc_set_threads.argtypes = [ctypes.c_int]
@@ -188,3 +192,22 @@ def unpack_scales_q4_k(s12):
     mc = np.zeros(8, dtype=np.int32)
     lib().orc_q4_k_unpack_scales(_ptr(s12), _ptr(sc), _ptr(mc))
     return sc, mc
+
+
+def gather(fmt: int, packed: np.ndarray, V: int, D: int, ids) -> np.ndarray:
+    """Embedding lookup: the dequantized rows ``ids`` of the packed [V x D]
+    table, float32 [len(ids) x D]."""
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    ids = np.ascontiguousarray(ids, dtype=np.int64)
+    out = np.zeros((ids.size, D), dtype=np.float32)
+    rc = lib().orc_gather(fmt, _ptr(packed), V, D, _ptr(ids), ids.size, _ptr(out))
+    if rc != 0:
+        raise ValueError("orc_gather failed: %d" % rc)
+    return out
+
+
+def q6_k_position(w: int):
+    """(ql byte, high nibble?, qh byte, bit shift) of weight w of a Q6_K superblock."""
+    pos = np.zeros(4, dtype=np.int32)
+    lib().orc_q6_k_position(int(w), _ptr(pos))
+    return tuple(int(v) for v in pos)

@@ -33,6 +33,22 @@
  *     bytes 16-143: four 32-byte chunks c; byte 32c+l holds weight l of
  *       sub-block 2c in its low nibble and weight l of sub-block 2c+1 in its
  *       high nibble.
+ *   Q6_K superblock (256 weights = 16 sub-blocks of 16, 210 bytes): the
+ *     page's Q*K table lists q6k at 6 bits, and its "Numeric shorthands"
+ *     table maps `--isq 6` to Q6K on CUDA; its "Sensitive tensor precision"
+ *     section gives Q6K to the embeddings and output head of a Q4K model.
+ *     The reading here (GGUF-shaped bytes, a plain symmetric quantizer):
+ *     s_j = max_i |x_i| / 31;  d16 = fp16_rne(max_j s_j / 127);
+ *     sc_j = clamp(roundf(s_j / d16), 0, 127)  (0 when d16 == 0);
+ *     S_j = d16 * sc_j (exact);  c_i = clamp(roundf(x_i / S_j), -32, 31)
+ *     (0 when S_j == 0);  dequantized value: S_j * c_i (exact in fp32).
+ *     bytes 0-127 ql, 128-191 qh, 192-207 int8 sc[16], 208-209 d16; with
+ *     q = c + 32 in 0..63 and weight w = 128h + 32s + l (h < 2, s < 4,
+ *     l < 32): low 4 bits of q in byte 64h + 32(s & 1) + l of ql (low
+ *     nibble for s < 2, high nibble for s >= 2), high 2 bits in bits 2s,
+ *     2s + 1 of byte 32h + l of qh; weight w uses sc[w / 16].
+ *   gather (embedding lookup): out[t][:] = dequantized row ids[t] of the
+ *     packed [V x D] table (Q8_0 is the page's common embedding target).
  *   matmul: Y[m][n] = sum_k double(w^[n][k]) * double(x[m][k]) over the exactly
  *     dequantized weights w^ and the bf16 activations, summed in k order in
  *     fp64; A[m][n] = sum_k |w^ x| in fp64 (the scale of the error bound).
@@ -288,13 +304,103 @@ static void dequantize_q4_k_superblock(const uint8_t *blk, float *y)
 }
 
 /* ------------------------------------------------------------------ */
+/* Q6_K: 256-weight superblock, 16 sub-blocks of 16; 210 bytes          */
+/* ------------------------------------------------------------------ */
+
+enum { Q6_K_QK = 256, Q6_K_BYTES = 210 };
+
+/* Byte positions of the 6-bit code of weight w (0..255) of a superblock:
+ * its low 4 bits in ql byte *lo_byte (high nibble when *lo_hi), its high 2
+ * bits at bit *hi_shift of qh byte *hi_byte (offsets from the block start). */
+static void q6_k_position(int w, int *lo_byte, int *lo_hi, int *hi_byte, int *hi_shift)
+{
+    int h = w / 128, s = (w / 32) % 4, l = w % 32;
+    *lo_byte = 64 * h + 32 * (s & 1) + l;
+    *lo_hi = s >= 2;
+    *hi_byte = 128 + 32 * h + l;
+    *hi_shift = 2 * s;
+}
+
+static void quantize_q6_k_superblock(const float *x, uint8_t *out)
+{
+    float s[16], smax = 0.0f;
+    for (int j = 0; j < 16; j++) {
+        float amax = 0.0f;
+        for (int i = 0; i < 16; i++) {
+            float a = fabsf(x[16 * j + i]);
+            if (a > amax)
+                amax = a;
+        }
+        s[j] = amax / 31.0f;
+        if (s[j] > smax)
+            smax = s[j];
+    }
+    uint16_t d16 = orc_f32_to_f16(smax / 127.0f);
+    float df = orc_f16_to_f32(d16);
+    memset(out, 0, Q6_K_BYTES);
+    for (int j = 0; j < 16; j++) {
+        int sc = df > 0.0f ? (int)clampf(roundf(s[j] / df), 0.0f, 127.0f) : 0;
+        float S = df * (float)sc;
+        out[192 + j] = (uint8_t)(int8_t)sc;
+        for (int i = 0; i < 16; i++) {
+            int w = 16 * j + i;
+            int c = S > 0.0f ? (int)clampf(roundf(x[w] / S), -32.0f, 31.0f) : 0;
+            int q = c + 32;
+            int lo_byte, lo_hi, hi_byte, hi_shift;
+            q6_k_position(w, &lo_byte, &lo_hi, &hi_byte, &hi_shift);
+            out[lo_byte] |= (uint8_t)((q & 15) << (lo_hi ? 4 : 0));
+            out[hi_byte] |= (uint8_t)((q >> 4) << hi_shift);
+        }
+    }
+    put_u16(out + 208, d16);
+}
+
+static void dequantize_q6_k_superblock(const uint8_t *blk, float *y)
+{
+    float df = orc_f16_to_f32(get_u16(blk + 208));
+    for (int w = 0; w < 256; w++) {
+        int lo_byte, lo_hi, hi_byte, hi_shift;
+        q6_k_position(w, &lo_byte, &lo_hi, &hi_byte, &hi_shift);
+        int q = ((lo_hi ? blk[lo_byte] >> 4 : blk[lo_byte]) & 15) | (((blk[hi_byte] >> hi_shift) & 3) << 4);
+        float S = df * (float)(int8_t)blk[192 + w / 16];
+        y[w] = S * (float)(q - 32);
+    }
+}
+
+/* ------------------------------------------------------------------ */
 /* Exported API                                                        */
 /* ------------------------------------------------------------------ */
 
-enum { ORC_Q8_0 = 8, ORC_Q4_K = 4 };
+enum { ORC_Q8_0 = 8, ORC_Q4_K = 4, ORC_Q6_K = 6 };
 
-static int qk_of(int fmt) { return fmt == ORC_Q8_0 ? Q8_0_QK : fmt == ORC_Q4_K ? Q4_K_QK : 0; }
-static int bytes_of(int fmt) { return fmt == ORC_Q8_0 ? Q8_0_BYTES : fmt == ORC_Q4_K ? Q4_K_BYTES : 0; }
+static int qk_of(int fmt)
+{
+    return fmt == ORC_Q8_0 ? Q8_0_QK : fmt == ORC_Q4_K ? Q4_K_QK : fmt == ORC_Q6_K ? Q6_K_QK : 0;
+}
+static int bytes_of(int fmt)
+{
+    return fmt == ORC_Q8_0 ? Q8_0_BYTES : fmt == ORC_Q4_K ? Q4_K_BYTES : fmt == ORC_Q6_K ? Q6_K_BYTES : 0;
+}
+
+static void quantize_block(int fmt, const float *x, uint8_t *out)
+{
+    if (fmt == ORC_Q8_0)
+        quantize_q8_0_block(x, out);
+    else if (fmt == ORC_Q4_K)
+        quantize_q4_k_superblock(x, out);
+    else
+        quantize_q6_k_superblock(x, out);
+}
+
+static void dequantize_block(int fmt, const uint8_t *blk, float *y)
+{
+    if (fmt == ORC_Q8_0)
+        dequantize_q8_0_block(blk, y);
+    else if (fmt == ORC_Q4_K)
+        dequantize_q4_k_superblock(blk, y);
+    else
+        dequantize_q6_k_superblock(blk, y);
+}
 
 int64_t orc_packed_bytes(int fmt, int64_t rows, int64_t cols)
 {
@@ -337,11 +443,7 @@ int orc_quantize(int fmt, int src_kind, const void *src, uint8_t *dst, int64_t r
         for (int64_t b = 0; b < nb; b++) {
             for (int i = 0; i < qk; i++)
                 x[i] = load_src(src_kind, src, r * cols + b * qk + i);
-            uint8_t *out = dst + r * row_bytes + b * bytes_of(fmt);
-            if (fmt == ORC_Q8_0)
-                quantize_q8_0_block(x, out);
-            else
-                quantize_q4_k_superblock(x, out);
+            quantize_block(fmt, x, dst + r * row_bytes + b * bytes_of(fmt));
         }
     }
     return 0;
@@ -357,12 +459,7 @@ int orc_dequantize(int fmt, const uint8_t *src, float *dst, int64_t rows, int64_
 #pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < rows; r++) {
         for (int64_t b = 0; b < nb; b++) {
-            const uint8_t *blk = src + r * row_bytes + b * bytes_of(fmt);
-            float *y = dst + r * cols + b * qk;
-            if (fmt == ORC_Q8_0)
-                dequantize_q8_0_block(blk, y);
-            else
-                dequantize_q4_k_superblock(blk, y);
+            dequantize_block(fmt, src + r * row_bytes + b * bytes_of(fmt), dst + r * cols + b * qk);
         }
     }
     return 0;
@@ -371,12 +468,26 @@ int orc_dequantize(int fmt, const uint8_t *src, float *dst, int64_t rows, int64_
 static void dequantize_row(int fmt, const uint8_t *src, float *dst, int64_t cols)
 {
     int qk = qk_of(fmt);
-    for (int64_t b = 0; b < cols / qk; b++) {
-        if (fmt == ORC_Q8_0)
-            dequantize_q8_0_block(src + b * Q8_0_BYTES, dst + b * qk);
-        else
-            dequantize_q4_k_superblock(src + b * Q4_K_BYTES, dst + b * qk);
-    }
+    for (int64_t b = 0; b < cols / qk; b++)
+        dequantize_block(fmt, src + b * bytes_of(fmt), dst + b * qk);
+}
+
+/* Embedding lookup: out[t][0 .. D) = dequantized row ids[t] of the packed
+ * table W[V x D].  Returns -1 (writing nothing) if an id is outside 0 .. V-1
+ * or the shape is not a whole number of blocks. */
+int orc_gather(int fmt, const uint8_t *W, int64_t V, int64_t D, const int64_t *ids, int64_t T,
+               float *out)
+{
+    int qk = qk_of(fmt);
+    if (qk == 0 || D % qk != 0 || V < 0 || T < 0)
+        return -1;
+    for (int64_t t = 0; t < T; t++)
+        if (ids[t] < 0 || ids[t] >= V)
+            return -1;
+    int64_t row_bytes = (D / qk) * bytes_of(fmt);
+    for (int64_t t = 0; t < T; t++)
+        dequantize_row(fmt, W + ids[t] * row_bytes, out + t * D, D);
+    return 0;
 }
 
 /* Y[m][t] and A[m][t] (row-major, M x count) for the output features n = ns[t]
@@ -428,6 +539,12 @@ int orc_matmul(int fmt, const uint8_t *W, const uint16_t *X, double *Y, double *
     int rc = orc_matmul_columns(fmt, W, X, M, K, ns, N, Y, A);
     free(ns);
     return rc;
+}
+
+/* Debug access to the code positions of Q6_K (used by the layout pins). */
+void orc_q6_k_position(int w, int *pos4)
+{
+    q6_k_position(w, &pos4[0], &pos4[1], &pos4[2], &pos4[3]);
 }
 
 /* Debug access to the scale-byte packing of Q4_K (used by the layout pins). */
