@@ -18,6 +18,9 @@ import threading
 
 QMM_Q8_0 = 8
 QMM_Q4_K = 4
+QMM_Q6_K = 6
+QMM_OUT_F32 = 0
+QMM_OUT_BF16 = 1
 QMM_SRC_BF16 = 0
 QMM_SRC_F32 = 1
 
@@ -30,8 +33,8 @@ QMM_ERR_WORKSPACE = -5
 QMM_ERR_CUDA = -6
 QMM_ERR_DEVICE = -7
 
-FORMATS = {"q8_0": QMM_Q8_0, "q4_k": QMM_Q4_K}
-BLOCK = {QMM_Q8_0: (32, 34), QMM_Q4_K: (256, 144)}
+FORMATS = {"q8_0": QMM_Q8_0, "q4_k": QMM_Q4_K, "q6_k": QMM_Q6_K}
+BLOCK = {QMM_Q8_0: (32, 34), QMM_Q4_K: (256, 144), QMM_Q6_K: (256, 210)}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libqmm.so")
@@ -74,6 +77,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
         L.qmm_device_error_take.restype = ctypes.c_int
         L.qmm_version.argtypes = []
         L.qmm_version.restype = ctypes.c_char_p
+        L.qmm_embedding.argtypes = [ctypes.c_int, vp, vp, i64, i64, i64, vp, ctypes.c_int, vp]
+        L.qmm_embedding.restype = ctypes.c_int
+        L.qmm_embedding_format.argtypes = [ctypes.c_int]
+        L.qmm_embedding_format.restype = ctypes.c_int
         L.qmm_selftest_bounded_wait.argtypes = [i64, vp]
         L.qmm_selftest_bounded_wait.restype = ctypes.c_int
         L.qmm_matmul_prefill_static.argtypes = [ctypes.c_int, vp, vp, vp, i64, i64, i64, vp]
@@ -118,7 +125,32 @@ def qmm_device_error_take() -> int:
     return int(load().qmm_device_error_take())
 
 
+QMM_DEVERR_EMBEDDING_ID = 301
 QMM_DEVERR_SELFTEST_TIMEOUT = 901
+
+
+def qmm_embedding_format(model_fmt: int) -> int:
+    return int(load().qmm_embedding_format(int(model_fmt)))
+
+
+def qmm_embedding(fmt: int, table, ids, D: int, out=None, dtype=None, stream=None):
+    """Embedding lookup: the dequantized rows ``ids`` (int64 CUDA tensor) of
+    the packed table (uint8 [V, row_bytes]) as fp32 (default) or bf16."""
+    import torch
+    if table.dtype != torch.uint8 or table.dim() != 2 or not table.is_contiguous():
+        raise ValueError("qmm_embedding: table must be a contiguous 2-D uint8 tensor")
+    if ids.dtype != torch.int64 or not ids.is_contiguous():
+        raise ValueError("qmm_embedding: ids must be a contiguous int64 tensor")
+    dtype = dtype or (out.dtype if out is not None else torch.float32)
+    if dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("qmm_embedding: output must be fp32 or bf16")
+    T = ids.numel()
+    if out is None:
+        out = torch.empty((T, D), dtype=dtype, device=table.device)
+    od = QMM_OUT_BF16 if dtype == torch.bfloat16 else QMM_OUT_F32
+    _check("qmm_embedding", load().qmm_embedding(int(fmt), _ptr(table), _ptr(ids), T, table.shape[0],
+                                                 int(D), _ptr(out), od, _stream_ptr(stream)))
+    return out
 
 
 def qmm_selftest_bounded_wait(limit_ns: int, stream=None) -> None:

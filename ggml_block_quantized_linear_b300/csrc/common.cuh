@@ -35,6 +35,7 @@ enum DeviceError : int {
     kErrGemvFullWait = 101,
     kErrGemvEmptyWait = 102,
     kErrGemmWait = 201,
+    kErrBadId = 301,
     kErrSelftestTimeout = 901,
     kErrSelftestUnexpected = 902,
 };

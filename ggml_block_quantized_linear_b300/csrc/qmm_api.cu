@@ -21,6 +21,13 @@ cudaError_t launch_gemv_rows(int fmt, const void *W, const uint16_t *X, float *Y
 cudaError_t launch_gemm(int fmt, const void *W, const uint16_t *X, float *Y, int M, int N, int K,
                         void *workspace, size_t workspace_bytes, int sms, cudaStream_t stream);
 size_t gemm_workspace_bytes(int fmt, int M, int N, int K, int sms);
+cudaError_t launch_q6k_quantize(int src_f32, const void *src, void *dst, int64_t nweights, int sms,
+                                cudaStream_t stream);
+cudaError_t launch_q6k_dequantize(const void *src, float *dst, int64_t nweights, int sms, cudaStream_t stream);
+cudaError_t launch_q6k_matmul(const void *W, const uint16_t *X, float *Y, int M, int N, int K, int sms,
+                              cudaStream_t stream);
+cudaError_t launch_embedding(int fmt, const void *table, const int64_t *ids, void *out, int bf16, int64_t T,
+                             int64_t V, int64_t D, int sms, cudaStream_t stream);
 
 constexpr int kMaxDecodeM = 16;
 // Largest dimension accepted (keeps every 32-bit index in the kernels exact).
@@ -65,7 +72,9 @@ static bool use_rows_kernel(int M, int N, int K, int sms) {
 }
 
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-static bool known_fmt(qmm_format f) { return f == QMM_Q8_0 || f == QMM_Q4_K; }
+static bool known_fmt(qmm_format f) { return f == QMM_Q8_0 || f == QMM_Q4_K || f == QMM_Q6_K; }
+static int64_t block_weights(qmm_format f) { return f == QMM_Q8_0 ? kQ8Weights : 256; }
+static int64_t block_bytes(qmm_format f) { return f == QMM_Q8_0 ? kQ8Bytes : f == QMM_Q4_K ? kQ4Bytes : 210; }
 
 static qmm_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA; }
 
@@ -97,8 +106,8 @@ extern "C" {
 
 size_t qmm_packed_bytes(qmm_format fmt, int64_t rows, int64_t cols) {
     if (!known_fmt(fmt) || rows < 0 || cols < 0) return 0;
-    const int64_t qk = fmt == QMM_Q8_0 ? kQ8Weights : kQ4Weights;
-    const int64_t bb = fmt == QMM_Q8_0 ? kQ8Bytes : kQ4Bytes;
+    const int64_t qk = block_weights(fmt);
+    const int64_t bb = block_bytes(fmt);
     if (cols % qk != 0) return 0;
     if (rows > kMaxDim || cols > kMaxDim) return 0;
     return (size_t)(rows * (cols / qk) * bb);
@@ -112,6 +121,9 @@ qmm_status qmm_quantize(qmm_format fmt, qmm_src_dtype st, const void *src, void 
     if (rows == 0) return QMM_OK;
     if (src == nullptr || dst_packed == nullptr) return QMM_ERR_INVALID_ARG;
     if (!aligned16(src) || !aligned16(dst_packed)) return QMM_ERR_ALIGNMENT;
+    if (fmt == QMM_Q6_K)
+        return from_cuda(launch_q6k_quantize(st == QMM_SRC_F32, src, dst_packed, rows * cols, sm_count(),
+                                             reinterpret_cast<cudaStream_t>(stream)));
     return from_cuda(launch_quantize((int)fmt, st == QMM_SRC_F32, src, dst_packed, rows * cols,
                                      sm_count(), reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -124,13 +136,16 @@ qmm_status qmm_dequantize(qmm_format fmt, const void *src_packed, float *dst, in
     if (rows == 0) return QMM_OK;
     if (src_packed == nullptr || dst == nullptr) return QMM_ERR_INVALID_ARG;
     if (!aligned16(src_packed) || !aligned16(dst)) return QMM_ERR_ALIGNMENT;
+    if (fmt == QMM_Q6_K)
+        return from_cuda(launch_q6k_dequantize(src_packed, dst, rows * cols, sm_count(),
+                                               reinterpret_cast<cudaStream_t>(stream)));
     return from_cuda(launch_dequantize((int)fmt, src_packed, dst, rows * cols, sm_count(),
                                        reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t qmm_matmul_workspace_bytes(qmm_format fmt, int64_t M, int64_t N, int64_t K) {
-    if (!known_fmt(fmt) || M <= kMaxDecodeM || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim ||
-        K > kMaxDim || K % kGroup != 0)
+    if (!known_fmt(fmt) || fmt == QMM_Q6_K || M <= kMaxDecodeM || N <= 0 || K <= 0 || M > kMaxDim ||
+        N > kMaxDim || K > kMaxDim || K % kGroup != 0)
         return 0;
     return gemm_workspace_bytes((int)fmt, (int)M, (int)N, (int)K, sm_count());
 }
@@ -146,6 +161,8 @@ qmm_status qmm_matmul(qmm_format fmt, const void *W_packed, const uint16_t *X_bf
     if (W_packed == nullptr || X_bf16 == nullptr || Y == nullptr) return QMM_ERR_INVALID_ARG;
     if (!aligned16(W_packed) || !aligned16(X_bf16) || !aligned16(Y)) return QMM_ERR_ALIGNMENT;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (fmt == QMM_Q6_K)
+        return from_cuda(launch_q6k_matmul(W_packed, X_bf16, Y, (int)M, (int)N, (int)K, sm_count(), s));
     if (M <= kMaxDecodeM) {
         if (use_rows_kernel((int)M, (int)N, (int)K, sm_count()))
             return from_cuda(launch_gemv_rows((int)fmt, W_packed, X_bf16, Y, (int)M, (int)N, (int)K,
@@ -165,7 +182,7 @@ const char *qmm_status_string(qmm_status s) {
     case QMM_OK: return "ok";
     case QMM_ERR_INVALID_ARG: return "invalid argument (null pointer, negative size or unknown enum)";
     case QMM_ERR_UNSUPPORTED: return "unsupported request";
-    case QMM_ERR_SHAPE: return "cols / K must be a positive multiple of 256";
+    case QMM_ERR_SHAPE: return "cols / K / D must be a positive multiple of 256";
     case QMM_ERR_ALIGNMENT: return "pointers must be 16-byte aligned";
     case QMM_ERR_WORKSPACE: return "workspace missing or too small";
     case QMM_ERR_CUDA: return "CUDA runtime error";
@@ -183,6 +200,27 @@ int qmm_device_error_take(void) {
         if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess) return -1;
     }
     return v;
+}
+
+qmm_status qmm_embedding(qmm_format fmt, const void *table_packed, const int64_t *ids, int64_t T, int64_t V,
+                         int64_t D, void *out, qmm_out_dtype out_dtype, qmm_stream_t stream) {
+    if (!known_fmt(fmt) || (out_dtype != QMM_OUT_F32 && out_dtype != QMM_OUT_BF16)) return QMM_ERR_INVALID_ARG;
+    if (T < 0 || V < 0 || D < 0 || T > kMaxDim || V > kMaxDim || D > kMaxDim) return QMM_ERR_INVALID_ARG;
+    if (D == 0 || D % kGroup != 0) return QMM_ERR_SHAPE;
+    if (T == 0) return QMM_OK;
+    if (V == 0 || table_packed == nullptr || ids == nullptr || out == nullptr) return QMM_ERR_INVALID_ARG;
+    if (!aligned16(table_packed) || !aligned16(out) || (reinterpret_cast<uintptr_t>(ids) & 7u) != 0)
+        return QMM_ERR_ALIGNMENT;
+    return from_cuda(launch_embedding((int)fmt, table_packed, ids, out, out_dtype == QMM_OUT_BF16, T, V, D,
+                                      sm_count(), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+qmm_format qmm_embedding_format(qmm_format model_fmt) {
+    // "Sensitive tensor precision": Q2K-Q4K models keep their embeddings and
+    // output head in Q6K, Q5K / Q6K / Q8_0 models in Q8_0
+    if (model_fmt == QMM_Q4_K) return QMM_Q6_K;
+    if (model_fmt == QMM_Q6_K || model_fmt == QMM_Q8_0) return QMM_Q8_0;
+    return (qmm_format)0;
 }
 
 qmm_status qmm_selftest_bounded_wait(int64_t limit_ns, qmm_stream_t stream) {

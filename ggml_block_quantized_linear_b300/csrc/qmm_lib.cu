@@ -5,4 +5,5 @@
 #include "gemv.cu"
 #include "gemv_rows.cu"
 #include "gemm.cu"
+#include "q6k.cu"
 #include "static_scratch.cu"

@@ -11,6 +11,13 @@
  *   qmm_quantize    bf16 (or fp32) weights W[rows x cols] -> packed blocks
  *   qmm_dequantize  packed blocks -> fp32 W^[rows x cols] (exact)
  *   qmm_matmul      Y[M x N] = X[M x K] * W^[N x K]^T   (fp32 out, bf16 X)
+ *   qmm_embedding   rows ids[] of a packed [V x D] table -> fp32 / bf16
+ *
+ * Formats: Q8_0 and Q4_K (the CUDA targets of `--isq 8` / `--isq 4`) for
+ * the linear layers, and Q6_K (`--isq 6`), which the page's section
+ * "Sensitive tensor precision" gives to the token embeddings and the output
+ * head of a Q4K model (Q8_0 for Q5K / Q6K / Q8_0 models; see
+ * qmm_embedding_format).
  *
  * The pages give names and widths only.  The byte layouts and the quantizer
  * used here (the library's reading, GGUF-shaped) are:
@@ -30,10 +37,19 @@
  *   Scale bytes of Q4_K, j = 0..3: byte j = sc_j | (sc_{j+4} >> 4) << 6;
  *   byte j+4 = mc_j | (mc_{j+4} >> 4) << 6; byte j+8 = (sc_{j+4} & 15) |
  *   (mc_{j+4} & 15) << 4.
+ *   Q6_K  256 weights -> 210 bytes: 16 sub-blocks of 16.  s_j = max|x| / 31;
+ *         d = fp16(max_j s_j / 127); sc_j = round(s_j / d) in 0..127 (int8);
+ *         c = clamp(round(x / (d*sc_j)), -32, 31), stored as q = c + 32.
+ *         Dequantized weight: (d*sc_j) * c.  Bytes 0-127 ql (low 4 bits of
+ *         q), 128-191 qh (high 2 bits), 192-207 sc[16], 208-209 d; weight
+ *         w = 128h + 32s + l (h < 2, s < 4, l < 32) has its low bits in ql
+ *         byte 64h + 32(s & 1) + l (high nibble when s >= 2) and its high
+ *         bits in bits 2s, 2s+1 of qh byte 32h + l.  Superblocks are only
+ *         2-byte aligned inside a packed row.
  *
  * A packed matrix is row-major in blocks: row n holds cols/32 Q8_0 blocks
- * (cols/32*34 bytes) or cols/256 Q4_K superblocks (cols/256*144 bytes),
- * rows back to back.
+ * (cols/32*34 bytes), cols/256 Q4_K superblocks (cols/256*144 bytes) or
+ * cols/256 Q6_K superblocks (cols/256*210 bytes), rows back to back.
  *
  * Conventions for every call:
  *  - Pointers are DEVICE pointers owned by the caller.  The library allocates
@@ -74,8 +90,12 @@ struct CUstream_st;
 typedef struct CUstream_st *qmm_stream_t;
 
 /* Block formats; the values mirror the ISQ shorthands `--isq 8` / `--isq 4`
- * (mistral.rs "Quantization types", section "Numeric shorthands"). */
-typedef enum { QMM_Q8_0 = 8, QMM_Q4_K = 4 } qmm_format;
+ * / `--isq 6` (mistral.rs "Quantization types", section "Numeric
+ * shorthands"). */
+typedef enum { QMM_Q8_0 = 8, QMM_Q4_K = 4, QMM_Q6_K = 6 } qmm_format;
+
+/* Element type of an embedding lookup's output. */
+typedef enum { QMM_OUT_F32 = 0, QMM_OUT_BF16 = 1 } qmm_out_dtype;
 
 /* Element type of the unquantized source of qmm_quantize.  BF16 is the ISQ
  * source (model weights); F32 lets tests feed values that bf16 cannot hold. */
@@ -114,6 +134,25 @@ QMM_API qmm_status qmm_quantize(qmm_format fmt, qmm_src_dtype st, const void *sr
 QMM_API qmm_status qmm_dequantize(qmm_format fmt, const void *src_packed, float *dst, int64_t rows,
                           int64_t cols, qmm_stream_t stream);
 
+/* Embedding lookup (mistral.rs "Quantization types", section "Sensitive
+ * tensor precision": quantized embedding kernels, Q8_0 the common target):
+ * out[t][0 .. D) = the dequantized row ids[t] of the packed table
+ * table_packed[V x D], for t < T, as fp32 (the exact dequantized values) or
+ * bf16 (those values rounded to nearest even).  ids: T int64 token ids in
+ * device memory (8-byte aligned); D a positive multiple of 256; table and
+ * out 16-byte aligned.  The ids are not read on the host: an id outside
+ * 0 .. V-1 writes zeros for that token and records
+ * QMM_DEVERR_EMBEDDING_ID (see qmm_device_error_take).  One kernel launch. */
+QMM_API qmm_status qmm_embedding(qmm_format fmt, const void *table_packed, const int64_t *ids, int64_t T,
+                                 int64_t V, int64_t D, void *out, qmm_out_dtype out_dtype,
+                                 qmm_stream_t stream);
+
+/* The format the page's section "Sensitive tensor precision" gives the token
+ * embeddings and output head of a model quantized to model_fmt: QMM_Q6_K for
+ * a Q4_K model, QMM_Q8_0 for Q6_K and Q8_0 models; 0 for an unknown format.
+ * Host only. */
+QMM_API qmm_format qmm_embedding_format(qmm_format model_fmt);
+
 /* Workspace qmm_matmul needs for this problem, in bytes (0 = none; then
  * workspace may be NULL). */
 QMM_API size_t qmm_matmul_workspace_bytes(qmm_format fmt, int64_t M, int64_t N, int64_t K);
@@ -128,7 +167,10 @@ QMM_API size_t qmm_matmul_workspace_bytes(qmm_format fmt, int64_t M, int64_t N, 
  * when the tiles fill the GPU (each tile's partial sums added in a fixed
  * order), otherwise split-K over a thread-block cluster reduced in
  * distributed shared memory in a fixed order; both are deterministic.
- * Larger M runs the tiled kernel (tcgen05 tensor cores, TMEM accumulators):
+ * Q6_K (output heads) runs a CUDA-core kernel for every M: a warp per
+ * weight row, exact integer codes times the activations, the sub-block
+ * scale applied per superblock, fp32 sums.  For Q8_0 / Q4_K, larger M runs
+ * the tiled kernel (tcgen05 tensor cores, TMEM accumulators):
  * token tiles of 32, 64, 128 or 256 (the smallest of 32 / 64 / 128 that holds
  * M, else 256); when the output tiles are fewer than the SMs, K is split into
  * parts whose partial tiles the last part to finish adds in part order, so
@@ -163,8 +205,8 @@ QMM_API qmm_status qmm_matmul(qmm_format fmt, const void *W_packed, const uint16
  * describe no counterpart of this call; it is an interface convenience.
  *  - Requires qmm_matmul_workspace_bytes(fmt, M, N, K) <= 64 MiB (M * K
  *    somewhat below 32 Mi); larger problems return QMM_ERR_WORKSPACE and
- *    launch nothing.  M <= 16 returns QMM_ERR_UNSUPPORTED: the decode path needs no
- *    scratch, call qmm_matmul with a NULL workspace.
+ *    launch nothing.  M <= 16 and Q6_K return QMM_ERR_UNSUPPORTED:
+ *    those paths need no scratch, call qmm_matmul with a NULL workspace.
  *  - Every call looks up the array's address in the current device's
  *    context (cudaGetSymbolAddress), so it stays valid after a device reset.
  *    The first call on a device may load the library's device code: make
@@ -186,6 +228,7 @@ typedef enum {
     QMM_DEVERR_GEMV_FULL_WAIT = 101,   /* decode: waited too long for a stage */
     QMM_DEVERR_GEMV_EMPTY_WAIT = 102,  /* decode: waited too long for a free slot */
     QMM_DEVERR_GEMM_WAIT = 201,        /* prefill: a pipeline wait ran out */
+    QMM_DEVERR_EMBEDDING_ID = 301,     /* qmm_embedding: an id outside 0 .. V-1 */
     QMM_DEVERR_SELFTEST_TIMEOUT = 901, /* qmm_selftest_bounded_wait: expected */
     QMM_DEVERR_SELFTEST_UNEXPECTED = 902
 } qmm_device_error;

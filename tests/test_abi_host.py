@@ -120,6 +120,35 @@ def test_workspace_query(lib):
     assert L.qmm_matmul(4, FAKE, FAKE, FAKE, 32, 64, 256, MISALIGNED, 1 << 20, S0) == q.QMM_ERR_ALIGNMENT
 
 
+def test_q6_k_sizes_and_policy(lib):
+    import json
+    assert q.qmm_packed_bytes(q.QMM_Q6_K, 4096, 4096) == 4096 * 16 * 210
+    assert q.qmm_packed_bytes(q.QMM_Q6_K, 3, 768) == 3 * 3 * 210
+    assert q.qmm_packed_bytes(q.QMM_Q6_K, 1, 256 + 32) == 0
+    assert q.qmm_matmul_workspace_bytes(q.QMM_Q6_K, 512, 4096, 4096) == 0
+    # the pages' sensitive-tensor table, read from the golden file
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "paper_widths.json")))
+    names = {"Q4K": q.QMM_Q4_K, "Q6K": q.QMM_Q6_K, "Q8_0": q.QMM_Q8_0}
+    for model, emb in g["sensitive_tensor_type"].items():
+        assert q.qmm_embedding_format(names[model]) == names[emb]
+    assert q.qmm_embedding_format(7) == 0
+
+
+def test_embedding_argument_errors(lib):
+    L = lib
+    ids8 = ctypes.c_void_p(0x1000)
+    ids_mis = ctypes.c_void_p(0x1004)
+    assert L.qmm_embedding(5, FAKE, ids8, 4, 10, 256, FAKE, 0, S0) == q.QMM_ERR_INVALID_ARG
+    assert L.qmm_embedding(8, FAKE, ids8, 4, 10, 256, FAKE, 2, S0) == q.QMM_ERR_INVALID_ARG
+    assert L.qmm_embedding(8, FAKE, ids8, -1, 10, 256, FAKE, 0, S0) == q.QMM_ERR_INVALID_ARG
+    assert L.qmm_embedding(8, FAKE, ids8, 4, 10, 300, FAKE, 0, S0) == q.QMM_ERR_SHAPE
+    assert L.qmm_embedding(6, FAKE, ids8, 4, 0, 256, FAKE, 0, S0) == q.QMM_ERR_INVALID_ARG
+    assert L.qmm_embedding(6, NULL, ids8, 4, 10, 256, FAKE, 0, S0) == q.QMM_ERR_INVALID_ARG
+    assert L.qmm_embedding(4, FAKE, ids_mis, 4, 10, 256, FAKE, 1, S0) == q.QMM_ERR_ALIGNMENT
+    assert L.qmm_embedding(4, MISALIGNED, ids8, 4, 10, 256, FAKE, 1, S0) == q.QMM_ERR_ALIGNMENT
+    assert L.qmm_embedding(4, NULL, NULL, 0, 10, 256, NULL, 1, S0) == q.QMM_OK  # no tokens
+
+
 def test_selftest_limit_checked_on_the_host(lib):
     for bad in (0, -5, 100000001):
         assert lib.qmm_selftest_bounded_wait(bad, S0) == q.QMM_ERR_INVALID_ARG
@@ -133,6 +162,7 @@ def test_static_prefill_argument_errors(lib):
     assert f(4, FAKE, FAKE, FAKE, 32, 64, 300, S0) == q.QMM_ERR_SHAPE
     assert f(4, NULL, FAKE, FAKE, 32, 64, 256, S0) == q.QMM_ERR_INVALID_ARG
     assert f(4, FAKE, MISALIGNED, FAKE, 32, 64, 256, S0) == q.QMM_ERR_ALIGNMENT
+    assert f(6, FAKE, FAKE, FAKE, 32, 64, 256, S0) == q.QMM_ERR_UNSUPPORTED  # Q6_K needs no scratch
 
 
 def test_missing_library_fails_loudly(tmp_path):
