@@ -14,7 +14,14 @@ each stage captured as a CUDA graph and replayed back to back:
   gemv_m1   decode GEMV, M = 1, all 8 linears          (-> value)
   gemv_m4   ... M = 4
   gemv_m16  ... M = 16
+  gemm_mid  tiled matmul at mid-size batches, M = 32 and 128, the 4 decode
+            shapes x 2 formats
   gemm      prefill GEMM, M = 512 and 2048, 3 shapes x 2 formats
+  head      output head of the 8B-shape decoder at M = 1 (128256 x 4096) in
+            the types the pages' sensitive-tensor policy gives it: Q6_K (Q4_K
+            model) and Q8_0 (Q8_0 model)
+  embed     token-embedding lookup of 2048 tokens from the 128256 x 4096
+            table, Q6_K and Q8_0, bf16 rows
   model     synthetic 8B-shape decoder (32 layers x 7 linears): ISQ of all
             224 bf16 weights to Q4_K and to Q8_0, then one M = 1 decode
             step (224 GEMVs) in each format
@@ -71,6 +78,9 @@ FAMILY_SOURCES = {
     "dequantize": ("common.cuh", "quantize.cu"),
     "gemv": ("common.cuh", "gemv.cu", "gemv_rows.cu"),
     "gemm": ("common.cuh", "gemm.cu"),
+    "gemm_mid": ("common.cuh", "gemm.cu"),
+    "head": ("common.cuh", "q6k.cu", "gemv_rows.cu"),
+    "embed": ("common.cuh", "q6k.cu"),
 }
 
 
@@ -185,12 +195,25 @@ class Workload:
                         for (n, k) in inputs.DECODE_SHAPES]
         self.x = {}
         self.y = {}
-        for mi, m in enumerate(inputs.DECODE_MS + inputs.PREFILL_MS):
+        for mi, m in enumerate(inputs.DECODE_MS + inputs.PREFILL_MS + inputs.MID_MS):
             self.x[m] = [inputs.activations(m, k, inputs.seed_for(2, si, mi), device=device)
                          for si, (n, k) in enumerate(inputs.DECODE_SHAPES)]
             self.y[m] = {f: [torch.empty((m, n), dtype=torch.float32, device=device)
                              for (n, k) in inputs.DECODE_SHAPES] for f in self.fmts}
         self.gemm_ok = self._probe_gemm()
+        # output head / embedding table of the 8B-shape decoder, in the types
+        # of the sensitive-tensor policy (Q4_K model -> Q6_K, Q8_0 -> Q8_0)
+        vocab, hidden = inputs.VOCAB, 4096
+        head_w = inputs.weights(vocab, hidden, 70000, device=device)
+        self.head_fmts = sorted({q.qmm_embedding_format(f) for f in self.fmts})
+        self.head = {f: q.qmm_quantize(f, head_w) for f in self.head_fmts}
+        del head_w
+        self.head_x = inputs.activations(1, hidden, 70001, device=device)
+        self.head_y = torch.empty((1, vocab), dtype=torch.float32, device=device)
+        g = torch.Generator(device="cpu")
+        g.manual_seed(70002)
+        self.embed_ids = torch.randint(0, vocab, (2048,), generator=g, dtype=torch.int64).to(device)
+        self.embed_out = torch.empty((2048, hidden), dtype=torch.bfloat16, device=device)
         self.model = None
         if with_model:
             self._make_model()
@@ -249,6 +272,32 @@ class Workload:
             S.append(("gemv_m%d" % m, gemv, 8, wbytes + io, 2.0 * 2 * m * nw, "gemv", 2 * nw))
 
         if self.gemm_ok:
+            for m in inputs.MID_MS:
+                def gemm_mid(m=m):
+                    for f in self.fmts:
+                        for (n, k), p, x, y in zip(shapes, self.packed[f], self.x[m], self.y[m][f]):
+                            q.qmm_matmul(f, p, x, n, out=y)
+                S.append(("gemm_m%d" % m, gemm_mid, 16, sum(nw * bw[f] for f in self.fmts),
+                          2 * 2.0 * m * nw, "gemm_mid", 2 * nw))
+
+        vocab, hidden = inputs.VOCAB, 4096
+        hbw = {f: q.BLOCK[f][1] / q.BLOCK[f][0] for f in self.head_fmts}
+
+        def head():
+            for f in self.head_fmts:
+                q.qmm_matmul(f, self.head[f], self.head_x, vocab, out=self.head_y)
+        S.append(("head_m1", head, len(self.head_fmts), sum(vocab * hidden * hbw[f] for f in self.head_fmts),
+                  2.0 * vocab * hidden * len(self.head_fmts), "head", vocab * hidden * len(self.head_fmts)))
+
+        def embed():
+            for f in self.head_fmts:
+                q.qmm_embedding(f, self.head[f], self.embed_ids, hidden, out=self.embed_out)
+        T = self.embed_ids.numel()
+        S.append(("embed_t2048", embed, len(self.head_fmts),
+                  sum(T * hidden * (hbw[f] + 2) + 8 * T for f in self.head_fmts), 0.0, "embed",
+                  T * hidden * len(self.head_fmts)))
+
+        if self.gemm_ok:
             pshapes = inputs.PREFILL_SHAPES
             for m in inputs.PREFILL_MS:
                 def gemm(m=m):
@@ -293,6 +342,8 @@ def time_graphs(torch, graphs, steps, warmup, dev):
     per = {n: [] for n in names}
     step_ms = []
     stream = torch.cuda.current_stream(dev)
+    # NVTX range around the timed steps (a profiler can capture exactly these)
+    torch.cuda.nvtx.range_push("qmm_timed_steps")
     for _ in range(steps):
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(graphs) + 1)]
         evs[0].record(stream)
@@ -303,14 +354,17 @@ def time_graphs(torch, graphs, steps, warmup, dev):
         for i, n in enumerate(names):
             per[n].append(evs[i].elapsed_time(evs[i + 1]))
         step_ms.append(evs[0].elapsed_time(evs[-1]))
+    torch.cuda.nvtx.range_pop()
     return per, step_ms
 
 
 def parity_check(wl):
     """Sampled parity of the benchmarked kernels against the CPU oracle: the
     decode-shaped linears (packed bytes of 64 rows; outputs of 4 rows at
-    M = 1, 16 and 2048) and the last layer of the model (packed bytes and
-    M = 1 outputs of 6 rows of each of its 7 linears, both formats)."""
+    M = 1, 16, 32 and 2048), the output head (bytes and M = 1 outputs of 4
+    rows) and 4 embedding rows in each head format, and the last layer of
+    the model (packed bytes and M = 1 outputs of 6 rows of each of its 7
+    linears, both formats)."""
     import numpy as np
     import oracle
     q, inputs = wl.q, wl.inputs
@@ -321,13 +375,34 @@ def parity_check(wl):
             want = oracle.quantize(f, inputs.bf16_bits(wl.w_bf16[si][:64].cpu()))
             if not np.array_equal(packed[:64], want):
                 return "FAIL: packed bytes differ (fmt %d shape %d)" % (f, si)
-            for m in (1, 16) + ((2048,) if wl.gemm_ok and (n, k) in inputs.PREFILL_SHAPES else ()):
+            for m in (1, 16) + ((32,) if wl.gemm_ok else ()) + (
+                    (2048,) if wl.gemm_ok and (n, k) in inputs.PREFILL_SHAPES else ()):
                 ns = np.array([0, 1, n // 2, n - 1], dtype=np.int64)
                 xb = inputs.bf16_bits(wl.x[m][si])
                 Y, A = oracle.matmul_columns(f, packed, xb, k, ns)
                 y = wl.y[m][f][si][:, ns].double().cpu().numpy()
                 r = float((np.abs(y - Y) / (1e-3 * A + 1e-6)).max())
                 worst = max(worst, r)
+    # output head (sampled rows, bytes and M = 1 outputs) and embedding rows
+    torch = wl.torch
+    vocab, hidden = inputs.VOCAB, 4096
+    head_w = inputs.weights(vocab, hidden, 70000, device=wl.dev)
+    rows = np.array([0, 1, vocab // 2, vocab - 1], dtype=np.int64)
+    ridx = torch.from_numpy(rows).to(wl.dev)
+    eids = wl.embed_ids[:4].cpu().numpy()
+    for f in wl.head_fmts:
+        want = oracle.quantize(f, inputs.bf16_bits(head_w[ridx]))
+        if not np.array_equal(wl.head[f][ridx].cpu().numpy(), want):
+            return "FAIL: output head packed bytes differ (fmt %d)" % f
+        y = q.qmm_matmul(f, wl.head[f], wl.head_x, vocab)[:, ridx].double().cpu().numpy()
+        Y, A = oracle.matmul(f, want, inputs.bf16_bits(wl.head_x), rows.size, hidden)
+        worst = max(worst, float((np.abs(y - Y) / (1e-3 * A + 1e-6)).max()))
+        ew = oracle.quantize(f, inputs.bf16_bits(head_w[torch.from_numpy(eids).to(wl.dev)]))
+        erow = oracle.dequantize(f, ew, eids.size, hidden)
+        got = q.qmm_embedding(f, wl.head[f], wl.embed_ids[:4], hidden, dtype=torch.bfloat16).cpu()
+        if not torch.equal(got, torch.from_numpy(erow).to(torch.bfloat16)):
+            return "FAIL: embedding rows differ (fmt %d)" % f
+    del head_w
     if wl.model is not None:
         # the last model layer: its 7 linears, packed bytes and M = 1 outputs
         # on a row sample, both formats
@@ -495,8 +570,10 @@ def run_reference(args):
 def workload_config():
     return {"workload": "decode-shaped Q8_0/Q4_K linears (N x K = 4096x4096, 1024x4096, "
                         "14336x4096, 4096x14336), GEMV at M=1 (headline) plus M=4/16, ISQ, "
-                        "dequant, prefill GEMM M=512/2048 and a 32-layer 8B-shape model "
-                        "(ISQ + 224-GEMV decode step) in each step",
+                        "dequant, mid-batch matmul M=32/128, prefill GEMM M=512/2048, a "
+                        "128256x4096 output head (Q6_K / Q8_0, M=1), a 2048-token embedding "
+                        "lookup and a 32-layer 8B-shape model (ISQ + 224-GEMV decode step) in "
+                        "each step",
             "weights": "bf16 ~N(0,0.02) with 0.1% x20 outliers, seeded",
             "activations": "bf16 ~N(0,1), seeded",
             "l2": "inputs larger than L2: each GEMV sweep reads > 200 MB of distinct packed "
@@ -596,12 +673,15 @@ def main(argv=None):
         r = {"ms": round(med[name], 4), "launches": launches}
         if nbytes:
             r["GBps"] = round(nbytes / t / 1e9, 1)
-        if fam == "gemm":
+        if fam in ("gemm", "gemm_mid"):
             r["TFLOPs"] = round(flops / t / 1e12, 1)
         rows[name] = r
         fam_time[fam] = fam_time.get(fam, 0.0) + med[name]
     for f, nm in ((q.QMM_Q8_0, "q8_0"), (q.QMM_Q4_K, "q4_k")):
         key = "model_decode_" + nm
+        if key in rows:
+            rows[key]["weight_GBps"] = rows[key].pop("GBps")
+    for key in ("gemm_m32", "gemm_m128", "head_m1"):
         if key in rows:
             rows[key]["weight_GBps"] = rows[key].pop("GBps")
 

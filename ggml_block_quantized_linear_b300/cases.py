@@ -27,7 +27,7 @@ from ggml_block_quantized_linear_b300 import inputs
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--op", choices=["quantize", "dequantize", "matmul"], required=True)
-    ap.add_argument("--fmt", choices=["q8_0", "q4_k"], default="q8_0")
+    ap.add_argument("--fmt", choices=["q8_0", "q4_k", "q6_k"], default="q8_0")
     ap.add_argument("--n", type=int, default=4096)
     ap.add_argument("--k", type=int, default=4096)
     ap.add_argument("--m", type=int, default=1)
@@ -74,7 +74,7 @@ def main(argv=None):
         ts.append(e0.elapsed_time(e1) * 1e-3)
     t = statistics.median(ts)
     nw = a.n * a.k
-    bw = {"q8_0": 34 / 32, "q4_k": 144 / 256}[a.fmt]
+    bw = {"q8_0": 34 / 32, "q4_k": 144 / 256, "q6_k": 210 / 256}[a.fmt]
     rec = {"op": a.op, "fmt": a.fmt, "N": a.n, "K": a.k, "M": a.m, "us": round(t * 1e6, 2)}
     if a.op == "quantize":
         rec["GBps"] = round(nw * (2 + bw) / t / 1e9, 1)

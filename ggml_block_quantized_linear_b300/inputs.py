@@ -29,6 +29,10 @@ DECODE_SHAPES = [(4096, 4096), (1024, 4096), (14336, 4096), (4096, 14336)]
 DECODE_MS = [1, 4, 16]
 PREFILL_SHAPES = [(4096, 4096), (14336, 4096), (4096, 14336)]
 PREFILL_MS = [512, 2048]
+# mid-size batches (continuous batching between decode and prefill)
+MID_MS = [32, 128]
+# output head / token embedding of the 8B-shape decoder: vocabulary x hidden
+VOCAB = 128256
 
 # Synthetic 8B-shape decoder: 32 layers, hidden 4096, 32 q heads / 8 kv heads
 # of 128, MLP 14336.  (name, N, K) per linear, in forward order.
