@@ -15,9 +15,13 @@
 // into the caller's workspace.
 //
 // Tile: 128 weight rows (the MMA's M side, "swap AB") x BN tokens (MMA N:
-// 32, 64, 128 or 256, the smallest that holds M up to 128, else 256) x 64 K
-// per stage; persistent CTAs (one per SM) walk the work units, and two fp32
-// accumulators of BN TMEM columns alternate between consecutive units.
+// 32, 64, 128 or 256, the smallest that holds M up to 128; above 256 tokens
+// 256 or 512) x 64 K per stage; persistent CTAs (one per SM) walk the work
+// units, and two fp32 accumulators of BN TMEM columns alternate between
+// consecutive units.  A 512-token unit is two 256-token MMA tiles that share
+// every dequantized weight stage, with one accumulator of all 512 TMEM
+// columns; its activation ring holds 256-token sub-stages, two per K step.
+// The planner takes it where it needs fewer waves of units.
 // When the output tiles are fewer than the SMs, K is split into parts (a
 // unit is one part of one tile).  256-token tiles: at most two parts, both
 // added onto a Y zeroed by the conversion launch (two additions onto zero
@@ -59,14 +63,16 @@ constexpr int kGemmThreads = (kGemmWarpPackedTma + 1) * 32;
 #define QMM_GEMM_STAGES_A_Q4 3
 #endif
 constexpr int kGemmStagesP = 2;     // packed weight groups
-// two BN-column fp32 accumulators (a power of two, at least 32 columns)
-__host__ __device__ constexpr int gemm_tmem_cols(int bn) { return 2 * bn < 32 ? 32 : 2 * bn; }
+// two BN-column fp32 accumulators (a power of two, at least 32 columns), or
+// one of 512 columns for 512-token units
+__host__ __device__ constexpr int gemm_tmem_cols(int bn) { return bn == 512 ? 512 : 2 * bn < 32 ? 32 : 2 * bn; }
+__host__ __device__ constexpr int gemm_sub(int bn) { return bn == 512 ? 2 : 1; }  // MMA tiles per unit
 // Q4_K (S_j, Mn_j) table: 16 floats per weight row, padded to 18 so that the
 // rows a warp reads together (2 apart) fall in different banks
 constexpr int kGemmCoefStride = 18;
 static_assert((kGemmBM / (4 * kGemmDeqWarps)) % 2 == 0, "dequantization passes come in even / odd row pairs");
 
-// activation stages (BN x 128 bytes each) and dequantized-weight stages (16 KB each)
+// activation stages (min(BN, 256) x 128 bytes each) and dequantized-weight stages (16 KB each)
 __host__ __device__ constexpr int gemm_stages_b(int fmt) { return fmt == 8 ? 3 : QMM_GEMM_STAGES_B_Q4; }
 __host__ __device__ constexpr int gemm_stages_a(int fmt) { return fmt == 8 ? 3 : QMM_GEMM_STAGES_A_Q4; }
 __host__ __device__ constexpr int gemm_group_bytes(int fmt) { return fmt == 8 ? kQ8GroupBytes : kQ4Bytes; }
@@ -79,7 +85,7 @@ __host__ __device__ inline GemmLayout gemm_layout(int fmt, int bn) {
     GemmLayout L;
     int off = 0;
     L.b = off;
-    off += gemm_stages_b(fmt) * bn * kGemmBK * 2;
+    off += gemm_stages_b(fmt) * (bn / gemm_sub(bn)) * kGemmBK * 2;
     L.a = off;
     off += gemm_stages_a(fmt) * kGemmBM * kGemmBK * 2;
     L.p = off;
@@ -273,7 +279,9 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
     constexpr int kSA = gemm_stages_a(kFmt);
     constexpr int kGemmStagesB = gemm_stages_b(kFmt);
     constexpr int kCB = gemm_group_bytes(kFmt);
-    constexpr uint32_t kBBytes = kBN * kGemmBK * 2;
+    constexpr int kSub = gemm_sub(kBN), kSubN = kBN / kSub;  // MMA tiles of a unit, tokens each
+    constexpr int kNbuf = kBN == 512 ? 1 : 2;                  // TMEM accumulators
+    constexpr uint32_t kBBytes = kSubN * kGemmBK * 2;          // one activation (sub-)stage
     constexpr int kTmemCols = gemm_tmem_cols(kBN);
     constexpr uint32_t kABytes = kGemmBM * kGemmBK * 2;
     constexpr uint32_t kPBytes = kGemmBM * kCB;
@@ -326,7 +334,7 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
             mbar_init(p_full(s), 1);
             mbar_init(p_empty(s), kGemmDeqWarps);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kNbuf; ++b) {
             mbar_init(acc_full(b), 1);
             mbar_init(acc_empty(b), kGemmEpiWarps);
         }
@@ -346,17 +354,19 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
             bool ok = true;
-            int ki = 0;  // running activation-stage counter
+            int bi = 0;  // running activation (sub-)stage counter
             for (int lt = 0; lt < my_tiles && ok; ++lt) {
                 const int m0 = tile_m0(lt), kbase = 4 * kg0(lt), ksteps = 4 * (kg1(lt) - kg0(lt));
-                for (int ks = 0; ks < ksteps && ok; ++ks, ++ki) {
-                    const int sb = ki % kGemmStagesB;
-                    if (ki >= kGemmStagesB)
-                        ok = mbar_wait(b_empty(sb), ((ki / kGemmStagesB) - 1) & 1, kErrGemmWait);
-                    if (!ok) break;
-                    mbar_arrive_expect_tx(b_full(sb), kBBytes);
-                    tma_load_2d(smem_addr(smem + L.b + sb * kBBytes), &xmap, (kbase + ks) * kGemmBK, m0,
-                                b_full(sb));
+                for (int ks = 0; ks < ksteps && ok; ++ks) {
+                    for (int j = 0; j < kSub && ok; ++j, ++bi) {
+                        const int sb = bi % kGemmStagesB;
+                        if (bi >= kGemmStagesB)
+                            ok = mbar_wait(b_empty(sb), ((bi / kGemmStagesB) - 1) & 1, kErrGemmWait);
+                        if (!ok) break;
+                        mbar_arrive_expect_tx(b_full(sb), kBBytes);
+                        tma_load_2d(smem_addr(smem + L.b + sb * kBBytes), &xmap, (kbase + ks) * kGemmBK,
+                                    m0 + j * kSubN, b_full(sb));
+                    }
                 }
             }
         }
@@ -382,27 +392,34 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = umma_idesc_f16(kGemmBM, kBN);
+            constexpr uint32_t idesc = umma_idesc_f16(kGemmBM, kSubN);
             bool ok = true;
-            int ki = 0;  // running k-step counter (A and activation rings)
+            int ki = 0;  // running k-step counter (A ring)
+            int bi = 0;  // running activation (sub-)stage counter
             for (int lt = 0; lt < my_tiles; ++lt) {
-                const int buf = lt & 1, use = lt >> 1;
+                const int buf = lt % kNbuf, use = lt / kNbuf;
                 const int ksteps = 4 * (kg1(lt) - kg0(lt));
                 const uint32_t dacc = tmem + (uint32_t)(buf * kBN);
                 if (ok && use > 0) ok = mbar_wait(acc_empty(buf), (use - 1) & 1, kErrGemmWait);
                 for (int ks = 0; ks < ksteps && ok; ++ks, ++ki) {
-                    const int sa = ki % kSA, sb = ki % kGemmStagesB;
-                    ok = mbar_wait(a_full(sa), (ki / kSA) & 1, kErrGemmWait) &&
-                         mbar_wait(b_full(sb), (ki / kGemmStagesB) & 1, kErrGemmWait);
+                    const int sa = ki % kSA;
+                    ok = mbar_wait(a_full(sa), (ki / kSA) & 1, kErrGemmWait);
                     if (!ok) break;
                     tc_fence_after();
                     const uint64_t ad = umma_desc_sw128(smem_addr(smem + L.a + sa * kABytes));
-                    const uint64_t bd = umma_desc_sw128(smem_addr(smem + L.b + sb * kBBytes));
+                    // every MMA tile of the unit multiplies the same dequantized weights
+                    for (int j = 0; j < kSub && ok; ++j, ++bi) {
+                        const int sb = bi % kGemmStagesB;
+                        ok = mbar_wait(b_full(sb), (bi / kGemmStagesB) & 1, kErrGemmWait);
+                        if (!ok) break;
+                        tc_fence_after();
+                        const uint64_t bd = umma_desc_sw128(smem_addr(smem + L.b + sb * kBBytes));
 #pragma unroll
-                    for (int kk = 0; kk < kGemmBK / 16; ++kk)  // +32 bytes of K per MMA
-                        umma_f16(dacc, ad + 2 * kk, bd + 2 * kk, idesc, (ks | kk) != 0);
+                        for (int kk = 0; kk < kGemmBK / 16; ++kk)  // +32 bytes of K per MMA
+                            umma_f16(dacc + (uint32_t)(j * kSubN), ad + 2 * kk, bd + 2 * kk, idesc, (ks | kk) != 0);
+                        umma_commit(b_empty(sb));
+                    }
                     umma_commit(a_empty(sa));
-                    umma_commit(b_empty(sb));
                 }
                 umma_commit(acc_full(buf));  // also after an error: releases the epilogue
             }
@@ -481,7 +498,7 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
         const int etid = tid - 32 * (2 + kGemmDeqWarps);  // 0 .. 127
         bool ok = true;
         for (int lt = 0; lt < my_tiles; ++lt) {
-            const int buf = lt & 1, use = lt >> 1;
+            const int buf = lt % kNbuf, use = lt / kNbuf;
             const int n0 = tile_n0(lt), m0 = tile_m0(lt);
             if (ok) ok = mbar_wait_warp(acc_full(buf), use & 1, kErrGemmWait);
             tc_fence_after();
@@ -584,18 +601,49 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
 struct GemmPlan {
     int bn, ksplit, tiles, tickets;
 };
+#ifndef QMM_GEMM_UNIT512  // 1: 512-token units where the cost model favours them
+#define QMM_GEMM_UNIT512 1
+#endif
+// Relative cost of one 64-wide K step of a 512-token unit against a 256-token
+// one, measured on the prefill shapes (14336 x 4096 and 4096 x 14336 at 2048
+// tokens, 4096 x 4096 at 2048): about 1.85, so sharing a dequantized stage
+// saves 7.5 % per token and the unit count decides the rest.
+constexpr double kGemmCost512 = 1.85;
+
 static GemmPlan gemm_plan(int M, int N, int K, int sms) {
     GemmPlan pl;
-    pl.bn = M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
-    pl.tiles = ((N + kGemmBM - 1) / kGemmBM) * ((M + pl.bn - 1) / pl.bn);
     const int groups = K / kGroup;
-    if (pl.bn == 256) {
-        // two K halves when the tiles fill under about half of the SMs
-        auto occupancy = [&](int u) {
-            const int waves = (u + sms - 1) / sms;
-            return (double)u / ((double)waves * sms);
+    const int tiles_n = (N + kGemmBM - 1) / kGemmBM;
+    // two K halves when the tiles fill under about half of the SMs
+    auto occupancy = [&](int u) {
+        const int waves = (u + sms - 1) / sms;
+        return (double)u / ((double)waves * sms);
+    };
+    auto halves = [&](int tiles) {
+        return (groups % 2 == 0 && occupancy(2 * tiles) > occupancy(tiles) + 0.2) ? 2 : 1;
+    };
+    if (M > 256) {
+        // 256- or 512-token units: waves of units times the K steps of a unit
+        auto cost = [&](int bn, int &tiles, int &ks) {
+            tiles = tiles_n * ((M + bn - 1) / bn);
+            ks = halves(tiles);
+            const int waves = (tiles * ks + sms - 1) / sms;
+            return waves * ((double)groups / ks) * (bn == 512 ? kGemmCost512 : 1.0);
         };
-        pl.ksplit = (groups % 2 == 0 && occupancy(2 * pl.tiles) > occupancy(pl.tiles) + 0.2) ? 2 : 1;
+        int t256, k256, t512, k512;
+        const double c256 = cost(256, t256, k256), c512 = cost(512, t512, k512);
+        if (QMM_GEMM_UNIT512 && c512 < c256) {
+            pl.bn = 512, pl.tiles = t512, pl.ksplit = k512;
+        } else {
+            pl.bn = 256, pl.tiles = t256, pl.ksplit = k256;
+        }
+        pl.tickets = 0;
+        return pl;
+    }
+    pl.bn = M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+    pl.tiles = tiles_n * ((M + pl.bn - 1) / pl.bn);
+    if (pl.bn == 256) {
+        pl.ksplit = halves(pl.tiles);
         pl.tickets = 0;
     } else {
         int ks = sms / pl.tiles;
@@ -650,7 +698,7 @@ static cudaError_t launch_gemm_t(const void *W, const uint16_t *X, float *Y, int
 
     CUtensorMap xmap, wmap;
     e = encode_tmap_2d(&xmap, Xh, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (uint64_t)K, (uint64_t)M,
-                       (uint64_t)K * 2, kGemmBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B);
+                       (uint64_t)K * 2, kGemmBK, kBN / gemm_sub(kBN), CU_TENSOR_MAP_SWIZZLE_128B);
     if (e != cudaSuccess) return e;
     constexpr int kCB = gemm_group_bytes(kFmt);
     const int64_t row_bytes = (int64_t)(K / kGroup) * kCB;
@@ -684,7 +732,8 @@ static cudaError_t launch_gemm_f(const void *W, const uint16_t *X, float *Y, int
     case 32: return launch_gemm_t<kFmt, 32>(W, X, Y, M, N, K, workspace, sms, stream);
     case 64: return launch_gemm_t<kFmt, 64>(W, X, Y, M, N, K, workspace, sms, stream);
     case 128: return launch_gemm_t<kFmt, 128>(W, X, Y, M, N, K, workspace, sms, stream);
-    default: return launch_gemm_t<kFmt, 256>(W, X, Y, M, N, K, workspace, sms, stream);
+    case 256: return launch_gemm_t<kFmt, 256>(W, X, Y, M, N, K, workspace, sms, stream);
+    default: return launch_gemm_t<kFmt, 512>(W, X, Y, M, N, K, workspace, sms, stream);
     }
 }
 

@@ -156,6 +156,20 @@ def test_prefill_split_k_full(fmt, n, k, m):
     assert torch.equal(y, run(fmt, packed, xb, n))  # parts added in a fixed order
 
 
+# 512-token units (two 256-token MMA tiles sharing each dequantized weight
+# stage), which the planner picks where they need fewer waves: ragged last
+# unit (1000 = 512 + 488 tokens; 1500 = 2 x 512 + 476), a unit whose second
+# MMA tile is entirely past M (1100 = 2 x 512 + 76), and K halves.
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("n,k,m", [(4096, 512, 1000), (2048, 1024, 1500), (4096, 512, 1100)])
+def test_prefill_512_token_units_full(fmt, n, k, m):
+    packed, xb = problem(fmt, n, k, m, 5000 + n + k + m)
+    Y, A = oracle.matmul(fmt, packed, xb, n, k)
+    y = run(fmt, packed, xb, n)
+    check_matmul(y, Y, A, "fmt=%d n=%d k=%d m=%d" % (fmt, n, k, m))
+    assert torch.equal(y, run(fmt, packed, xb, n))
+
+
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("n,k", [(128, 256), (200, 512), (384, 1024), (130, 2304)])
 @pytest.mark.parametrize("m", [17, 64, 255, 256, 300])
