@@ -21,6 +21,7 @@ import numpy as np
 Q8_0 = 8
 Q4_K = 4
 Q6_K = 6
+FP8 = 80
 SRC_BF16 = 0
 SRC_F32 = 1
 
@@ -32,6 +33,7 @@ _lock = threading.Lock()
 _lib = None
 
 BLOCK = {Q8_0: (32, 34), Q4_K: (256, 144), Q6_K: (256, 210)}
+FP8_ROW_PAD = 16  # FP8 rows: K codes, the fp32 row scale, 12 zero bytes
 
 
 def build(force: bool = False) -> str:
@@ -71,6 +73,8 @@ def lib() -> ctypes.CDLL:
             L.orc_matmul.restype = ctypes.c_int
             L.orc_matmul_columns.argtypes = [ctypes.c_int, vp, vp, i64, i64, vp, i64, vp, vp]
             L.orc_matmul_columns.restype = ctypes.c_int
+            L.orc_f32_to_e4m3_array.argtypes = [vp, vp, i64]
+            L.orc_e4m3_to_f32_array.argtypes = [vp, vp, i64]
             L.orc_gather.argtypes = [ctypes.c_int, vp, i64, i64, vp, i64, vp]
             L.orc_gather.restype = ctypes.c_int
             L.orc_q6_k_position.argtypes = [ctypes.c_int, vp]
@@ -211,3 +215,18 @@ def q6_k_position(w: int):
     pos = np.zeros(4, dtype=np.int32)
     lib().orc_q6_k_position(int(w), _ptr(pos))
     return tuple(int(v) for v in pos)
+
+
+def f32_to_e4m3_bits(values) -> np.ndarray:
+    """E4M3 encoding (round to nearest even, saturating at +-448) of float32 values."""
+    v = np.ascontiguousarray(np.asarray(values, dtype=np.float32).ravel())
+    out = np.zeros(v.size, dtype=np.uint8)
+    lib().orc_f32_to_e4m3_array(_ptr(v), _ptr(out), v.size)
+    return out
+
+
+def e4m3_bits_to_f32(bits) -> np.ndarray:
+    b = np.ascontiguousarray(np.asarray(bits, dtype=np.uint8).ravel())
+    out = np.zeros(b.size, dtype=np.float32)
+    lib().orc_e4m3_to_f32_array(_ptr(b), _ptr(out), b.size)
+    return out

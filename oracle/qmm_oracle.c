@@ -47,6 +47,14 @@
  *     l < 32): low 4 bits of q in byte 64h + 32(s & 1) + l of ql (low
  *     nibble for s < 2, high nibble for s >= 2), high 2 bits in bits 2s,
  *     2s + 1 of byte 32h + l of qh; weight w uses sc[w / 16].
+ *   FP8 E4M3 with a scale per row (W8A16): the page's section "FP8" says
+ *     E4M3 FP8 can be produced with ISQ and lists symmetric E4M3 W8A16 with
+ *     tensor, channel or block weight scales; the reading here is one fp32
+ *     scale per output row (channel): s = max_k |x_k| / 448 (448 is E4M3's
+ *     largest finite value); code = E4M3(x_k / s), round to nearest even,
+ *     saturating at +-448 (all codes 0 when s == 0); dequantized value:
+ *     float(E4M3 value) * s, one fp32 rounding.  A packed row is the K codes,
+ *     then s (little-endian fp32), then 12 zero bytes: K + 16 bytes.
  *   gather (embedding lookup): out[t][:] = dequantized row ids[t] of the
  *     packed [V x D] table (Q8_0 is the page's common embedding target).
  *   matmul: Y[m][n] = sum_k double(w^[n][k]) * double(x[m][k]) over the exactly
@@ -368,10 +376,108 @@ static void dequantize_q6_k_superblock(const uint8_t *blk, float *y)
 }
 
 /* ------------------------------------------------------------------ */
+/* FP8 E4M3 (OCP 8-bit floating point, E4M3: 1 sign, 4 exponent bits with  */
+/* bias 7, 3 fraction bits, no infinities, S.1111.111 is NaN)            */
+/* ------------------------------------------------------------------ */
+
+enum { FP8_ROW_PAD = 16 };
+
+/* E4M3 -> float.  E == 0: subnormal F * 2^-9; (E, F) == (15, 7): NaN;
+ * otherwise (8 + F) * 2^(E - 10). */
+float orc_e4m3_to_f32(uint8_t b)
+{
+    int sign = b >> 7, E = (b >> 3) & 15, F = b & 7;
+    double v;
+    if (E == 0)
+        v = ldexp((double)F, -9);
+    else if (E == 15 && F == 7)
+        v = NAN;
+    else
+        v = ldexp((double)(8 + F), E - 10);
+    return (float)(sign ? -v : v);
+}
+
+/* float (finite) -> E4M3, round to nearest even, saturating at +-448.
+ * With e = floor(log2 |f|) clamped below at -6 (subnormals share the
+ * exponent of the smallest normal), the grid around |f| has quantum
+ * 2^(e-3); N = rint(|f| / 2^(e-3)) (exact scaling in double, ties to
+ * even), and N * 2^(e-3) is encoded after clamping to 448. */
+uint8_t orc_f32_to_e4m3(float f)
+{
+    uint8_t sign = signbit(f) ? 0x80 : 0;
+    double a = fabs((double)f);
+    if (a == 0.0)
+        return sign;
+    int ex;
+    frexp(a, &ex);
+    int e = ex - 1;
+    if (e < -6)
+        e = -6;
+    double v = ldexp(rint(ldexp(a, 3 - e)), e - 3);
+    if (v > 448.0)
+        v = 448.0;
+    if (v == 0.0)
+        return sign;
+    frexp(v, &ex);
+    e = ex - 1;
+    if (e < -6)
+        return (uint8_t)(sign | (int)ldexp(v, 9)); /* subnormal: v = F * 2^-9 */
+    int frac = (int)ldexp(v, 3 - e) - 8;          /* v = (8 + F) * 2^(e - 3) */
+    return (uint8_t)(sign | ((e + 7) << 3) | frac);
+}
+
+static void quantize_fp8_row(const float *x, int64_t K, uint8_t *out)
+{
+    float amax = 0.0f;
+    for (int64_t k = 0; k < K; k++) {
+        float a = fabsf(x[k]);
+        if (a > amax)
+            amax = a;
+    }
+    float s = amax / 448.0f;
+    for (int64_t k = 0; k < K; k++)
+        out[k] = s > 0.0f ? orc_f32_to_e4m3(x[k] / s) : 0;
+    memcpy(out + K, &s, 4);
+    memset(out + K + 4, 0, FP8_ROW_PAD - 4);
+}
+
+static void dequantize_fp8_row(const uint8_t *in, int64_t K, float *y)
+{
+    float s;
+    memcpy(&s, in + K, 4);
+    for (int64_t k = 0; k < K; k++)
+        y[k] = orc_e4m3_to_f32(in[k]) * s;
+}
+
+void orc_f32_to_e4m3_array(const float *x, uint8_t *b, int64_t n)
+{
+    for (int64_t i = 0; i < n; i++)
+        b[i] = orc_f32_to_e4m3(x[i]);
+}
+
+void orc_e4m3_to_f32_array(const uint8_t *b, float *x, int64_t n)
+{
+    for (int64_t i = 0; i < n; i++)
+        x[i] = orc_e4m3_to_f32(b[i]);
+}
+
+/* ------------------------------------------------------------------ */
 /* Exported API                                                        */
 /* ------------------------------------------------------------------ */
 
-enum { ORC_Q8_0 = 8, ORC_Q4_K = 4, ORC_Q6_K = 6 };
+enum { ORC_Q8_0 = 8, ORC_Q4_K = 4, ORC_Q6_K = 6, ORC_FP8 = 80 };
+
+/* Bytes of one packed row of `cols` weights (0 if cols is not a whole
+ * number of blocks). */
+static int64_t row_bytes_of(int fmt, int64_t cols)
+{
+    if (fmt == ORC_FP8)
+        return cols % 256 == 0 ? cols + FP8_ROW_PAD : 0;
+    int qk = fmt == ORC_Q8_0 ? Q8_0_QK : (fmt == ORC_Q4_K || fmt == ORC_Q6_K) ? 256 : 0;
+    if (qk == 0 || cols % qk != 0)
+        return 0;
+    return (cols / qk) * (fmt == ORC_Q8_0 ? Q8_0_BYTES : fmt == ORC_Q4_K ? Q4_K_BYTES : Q6_K_BYTES);
+}
 
 static int qk_of(int fmt)
 {
@@ -404,10 +510,10 @@ static void dequantize_block(int fmt, const uint8_t *blk, float *y)
 
 int64_t orc_packed_bytes(int fmt, int64_t rows, int64_t cols)
 {
-    int qk = qk_of(fmt);
-    if (qk == 0 || rows < 0 || cols < 0 || cols % qk != 0)
+    if (rows < 0 || cols <= 0)
         return -1;
-    return rows * (cols / qk) * bytes_of(fmt);
+    int64_t rb = row_bytes_of(fmt, cols);
+    return rb > 0 ? rows * rb : -1;
 }
 
 void orc_set_threads(int n)
@@ -432,8 +538,29 @@ int orc_max_threads(void)
 /* src_kind: 0 = bf16 (raw uint16 bits), 1 = fp32.  Returns 0 on success. */
 int orc_quantize(int fmt, int src_kind, const void *src, uint8_t *dst, int64_t rows, int64_t cols)
 {
+    if (src_kind != 0 && src_kind != 1)
+        return -1;
+    if (fmt == ORC_FP8) {
+        int64_t rb = row_bytes_of(fmt, cols);
+        if (rb == 0)
+            return -1;
+        int bad = 0;
+#pragma omp parallel for schedule(static) reduction(| : bad)
+        for (int64_t r = 0; r < rows; r++) {
+            float *x = (float *)malloc((size_t)cols * sizeof(float));
+            if (!x) {
+                bad |= 1;
+                continue;
+            }
+            for (int64_t k = 0; k < cols; k++)
+                x[k] = load_src(src_kind, src, r * cols + k);
+            quantize_fp8_row(x, cols, dst + r * rb);
+            free(x);
+        }
+        return bad ? -2 : 0;
+    }
     int qk = qk_of(fmt);
-    if (qk == 0 || cols % qk != 0 || (src_kind != 0 && src_kind != 1))
+    if (qk == 0 || cols % qk != 0)
         return -1;
     int64_t nb = cols / qk;
     int64_t row_bytes = nb * bytes_of(fmt);
@@ -451,6 +578,15 @@ int orc_quantize(int fmt, int src_kind, const void *src, uint8_t *dst, int64_t r
 
 int orc_dequantize(int fmt, const uint8_t *src, float *dst, int64_t rows, int64_t cols)
 {
+    if (fmt == ORC_FP8) {
+        int64_t rb = row_bytes_of(fmt, cols);
+        if (rb == 0)
+            return -1;
+#pragma omp parallel for schedule(static)
+        for (int64_t r = 0; r < rows; r++)
+            dequantize_fp8_row(src + r * rb, cols, dst + r * cols);
+        return 0;
+    }
     int qk = qk_of(fmt);
     if (qk == 0 || cols % qk != 0)
         return -1;
@@ -467,6 +603,10 @@ int orc_dequantize(int fmt, const uint8_t *src, float *dst, int64_t rows, int64_
 
 static void dequantize_row(int fmt, const uint8_t *src, float *dst, int64_t cols)
 {
+    if (fmt == ORC_FP8) {
+        dequantize_fp8_row(src, cols, dst);
+        return;
+    }
     int qk = qk_of(fmt);
     for (int64_t b = 0; b < cols / qk; b++)
         dequantize_block(fmt, src + b * bytes_of(fmt), dst + b * qk);
@@ -478,13 +618,12 @@ static void dequantize_row(int fmt, const uint8_t *src, float *dst, int64_t cols
 int orc_gather(int fmt, const uint8_t *W, int64_t V, int64_t D, const int64_t *ids, int64_t T,
                float *out)
 {
-    int qk = qk_of(fmt);
-    if (qk == 0 || D % qk != 0 || V < 0 || T < 0)
+    int64_t row_bytes = row_bytes_of(fmt, D);
+    if (row_bytes == 0 || V < 0 || T < 0)
         return -1;
     for (int64_t t = 0; t < T; t++)
         if (ids[t] < 0 || ids[t] >= V)
             return -1;
-    int64_t row_bytes = (D / qk) * bytes_of(fmt);
     for (int64_t t = 0; t < T; t++)
         dequantize_row(fmt, W + ids[t] * row_bytes, out + t * D, D);
     return 0;
@@ -497,10 +636,9 @@ int orc_gather(int fmt, const uint8_t *W, int64_t V, int64_t D, const int64_t *i
 int orc_matmul_columns(int fmt, const uint8_t *W, const uint16_t *X, int64_t M, int64_t K,
                        const int64_t *ns, int64_t count, double *Y, double *A)
 {
-    int qk = qk_of(fmt);
-    if (qk == 0 || K % qk != 0)
+    int64_t row_bytes = row_bytes_of(fmt, K);
+    if (row_bytes == 0)
         return -1;
-    int64_t row_bytes = (K / qk) * bytes_of(fmt);
     int bad = 0;
 #pragma omp parallel for schedule(dynamic, 4) reduction(| : bad)
     for (int64_t t = 0; t < count; t++) {
