@@ -19,6 +19,7 @@ import threading
 QMM_Q8_0 = 8
 QMM_Q4_K = 4
 QMM_Q6_K = 6
+QMM_FP8_E4M3 = 80
 QMM_OUT_F32 = 0
 QMM_OUT_BF16 = 1
 QMM_SRC_BF16 = 0
@@ -33,7 +34,7 @@ QMM_ERR_WORKSPACE = -5
 QMM_ERR_CUDA = -6
 QMM_ERR_DEVICE = -7
 
-FORMATS = {"q8_0": QMM_Q8_0, "q4_k": QMM_Q4_K, "q6_k": QMM_Q6_K}
+FORMATS = {"q8_0": QMM_Q8_0, "q4_k": QMM_Q4_K, "q6_k": QMM_Q6_K, "fp8": QMM_FP8_E4M3}
 BLOCK = {QMM_Q8_0: (32, 34), QMM_Q4_K: (256, 144), QMM_Q6_K: (256, 210)}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))

@@ -7,6 +7,7 @@
 #include <cuda.h>  // CUtensorMap (types only; the driver is reached through the runtime)
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 #include <stdint.h>
@@ -24,6 +25,10 @@ constexpr int kQ4Bytes = 144;
 // one Q4_K superblock = 144 bytes); both are multiples of 16 bytes.
 constexpr int kGroup = 256;
 constexpr int kQ8GroupBytes = 272;
+// FP8 E4M3 with a scale per row: a packed row is K codes, the fp32 row scale
+// and 12 zero bytes (format value 80).
+constexpr int kFp8 = 80;
+constexpr int kFp8RowPad = 16;
 
 // Device error word: nonzero codes are written by kernels whose bounded wait
 // ran out (see qmm_device_error_take).  The library is one translation unit
@@ -287,6 +292,12 @@ __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b16) {
     return __uint_as_float(b16 << 16);
+}
+
+// Two E4M3 codes (low byte first) -> their values as a binary16 pair, exactly.
+__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t two_codes) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two_codes & 0xFFFFu), __NV_E4M3);
+    return (uint32_t)h.x | ((uint32_t)h.y << 16);
 }
 
 }  // namespace qmm

@@ -73,9 +73,13 @@ constexpr int kGemmCoefStride = 18;
 static_assert((kGemmBM / (4 * kGemmDeqWarps)) % 2 == 0, "dequantization passes come in even / odd row pairs");
 
 // activation stages (min(BN, 256) x 128 bytes each) and dequantized-weight stages (16 KB each)
-__host__ __device__ constexpr int gemm_stages_b(int fmt) { return fmt == 8 ? 3 : QMM_GEMM_STAGES_B_Q4; }
-__host__ __device__ constexpr int gemm_stages_a(int fmt) { return fmt == 8 ? 3 : QMM_GEMM_STAGES_A_Q4; }
-__host__ __device__ constexpr int gemm_group_bytes(int fmt) { return fmt == 8 ? kQ8GroupBytes : kQ4Bytes; }
+__host__ __device__ constexpr int gemm_stages_b(int fmt) { return fmt == 4 ? QMM_GEMM_STAGES_B_Q4 : 3; }
+__host__ __device__ constexpr int gemm_stages_a(int fmt) { return fmt == 4 ? QMM_GEMM_STAGES_A_Q4 : 3; }
+// Shared-memory pitch of a packed weight row in a stage (FP8: a 256-byte group
+// plus 16 bytes of the next, which keeps the dequantizing warps' loads on
+// distinct banks as Q8_0's 272 bytes do), and a group's advance in a row.
+__host__ __device__ constexpr int gemm_group_bytes(int fmt) { return fmt == 4 ? kQ4Bytes : kQ8GroupBytes; }
+__host__ __device__ constexpr int gemm_group_advance(int fmt) { return fmt == 8 ? kQ8GroupBytes : fmt == 4 ? kQ4Bytes : 256; }
 
 struct GemmLayout {
     int b, a, p, coef, bars, total;  // offsets from the 1024-aligned base
@@ -256,9 +260,18 @@ __device__ __forceinline__ uint4 deq8_q4_k(const uint8_t *prow, const float *coe
     return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
+// FP8: 8 weights (k = 8c .. 8c+7 of k-step j) converted exactly to binary16;
+// the row scale is applied to the finished sums.
+__device__ __forceinline__ uint4 deq8_fp8(const uint8_t *prow, int j, int c) {
+    const uint2 q = *reinterpret_cast<const uint2 *>(prow + 64 * j + 8 * c);
+    return make_uint4(e4m3x2_to_h2(q.x), e4m3x2_to_h2(q.x >> 16), e4m3x2_to_h2(q.y), e4m3x2_to_h2(q.y >> 16));
+}
+
 // ------------------------------------------------------------------ kernel
 struct GemmParams {
     float *Y;
+    const uint8_t *W;   // FP8: the packed rows, for the row scales
+    int64_t row_bytes;  // packed bytes per row
     float *partials;  // ticket mode: [tile][part][128 rows][BN columns] fp32
     int *tickets;     // ticket mode: parts of each tile done so far (cleared by the conversion launch)
     int M, N, K;
@@ -384,8 +397,8 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
                         ok = mbar_wait(p_empty(sp), ((gi / kGemmStagesP) - 1) & 1, kErrGemmWait);
                     if (!ok) break;
                     mbar_arrive_expect_tx(p_full(sp), kPBytes);
-                    tma_load_2d(smem_addr(smem + L.p + sp * kPBytes), &wmap, (gbase + g) * (kCB / 2), n0,
-                                p_full(sp));
+                    tma_load_2d(smem_addr(smem + L.p + sp * kPBytes), &wmap,
+                                (gbase + g) * (gemm_group_advance(kFmt) / 2), n0, p_full(sp));
                 }
             }
         }
@@ -475,7 +488,9 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
                             // code loads of the 32 lanes free of bank conflicts
                             const int r = (pass >> 1) * 8 * kGemmDeqWarps + 8 * dw + 2 * rsub + (pass & 1);
                             uint4 v;
-                            if constexpr (kFmt == 8)
+                            if constexpr (kFmt == kFp8)
+                                v = deq8_fp8(pst + r * kCB, j, c);
+                            else if constexpr (kFmt == 8)
                                 v = deq8_q8_0(pst + r * kCB, j, c);
                             else
                                 v = deq8_q4_k(pst + r * kCB, coef + r * kGemmCoefStride, j, c);
@@ -504,12 +519,20 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
             tc_fence_after();
             const int n = n0 + r;
             const int tile = tile_base(lt);
+            // FP8: this row's scale (rows past N read nothing)
+            float rs = 1.f;
+            if constexpr (kFmt == kFp8)
+                if (n < p.N) rs = __ldg(reinterpret_cast<const float *>(p.W + (int64_t)n * p.row_bytes + p.K));
             float *pw = p.partials + ((int64_t)tile * ksplit + kpart(lt)) * (kBN * kGemmBM);
             if (ok) {
 #pragma unroll 1
                 for (int col = 0; col < kBN; col += 32) {
                     uint32_t v[32];
                     tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(buf * kBN + col), v);
+                    if constexpr (kFmt == kFp8) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * rs);
+                    }
                     if (!p.tickets_mode) {
                         if (n < p.N) {
 #pragma unroll
@@ -700,8 +723,10 @@ static cudaError_t launch_gemm_t(const void *W, const uint16_t *X, float *Y, int
     e = encode_tmap_2d(&xmap, Xh, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (uint64_t)K, (uint64_t)M,
                        (uint64_t)K * 2, kGemmBK, kBN / gemm_sub(kBN), CU_TENSOR_MAP_SWIZZLE_128B);
     if (e != cudaSuccess) return e;
+    // a box is 128 rows x one stage pitch (FP8: past a row's end, zero-filled)
     constexpr int kCB = gemm_group_bytes(kFmt);
-    const int64_t row_bytes = (int64_t)(K / kGroup) * kCB;
+    const int64_t row_bytes =
+        kFmt == kFp8 ? (int64_t)K + kFp8RowPad : (int64_t)(K / kGroup) * gemm_group_advance(kFmt);
     e = encode_tmap_2d(&wmap, W, CU_TENSOR_MAP_DATA_TYPE_UINT16, (uint64_t)(row_bytes / 2),
                        (uint64_t)N, (uint64_t)row_bytes, kCB / 2, kGemmBM);
     if (e != cudaSuccess) return e;
@@ -712,6 +737,8 @@ static cudaError_t launch_gemm_t(const void *W, const uint16_t *X, float *Y, int
     if (e != cudaSuccess) return e;
     GemmParams p;
     p.Y = Y;
+    p.W = static_cast<const uint8_t *>(W);
+    p.row_bytes = row_bytes;
     p.partials = reinterpret_cast<float *>(wb + ws.partials);
     p.tickets = reinterpret_cast<int *>(wb + ws.tickets);
     p.M = M;
@@ -741,6 +768,7 @@ cudaError_t launch_gemm(int fmt, const void *W, const uint16_t *X, float *Y, int
                         void *workspace, size_t workspace_bytes, int sms, cudaStream_t stream) {
     if (workspace_bytes < gemm_workspace_bytes(fmt, M, N, K, sms)) return cudaErrorInvalidValue;
     if (fmt == 8) return launch_gemm_f<8>(W, X, Y, M, N, K, workspace, sms, stream);
+    if (fmt == kFp8) return launch_gemm_f<kFp8>(W, X, Y, M, N, K, workspace, sms, stream);
     return launch_gemm_f<4>(W, X, Y, M, N, K, workspace, sms, stream);
 }
 

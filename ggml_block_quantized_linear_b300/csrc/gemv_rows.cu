@@ -51,9 +51,15 @@ struct RowsLayout {
     int ring, xh, xs, coef, ypart, bars, total;
 };
 
+// Bytes a chunk advances in a packed row, and half the shared-memory pitch of
+// a stage row (FP8: two 256-byte chunks plus 32 bytes of the next, a 544-byte
+// pitch that keeps a warp's code loads on distinct banks, as Q8_0's does).
+__host__ __device__ constexpr int rows_chunk_bytes(int fmt) { return fmt == 8 ? kQ8GroupBytes : fmt == 4 ? kQ4Bytes : 256; }
+__host__ __device__ constexpr int rows_half_pitch(int fmt) { return fmt == 4 ? kQ4Bytes : kQ8GroupBytes; }
+
 // mt = 8 * (token tiles): the stride of the Q4_K block sums per 32-block.
 __host__ __device__ inline RowsLayout rows_layout(int fmt, int M, int dpp, int win, int mt) {
-    const int cb = fmt == 8 ? kQ8GroupBytes : kQ4Bytes;
+    const int cb = rows_half_pitch(fmt);
     RowsLayout L;
     int off = 0;
     L.ring = off;
@@ -76,6 +82,8 @@ __host__ __device__ inline RowsLayout rows_layout(int fmt, int M, int dpp, int w
 struct RowsParams {
     float *Y;
     const uint16_t *X;
+    const uint8_t *W;   // FP8: the packed rows, for the row scales
+    int64_t row_bytes;  // packed bytes per row
     int M, N, K;
     int nchunks;  // K / 256
     int ntiles;   // ceil(N / 16)
@@ -182,6 +190,32 @@ __device__ __forceinline__ void rq8_block(const uint8_t *r0, const uint8_t *r1, 
     }
 }
 
+// FP8 E4M3: one 32-weight block of rows g and g + 8, the lane's codes 8t ..
+// 8t + 7 paired (0, 2), (1, 3) like the staged activations; the codes convert
+// exactly to binary16 and there is no block scale (the row scale is applied
+// to the finished sums).  Each block's two MMAs start from zero and are then
+// added to acc, which keeps the MMA dependency chains two long.
+template <int kB, int kNT>
+__device__ __forceinline__ void r8_block(const uint8_t *r0, const uint8_t *r1, const __half *xb, int xstride,
+                                         int t, bool v0, bool v1, float (&acc)[kNT][4]) {
+    const uint2 a = *reinterpret_cast<const uint2 *>(r0 + 32 * kB + 8 * t);
+    const uint2 b = *reinterpret_cast<const uint2 *>(r1 + 32 * kB + 8 * t);
+    // bytes (0, 2) and (1, 3) of a word as one E4M3 pair each
+    auto p02 = [](uint32_t w) { return e4m3x2_to_h2(prmt(w, 0u, 0x4420u)); };
+    auto p13 = [](uint32_t w) { return e4m3x2_to_h2(prmt(w, 0u, 0x4431u)); };
+    const uint32_t A0[4] = {p02(a.x), p02(b.x), p13(a.x), p13(b.x)};
+    const uint32_t A1[4] = {p02(a.y), p02(b.y), p13(a.y), p13(b.y)};
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt) {
+        const uint4 xv = x_frag(xb + nt * 8 * xstride + kQ8Weights * kB + 8 * t, nt == 0 ? v0 : v1);
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_f16_16816(c, A0, xv.x, xv.y);
+        mma_f16_16816(c, A1, xv.z, xv.w);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[nt][e] += c[e];
+    }
+}
+
 // Q4_K scale/min decode of one chunk (16 rows x 8 sub-blocks): lane r + 16 h
 // decodes row r, sub-blocks 4h .. 4h + 3, with word-parallel unpacking of the
 // 6-bit fields; writes (S_j * 2^24 or S_j * 2^20, -Mn_j) pairs to cw.
@@ -249,8 +283,8 @@ template <int kFmt, int kNT>
 __global__ void __launch_bounds__(kThreadsR, kNT == 1 ? 3 : 2)
 qmm_gemv_rows_kernel(const __grid_constant__ CUtensorMap wmap, const RowsParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
-    constexpr int kCB = kFmt == 8 ? kQ8GroupBytes : kQ4Bytes;
-    constexpr int kPitch = 2 * kCB;               // stage row: two chunks
+    constexpr int kCB = rows_chunk_bytes(kFmt);            // a chunk's advance in a packed row
+    constexpr int kPitch = 2 * rows_half_pitch(kFmt);      // stage row: two chunks (FP8: + 32 bytes)
     constexpr int kStage = kRowsR * kPitch;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nch = p.nchunks, dpp = p.dpp, win = p.win, M = p.M;
@@ -365,6 +399,8 @@ qmm_gemv_rows_kernel(const __grid_constant__ CUtensorMap wmap, const RowsParams 
                     float sum = 0.f;
 #pragma unroll
                     for (int w = 0; w < kWarpsR; ++w) sum += yb[(w * kRowsR + r) * M + m];
+                    if constexpr (kFmt == kFp8)  // the row scale follows the row's codes
+                        sum *= __ldg(reinterpret_cast<const float *>(p.W + (int64_t)(row0 + r) * p.row_bytes + p.K));
                     p.Y[(int64_t)m * p.N + row0 + r] = sum;
                 }
             }
@@ -402,7 +438,16 @@ qmm_gemv_rows_kernel(const __grid_constant__ CUtensorMap wmap, const RowsParams 
                         const uint8_t *r0 = cbase + g * kPitch;
                         const uint8_t *r1 = cbase + (g + 8) * kPitch;
                         const __half *xb = xrow + li * kGroup;
-                        if constexpr (kFmt == 8) {
+                        if constexpr (kFmt == kFp8) {
+                            r8_block<0, kNT>(r0, r1, xb, xstride, t, v0, v1, acc);
+                            r8_block<1, kNT>(r0, r1, xb, xstride, t, v0, v1, acc);
+                            r8_block<2, kNT>(r0, r1, xb, xstride, t, v0, v1, acc);
+                            r8_block<3, kNT>(r0, r1, xb, xstride, t, v0, v1, acc);
+                            r8_block<4, kNT>(r0, r1, xb, xstride, t, v0, v1, acc);
+                            r8_block<5, kNT>(r0, r1, xb, xstride, t, v0, v1, acc);
+                            r8_block<6, kNT>(r0, r1, xb, xstride, t, v0, v1, acc);
+                            r8_block<7, kNT>(r0, r1, xb, xstride, t, v0, v1, acc);
+                        } else if constexpr (kFmt == 8) {
                             rq8_block<0, kNT>(r0, r1, xb, xstride, t, v0, v1, acc);
                             rq8_block<1, kNT>(r0, r1, xb, xstride, t, v0, v1, acc);
                             rq8_block<2, kNT>(r0, r1, xb, xstride, t, v0, v1, acc);
@@ -492,7 +537,7 @@ struct RowsPlan {
 // CTAs on ties.
 template <int kFmt, int kNT>
 static RowsPlan rows_plan_compute(int dev, int M, int K) {
-    constexpr int kCB = kFmt == 8 ? kQ8GroupBytes : kQ4Bytes;
+    constexpr int kCB = rows_half_pitch(kFmt);
     const int nch = K / kGroup;
     int win = nch;
     if (M * nch > kRowsXChunkBudget) {
@@ -532,7 +577,8 @@ static RowsPlan rows_plan(int dev, int M, int K) {
 
 template <int kFmt, int kNT>
 static cudaError_t launch_rows_t(const void *W, RowsParams &p, int sms, cudaStream_t stream) {
-    constexpr int kCB = kFmt == 8 ? kQ8GroupBytes : kQ4Bytes;
+    constexpr int kCB = rows_chunk_bytes(kFmt);
+    constexpr int kHalfPitch = rows_half_pitch(kFmt);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -546,11 +592,14 @@ static cudaError_t launch_rows_t(const void *W, RowsParams &p, int sms, cudaStre
     p.win = pl.win;
     const long cap = (long)sms * pl.occ;
     const int grid = (int)(p.ntiles < cap ? p.ntiles : cap);
-    // the matrix as 8-byte elements; a box is 16 rows x 2 chunks
-    const int64_t row_bytes = (int64_t)p.nchunks * kCB;
+    // the matrix as 8-byte elements; a box is 16 rows x 2 chunks (FP8: + 32
+    // bytes; past a row's end the box is zero-filled)
+    const int64_t row_bytes = kFmt == kFp8 ? (int64_t)p.K + kFp8RowPad : (int64_t)p.nchunks * kCB;
+    p.W = static_cast<const uint8_t *>(W);
+    p.row_bytes = row_bytes;
     CUtensorMap wmap;
     e = encode_tmap_2d(&wmap, W, CU_TENSOR_MAP_DATA_TYPE_UINT64, (uint64_t)(row_bytes / 8),
-                       (uint64_t)p.N, (uint64_t)row_bytes, (uint32_t)(2 * kCB / 8), kRowsR);
+                       (uint64_t)p.N, (uint64_t)row_bytes, (uint32_t)(2 * kHalfPitch / 8), kRowsR);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
@@ -573,6 +622,8 @@ cudaError_t launch_gemv_rows(int fmt, const void *W, const uint16_t *X, float *Y
     p.M = M;
     p.N = N;
     p.K = K;
+    if (fmt == kFp8)
+        return M > 8 ? launch_rows_t<kFp8, 2>(W, p, sms, stream) : launch_rows_t<kFp8, 1>(W, p, sms, stream);
     if (M > 8)
         return fmt == 8 ? launch_rows_t<8, 2>(W, p, sms, stream) : launch_rows_t<4, 2>(W, p, sms, stream);
     return fmt == 8 ? launch_rows_t<8, 1>(W, p, sms, stream) : launch_rows_t<4, 1>(W, p, sms, stream);

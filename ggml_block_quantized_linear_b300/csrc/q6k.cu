@@ -226,7 +226,8 @@ __global__ void __launch_bounds__(kQ6Threads) qmm_embedding_kernel(const uint8_t
                                                                    int64_t V, int64_t D) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t groups = D / 256;
-    constexpr int kGB = kFmt == 8 ? kQ8GroupBytes : kFmt == 4 ? kQ4Bytes : kQ6Bytes;
+    constexpr int kGB = kFmt == 8 ? kQ8GroupBytes : kFmt == 4 ? kQ4Bytes : kFmt == 6 ? kQ6Bytes : 256;
+    const int64_t row_bytes = kFmt == kFp8 ? D + kFp8RowPad : groups * kGB;
     for (int64_t u = (int64_t)blockIdx.x * (kQ6Threads / 32) + warp; u < T * groups;
          u += (int64_t)gridDim.x * (kQ6Threads / 32)) {
         const int64_t t = u / groups, g = u - t * groups;
@@ -239,8 +240,20 @@ __global__ void __launch_bounds__(kQ6Threads) qmm_embedding_kernel(const uint8_t
             for (int e = 0; e < 8; ++e) v[e] = 0.f;
             k0 = 8 * lane;
         } else {
-            const uint8_t *grp = table + id * groups * kGB + g * kGB;
-            if constexpr (kFmt == 8) {
+            const uint8_t *grp = table + id * row_bytes + g * kGB;
+            if constexpr (kFmt == kFp8) {
+                // codes 8 lane .. 8 lane + 7 of the group, times the row scale
+                const float sc = __ldg(reinterpret_cast<const float *>(table + id * row_bytes + D));
+                const uint2 q = __ldg(reinterpret_cast<const uint2 *>(grp + 8 * lane));
+                const uint32_t w[2] = {q.x, q.y};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const uint32_t h2 = e4m3x2_to_h2(w[e >> 1] >> (16 * (e & 1)));
+                    v[2 * e] = __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))) * sc;
+                    v[2 * e + 1] = __half2float(__ushort_as_half((unsigned short)(h2 >> 16))) * sc;
+                }
+                k0 = 8 * lane;
+            } else if constexpr (kFmt == 8) {
                 // block lane / 4, codes 8 (lane % 4) .. + 7
                 const uint8_t *blk = grp + kQ8Bytes * (lane >> 2);
                 const float d = __half2float(__ushort_as_half(__ldg(reinterpret_cast<const uint16_t *>(blk))));
@@ -357,6 +370,7 @@ cudaError_t launch_embedding(int fmt, const void *table, const int64_t *ids, voi
                              int64_t V, int64_t D, int sms, cudaStream_t stream) {
     if (fmt == 8) return launch_embedding_t<8>(table, ids, out, bf16, T, V, D, sms, stream);
     if (fmt == 4) return launch_embedding_t<4>(table, ids, out, bf16, T, V, D, sms, stream);
+    if (fmt == kFp8) return launch_embedding_t<kFp8>(table, ids, out, bf16, T, V, D, sms, stream);
     return launch_embedding_t<6>(table, ids, out, bf16, T, V, D, sms, stream);
 }
 

@@ -28,6 +28,10 @@ cudaError_t launch_q6k_matmul(const void *W, const uint16_t *X, float *Y, int M,
                               cudaStream_t stream);
 cudaError_t launch_embedding(int fmt, const void *table, const int64_t *ids, void *out, int bf16, int64_t T,
                              int64_t V, int64_t D, int sms, cudaStream_t stream);
+cudaError_t launch_fp8_quantize(int src_f32, const void *src, void *dst, int64_t rows, int64_t K, int sms,
+                                cudaStream_t stream);
+cudaError_t launch_fp8_dequantize(const void *src, float *dst, int64_t rows, int64_t K, int sms,
+                                  cudaStream_t stream);
 
 constexpr int kMaxDecodeM = 16;
 // Largest dimension accepted (keeps every 32-bit index in the kernels exact).
@@ -72,7 +76,9 @@ static bool use_rows_kernel(int M, int N, int K, int sms) {
 }
 
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-static bool known_fmt(qmm_format f) { return f == QMM_Q8_0 || f == QMM_Q4_K || f == QMM_Q6_K; }
+static bool known_fmt(qmm_format f) {
+    return f == QMM_Q8_0 || f == QMM_Q4_K || f == QMM_Q6_K || f == QMM_FP8_E4M3;
+}
 static int64_t block_weights(qmm_format f) { return f == QMM_Q8_0 ? kQ8Weights : 256; }
 static int64_t block_bytes(qmm_format f) { return f == QMM_Q8_0 ? kQ8Bytes : f == QMM_Q4_K ? kQ4Bytes : 210; }
 
@@ -106,10 +112,12 @@ extern "C" {
 
 size_t qmm_packed_bytes(qmm_format fmt, int64_t rows, int64_t cols) {
     if (!known_fmt(fmt) || rows < 0 || cols < 0) return 0;
+    if (rows > kMaxDim || cols > kMaxDim) return 0;
+    if (fmt == QMM_FP8_E4M3)  // K codes, the fp32 row scale, 12 zero bytes
+        return cols % kGroup == 0 && cols > 0 ? (size_t)(rows * (cols + kFp8RowPad)) : 0;
     const int64_t qk = block_weights(fmt);
     const int64_t bb = block_bytes(fmt);
     if (cols % qk != 0) return 0;
-    if (rows > kMaxDim || cols > kMaxDim) return 0;
     return (size_t)(rows * (cols / qk) * bb);
 }
 
@@ -123,6 +131,9 @@ qmm_status qmm_quantize(qmm_format fmt, qmm_src_dtype st, const void *src, void 
     if (!aligned16(src) || !aligned16(dst_packed)) return QMM_ERR_ALIGNMENT;
     if (fmt == QMM_Q6_K)
         return from_cuda(launch_q6k_quantize(st == QMM_SRC_F32, src, dst_packed, rows * cols, sm_count(),
+                                             reinterpret_cast<cudaStream_t>(stream)));
+    if (fmt == QMM_FP8_E4M3)
+        return from_cuda(launch_fp8_quantize(st == QMM_SRC_F32, src, dst_packed, rows, cols, sm_count(),
                                              reinterpret_cast<cudaStream_t>(stream)));
     return from_cuda(launch_quantize((int)fmt, st == QMM_SRC_F32, src, dst_packed, rows * cols,
                                      sm_count(), reinterpret_cast<cudaStream_t>(stream)));
@@ -138,6 +149,9 @@ qmm_status qmm_dequantize(qmm_format fmt, const void *src_packed, float *dst, in
     if (!aligned16(src_packed) || !aligned16(dst)) return QMM_ERR_ALIGNMENT;
     if (fmt == QMM_Q6_K)
         return from_cuda(launch_q6k_dequantize(src_packed, dst, rows * cols, sm_count(),
+                                               reinterpret_cast<cudaStream_t>(stream)));
+    if (fmt == QMM_FP8_E4M3)
+        return from_cuda(launch_fp8_dequantize(src_packed, dst, rows, cols, sm_count(),
                                                reinterpret_cast<cudaStream_t>(stream)));
     return from_cuda(launch_dequantize((int)fmt, src_packed, dst, rows * cols, sm_count(),
                                        reinterpret_cast<cudaStream_t>(stream)));
@@ -164,7 +178,8 @@ qmm_status qmm_matmul(qmm_format fmt, const void *W_packed, const uint16_t *X_bf
     if (fmt == QMM_Q6_K)
         return from_cuda(launch_q6k_matmul(W_packed, X_bf16, Y, (int)M, (int)N, (int)K, sm_count(), s));
     if (M <= kMaxDecodeM) {
-        if (use_rows_kernel((int)M, (int)N, (int)K, sm_count()))
+        // FP8 has only the row-tile decode kernel
+        if (fmt == QMM_FP8_E4M3 || use_rows_kernel((int)M, (int)N, (int)K, sm_count()))
             return from_cuda(launch_gemv_rows((int)fmt, W_packed, X_bf16, Y, (int)M, (int)N, (int)K,
                                               sm_count(), s));
         return from_cuda(launch_gemv((int)fmt, W_packed, X_bf16, Y, (int)M, (int)N, (int)K,

@@ -6,4 +6,5 @@
 #include "gemv_rows.cu"
 #include "gemm.cu"
 #include "q6k.cu"
+#include "fp8.cu"
 #include "static_scratch.cu"

@@ -13,8 +13,9 @@
  *   qmm_matmul      Y[M x N] = X[M x K] * W^[N x K]^T   (fp32 out, bf16 X)
  *   qmm_embedding   rows ids[] of a packed [V x D] table -> fp32 / bf16
  *
- * Formats: Q8_0 and Q4_K (the CUDA targets of `--isq 8` / `--isq 4`) for
- * the linear layers, and Q6_K (`--isq 6`), which the page's section
+ * Formats: Q8_0 and Q4_K (the CUDA targets of `--isq 8` / `--isq 4`) and
+ * FP8 E4M3 with row scales (W8A16) for the linear layers, and Q6_K
+ * (`--isq 6`), which the page's section
  * "Sensitive tensor precision" gives to the token embeddings and the output
  * head of a Q4K model (Q8_0 for Q5K / Q6K / Q8_0 models; see
  * qmm_embedding_format).
@@ -46,10 +47,17 @@
  *         byte 64h + 32(s & 1) + l (high nibble when s >= 2) and its high
  *         bits in bits 2s, 2s+1 of qh byte 32h + l.  Superblocks are only
  *         2-byte aligned inside a packed row.
+ *   FP8_E4M3  (W8A16; the page's section "FP8": E4M3 produced by ISQ,
+ *         symmetric weights with channel scales): one fp32 scale per row,
+ *         s = max|x| / 448; code = E4M3(x / s), round to nearest even,
+ *         saturating at +-448 (E4M3: 1 sign, 4 exponent bits with bias 7, 3
+ *         fraction bits, no infinities).  Dequantized weight: E4M3 value * s.
+ *         A packed row is the K codes, s (fp32), 12 zero bytes: K + 16.
  *
  * A packed matrix is row-major in blocks: row n holds cols/32 Q8_0 blocks
- * (cols/32*34 bytes), cols/256 Q4_K superblocks (cols/256*144 bytes) or
- * cols/256 Q6_K superblocks (cols/256*210 bytes), rows back to back.
+ * (cols/32*34 bytes), cols/256 Q4_K superblocks (cols/256*144 bytes),
+ * cols/256 Q6_K superblocks (cols/256*210 bytes) or the FP8 codes and row
+ * scale (cols + 16 bytes), rows back to back.
  *
  * Conventions for every call:
  *  - Pointers are DEVICE pointers owned by the caller.  The library allocates
@@ -92,7 +100,7 @@ typedef struct CUstream_st *qmm_stream_t;
 /* Block formats; the values mirror the ISQ shorthands `--isq 8` / `--isq 4`
  * / `--isq 6` (mistral.rs "Quantization types", section "Numeric
  * shorthands"). */
-typedef enum { QMM_Q8_0 = 8, QMM_Q4_K = 4, QMM_Q6_K = 6 } qmm_format;
+typedef enum { QMM_Q8_0 = 8, QMM_Q4_K = 4, QMM_Q6_K = 6, QMM_FP8_E4M3 = 80 } qmm_format;
 
 /* Element type of an embedding lookup's output. */
 typedef enum { QMM_OUT_F32 = 0, QMM_OUT_BF16 = 1 } qmm_out_dtype;
@@ -167,6 +175,10 @@ QMM_API size_t qmm_matmul_workspace_bytes(qmm_format fmt, int64_t M, int64_t N, 
  * when the tiles fill the GPU (each tile's partial sums added in a fixed
  * order), otherwise split-K over a thread-block cluster reduced in
  * distributed shared memory in a fixed order; both are deterministic.
+ * FP8 runs the row-tile decode kernel for every M <= 16 (codes converted
+ * exactly to binary16 in the MMA fragments, the row scale applied to the
+ * finished sums) and the tiled kernel above that (each weight tile converted
+ * to binary16 inside the GEMM, the row scale applied in the epilogue).
  * Q6_K (output heads) runs a CUDA-core kernel for every M: a warp per
  * weight row, exact integer codes times the activations, the sub-block
  * scale applied per superblock, fp32 sums.  For Q8_0 / Q4_K, larger M runs

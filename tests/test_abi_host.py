@@ -134,6 +134,13 @@ def test_q6_k_sizes_and_policy(lib):
     assert q.qmm_embedding_format(7) == 0
 
 
+def test_fp8_sizes(lib):
+    assert q.qmm_packed_bytes(q.QMM_FP8_E4M3, 4096, 4096) == 4096 * (4096 + 16)
+    assert q.qmm_packed_bytes(q.QMM_FP8_E4M3, 3, 256) == 3 * 272
+    assert q.qmm_packed_bytes(q.QMM_FP8_E4M3, 1, 288) == 0
+    assert q.qmm_matmul_workspace_bytes(q.QMM_FP8_E4M3, 512, 4096, 4096) == 512 * 4096 * 2
+
+
 def test_embedding_argument_errors(lib):
     L = lib
     ids8 = ctypes.c_void_p(0x1000)

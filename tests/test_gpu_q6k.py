@@ -102,7 +102,7 @@ def test_output_head_of_a_q4_k_model():
     check_matmul(y[:, ridx], Y, A, "output head")
 
 
-@pytest.mark.parametrize("fmt", [q.QMM_Q8_0, q.QMM_Q4_K, q.QMM_Q6_K])
+@pytest.mark.parametrize("fmt", [q.QMM_Q8_0, q.QMM_Q4_K, q.QMM_Q6_K, q.QMM_FP8_E4M3])
 @pytest.mark.parametrize("V,D", [(1000, 4096), (37, 768)])
 def test_embedding_lookup(fmt, V, D):
     w = inputs.weights(V, D, 68)
