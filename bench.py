@@ -17,6 +17,8 @@ each stage captured as a CUDA graph and replayed back to back:
   gemm_mid  tiled matmul at mid-size batches, M = 32 and 128, the 4 decode
             shapes x 2 formats
   gemm      prefill GEMM, M = 512 and 2048, 3 shapes x 2 formats
+  fp8       FP8 E4M3 (row scales, W8A16) ISQ of the four decode weights, the
+            M = 1 decode sweep over them and prefill at M = 2048
   head      output head of the 8B-shape decoder at M = 1 (128256 x 4096) in
             the types the pages' sensitive-tensor policy gives it: Q6_K (Q4_K
             model) and Q8_0 (Q8_0 model)
@@ -77,6 +79,8 @@ FAMILY_SOURCES = {
     "quantize": ("common.cuh", "quantize.cu"),
     "dequantize": ("common.cuh", "quantize.cu"),
     "gemv": ("common.cuh", "gemv.cu", "gemv_rows.cu"),
+    "gemv_fp8": ("common.cuh", "gemv_rows.cu"),
+    "quantize_fp8": ("common.cuh", "fp8.cu"),
     "gemm": ("common.cuh", "gemm.cu"),
     "gemm_mid": ("common.cuh", "gemm.cu"),
     "head": ("common.cuh", "q6k.cu", "gemv_rows.cu"),
@@ -201,6 +205,11 @@ class Workload:
             self.y[m] = {f: [torch.empty((m, n), dtype=torch.float32, device=device)
                              for (n, k) in inputs.DECODE_SHAPES] for f in self.fmts}
         self.gemm_ok = self._probe_gemm()
+        # FP8 E4M3 weights with row scales (W8A16) of the same decode weights
+        self.fp8 = [q.qmm_quantize(q.QMM_FP8_E4M3, w) for w in self.w_bf16]
+        self.fp8_isq_out = [torch.empty_like(p) for p in self.fp8]
+        self.fp8_y = {m: [torch.empty((m, n), dtype=torch.float32, device=device)
+                          for (n, k) in inputs.DECODE_SHAPES] for m in (1, 2048)}
         # output head / embedding table of the 8B-shape decoder, in the types
         # of the sensitive-tensor policy (Q4_K model -> Q6_K, Q8_0 -> Q8_0)
         vocab, hidden = inputs.VOCAB, 4096
@@ -279,6 +288,28 @@ class Workload:
                             q.qmm_matmul(f, p, x, n, out=y)
                 S.append(("gemm_m%d" % m, gemm_mid, 16, sum(nw * bw[f] for f in self.fmts),
                           2 * 2.0 * m * nw, "gemm_mid", 2 * nw))
+
+        f8 = q.QMM_FP8_E4M3
+        f8bytes = sum(p.numel() for p in self.fp8)
+
+        def fp8_isq():
+            for w, o in zip(self.w_bf16, self.fp8_isq_out):
+                q.qmm_quantize(f8, w, out=o)
+        S.append(("isq_fp8", fp8_isq, 4, 2 * nw + f8bytes, 0.0, "quantize_fp8", nw))
+
+        def fp8_gemv():
+            for (n, k), p, x, y in zip(shapes, self.fp8, self.x[1], self.fp8_y[1]):
+                q.qmm_matmul(f8, p, x, n, out=y)
+        S.append(("gemv_fp8_m1", fp8_gemv, 4, f8bytes, 2.0 * nw, "gemv_fp8", nw))
+        if self.gemm_ok:
+            pshapes = inputs.PREFILL_SHAPES
+
+            def fp8_gemm():
+                for si, (n, k) in enumerate(shapes):
+                    if (n, k) in pshapes:
+                        q.qmm_matmul(f8, self.fp8[si], self.x[2048][si], n, out=self.fp8_y[2048][si])
+            S.append(("gemm_fp8_m2048", fp8_gemm, 6, 0, 2 * 2048.0 * sum(n * k for n, k in pshapes),
+                      "gemm", sum(n * k for n, k in pshapes)))
 
         vocab, hidden = inputs.VOCAB, 4096
         hbw = {f: q.BLOCK[f][1] / q.BLOCK[f][0] for f in self.head_fmts}
@@ -361,7 +392,8 @@ def time_graphs(torch, graphs, steps, warmup, dev):
 def parity_check(wl):
     """Sampled parity of the benchmarked kernels against the CPU oracle: the
     decode-shaped linears (packed bytes of 64 rows; outputs of 4 rows at
-    M = 1, 16, 32 and 2048), the output head (bytes and M = 1 outputs of 4
+    M = 1, 16, 32 and 2048; FP8 bytes of 64 rows and outputs of 3 rows at
+    M = 1 and 2048), the output head (bytes and M = 1 outputs of 4
     rows) and 4 embedding rows in each head format, and the last layer of
     the model (packed bytes and M = 1 outputs of 6 rows of each of its 7
     linears, both formats)."""
@@ -375,6 +407,18 @@ def parity_check(wl):
             want = oracle.quantize(f, inputs.bf16_bits(wl.w_bf16[si][:64].cpu()))
             if not np.array_equal(packed[:64], want):
                 return "FAIL: packed bytes differ (fmt %d shape %d)" % (f, si)
+            # FP8: bytes of the same rows, outputs at M = 1 and 2048
+            f8 = q.QMM_FP8_E4M3
+            want8 = oracle.quantize(f8, inputs.bf16_bits(wl.w_bf16[si][:64].cpu()))
+            if not np.array_equal(wl.fp8[si][:64].cpu().numpy(), want8):
+                return "FAIL: FP8 packed bytes differ (shape %d)" % si
+            if f == wl.fmts[0]:
+                for m in (1,) + ((2048,) if wl.gemm_ok and (n, k) in inputs.PREFILL_SHAPES else ()):
+                    ns = np.array([0, 1, 63], dtype=np.int64)
+                    xb = inputs.bf16_bits(wl.x[m][si])
+                    Y, A = oracle.matmul(f8, want8[ns], xb, ns.size, k)
+                    y = wl.fp8_y[m][si][:, ns].double().cpu().numpy()
+                    worst = max(worst, float((np.abs(y - Y) / (1e-3 * A + 1e-6)).max()))
             for m in (1, 16) + ((32,) if wl.gemm_ok else ()) + (
                     (2048,) if wl.gemm_ok and (n, k) in inputs.PREFILL_SHAPES else ()):
                 ns = np.array([0, 1, n // 2, n - 1], dtype=np.int64)
@@ -570,7 +614,8 @@ def run_reference(args):
 def workload_config():
     return {"workload": "decode-shaped Q8_0/Q4_K linears (N x K = 4096x4096, 1024x4096, "
                         "14336x4096, 4096x14336), GEMV at M=1 (headline) plus M=4/16, ISQ, "
-                        "dequant, mid-batch matmul M=32/128, prefill GEMM M=512/2048, a "
+                        "dequant, mid-batch matmul M=32/128, prefill GEMM M=512/2048, FP8 "
+                        "E4M3 W8A16 ISQ + M=1 sweep + M=2048 prefill, a "
                         "128256x4096 output head (Q6_K / Q8_0, M=1), a 2048-token embedding "
                         "lookup and a 32-layer 8B-shape model (ISQ + 224-GEMV decode step) in "
                         "each step",
@@ -681,7 +726,7 @@ def main(argv=None):
         key = "model_decode_" + nm
         if key in rows:
             rows[key]["weight_GBps"] = rows[key].pop("GBps")
-    for key in ("gemm_m32", "gemm_m128", "head_m1"):
+    for key in ("gemm_m32", "gemm_m128", "head_m1", "gemv_fp8_m1"):
         if key in rows:
             rows[key]["weight_GBps"] = rows[key].pop("GBps")
 
