@@ -61,6 +61,24 @@ def test_decode_row_tiles_full(fmt, n, k, m):
     check_matmul(run(fmt, packed, xb, n), Y, A, "fmt=%d n=%d k=%d m=%d" % (fmt, n, k, m))
 
 
+# More decode shapes checked in full and repeated bit for bit: ragged N, odd
+# chunk counts (a half-filled last 2-chunk copy), fewer tiles than resident
+# CTAs and a short last round of tiles, both decode kernels.
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("n,k,m", [(4000, 4096, 1), (4000, 4096, 4), (1100, 1280, 2), (3000, 2304, 4),
+                                   (2500, 768, 1), (5000, 4096, 3), (1024, 4096, 1), (1024, 4096, 2),
+                                   (2368, 3328, 8), (2600, 4096, 16), (7000, 512, 1), (300, 14336, 1)])
+def test_decode_more_shapes_full(fmt, n, k, m):
+    packed, xb = problem(fmt, n, k, m, 3000 + n + k + m)
+    Y, A = oracle.matmul(fmt, packed, xb, n, k)
+    w, x = to_dev_u8(packed), bf16_from_bits(xb)
+    y = q.qmm_matmul(fmt, w, x, n)
+    check_matmul(y, Y, A, "fmt=%d n=%d k=%d m=%d" % (fmt, n, k, m))
+    for _ in range(2):
+        assert torch.equal(q.qmm_matmul(fmt, w, x, n), y)
+    assert q.qmm_device_error_take() == 0
+
+
 @pytest.mark.parametrize("fmt", FMTS)
 def test_tiny_linear_config(fmt):
     # fp32 W 256 x 512 quantized, X bf16 1 x 512

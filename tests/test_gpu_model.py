@@ -101,11 +101,12 @@ def test_chained_decode_eager_and_graph(fmt, m):
 
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("m", [1, 16])
-def test_next_call_overwrites_previous_input(fmt, m):
+@pytest.mark.parametrize("n1", [4096, 1024])
+def test_next_call_overwrites_previous_input(fmt, m, n1):
     # call A reads X from `buf`; call B, next in the stream, writes its output
     # into the same bytes.  B may start before A has finished, but it must not
     # write before A is complete.
-    n1, k1 = 4096, 4096
+    k1 = 4096  # n1 = 1024: the cluster split-K kernel reads X
     n2, k2 = 4096, 4096
     w1 = inputs.weights(n1, k1, 801, device=DEV)
     w2 = inputs.weights(n2, k2, 802, device=DEV)
@@ -126,3 +127,4 @@ def test_next_call_overwrites_previous_input(fmt, m):
         assert torch.equal(ya, ya_ref)
         assert torch.equal(yb_view, yb_ref)
     assert q.qmm_device_error_take() == 0
+
