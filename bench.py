@@ -738,9 +738,12 @@ def main(argv=None):
             fl = sum(s[4] for s in sel)
             peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
             ach = fl / t / 1e12
+            sus = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
             return {"bound": "tensor", "achieved": round(ach, 1), "peak": peak, "unit": "TFLOP/s",
                     "frac": round(ach / peak, 4), "traffic": None,
                     "peak_source": peak_kind + " bf16 burst (f16 same nominal rate)",
+                    # the GEMM stages run back to back for milliseconds, under the power cap
+                    "peak_sustained": sus, "frac_sustained": round(ach / sus, 4),
                     "launches": launches}
         nb = sum(s[3] for s in sel)
         nw = sum(s[6] for s in sel)

@@ -15,13 +15,18 @@
 // into the caller's workspace.
 //
 // Tile: 128 weight rows (the MMA's M side, "swap AB") x BN tokens (MMA N:
-// 32, 64, 128 or 256, the smallest that holds M up to 128; above 256 tokens
-// 256 or 512) x 64 K per stage; persistent CTAs (one per SM) walk the work
-// units, and two fp32 accumulators of BN TMEM columns alternate between
-// consecutive units.  A 512-token unit is two 256-token MMA tiles that share
-// every dequantized weight stage, with one accumulator of all 512 TMEM
-// columns; its activation ring holds 256-token sub-stages, two per K step.
-// The planner takes it where it needs fewer waves of units.
+// 32, 64, 128 or 256, the smallest that holds M up to 128; above that 256)
+// x 64 K per stage; persistent CTAs (one per SM) walk the work units.  The
+// dequantized weights go to tensor memory, not shared memory: each
+// dequantizing thread owns one weight row (one TMEM lane) and a 16-wide
+// slice of K, converts its 16 weights in registers and writes them with one
+// tcgen05.st; the MMA reads A from TMEM and only the activations from shared
+// memory (tcgen05.mma with A in TMEM).  That takes the A stores, their bank
+// conflicts and the MMA's A reads off the shared-memory port, which carried
+// every operand before.  TMEM holds the A stages (32 columns each) and the
+// fp32 accumulators: two of BN columns alternating between units for BN up
+// to 128, one of 256 columns for 256-token tiles (whose epilogue then does
+// not overlap the next unit's main loop).
 // When the output tiles are fewer than the SMs, K is split into parts (a
 // unit is one part of one tile).  256-token tiles: at most two parts, both
 // added onto a Y zeroed by the conversion launch (two additions onto zero
@@ -31,22 +36,24 @@
 // order and writes Y.  Both are deterministic and nothing ever waits for
 // another CTA.
 //   warp 0       TMA producer of the binary16 activation tiles (128B-swizzled
-//                boxes, each CTA loading its own)
+//                boxes)
 //   warp 1       TMEM allocator and single-thread MMA issuer
-//   warps 2-17   dequantize packed weights into 128B-swizzled K-major f16
-//                A stages
-//   warps 18-21  epilogue: read an accumulator back (tcgen05.ld) and store
-//                Y while the next tile's main loop runs
+//   warps 2-17   dequantize packed weights into the TMEM A stages (warp w
+//                writes TMEM lanes 32 (w mod 4) .. + 31, K slice (w - 2) / 4)
+//   warps 18-21  epilogue: read an accumulator back (tcgen05.ld) and store Y
 //   warp 22      TMA producer of the packed weights (separate from warp 0 so
 //                that the dequantizing warps never wait behind activation
 //                stages)
 // Every wait is bounded (common.cuh); TMEM is always released.
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace qmm {
 
 constexpr int kGemmBM = 128;        // weight rows per CTA (MMA M)
-constexpr int kGemmBK = 64;         // K per stage (one 128-byte swizzle atom of f16)
+constexpr int kGemmBK = 128;        // K per stage: two 128-byte swizzle atoms of f16
+constexpr int kGemmAtomK = 64;      // K of one 128B-swizzled atom (one TMA box, one descriptor base)
 #ifndef QMM_GEMM_DEQ_WARPS
 #define QMM_GEMM_DEQ_WARPS 16
 #endif
@@ -56,25 +63,25 @@ constexpr int kGemmEpiWarps = 4;
 // epilogue warps and the packed-weight producer
 constexpr int kGemmWarpPackedTma = 2 + kGemmDeqWarps + kGemmEpiWarps;
 constexpr int kGemmThreads = (kGemmWarpPackedTma + 1) * 32;
-#ifndef QMM_GEMM_STAGES_B_Q4
-#define QMM_GEMM_STAGES_B_Q4 4
-#endif
-#ifndef QMM_GEMM_STAGES_A_Q4
-#define QMM_GEMM_STAGES_A_Q4 3
-#endif
 constexpr int kGemmStagesP = 2;     // packed weight groups
-// two BN-column fp32 accumulators (a power of two, at least 32 columns), or
-// one of 512 columns for 512-token units
-__host__ __device__ constexpr int gemm_tmem_cols(int bn) { return bn == 512 ? 512 : 2 * bn < 32 ? 32 : 2 * bn; }
-__host__ __device__ constexpr int gemm_sub(int bn) { return bn == 512 ? 2 : 1; }  // MMA tiles per unit
-// Q4_K (S_j, Mn_j) table: 16 floats per weight row, padded to 18 so that the
-// rows a warp reads together (2 apart) fall in different banks
-constexpr int kGemmCoefStride = 18;
-static_assert((kGemmBM / (4 * kGemmDeqWarps)) % 2 == 0, "dequantization passes come in even / odd row pairs");
-
-// activation stages (min(BN, 256) x 128 bytes each) and dequantized-weight stages (16 KB each)
-__host__ __device__ constexpr int gemm_stages_b(int fmt) { return fmt == 4 ? QMM_GEMM_STAGES_B_Q4 : 3; }
-__host__ __device__ constexpr int gemm_stages_a(int fmt) { return fmt == 4 ? QMM_GEMM_STAGES_A_Q4 : 3; }
+constexpr int kGemmACols = kGemmBK / 2;  // TMEM columns of one A stage (two binary16 per column)
+constexpr int kGemmStepsPerGroup = kGroup / kGemmBK;  // K steps per packed 256-weight group
+static_assert(kGemmDeqWarps == 16, "four warps per TMEM lane quarter, one per 16-wide K slice");
+// accumulators: two of BN columns (BN <= 128) or one of 256
+__host__ __device__ constexpr int gemm_nbuf(int bn) { return bn == 256 ? 1 : 2; }
+// K-step stages: an activation stage (BN x 256 bytes of shared memory) and
+// a TMEM A stage (64 columns) each, filled and released together; two for
+// 256-token tiles (shared memory and TMEM bound it), three below
+__host__ __device__ constexpr int gemm_stages(int bn) { return bn == 256 ? 2 : 3; }
+// TMEM columns allocated: accumulators then A stages, rounded up to a power of two
+__host__ __device__ constexpr int gemm_tmem_cols(int fmt, int bn) {
+    return gemm_nbuf(bn) * bn + gemm_stages(bn) * kGemmACols <= 32    ? 32
+           : gemm_nbuf(bn) * bn + gemm_stages(bn) * kGemmACols <= 64  ? 64
+           : gemm_nbuf(bn) * bn + gemm_stages(bn) * kGemmACols <= 128 ? 128
+           : gemm_nbuf(bn) * bn + gemm_stages(bn) * kGemmACols <= 256 ? 256
+                                                                          : 512;
+}
+static_assert(2 * 128 + 3 * 64 <= 512 && 256 + 2 * 64 <= 512, "accumulators and A stages fit TMEM");
 // Shared-memory pitch of a packed weight row in a stage (FP8: a 256-byte group
 // plus 16 bytes of the next, which keeps the dequantizing warps' loads on
 // distinct banks as Q8_0's 272 bytes do), and a group's advance in a row.
@@ -82,20 +89,16 @@ __host__ __device__ constexpr int gemm_group_bytes(int fmt) { return fmt == 4 ? 
 __host__ __device__ constexpr int gemm_group_advance(int fmt) { return fmt == 8 ? kQ8GroupBytes : fmt == 4 ? kQ4Bytes : 256; }
 
 struct GemmLayout {
-    int b, a, p, coef, bars, total;  // offsets from the 1024-aligned base
+    int b, p, bars, total;  // offsets from the 1024-aligned base
 };
 
 __host__ __device__ inline GemmLayout gemm_layout(int fmt, int bn) {
     GemmLayout L;
     int off = 0;
     L.b = off;
-    off += gemm_stages_b(fmt) * (bn / gemm_sub(bn)) * kGemmBK * 2;
-    L.a = off;
-    off += gemm_stages_a(fmt) * kGemmBM * kGemmBK * 2;
+    off += gemm_stages(bn) * bn * kGemmBK * 2;
     L.p = off;
     off += kGemmStagesP * kGemmBM * gemm_group_bytes(fmt);
-    L.coef = off;
-    off += fmt == 4 ? kGemmBM * kGemmCoefStride * 4 : 0;
     off = (off + 15) & ~15;
     L.bars = off;
     off += 64 * 8;  // barriers, TMEM address slot, last-part flag
@@ -132,6 +135,33 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint6
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16: A's 128 rows are the TMEM
+// lanes, two binary16 K values per 32-bit column (16 K = 8 columns).
+__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// 8 consecutive 32-bit columns of this thread's TMEM lane, and the wait
+// for this thread's TMEM stores.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
+                 "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 // Arrive (once) on an mbarrier when all previously issued tcgen05 ops of
 // this thread have completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -204,67 +234,94 @@ __global__ void __launch_bounds__(256) qmm_x_to_f16_kernel(const uint16_t *__res
 }
 
 // --------------------------------------------------------- dequantization
-// Byte offset of element (row r, k) in a 128B-swizzled K-major f16 tile.
-__device__ __forceinline__ uint32_t sw128_chunk_off(int r, int chunk) {
-    return (uint32_t)(r * 128 + ((chunk ^ (r & 7)) << 4));
-}
+// Each function turns 16 weights of one packed row (the row's K slice
+// 16 kq .. 16 kq + 15 of 64-wide K step kJ of a 256-weight group) into 8
+// binary16 pairs, lower K in the low half.
 
-// Q8_0: 8 weights (k = 8c .. 8c+7 of k-step j) of packed row `prow`.
-__device__ __forceinline__ uint4 deq8_q8_0(const uint8_t *prow, int j, int c) {
-    const int b = 2 * j + (c >> 2);                 // block inside the 256-weight group
-    const int off = kQ8Bytes * b + 2 + 8 * (c & 3);  // first code byte (2-byte aligned)
-    const uint32_t *w = reinterpret_cast<const uint32_t *>(prow + (off & ~3));
-    const uint32_t sh = (uint32_t)(off & 3) * 8u;    // 0 or 16
-    const uint32_t w0 = __funnelshift_r(w[0], w[1], sh);
-    const uint32_t w1 = __funnelshift_r(w[1], w[2], sh);
-    const __half d = __ushort_as_half(*reinterpret_cast<const uint16_t *>(prow + kQ8Bytes * b));
+// Q8_0: the slice is half of block 2 kJ + kq / 2; its 16 code bytes start 2
+// bytes into the block (+16 for the second half), read as two aligned
+// 16-byte words and shifted into place; d * q is rounded once.
+template <int kJ, int kHi>
+__device__ __forceinline__ void deq16_q8_0(const uint8_t *prow, int h, uint32_t (&r)[8]) {
+    constexpr int kB = 2 * kJ + kHi;            // block inside the group
+    constexpr int kOff = kQ8Bytes * kB + 2;     // first code byte of the block
+    constexpr int kS = kOff & 15, kBase = kOff & ~15;
+    // (the last block's codes end the 272-byte row: one aligned word, kS = 0)
+    const uint4 *w = reinterpret_cast<const uint4 *>(prow + kBase + 16 * h);
+    const uint4 a = w[0], b = kS != 0 ? w[1] : make_uint4(0u, 0u, 0u, 0u);
+    const uint32_t v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t c[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        c[i] = (kS & 3) ? __funnelshift_r(v[kS / 4 + i], v[kS / 4 + i + 1], 16) : v[kS / 4 + i];
+    const __half d = __ushort_as_half(*reinterpret_cast<const uint16_t *>(prow + kQ8Bytes * kB));
     const __half2 d2 = __halves2half2(d, d);
     const __half2 bias = __floats2half2_rn(1152.0f, 1152.0f);
-    const uint32_t u0 = w0 ^ 0x80808080u, u1 = w1 ^ 0x80808080u;
-    uint32_t r[4] = {prmt(u0, 0x64646464u, 0x4140u), prmt(u0, 0x64646464u, 0x4342u),
-                     prmt(u1, 0x64646464u, 0x4140u), prmt(u1, 0x64646464u, 0x4342u)};
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        __half2 h = *reinterpret_cast<__half2 *>(&r[e]);
-        h = __hmul2(__hsub2(h, bias), d2);  // q exact, then one rounding of d * q
-        r[e] = *reinterpret_cast<uint32_t *>(&h);
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t u = c[i] ^ 0x80808080u;
+        uint32_t lo = prmt(u, 0x64646464u, 0x4140u), hi = prmt(u, 0x64646464u, 0x4342u);
+        __half2 hl = __hmul2(__hsub2(*reinterpret_cast<__half2 *>(&lo), bias), d2);  // q exact, then d * q
+        __half2 hh = __hmul2(__hsub2(*reinterpret_cast<__half2 *>(&hi), bias), d2);
+        r[2 * i] = *reinterpret_cast<uint32_t *>(&hl);
+        r[2 * i + 1] = *reinterpret_cast<uint32_t *>(&hh);
     }
-    return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
-// Q4_K: 8 weights (k = 8c .. 8c+7 of k-step j = sub-blocks 2j, 2j+1).
-// coefr[2 sj + {0,1}] = (S_j, Mn_j) of the row's superblock.
-__device__ __forceinline__ uint4 deq8_q4_k(const uint8_t *prow, const float *coefr, int j, int c) {
-    const int sj = 2 * j + (c >> 2);
-    const uint2 q = *reinterpret_cast<const uint2 *>(prow + 16 + 32 * j + 8 * (c & 3));
-    const int sh = (c >> 2) * 4;
-    const uint32_t n0 = (q.x >> sh) & 0x0F0F0F0Fu, n1 = (q.y >> sh) & 0x0F0F0F0Fu;
-    const float2 sm = *reinterpret_cast<const float2 *>(coefr + 2 * sj);
-    // q (exact, from 2^23 + q) and S q - Mn with one rounding, two weights
-    // per packed fp32 instruction
-    const uint64_t s2 = f2_pack(sm.x, sm.x), nm2 = f2_pack(-sm.y, -sm.y);
+// Q4_K: the slice is weights 16 (kq % 2) .. + 15 of sub-block 2 kJ + kq / 2,
+// i.e. one nibble of 16 consecutive code bytes; S q - Mn with one rounding
+// in fp32 (two weights per packed instruction), then binary16.
+__device__ __forceinline__ void deq16_q4_k(const uint8_t *prow, int j, int kq, float S, float Mn,
+                                           uint32_t (&r)[8]) {
+    const uint4 q = *reinterpret_cast<const uint4 *>(prow + 16 + 32 * j + 16 * (kq & 1));
+    const int sh = (kq >> 1) * 4;
+    const uint32_t n[4] = {(q.x >> sh) & 0x0F0F0F0Fu, (q.y >> sh) & 0x0F0F0F0Fu, (q.z >> sh) & 0x0F0F0F0Fu,
+                           (q.w >> sh) & 0x0F0F0F0Fu};
+    const uint64_t s2 = f2_pack(S, S), nm2 = f2_pack(-Mn, -Mn);
     const uint64_t k2 = f2_pack(-8388608.0f, -8388608.0f);
-    uint32_t r[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const uint32_t nw = e < 2 ? n0 : n1;
+    for (int e = 0; e < 8; ++e) {
+        const uint32_t nw = n[e >> 1];
         const int b0 = (2 * e) & 3;
         const uint64_t qq = f2_add(f2_pack(__uint_as_float(prmt(nw, 0x4B000000u, 0x7440u + b0)),
                                            __uint_as_float(prmt(nw, 0x4B000000u, 0x7440u + b0 + 1))),
                                    k2);
         float v0, v1;
         f2_unpack(f2_fma(s2, qq, nm2), v0, v1);
-        const __half2 h = __floats2half2_rn(v0, v1);
-        r[e] = *reinterpret_cast<const uint32_t *>(&h);
+        const __half2 hv = __floats2half2_rn(v0, v1);
+        r[e] = *reinterpret_cast<const uint32_t *>(&hv);
     }
-    return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
-// FP8: 8 weights (k = 8c .. 8c+7 of k-step j) converted exactly to binary16;
-// the row scale is applied to the finished sums.
-__device__ __forceinline__ uint4 deq8_fp8(const uint8_t *prow, int j, int c) {
-    const uint2 q = *reinterpret_cast<const uint2 *>(prow + 64 * j + 8 * c);
-    return make_uint4(e4m3x2_to_h2(q.x), e4m3x2_to_h2(q.x >> 16), e4m3x2_to_h2(q.y), e4m3x2_to_h2(q.y >> 16));
+// FP8: 16 codes converted exactly to binary16; the row scale is applied to
+// the finished sums.
+__device__ __forceinline__ void deq16_fp8(const uint8_t *prow, int j, int kq, uint32_t (&r)[8]) {
+    const uint4 q = *reinterpret_cast<const uint4 *>(prow + 64 * j + 16 * kq);
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        r[2 * i] = e4m3x2_to_h2(w[i]);
+        r[2 * i + 1] = e4m3x2_to_h2(w[i] >> 16);
+    }
+}
+
+// Q4_K (S_j, Mn_j) of sub-block sj from the row's superblock header (d,
+// dmin, 12 scale bytes as the words h.y, h.z, h.w): exact fp32 products.
+__device__ __forceinline__ void q4k_coef(const uint4 &h, int sj, float &S, float &Mn) {
+    const float dsc = __half2float(__ushort_as_half((unsigned short)(h.x & 0xFFFF)));
+    const float dmn = __half2float(__ushort_as_half((unsigned short)(h.x >> 16)));
+    const uint32_t sw[3] = {h.y, h.z, h.w};
+    auto sb = [&](int k) { return (sw[k >> 2] >> (8 * (k & 3))) & 0xFFu; };
+    uint32_t sc, mc;
+    if (sj < 4) {
+        sc = sb(sj) & 63u;
+        mc = sb(sj + 4) & 63u;
+    } else {
+        sc = (sb(sj + 4) & 15u) | ((sb(sj - 4) >> 6) << 4);
+        mc = (sb(sj + 4) >> 4) | ((sb(sj) >> 6) << 4);
+    }
+    S = dsc * (float)sc;
+    Mn = dmn * (float)mc;
 }
 
 // ------------------------------------------------------------------ kernel
@@ -289,14 +346,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
                 const GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
-    constexpr int kSA = gemm_stages_a(kFmt);
-    constexpr int kGemmStagesB = gemm_stages_b(kFmt);
+    constexpr int kSA = gemm_stages(kBN);
     constexpr int kCB = gemm_group_bytes(kFmt);
-    constexpr int kSub = gemm_sub(kBN), kSubN = kBN / kSub;  // MMA tiles of a unit, tokens each
-    constexpr int kNbuf = kBN == 512 ? 1 : 2;                  // TMEM accumulators
-    constexpr uint32_t kBBytes = kSubN * kGemmBK * 2;          // one activation (sub-)stage
-    constexpr int kTmemCols = gemm_tmem_cols(kBN);
-    constexpr uint32_t kABytes = kGemmBM * kGemmBK * 2;
+    constexpr int kNbuf = gemm_nbuf(kBN);                    // TMEM accumulators
+    constexpr uint32_t kBBytes = kBN * kGemmBK * 2;          // one activation stage
+    constexpr int kTmemCols = gemm_tmem_cols(kFmt, kBN);
+    constexpr uint32_t kBAtom = kBN * 128;                   // one 64-K atom of an activation stage
+    constexpr int kACol0 = kNbuf * kBN;                      // first TMEM column of the A stages
     constexpr uint32_t kPBytes = kGemmBM * kCB;
     const GemmLayout L = gemm_layout(kFmt, kBN);
     // 1024-byte aligned base for the 128B-swizzled stages, kept as an offset
@@ -323,10 +379,10 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
     auto kg1 = [&](int lt) { return (int)((int64_t)gtot * (kpart(lt) + 1) / ksplit); };
 
     const uint32_t bar = smem_addr(smem + L.bars);
-    auto b_full = [&](int s) { return bar + 8u * s; };
-    auto b_empty = [&](int s) { return bar + 8u * (4 + s); };
-    auto a_full = [&](int s) { return bar + 8u * (8 + s); };
-    auto a_empty = [&](int s) { return bar + 8u * (12 + s); };
+    // stage s is full when its activation copy has landed and all dequantizing
+    // warps have stored their A slices; one MMA commit empties it
+    auto full = [&](int s) { return bar + 8u * s; };
+    auto empty = [&](int s) { return bar + 8u * (4 + s); };
     auto p_full = [&](int s) { return bar + 8u * (16 + s); };
     auto p_empty = [&](int s) { return bar + 8u * (18 + s); };
     auto acc_full = [&](int b) { return bar + 8u * (20 + b); };
@@ -335,13 +391,9 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
     volatile int *last_slot = reinterpret_cast<volatile int *>(smem + L.bars + 8 * 25);
 
     if (tid == 0) {
-        for (int s = 0; s < kGemmStagesB; ++s) {
-            mbar_init(b_full(s), 1);
-            mbar_init(b_empty(s), 1);
-        }
         for (int s = 0; s < kSA; ++s) {
-            mbar_init(a_full(s), kGemmDeqWarps);
-            mbar_init(a_empty(s), 1);
+            mbar_init(full(s), kGemmDeqWarps + 1);
+            mbar_init(empty(s), 1);
         }
         for (int s = 0; s < kGemmStagesP; ++s) {
             mbar_init(p_full(s), 1);
@@ -349,7 +401,7 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
         }
         for (int b = 0; b < kNbuf; ++b) {
             mbar_init(acc_full(b), 1);
-            mbar_init(acc_empty(b), kGemmEpiWarps);
+            mbar_init(acc_empty(b), kNbuf == 1 ? kGemmDeqWarps : kGemmEpiWarps);
         }
         fence_mbar_init();
     }
@@ -367,19 +419,19 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
             bool ok = true;
-            int bi = 0;  // running activation (sub-)stage counter
+            int bi = 0;  // running activation stage counter
             for (int lt = 0; lt < my_tiles && ok; ++lt) {
-                const int m0 = tile_m0(lt), kbase = 4 * kg0(lt), ksteps = 4 * (kg1(lt) - kg0(lt));
-                for (int ks = 0; ks < ksteps && ok; ++ks) {
-                    for (int j = 0; j < kSub && ok; ++j, ++bi) {
-                        const int sb = bi % kGemmStagesB;
-                        if (bi >= kGemmStagesB)
-                            ok = mbar_wait(b_empty(sb), ((bi / kGemmStagesB) - 1) & 1, kErrGemmWait);
-                        if (!ok) break;
-                        mbar_arrive_expect_tx(b_full(sb), kBBytes);
-                        tma_load_2d(smem_addr(smem + L.b + sb * kBBytes), &xmap, (kbase + ks) * kGemmBK,
-                                    m0 + j * kSubN, b_full(sb));
-                    }
+                const int m0 = tile_m0(lt), kbase = kGemmStepsPerGroup * kg0(lt);
+                const int ksteps = kGemmStepsPerGroup * (kg1(lt) - kg0(lt));
+                for (int ks = 0; ks < ksteps && ok; ++ks, ++bi) {
+                    const int sb = bi % kSA;
+                    if (bi >= kSA) ok = mbar_wait(empty(sb), ((bi / kSA) - 1) & 1, kErrGemmWait);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(full(sb), kBBytes);
+#pragma unroll
+                    for (int a = 0; a < kGemmBK / kGemmAtomK; ++a)  // one box per 64-K atom
+                        tma_load_2d(smem_addr(smem + L.b + sb * kBBytes + a * kBAtom), &xmap,
+                                    (kbase + ks) * kGemmBK + a * kGemmAtomK, m0, full(sb));
                 }
             }
         }
@@ -405,114 +457,151 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = umma_idesc_f16(kGemmBM, kSubN);
+            constexpr uint32_t idesc = umma_idesc_f16(kGemmBM, kBN);
             bool ok = true;
-            int ki = 0;  // running k-step counter (A ring)
-            int bi = 0;  // running activation (sub-)stage counter
+            int ki = 0;  // running k-step counter (A and activation rings)
             for (int lt = 0; lt < my_tiles; ++lt) {
                 const int buf = lt % kNbuf, use = lt / kNbuf;
-                const int ksteps = 4 * (kg1(lt) - kg0(lt));
+                const int ksteps = kGemmStepsPerGroup * (kg1(lt) - kg0(lt));
                 const uint32_t dacc = tmem + (uint32_t)(buf * kBN);
                 if (ok && use > 0) ok = mbar_wait(acc_empty(buf), (use - 1) & 1, kErrGemmWait);
                 for (int ks = 0; ks < ksteps && ok; ++ks, ++ki) {
-                    const int sa = ki % kSA;
-                    ok = mbar_wait(a_full(sa), (ki / kSA) & 1, kErrGemmWait);
+                    const int s = ki % kSA;
+                    ok = mbar_wait(full(s), (ki / kSA) & 1, kErrGemmWait);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint64_t ad = umma_desc_sw128(smem_addr(smem + L.a + sa * kABytes));
-                    // every MMA tile of the unit multiplies the same dequantized weights
-                    for (int j = 0; j < kSub && ok; ++j, ++bi) {
-                        const int sb = bi % kGemmStagesB;
-                        ok = mbar_wait(b_full(sb), (bi / kGemmStagesB) & 1, kErrGemmWait);
-                        if (!ok) break;
-                        tc_fence_after();
-                        const uint64_t bd = umma_desc_sw128(smem_addr(smem + L.b + sb * kBBytes));
+                    const uint32_t at = tmem + (uint32_t)(kACol0 + s * kGemmACols);
+                    const uint32_t bs = smem_addr(smem + L.b + s * kBBytes);
 #pragma unroll
-                        for (int kk = 0; kk < kGemmBK / 16; ++kk)  // +32 bytes of K per MMA
-                            umma_f16(dacc + (uint32_t)(j * kSubN), ad + 2 * kk, bd + 2 * kk, idesc, (ks | kk) != 0);
-                        umma_commit(b_empty(sb));
+                    for (int kk = 0; kk < kGemmBK / 16; ++kk) {
+                        // 16 K per MMA: 8 TMEM columns of A; B: atom kk / 4, +32 bytes per step inside it
+                        const uint64_t bd = umma_desc_sw128(bs + (uint32_t)((kk >> 2) * kBAtom)) + 2 * (kk & 3);
+                        umma_f16_ts(dacc, at + (uint32_t)(8 * kk), bd, idesc, (ks | kk) != 0);
                     }
-                    umma_commit(a_empty(sa));
+                    umma_commit(empty(s));
                 }
                 umma_commit(acc_full(buf));  // also after an error: releases the epilogue
             }
         }
     } else if (warp < 2 + kGemmDeqWarps) {
-        // ------------------------------------------------ dequantize packed tiles
-        const int dw = warp - 2;              // 0 .. kGemmDeqWarps - 1
-        const int c = lane & 7;               // 16-byte chunk (8 k) of the 64-k step
-        const int rsub = lane >> 3;           // 0..3
-        float *coef = reinterpret_cast<float *>(smem + L.coef);
+        // ------------------------------------------------ dequantize packed tiles into TMEM
+        // K step j of a group (128 K) splits into four 32-wide slices, one per
+        // warp of a lane quarter; a slice is two of the 16-wide pieces the
+        // deq16_* functions convert (64-wide index J = 2 j + kq / 2, piece
+        // 2 (kq % 2) + h), and 16 TMEM columns
+        const int q = warp & 3;          // TMEM lane quarter this warp may access
+        const int kq = (warp - 2) >> 2;  // 32-wide K slice of each 128-wide K step
+        const int r = 32 * q + lane;     // this thread's weight row (TMEM lane)
+        const uint32_t alane = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(kACol0 + 16 * kq);
         bool ok = true;
         int gi = 0, ki = 0;
+        // With one accumulator (256-token tiles) these warps also drain it:
+        // unit u's epilogue runs where they would otherwise wait for the MMA
+        // to finish u (the K step kSA - 1 steps into unit u + 1, whose stage
+        // slot the last K step of u frees), sixteen warps instead of four,
+        // each storing 64 of the 256 columns of its 32 rows.
+        int epi_unit = -1, epi_at = 0;
+        auto drain = [&](int lt) {
+            if (ok) ok = mbar_wait_warp(acc_full(0), lt & 1, kErrGemmWait);
+            tc_fence_after();
+            const int n = tile_n0(lt) + r, m0 = tile_m0(lt);
+            float rs = 1.f;
+            if constexpr (kFmt == kFp8)
+                if (n < p.N) rs = __ldg(reinterpret_cast<const float *>(p.W + (int64_t)n * p.row_bytes + p.K));
+            if (ok) {
+#pragma unroll 1
+                for (int c = 0; c < 2; ++c) {
+                    const int col = 64 * kq + 32 * c;
+                    uint32_t v[32];
+                    tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)col, v);
+                    if (n < p.N) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const int m = m0 + col + i;
+                            if (m >= p.M) continue;
+                            const float y = __uint_as_float(v[i]) * rs;
+                            if (ksplit == 1) p.Y[(int64_t)m * p.N + n] = y;
+                            else atomicAdd(p.Y + (int64_t)m * p.N + n, y);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty(0));
+        };
         for (int lt = 0; lt < my_tiles; ++lt) {
             for (int g = kg0(lt); g < kg1(lt); ++g, ++gi) {
                 const int sp = gi % kGemmStagesP;
                 if (ok) ok = mbar_wait_warp(p_full(sp), (gi / kGemmStagesP) & 1, kErrGemmWait);
-                const uint8_t *pst = smem + L.p + sp * kPBytes;
+                const uint8_t *prow = smem + L.p + sp * kPBytes + r * kCB;
+                float S[2], Mn[2];  // Q4_K: (S_j, Mn_j) of this thread's sub-block 4 j + kq in each K step
                 if constexpr (kFmt == 4) {
-                    // (S_j, Mn_j) of the 8 sub-blocks of each row's superblock
-                    if (ok && tid >= 64 && tid < 64 + kGemmBM) {
-                        const int r = tid - 64;
-                        const uint4 h = *reinterpret_cast<const uint4 *>(pst + r * kCB);
-                        const float dsc = __half2float(__ushort_as_half((unsigned short)(h.x & 0xFFFF)));
-                        const float dmn = __half2float(__ushort_as_half((unsigned short)(h.x >> 16)));
-                        const uint32_t sw[3] = {h.y, h.z, h.w};
-#pragma unroll
-                        for (int sj = 0; sj < 8; ++sj) {
-                            auto sb = [&](int k) { return (sw[k >> 2] >> (8 * (k & 3))) & 0xFFu; };
-                            uint32_t sc, mc;
-                            if (sj < 4) {
-                                sc = sb(sj) & 63u;
-                                mc = sb(sj + 4) & 63u;
-                            } else {
-                                sc = (sb(sj + 4) & 15u) | ((sb(sj - 4) >> 6) << 4);
-                                mc = (sb(sj + 4) >> 4) | ((sb(sj) >> 6) << 4);
-                            }
-                            coef[r * kGemmCoefStride + 2 * sj] = dsc * (float)sc;
-                            coef[r * kGemmCoefStride + 2 * sj + 1] = dmn * (float)mc;
-                        }
-                    }
-                    named_bar_sync(1, kGemmDeqWarps * 32);
-                }
-                for (int j = 0; j < 4; ++j, ++ki) {
-                    const int sa = ki % kSA;
-                    if (ok && ki >= kSA) ok = mbar_wait_warp(a_empty(sa), ((ki / kSA) - 1) & 1, kErrGemmWait);
-                    uint8_t *ast = smem + L.a + sa * kABytes;
                     if (ok) {
+                        const uint4 h = *reinterpret_cast<const uint4 *>(prow);
 #pragma unroll
-                        for (int pass = 0; pass < kGemmBM / (4 * kGemmDeqWarps); ++pass) {
-                            // warp dw owns 8-row blocks; one pass takes their even
-                            // rows, the next the odd ones: with packed row pitches of
-                            // 4 banks mod 32 (272 and 144 bytes), rows 2 apart keep the
-                            // code loads of the 32 lanes free of bank conflicts
-                            const int r = (pass >> 1) * 8 * kGemmDeqWarps + 8 * dw + 2 * rsub + (pass & 1);
-                            uint4 v;
-                            if constexpr (kFmt == kFp8)
-                                v = deq8_fp8(pst + r * kCB, j, c);
-                            else if constexpr (kFmt == 8)
-                                v = deq8_q8_0(pst + r * kCB, j, c);
-                            else
-                                v = deq8_q4_k(pst + r * kCB, coef + r * kGemmCoefStride, j, c);
-                            *reinterpret_cast<uint4 *>(ast + sw128_chunk_off(r, c)) = v;
-                        }
+                        for (int j = 0; j < 2; ++j) q4k_coef(h, 4 * j + kq, S[j], Mn[j]);
                     }
-                    fence_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(a_full(sa));
                 }
-                if constexpr (kFmt == 4) named_bar_sync(1, kGemmDeqWarps * 32);  // coef reused next group
+                // the two 128-wide K steps of the group (j a compile-time constant)
+                auto step = [&](auto jc) {
+                    constexpr int j = decltype(jc)::value;
+                    const int sa = ki % kSA;
+                    if (kNbuf == 1 && epi_unit >= 0 && ki == epi_at) {
+                        drain(epi_unit);
+                        epi_unit = -1;
+                    }
+                    if (ok && ki >= kSA) ok = mbar_wait_warp(empty(sa), ((ki / kSA) - 1) & 1, kErrGemmWait);
+                    if (ok) {
+                        tc_fence_after();
+                        uint32_t v[16];
+                        uint32_t(&v0)[8] = *reinterpret_cast<uint32_t(*)[8]>(&v[0]);
+                        uint32_t(&v1)[8] = *reinterpret_cast<uint32_t(*)[8]>(&v[8]);
+                        const int J = 2 * j + (kq >> 1), pc = 2 * (kq & 1);
+                        if constexpr (kFmt == kFp8) {
+                            deq16_fp8(prow, J, pc, v0);
+                            deq16_fp8(prow, J, pc + 1, v1);
+                        } else if constexpr (kFmt == 8) {
+                            // piece pc + h of 64-wide step J: block 2 J + (pc + h) / 2 = 2 J + (kq % 2), half h
+                            if (kq >> 1) {
+                                if (kq & 1) { deq16_q8_0<2 * j + 1, 1>(prow, 0, v0); deq16_q8_0<2 * j + 1, 1>(prow, 1, v1); }
+                                else        { deq16_q8_0<2 * j + 1, 0>(prow, 0, v0); deq16_q8_0<2 * j + 1, 0>(prow, 1, v1); }
+                            } else {
+                                if (kq & 1) { deq16_q8_0<2 * j, 1>(prow, 0, v0); deq16_q8_0<2 * j, 1>(prow, 1, v1); }
+                                else        { deq16_q8_0<2 * j, 0>(prow, 0, v0); deq16_q8_0<2 * j, 0>(prow, 1, v1); }
+                            }
+                        } else {
+                            deq16_q4_k(prow, J, pc, S[j], Mn[j], v0);
+                            deq16_q4_k(prow, J, pc + 1, S[j], Mn[j], v1);
+                        }
+                        tmem_st16(alane + (uint32_t)(sa * kGemmACols), v);
+                        tmem_wait_st();
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(full(sa));
+                    ++ki;
+                };
+                step(std::integral_constant<int, 0>{});
+                step(std::integral_constant<int, 1>{});
                 __syncwarp();
                 if (lane == 0) mbar_arrive(p_empty(sp));
             }
+            if (kNbuf == 1) {
+                if (epi_unit >= 0) drain(epi_unit);  // a unit shorter than kSA steps (none today)
+                epi_unit = lt;
+                epi_at = ki + kSA - 1;
+            }
         }
+        if (kNbuf == 1 && epi_unit >= 0) drain(epi_unit);
     } else {
-        // ------------------------------------------------ epilogue: TMEM -> Y
+        // ------------------------------------------------ epilogue: TMEM -> Y (two accumulators;
+        // with one, the dequantizing warps drain it)
         const int quarter = warp & 3;  // this warp may read TMEM lanes 32*quarter .. +31
         const int r = 32 * quarter + lane;  // weight row within the tile
         const int etid = tid - 32 * (2 + kGemmDeqWarps);  // 0 .. 127
         bool ok = true;
-        for (int lt = 0; lt < my_tiles; ++lt) {
+        for (int lt = 0; lt < (kNbuf == 1 ? 0 : my_tiles); ++lt) {
             const int buf = lt % kNbuf, use = lt / kNbuf;
             const int n0 = tile_n0(lt), m0 = tile_m0(lt);
             if (ok) ok = mbar_wait_warp(acc_full(buf), use & 1, kErrGemmWait);
@@ -624,15 +713,6 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
 struct GemmPlan {
     int bn, ksplit, tiles, tickets;
 };
-#ifndef QMM_GEMM_UNIT512  // 1: 512-token units where the cost model favours them
-#define QMM_GEMM_UNIT512 1
-#endif
-// Relative cost of one 64-wide K step of a 512-token unit against a 256-token
-// one, measured on the prefill shapes (14336 x 4096 and 4096 x 14336 at 2048
-// tokens, 4096 x 4096 at 2048): about 1.85, so sharing a dequantized stage
-// saves 7.5 % per token and the unit count decides the rest.
-constexpr double kGemmCost512 = 1.85;
-
 static GemmPlan gemm_plan(int M, int N, int K, int sms) {
     GemmPlan pl;
     const int groups = K / kGroup;
@@ -645,24 +725,6 @@ static GemmPlan gemm_plan(int M, int N, int K, int sms) {
     auto halves = [&](int tiles) {
         return (groups % 2 == 0 && occupancy(2 * tiles) > occupancy(tiles) + 0.2) ? 2 : 1;
     };
-    if (M > 256) {
-        // 256- or 512-token units: waves of units times the K steps of a unit
-        auto cost = [&](int bn, int &tiles, int &ks) {
-            tiles = tiles_n * ((M + bn - 1) / bn);
-            ks = halves(tiles);
-            const int waves = (tiles * ks + sms - 1) / sms;
-            return waves * ((double)groups / ks) * (bn == 512 ? kGemmCost512 : 1.0);
-        };
-        int t256, k256, t512, k512;
-        const double c256 = cost(256, t256, k256), c512 = cost(512, t512, k512);
-        if (QMM_GEMM_UNIT512 && c512 < c256) {
-            pl.bn = 512, pl.tiles = t512, pl.ksplit = k512;
-        } else {
-            pl.bn = 256, pl.tiles = t256, pl.ksplit = k256;
-        }
-        pl.tickets = 0;
-        return pl;
-    }
     pl.bn = M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
     pl.tiles = tiles_n * ((M + pl.bn - 1) / pl.bn);
     if (pl.bn == 256) {
@@ -721,7 +783,7 @@ static cudaError_t launch_gemm_t(const void *W, const uint16_t *X, float *Y, int
 
     CUtensorMap xmap, wmap;
     e = encode_tmap_2d(&xmap, Xh, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (uint64_t)K, (uint64_t)M,
-                       (uint64_t)K * 2, kGemmBK, kBN / gemm_sub(kBN), CU_TENSOR_MAP_SWIZZLE_128B);
+                       (uint64_t)K * 2, kGemmAtomK, kBN, CU_TENSOR_MAP_SWIZZLE_128B);
     if (e != cudaSuccess) return e;
     // a box is 128 rows x one stage pitch (FP8: past a row's end, zero-filled)
     constexpr int kCB = gemm_group_bytes(kFmt);
@@ -759,8 +821,7 @@ static cudaError_t launch_gemm_f(const void *W, const uint16_t *X, float *Y, int
     case 32: return launch_gemm_t<kFmt, 32>(W, X, Y, M, N, K, workspace, sms, stream);
     case 64: return launch_gemm_t<kFmt, 64>(W, X, Y, M, N, K, workspace, sms, stream);
     case 128: return launch_gemm_t<kFmt, 128>(W, X, Y, M, N, K, workspace, sms, stream);
-    case 256: return launch_gemm_t<kFmt, 256>(W, X, Y, M, N, K, workspace, sms, stream);
-    default: return launch_gemm_t<kFmt, 512>(W, X, Y, M, N, K, workspace, sms, stream);
+    default: return launch_gemm_t<kFmt, 256>(W, X, Y, M, N, K, workspace, sms, stream);
     }
 }
 

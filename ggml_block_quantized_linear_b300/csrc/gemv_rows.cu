@@ -34,10 +34,12 @@
 namespace qmm {
 
 constexpr int kRowsR = 16;
-constexpr int kWarpsR = 8;  // consumer warps
-constexpr int kPairsR = kWarpsR / 2;
-constexpr int kProdWarpR = kWarpsR, kRedWarpR = kWarpsR + 1;
-constexpr int kThreadsR = (kWarpsR + 2) * 32;
+// Consumer warps per CTA: 8, or 16 when only one CTA fits on an SM (many
+// tokens or a long K keep a large activation window resident); warp pairs
+// are half that, then the producer warp and the reducer warp.
+template <int kW> struct RowsWarps {
+    static constexpr int kPairs = kW / 2, kProd = kW, kRed = kW + 1, kThreads = (kW + 2) * 32;
+};
 constexpr int kYBufsR = 2;
 constexpr int kCoefStrideR = 20;  // floats per row of a warp's Q4_K coefficient table (padded)
 // Activations held in shared memory at once: M * window chunks <= 256
@@ -58,23 +60,23 @@ __host__ __device__ constexpr int rows_chunk_bytes(int fmt) { return fmt == 8 ? 
 __host__ __device__ constexpr int rows_half_pitch(int fmt) { return fmt == 4 ? kQ4Bytes : kQ8GroupBytes; }
 
 // mt = 8 * (token tiles): the stride of the Q4_K block sums per 32-block.
-__host__ __device__ inline RowsLayout rows_layout(int fmt, int M, int dpp, int win, int mt) {
+__host__ __device__ inline RowsLayout rows_layout(int fmt, int M, int dpp, int win, int mt, int nw) {
     const int cb = rows_half_pitch(fmt);
     RowsLayout L;
     int off = 0;
     L.ring = off;
-    off += kPairsR * dpp * kRowsR * 2 * cb;  // a stage: 16 rows x 2 chunks (multiple of 128 bytes)
+    off += (nw / 2) * dpp * kRowsR * 2 * cb;  // a stage: 16 rows x 2 chunks (multiple of 128 bytes)
     L.xh = off;
     off += M * (win * kGroup + 32) * 2;       // token rows, 32 halves of padding between them
     L.xs = off;
     off += fmt == 4 ? win * 8 * mt * 4 : 0;   // Q4_K: sum of x per 32-block and token
     L.coef = off;
-    off += fmt == 4 ? kWarpsR * kRowsR * kCoefStrideR * 4 : 0;
+    off += fmt == 4 ? nw * kRowsR * kCoefStrideR * 4 : 0;
     L.ypart = off;
-    off += kYBufsR * kWarpsR * kRowsR * M * 4;
+    off += kYBufsR * nw * kRowsR * M * 4;
     off = (off + 15) & ~15;
     L.bars = off;
-    off += (2 * kPairsR * dpp + 2 + 2 * kYBufsR) * 8;
+    off += (2 * (nw / 2) * dpp + 2 + 2 * kYBufsR) * 8;
     L.total = off;
     return L;
 }
@@ -95,7 +97,7 @@ struct RowsParams {
 // at xh + m * xstride), in place to binary16 (round to nearest), each group
 // of 4 stored in the order (0, 2, 1, 3) so that one 16-byte load yields both
 // B fragments of an MMA; Q4_K also sums each 32-weight block per token.
-template <int kFmt, int kMT>
+template <int kFmt, int kMT, int kW>
 __device__ __forceinline__ void rows_convert_x(int M, __half *xh, float *xs, int xstride, int wn,
                                                int tid) {
     const int ngr = (wn * kGroup) / 8;  // 8-element groups per token
@@ -130,7 +132,7 @@ __device__ __forceinline__ void rows_convert_x(int M, __half *xh, float *xs, int
             sum += __shfl_xor_sync(0xffffffffu, sum, 2);
             if ((kg & 3) == 0) xs[(kg >> 2) * kMT + m] = sum;
         }
-        kg += kWarpsR * 32;
+        kg += kW * 32;
         while (kg >= ngr && m < M) { kg -= ngr; ++m; }
     }
 }
@@ -279,9 +281,12 @@ __device__ __forceinline__ void rq4_group(const uint8_t *r0, const uint8_t *r1, 
 
 // kNT token tiles of 8 (M <= 8 kNT); two tiles double the accumulators, so
 // their register budget allows two CTAs per SM instead of three.
-template <int kFmt, int kNT>
-__global__ void __launch_bounds__(kThreadsR, kNT == 1 ? 3 : 2)
+template <int kFmt, int kNT, int kW>
+__global__ void __launch_bounds__(RowsWarps<kW>::kThreads, kW == 8 ? (kNT == 1 ? 3 : 2) : 1)
 qmm_gemv_rows_kernel(const __grid_constant__ CUtensorMap wmap, const RowsParams p) {
+    constexpr int kWarpsR = kW, kPairsR = RowsWarps<kW>::kPairs;
+    constexpr int kProdWarpR = RowsWarps<kW>::kProd, kRedWarpR = RowsWarps<kW>::kRed;
+    constexpr int kThreadsR = RowsWarps<kW>::kThreads;
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int kCB = rows_chunk_bytes(kFmt);            // a chunk's advance in a packed row
     constexpr int kPitch = 2 * rows_half_pitch(kFmt);      // stage row: two chunks (FP8: + 32 bytes)
@@ -290,7 +295,7 @@ qmm_gemv_rows_kernel(const __grid_constant__ CUtensorMap wmap, const RowsParams 
     const int nch = p.nchunks, dpp = p.dpp, win = p.win, M = p.M;
     const bool resident = win >= nch;  // activations staged once per CTA
     const int xstride = win * kGroup + 32;
-    const RowsLayout L = rows_layout(kFmt, M, dpp, win, 8 * kNT);
+    const RowsLayout L = rows_layout(kFmt, M, dpp, win, 8 * kNT, kW);
     uint8_t *ring = smem + L.ring;
     __half *xh = reinterpret_cast<__half *>(smem + L.xh);
     float *xs = reinterpret_cast<float *>(smem + L.xs);
@@ -339,8 +344,13 @@ qmm_gemv_rows_kernel(const __grid_constant__ CUtensorMap wmap, const RowsParams 
         if (lane == 0) {
             bool ok = true;
             int xseq = 0;
-            int dpos[kPairsR] = {0, 0, 0, 0}, ph[kPairsR] = {0, 0, 0, 0};
-            bool lap[kPairsR] = {false, false, false, false};  // slot used before
+            int dpos[kPairsR], ph[kPairsR];
+            bool lap[kPairsR];  // slot used before
+#pragma unroll
+            for (int i = 0; i < kPairsR; ++i) {
+                dpos[i] = ph[i] = 0;
+                lap[i] = false;
+            }
             for (int tile = blockIdx.x; ok && tile < p.ntiles; tile += gridDim.x) {
                 const int row0 = tile * kRowsR;
                 for (int w0 = 0; ok && w0 < nch; w0 += win) {
@@ -422,7 +432,7 @@ qmm_gemv_rows_kernel(const __grid_constant__ CUtensorMap wmap, const RowsParams 
                 const int wn = min(win, nch - w0);
                 if (!resident || xseq == 0) {
                     if (ok) ok = mbar_wait_warp(xfull, xseq & 1, kErrGemvFullWait);
-                    if (ok) rows_convert_x<kFmt, kMT>(M, xh, xs, xstride, wn, tid);
+                    if (ok) rows_convert_x<kFmt, kMT, kW>(M, xh, xs, xstride, wn, tid);
                     named_bar_sync(1, kWarpsR * 32);
                 }
                 const int j_end = (w0 + wn + 1) / 2;
@@ -503,19 +513,21 @@ qmm_gemv_rows_kernel(const __grid_constant__ CUtensorMap wmap, const RowsParams 
     }
 }
 
-template <int kFmt, int kNT>
+template <int kFmt, int kNT, int kW>
 static cudaError_t rows_set_attrs() {
     static std::atomic<uint64_t> done{0};
-    return set_smem_limit_once(reinterpret_cast<const void *>(qmm_gemv_rows_kernel<kFmt, kNT>), 227 * 1024, done);
+    return set_smem_limit_once(reinterpret_cast<const void *>(qmm_gemv_rows_kernel<kFmt, kNT, kW>), 227 * 1024,
+                               done);
 }
 
 // Resident CTAs per SM for a given dynamic shared-memory size (registers,
 // threads and shared memory all counted by the runtime).
-template <int kFmt, int kNT>
+template <int kFmt, int kNT, int kW>
 static int rows_occupancy(int smem) {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, qmm_gemv_rows_kernel<kFmt, kNT>, kThreadsR,
-                                                      (size_t)smem) != cudaSuccess)
+    if (rows_set_attrs<kFmt, kNT, kW>() != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, qmm_gemv_rows_kernel<kFmt, kNT, kW>,
+                                                      RowsWarps<kW>::kThreads, (size_t)smem) != cudaSuccess)
         return 1;
     return n < 1 ? 1 : n;
 }
@@ -528,15 +540,15 @@ static int rows_occupancy(int smem) {
 #endif
 
 struct RowsPlan {
-    int dev, M, K, dpp, win, smem, occ;
+    int dev, M, K, dpp, win, smem, occ, warps;
 };
 
-// Plan for (M, K): activation window (all of K when M * chunks fits the
-// budget), then the sub-ring depth per warp pair with the most weight bytes
-// in flight per SM (resident CTAs x ring bytes), preferring more resident
-// CTAs on ties.
-template <int kFmt, int kNT>
-static RowsPlan rows_plan_compute(int dev, int M, int K) {
+// Plan for (M, K) with kW consumer warps: activation window (all of K when
+// M * chunks fits the budget), then the sub-ring depth per warp pair with
+// the most weight bytes in flight per SM (resident CTAs x ring bytes),
+// preferring more resident CTAs on ties.
+template <int kFmt, int kNT, int kW>
+static RowsPlan rows_plan_warps(int dev, int M, int K) {
     constexpr int kCB = rows_half_pitch(kFmt);
     const int nch = K / kGroup;
     int win = nch;
@@ -544,20 +556,43 @@ static RowsPlan rows_plan_compute(int dev, int M, int K) {
         win = (kRowsXChunkBudget / M) / 8 * 8;
         if (win < 8) win = 8;
     }
-    RowsPlan best{dev, M, K, 0, win, 0, 0};
+    RowsPlan best{dev, M, K, 0, win, 0, 0, kW};
     long best_bytes = -1;
     for (int d = 1; d <= QMM_ROWS_MAX_DPP; ++d) {
         if (QMM_ROWS_FORCE_DPP > 0 && d != QMM_ROWS_FORCE_DPP) continue;
-        const int sm = rows_layout(kFmt, M, d, win, 8 * kNT).total;
+        const int sm = rows_layout(kFmt, M, d, win, 8 * kNT, kW).total;
         if (sm > 227 * 1024) break;
-        const int occ = rows_occupancy<kFmt, kNT>(sm);
-        const long bytes = (long)occ * kPairsR * d * kRowsR * 2 * kCB;
+        const int occ = rows_occupancy<kFmt, kNT, kW>(sm);
+        const long bytes = (long)occ * (kW / 2) * d * kRowsR * 2 * kCB;
         if (bytes > best_bytes || (bytes == best_bytes && occ > best.occ)) {
             best_bytes = bytes;
-            best = RowsPlan{dev, M, K, d, win, sm, occ};
+            best = RowsPlan{dev, M, K, d, win, sm, occ, kW};
         }
     }
     return best;
+}
+
+#ifndef QMM_ROWS_WARPS  // 0: chosen by the plan; 8 or 16 forces that many consumer warps
+#define QMM_ROWS_WARPS 0
+#endif
+
+// Eight consumer warps per CTA while two or more CTAs fit on an SM;
+// sixteen when a single CTA does (the activations of many tokens or of a
+// long K fill shared memory), which doubles the warps that hide latency.
+// Q4_K, whose consumers do the most arithmetic per byte, always gains from
+// them; Q8_0 and FP8 only while the ring keeps as many stages in flight
+// (eight pairs' rings of one stage can hold fewer than four pairs' deeper
+// ones), measured on the decode shapes.
+template <int kFmt, int kNT>
+static RowsPlan rows_plan_compute(int dev, int M, int K) {
+    const RowsPlan p8 = rows_plan_warps<kFmt, kNT, 8>(dev, M, K);
+    if (QMM_ROWS_WARPS == 8) return p8;
+    if (QMM_ROWS_WARPS != 16 && p8.dpp > 0 && p8.occ > 1) return p8;
+    const RowsPlan p16 = rows_plan_warps<kFmt, kNT, 16>(dev, M, K);
+    if (p16.dpp == 0) return p8;
+    if (QMM_ROWS_WARPS == 16 || p8.dpp == 0 || kFmt == 4) return p16;
+    const long b8 = (long)p8.occ * 4 * p8.dpp, b16 = (long)p16.occ * 8 * p16.dpp;  // stages in flight per SM
+    return b16 >= b8 ? p16 : p8;
 }
 
 // The plan depends on (device, M, K) only; it is computed once (the
@@ -575,17 +610,13 @@ static RowsPlan rows_plan(int dev, int M, int K) {
     return pl;
 }
 
-template <int kFmt, int kNT>
-static cudaError_t launch_rows_t(const void *W, RowsParams &p, int sms, cudaStream_t stream) {
+template <int kFmt, int kNT, int kW>
+static cudaError_t launch_rows_w(const void *W, RowsParams &p, const RowsPlan &pl, int sms,
+                                 cudaStream_t stream) {
     constexpr int kCB = rows_chunk_bytes(kFmt);
     constexpr int kHalfPitch = rows_half_pitch(kFmt);
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    cudaError_t e = rows_set_attrs<kFmt, kNT, kW>();
     if (e != cudaSuccess) return e;
-    e = rows_set_attrs<kFmt, kNT>();
-    if (e != cudaSuccess) return e;
-    const RowsPlan pl = rows_plan<kFmt, kNT>(dev, p.M, p.K);
-    if (pl.dpp == 0) return cudaErrorInvalidConfiguration;  // no plan fits shared memory
     p.nchunks = p.K / kGroup;
     p.ntiles = (p.N + kRowsR - 1) / kRowsR;
     p.dpp = pl.dpp;
@@ -603,7 +634,7 @@ static cudaError_t launch_rows_t(const void *W, RowsParams &p, int sms, cudaStre
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
-    cfg.blockDim = dim3(kThreadsR, 1, 1);
+    cfg.blockDim = dim3(RowsWarps<kW>::kThreads, 1, 1);
     cfg.dynamicSmemBytes = (size_t)pl.smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -611,7 +642,18 @@ static cudaError_t launch_rows_t(const void *W, RowsParams &p, int sms, cudaStre
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, qmm_gemv_rows_kernel<kFmt, kNT>, wmap, p);
+    return cudaLaunchKernelEx(&cfg, qmm_gemv_rows_kernel<kFmt, kNT, kW>, wmap, p);
+}
+
+template <int kFmt, int kNT>
+static cudaError_t launch_rows_t(const void *W, RowsParams &p, int sms, cudaStream_t stream) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const RowsPlan pl = rows_plan<kFmt, kNT>(dev, p.M, p.K);
+    if (pl.dpp == 0) return cudaErrorInvalidConfiguration;  // no plan fits shared memory
+    return pl.warps == 16 ? launch_rows_w<kFmt, kNT, 16>(W, p, pl, sms, stream)
+                          : launch_rows_w<kFmt, kNT, 8>(W, p, pl, sms, stream);
 }
 
 cudaError_t launch_gemv_rows(int fmt, const void *W, const uint16_t *X, float *Y, int M, int N, int K,
