@@ -1,4 +1,4 @@
-"""CPU oracle for the GGML block-quantized linear layer (Q8_0, Q4_K).
+"""CPU oracle for the GGML block-quantized linear layer (Q8_0, Q2_K-Q6_K, FP8).
 
 TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the
 ``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
@@ -21,6 +21,9 @@ import numpy as np
 Q8_0 = 8
 Q4_K = 4
 Q6_K = 6
+Q5_K = 5
+Q3_K = 3
+Q2_K = 2
 FP8 = 80
 SRC_BF16 = 0
 SRC_F32 = 1
@@ -32,7 +35,8 @@ _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-BLOCK = {Q8_0: (32, 34), Q4_K: (256, 144), Q6_K: (256, 210)}
+BLOCK = {Q8_0: (32, 34), Q4_K: (256, 144), Q6_K: (256, 210), Q5_K: (256, 176), Q3_K: (256, 110),
+         Q2_K: (256, 84)}
 FP8_ROW_PAD = 16  # FP8 rows: K codes, the fp32 row scale, 12 zero bytes
 
 
@@ -78,6 +82,9 @@ def lib() -> ctypes.CDLL:
             L.orc_gather.argtypes = [ctypes.c_int, vp, i64, i64, vp, i64, vp]
             L.orc_gather.restype = ctypes.c_int
             L.orc_q6_k_position.argtypes = [ctypes.c_int, vp]
+            L.orc_q3_k_position.argtypes = [ctypes.c_int, vp]
+            L.orc_q3_k_get_field.argtypes = [vp, ctypes.c_int]
+            L.orc_q3_k_get_field.restype = ctypes.c_int
             L.orc_q4_k_pack_scales.argtypes = [vp, vp, vp]
             L.orc_q4_k_unpack_scales.argtypes = [vp, vp, vp]
             L.orc_set_threads.argtypes = [ctypes.c_int]
@@ -215,6 +222,20 @@ def q6_k_position(w: int):
     pos = np.zeros(4, dtype=np.int32)
     lib().orc_q6_k_position(int(w), _ptr(pos))
     return tuple(int(v) for v in pos)
+
+
+def q3_k_position(w: int):
+    """(qs byte, bit shift, hmask byte, bit) of weight w of a Q3_K superblock."""
+    pos = np.zeros(4, dtype=np.int32)
+    lib().orc_q3_k_position(int(w), _ptr(pos))
+    return tuple(int(v) for v in pos)
+
+
+def q3_k_scale_field(scale_bytes, j: int) -> int:
+    """The 6-bit field j (0..15) of a Q3_K superblock's 12 scale bytes."""
+    b = np.ascontiguousarray(np.asarray(scale_bytes, dtype=np.uint8))
+    assert b.size == 12
+    return int(lib().orc_q3_k_get_field(_ptr(b), int(j)))
 
 
 def f32_to_e4m3_bits(values) -> np.ndarray:

@@ -1,6 +1,6 @@
 /*
  * qmm_oracle.c -- plain, slow, CPU reference for the GGML block-quantized
- * linear layer (Q8_0 and Q4_K).  TEST INFRASTRUCTURE ONLY: the tests, the
+ * linear layer (Q8_0, the K-quants Q2_K to Q6_K, FP8 E4M3).  TEST INFRASTRUCTURE ONLY: the tests, the
  * package's smoke check and the CPU-baseline leg of the benchmark call this
  * library; the product path never does.  It shares no code, header, table or
  * constant with the CUDA library.
@@ -47,6 +47,35 @@
  *     l < 32): low 4 bits of q in byte 64h + 32(s & 1) + l of ql (low
  *     nibble for s < 2, high nibble for s >= 2), high 2 bits in bits 2s,
  *     2s + 1 of byte 32h + l of qh; weight w uses sc[w / 16].
+ *   Q5_K, Q3_K, Q2_K (the page's Q*K table lists q5k, q3k, q2k at 5, 3
+ *     and 2 bits; its "Numeric shorthands" table maps `--isq 5 / 3 / 2` to
+ *     Q5K / Q3K / Q2K on CUDA).  Readings in the same plain style:
+ *   Q5_K superblock (8 sub-blocks of 32, 176 bytes): Q4_K's quantizer with
+ *     5-bit codes: s_j = (mx_j - mn_j) / 31, m_j = 0 - mn_j, d16 / dmin16 /
+ *     sc_j / mc_j / S_j / Mn_j as for Q4_K, q_i = clamp(roundf((x_i + Mn_j) /
+ *     S_j), 0, 31); value S_j * q - Mn_j.  Bytes 0-1 d16, 2-3 dmin16, 4-15
+ *     the scale bytes (Q4_K's packing), 16-47 qh, 48-175 qs: byte 48+32c+l
+ *     holds the low 4 bits of weight l of sub-block 2c (low nibble) and of
+ *     sub-block 2c+1 (high nibble); bit j of qh byte 16+l is bit 4 of weight
+ *     l of sub-block j.
+ *   Q3_K superblock (16 sub-blocks of 16, 110 bytes), symmetric like Q6_K:
+ *     s_j = max_i |x_i| / 3; d16 = fp16_rne(max_j s_j / 31); sc_j =
+ *     clamp(roundf(s_j / d16), 0, 31) (0 when d16 == 0); S_j = d16 * sc_j;
+ *     c_i = clamp(roundf(x_i / S_j), -4, 3) (0 when S_j == 0); value S_j * c_i
+ *     (exact).  Bytes 0-31 hmask, 32-95 qs, 96-107 the sixteen 6-bit scale
+ *     fields (each sc_j + 32), 108-109 d16.  With q = c + 4 in 0..7 and weight
+ *     w = 128h + 32s + l (h < 2, s < 4, l < 32): bits 0-1 of q in bits 2s,
+ *     2s+1 of qs byte 32h + l; bit 2 of q in bit 4h + s of hmask byte l.
+ *     Scale field j: low 4 bits in scale byte j mod 8 (low nibble for j < 8,
+ *     high nibble for j >= 8), high 2 bits in bits 2(j div 4), 2(j div 4)+1
+ *     of scale byte 8 + j mod 4.
+ *   Q2_K superblock (16 sub-blocks of 16, 84 bytes), affine like Q4_K:
+ *     s_j = (mx_j - mn_j) / 3, m_j = 0 - mn_j; d16 = fp16_rne(max_j s_j / 15),
+ *     dmin16 = fp16_rne(max_j m_j / 15); sc_j, mc_j = clamped roundf of
+ *     s_j / d16, m_j / dmin16 in 0..15; q_i = clamp(roundf((x_i + Mn_j) /
+ *     S_j), 0, 3); value S_j * q - Mn_j.  Bytes 0-15 the scales (byte j: sc_j
+ *     in the low nibble, mc_j in the high one), 16-79 qs (weight w = 128h +
+ *     32s + l in bits 2s, 2s+1 of byte 16 + 32h + l), 80-81 d16, 82-83 dmin16.
  *   FP8 E4M3 with a scale per row (W8A16): the page's section "FP8" says
  *     E4M3 FP8 can be produced with ISQ and lists symmetric E4M3 W8A16 with
  *     tensor, channel or block weight scales; the reading here is one fp32
@@ -376,6 +405,203 @@ static void dequantize_q6_k_superblock(const uint8_t *blk, float *y)
 }
 
 /* ------------------------------------------------------------------ */
+/* Q5_K: Q4_K with 5-bit codes; 176 bytes                              */
+/* ------------------------------------------------------------------ */
+
+enum { Q5_K_QK = 256, Q5_K_BYTES = 176, Q3_K_QK = 256, Q3_K_BYTES = 110, Q2_K_QK = 256, Q2_K_BYTES = 84 };
+
+/* Per-sub-block range statistics of an affine K-quant: s_j = (max - min(0,
+ * min)) / levels, m_j = 0 - min(0, min) over sub-blocks of `len` weights. */
+static void affine_stats(const float *x, int nsub, int len, float levels, float *s, float *m, float *smax,
+                         float *mmax)
+{
+    *smax = 0.0f;
+    *mmax = 0.0f;
+    for (int j = 0; j < nsub; j++) {
+        const float *xs = x + len * j;
+        float mx = xs[0], mn = 0.0f;
+        for (int i = 0; i < len; i++) {
+            if (xs[i] > mx)
+                mx = xs[i];
+            if (xs[i] < mn)
+                mn = xs[i];
+        }
+        s[j] = (mx - mn) / levels;
+        m[j] = 0.0f - mn;
+        if (s[j] > *smax)
+            *smax = s[j];
+        if (m[j] > *mmax)
+            *mmax = m[j];
+    }
+}
+
+static void quantize_q5_k_superblock(const float *x, uint8_t *out)
+{
+    float s[8], m[8], smax, mmax;
+    affine_stats(x, 8, 32, 31.0f, s, m, &smax, &mmax);
+    uint16_t d16 = orc_f32_to_f16(smax / 63.0f);
+    uint16_t dmin16 = orc_f32_to_f16(mmax / 63.0f);
+    float df = orc_f16_to_f32(d16), dminf = orc_f16_to_f32(dmin16);
+    int sc[8], mc[8];
+    for (int j = 0; j < 8; j++) {
+        sc[j] = df > 0.0f ? (int)clampf(roundf(s[j] / df), 0.0f, 63.0f) : 0;
+        mc[j] = dminf > 0.0f ? (int)clampf(roundf(m[j] / dminf), 0.0f, 63.0f) : 0;
+    }
+    memset(out, 0, Q5_K_BYTES);
+    put_u16(out, d16);
+    put_u16(out + 2, dmin16);
+    pack_scales_q4_k(sc, mc, out + 4);
+    for (int j = 0; j < 8; j++) {
+        float S = df * (float)sc[j];
+        float Mn = dminf * (float)mc[j];
+        for (int l = 0; l < 32; l++) {
+            int q = 0;
+            if (S > 0.0f)
+                q = (int)clampf(roundf((x[32 * j + l] + Mn) / S), 0.0f, 31.0f);
+            out[48 + 32 * (j / 2) + l] |= (uint8_t)((q & 15) << (4 * (j % 2)));
+            out[16 + l] |= (uint8_t)((q >> 4) << j);
+        }
+    }
+}
+
+static void dequantize_q5_k_superblock(const uint8_t *blk, float *y)
+{
+    float df = orc_f16_to_f32(get_u16(blk));
+    float dminf = orc_f16_to_f32(get_u16(blk + 2));
+    int sc[8], mc[8];
+    unpack_scales_q4_k(blk + 4, sc, mc);
+    for (int j = 0; j < 8; j++) {
+        float S = df * (float)sc[j];
+        float Mn = dminf * (float)mc[j];
+        for (int l = 0; l < 32; l++) {
+            int q = ((blk[48 + 32 * (j / 2) + l] >> (4 * (j % 2))) & 15) | (((blk[16 + l] >> j) & 1) << 4);
+            float prod = S * (float)q;
+            y[32 * j + l] = prod - Mn;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* Q3_K: 16 sub-blocks of 16, symmetric 3-bit codes; 110 bytes          */
+/* ------------------------------------------------------------------ */
+
+/* Scale field j (0..15) of Q3_K: returns the 6-bit field and writes it. */
+static int q3_k_get_field(const uint8_t *sb, int j)
+{
+    int lo = (sb[j % 8] >> (j < 8 ? 0 : 4)) & 15;
+    int hi = (sb[8 + j % 4] >> (2 * (j / 4))) & 3;
+    return lo | (hi << 4);
+}
+static void q3_k_put_field(uint8_t *sb, int j, int v)
+{
+    sb[j % 8] |= (uint8_t)((v & 15) << (j < 8 ? 0 : 4));
+    sb[8 + j % 4] |= (uint8_t)(((v >> 4) & 3) << (2 * (j / 4)));
+}
+
+/* Positions of the 3-bit code of weight w: bits 0-1 at bit *lo_shift of
+ * byte *lo_byte (qs), bit 2 at bit *hi_bit of byte *hi_byte (hmask);
+ * offsets from the block start. */
+static void q3_k_position(int w, int *lo_byte, int *lo_shift, int *hi_byte, int *hi_bit)
+{
+    int h = w / 128, s = (w / 32) % 4, l = w % 32;
+    *lo_byte = 32 + 32 * h + l;
+    *lo_shift = 2 * s;
+    *hi_byte = l;
+    *hi_bit = 4 * h + s;
+}
+
+static void quantize_q3_k_superblock(const float *x, uint8_t *out)
+{
+    float s[16], smax = 0.0f;
+    for (int j = 0; j < 16; j++) {
+        float amax = 0.0f;
+        for (int i = 0; i < 16; i++) {
+            float a = fabsf(x[16 * j + i]);
+            if (a > amax)
+                amax = a;
+        }
+        s[j] = amax / 3.0f;
+        if (s[j] > smax)
+            smax = s[j];
+    }
+    uint16_t d16 = orc_f32_to_f16(smax / 31.0f);
+    float df = orc_f16_to_f32(d16);
+    memset(out, 0, Q3_K_BYTES);
+    for (int j = 0; j < 16; j++) {
+        int sc = df > 0.0f ? (int)clampf(roundf(s[j] / df), 0.0f, 31.0f) : 0;
+        float S = df * (float)sc;
+        q3_k_put_field(out + 96, j, sc + 32);
+        for (int i = 0; i < 16; i++) {
+            int w = 16 * j + i;
+            int c = S > 0.0f ? (int)clampf(roundf(x[w] / S), -4.0f, 3.0f) : 0;
+            int q = c + 4;
+            int lo_byte, lo_shift, hi_byte, hi_bit;
+            q3_k_position(w, &lo_byte, &lo_shift, &hi_byte, &hi_bit);
+            out[lo_byte] |= (uint8_t)((q & 3) << lo_shift);
+            out[hi_byte] |= (uint8_t)((q >> 2) << hi_bit);
+        }
+    }
+    put_u16(out + 108, d16);
+}
+
+static void dequantize_q3_k_superblock(const uint8_t *blk, float *y)
+{
+    float df = orc_f16_to_f32(get_u16(blk + 108));
+    for (int w = 0; w < 256; w++) {
+        int lo_byte, lo_shift, hi_byte, hi_bit;
+        q3_k_position(w, &lo_byte, &lo_shift, &hi_byte, &hi_bit);
+        int q = ((blk[lo_byte] >> lo_shift) & 3) | (((blk[hi_byte] >> hi_bit) & 1) << 2);
+        float S = df * (float)(q3_k_get_field(blk + 96, w / 16) - 32);
+        y[w] = S * (float)(q - 4);
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* Q2_K: 16 sub-blocks of 16, affine 2-bit codes; 84 bytes              */
+/* ------------------------------------------------------------------ */
+
+static void quantize_q2_k_superblock(const float *x, uint8_t *out)
+{
+    float s[16], m[16], smax, mmax;
+    affine_stats(x, 16, 16, 3.0f, s, m, &smax, &mmax);
+    uint16_t d16 = orc_f32_to_f16(smax / 15.0f);
+    uint16_t dmin16 = orc_f32_to_f16(mmax / 15.0f);
+    float df = orc_f16_to_f32(d16), dminf = orc_f16_to_f32(dmin16);
+    memset(out, 0, Q2_K_BYTES);
+    for (int j = 0; j < 16; j++) {
+        int sc = df > 0.0f ? (int)clampf(roundf(s[j] / df), 0.0f, 15.0f) : 0;
+        int mc = dminf > 0.0f ? (int)clampf(roundf(m[j] / dminf), 0.0f, 15.0f) : 0;
+        out[j] = (uint8_t)(sc | (mc << 4));
+        float S = df * (float)sc;
+        float Mn = dminf * (float)mc;
+        for (int i = 0; i < 16; i++) {
+            int w = 16 * j + i;
+            int q = 0;
+            if (S > 0.0f)
+                q = (int)clampf(roundf((x[w] + Mn) / S), 0.0f, 3.0f);
+            int h = w / 128, sh = (w / 32) % 4, l = w % 32;
+            out[16 + 32 * h + l] |= (uint8_t)(q << (2 * sh));
+        }
+    }
+    put_u16(out + 80, d16);
+    put_u16(out + 82, dmin16);
+}
+
+static void dequantize_q2_k_superblock(const uint8_t *blk, float *y)
+{
+    float df = orc_f16_to_f32(get_u16(blk + 80));
+    float dminf = orc_f16_to_f32(get_u16(blk + 82));
+    for (int w = 0; w < 256; w++) {
+        int j = w / 16, h = w / 128, sh = (w / 32) % 4, l = w % 32;
+        float S = df * (float)(blk[j] & 15);
+        float Mn = dminf * (float)(blk[j] >> 4);
+        int q = (blk[16 + 32 * h + l] >> (2 * sh)) & 3;
+        float prod = S * (float)q;
+        y[w] = prod - Mn;
+    }
+}
+
+/* ------------------------------------------------------------------ */
 /* FP8 E4M3 (OCP 8-bit floating point, E4M3: 1 sign, 4 exponent bits with  */
 /* bias 7, 3 fraction bits, no infinities, S.1111.111 is NaN)            */
 /* ------------------------------------------------------------------ */
@@ -465,7 +691,10 @@ void orc_e4m3_to_f32_array(const uint8_t *b, float *x, int64_t n)
 /* Exported API                                                        */
 /* ------------------------------------------------------------------ */
 
-enum { ORC_Q8_0 = 8, ORC_Q4_K = 4, ORC_Q6_K = 6, ORC_FP8 = 80 };
+enum { ORC_Q8_0 = 8, ORC_Q4_K = 4, ORC_Q6_K = 6, ORC_Q5_K = 5, ORC_Q3_K = 3, ORC_Q2_K = 2, ORC_FP8 = 80 };
+
+static int qk_of(int fmt);
+static int bytes_of(int fmt);
 
 /* Bytes of one packed row of `cols` weights (0 if cols is not a whole
  * number of blocks). */
@@ -473,39 +702,59 @@ static int64_t row_bytes_of(int fmt, int64_t cols)
 {
     if (fmt == ORC_FP8)
         return cols % 256 == 0 ? cols + FP8_ROW_PAD : 0;
-    int qk = fmt == ORC_Q8_0 ? Q8_0_QK : (fmt == ORC_Q4_K || fmt == ORC_Q6_K) ? 256 : 0;
+    int qk = qk_of(fmt);
     if (qk == 0 || cols % qk != 0)
         return 0;
-    return (cols / qk) * (fmt == ORC_Q8_0 ? Q8_0_BYTES : fmt == ORC_Q4_K ? Q4_K_BYTES : Q6_K_BYTES);
+    return (cols / qk) * bytes_of(fmt);
 }
 
 static int qk_of(int fmt)
 {
-    return fmt == ORC_Q8_0 ? Q8_0_QK : fmt == ORC_Q4_K ? Q4_K_QK : fmt == ORC_Q6_K ? Q6_K_QK : 0;
+    switch (fmt) {
+    case ORC_Q8_0: return Q8_0_QK;
+    case ORC_Q4_K: return Q4_K_QK;
+    case ORC_Q6_K: return Q6_K_QK;
+    case ORC_Q5_K: return Q5_K_QK;
+    case ORC_Q3_K: return Q3_K_QK;
+    case ORC_Q2_K: return Q2_K_QK;
+    default: return 0;
+    }
 }
 static int bytes_of(int fmt)
 {
-    return fmt == ORC_Q8_0 ? Q8_0_BYTES : fmt == ORC_Q4_K ? Q4_K_BYTES : fmt == ORC_Q6_K ? Q6_K_BYTES : 0;
+    switch (fmt) {
+    case ORC_Q8_0: return Q8_0_BYTES;
+    case ORC_Q4_K: return Q4_K_BYTES;
+    case ORC_Q6_K: return Q6_K_BYTES;
+    case ORC_Q5_K: return Q5_K_BYTES;
+    case ORC_Q3_K: return Q3_K_BYTES;
+    case ORC_Q2_K: return Q2_K_BYTES;
+    default: return 0;
+    }
 }
 
 static void quantize_block(int fmt, const float *x, uint8_t *out)
 {
-    if (fmt == ORC_Q8_0)
-        quantize_q8_0_block(x, out);
-    else if (fmt == ORC_Q4_K)
-        quantize_q4_k_superblock(x, out);
-    else
-        quantize_q6_k_superblock(x, out);
+    switch (fmt) {
+    case ORC_Q8_0: quantize_q8_0_block(x, out); break;
+    case ORC_Q4_K: quantize_q4_k_superblock(x, out); break;
+    case ORC_Q6_K: quantize_q6_k_superblock(x, out); break;
+    case ORC_Q5_K: quantize_q5_k_superblock(x, out); break;
+    case ORC_Q3_K: quantize_q3_k_superblock(x, out); break;
+    case ORC_Q2_K: quantize_q2_k_superblock(x, out); break;
+    }
 }
 
 static void dequantize_block(int fmt, const uint8_t *blk, float *y)
 {
-    if (fmt == ORC_Q8_0)
-        dequantize_q8_0_block(blk, y);
-    else if (fmt == ORC_Q4_K)
-        dequantize_q4_k_superblock(blk, y);
-    else
-        dequantize_q6_k_superblock(blk, y);
+    switch (fmt) {
+    case ORC_Q8_0: dequantize_q8_0_block(blk, y); break;
+    case ORC_Q4_K: dequantize_q4_k_superblock(blk, y); break;
+    case ORC_Q6_K: dequantize_q6_k_superblock(blk, y); break;
+    case ORC_Q5_K: dequantize_q5_k_superblock(blk, y); break;
+    case ORC_Q3_K: dequantize_q3_k_superblock(blk, y); break;
+    case ORC_Q2_K: dequantize_q2_k_superblock(blk, y); break;
+    }
 }
 
 int64_t orc_packed_bytes(int fmt, int64_t rows, int64_t cols)
@@ -688,3 +937,10 @@ void orc_q6_k_position(int w, int *pos4)
 /* Debug access to the scale-byte packing of Q4_K (used by the layout pins). */
 void orc_q4_k_pack_scales(const int *sc, const int *mc, uint8_t *s12) { pack_scales_q4_k(sc, mc, s12); }
 void orc_q4_k_unpack_scales(const uint8_t *s12, int *sc, int *mc) { unpack_scales_q4_k(s12, sc, mc); }
+
+/* Debug access to the code positions of Q3_K and its scale fields (layout pins). */
+void orc_q3_k_position(int w, int *pos4)
+{
+    q3_k_position(w, &pos4[0], &pos4[1], &pos4[2], &pos4[3]);
+}
+int orc_q3_k_get_field(const uint8_t *sb12, int j) { return q3_k_get_field(sb12, j); }

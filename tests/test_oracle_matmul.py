@@ -22,7 +22,7 @@ def make(fmt, n, k, m, seed):
     return packed, inputs.bf16_bits(x), x.float().numpy()
 
 
-@pytest.mark.parametrize("fmt,k", [(oracle.Q8_0, 64), (oracle.Q4_K, 256), (oracle.Q6_K, 256), (oracle.FP8, 256)])
+@pytest.mark.parametrize("fmt,k", [(oracle.Q8_0, 64), (oracle.Q4_K, 256), (oracle.Q6_K, 256), (oracle.FP8, 256), (oracle.Q5_K, 256), (oracle.Q3_K, 256), (oracle.Q2_K, 256)])
 def test_exact_rational_tiny(fmt, k):
     n, m = 5, 3
     packed, xb, xf = make(fmt, n, k, m, 31)
@@ -36,7 +36,7 @@ def test_exact_rational_tiny(fmt, k):
             assert abs(Fraction(A[i, j]) - absum) <= Fraction(k) * Fraction(2.0 ** -52) * absum
 
 
-@pytest.mark.parametrize("fmt", [oracle.Q8_0, oracle.Q4_K, oracle.Q6_K, oracle.FP8])
+@pytest.mark.parametrize("fmt", [oracle.Q8_0, oracle.Q4_K, oracle.Q6_K, oracle.FP8, oracle.Q5_K, oracle.Q3_K, oracle.Q2_K])
 def test_one_hot_rows_select_weights(fmt):
     n, k = 6, 512
     packed, _, _ = make(fmt, n, k, 1, 32)
@@ -49,7 +49,7 @@ def test_one_hot_rows_select_weights(fmt):
     assert np.array_equal(Y, wd[:, cols].T.astype(np.float64))
 
 
-@pytest.mark.parametrize("fmt", [oracle.Q8_0, oracle.Q4_K, oracle.Q6_K, oracle.FP8])
+@pytest.mark.parametrize("fmt", [oracle.Q8_0, oracle.Q4_K, oracle.Q6_K, oracle.FP8, oracle.Q5_K, oracle.Q3_K, oracle.Q2_K])
 def test_zero_weights(fmt):
     n, k = 4, 256
     packed = oracle.quantize(fmt, np.zeros((n, k), dtype=np.float32))
@@ -58,7 +58,7 @@ def test_zero_weights(fmt):
     assert not Y.any() and not A.any()
 
 
-@pytest.mark.parametrize("fmt", [oracle.Q8_0, oracle.Q4_K, oracle.Q6_K, oracle.FP8])
+@pytest.mark.parametrize("fmt", [oracle.Q8_0, oracle.Q4_K, oracle.Q6_K, oracle.FP8, oracle.Q5_K, oracle.Q3_K, oracle.Q2_K])
 def test_linearity(fmt):
     n, k = 8, 512
     packed, _, _ = make(fmt, n, k, 1, 33)
@@ -74,7 +74,7 @@ def test_linearity(fmt):
     assert np.abs(Y1).max() > 0 and np.abs(Y12 - Y1).max() > 0
 
 
-@pytest.mark.parametrize("fmt", [oracle.Q8_0, oracle.Q4_K, oracle.Q6_K, oracle.FP8])
+@pytest.mark.parametrize("fmt", [oracle.Q8_0, oracle.Q4_K, oracle.Q6_K, oracle.FP8, oracle.Q5_K, oracle.Q3_K, oracle.Q2_K])
 def test_columns_match_full_product(fmt):
     n, k, m = 40, 512, 3
     packed, xb, _ = make(fmt, n, k, m, 34)

@@ -170,7 +170,7 @@ def test_fp32_and_bf16_sources_agree_on_bf16_values():
     assert np.array_equal(a, b)
 
 
-@pytest.mark.parametrize("fmt", [oracle.Q8_0, oracle.Q4_K, oracle.Q6_K, oracle.FP8])
+@pytest.mark.parametrize("fmt", [oracle.Q8_0, oracle.Q4_K, oracle.Q6_K, oracle.FP8, oracle.Q5_K, oracle.Q3_K, oracle.Q2_K])
 def test_gather_is_dequantize_of_the_listed_rows(fmt):
     V, D = 37, 512
     packed = oracle.quantize(fmt, inputs.bf16_bits(inputs.weights(V, D, 24)))
