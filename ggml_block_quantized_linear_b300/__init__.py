@@ -19,6 +19,9 @@ import threading
 QMM_Q8_0 = 8
 QMM_Q4_K = 4
 QMM_Q6_K = 6
+QMM_Q5_K = 5
+QMM_Q3_K = 3
+QMM_Q2_K = 2
 QMM_FP8_E4M3 = 80
 QMM_OUT_F32 = 0
 QMM_OUT_BF16 = 1
@@ -34,8 +37,10 @@ QMM_ERR_WORKSPACE = -5
 QMM_ERR_CUDA = -6
 QMM_ERR_DEVICE = -7
 
-FORMATS = {"q8_0": QMM_Q8_0, "q4_k": QMM_Q4_K, "q6_k": QMM_Q6_K, "fp8": QMM_FP8_E4M3}
-BLOCK = {QMM_Q8_0: (32, 34), QMM_Q4_K: (256, 144), QMM_Q6_K: (256, 210)}
+FORMATS = {"q8_0": QMM_Q8_0, "q4_k": QMM_Q4_K, "q6_k": QMM_Q6_K, "q5_k": QMM_Q5_K, "q3_k": QMM_Q3_K,
+           "q2_k": QMM_Q2_K, "fp8": QMM_FP8_E4M3}
+BLOCK = {QMM_Q8_0: (32, 34), QMM_Q4_K: (256, 144), QMM_Q6_K: (256, 210), QMM_Q5_K: (256, 176),
+         QMM_Q3_K: (256, 110), QMM_Q2_K: (256, 84)}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libqmm.so")

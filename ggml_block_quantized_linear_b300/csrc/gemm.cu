@@ -557,7 +557,7 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
                         uint32_t v[16];
                         uint32_t(&v0)[8] = *reinterpret_cast<uint32_t(*)[8]>(&v[0]);
                         uint32_t(&v1)[8] = *reinterpret_cast<uint32_t(*)[8]>(&v[8]);
-                        const int J = 2 * j + (kq >> 1), pc = 2 * (kq & 1);
+                        [[maybe_unused]] const int J = 2 * j + (kq >> 1), pc = 2 * (kq & 1);
                         if constexpr (kFmt == kFp8) {
                             deq16_fp8(prow, J, pc, v0);
                             deq16_fp8(prow, J, pc + 1, v1);

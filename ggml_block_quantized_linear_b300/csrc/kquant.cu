@@ -1,0 +1,418 @@
+// kquant.cu -- the K-quants Q5_K, Q3_K and Q2_K: ISQ, dequantization, the
+// linear layer and their rows of the embedding lookup.
+//
+// mistral.rs, "Quantization types": the table "Q*K family" lists q5k, q3k and
+// q2k at 5, 3 and 2 bits, and section "Numeric shorthands" resolves `--isq 5`,
+// `3` and `2` to Q5K, Q3K and Q2K on CUDA.  The byte layouts (GGUF-shaped)
+// and the quantizers are this library's reading, stated in include/qmm.h:
+//   Q5_K  176 bytes: d, dmin, 12 scale bytes (Q4_K's packing), qh[32], qs[128];
+//         affine, 8 sub-blocks of 32, 5-bit codes.
+//   Q3_K  110 bytes: hmask[32], qs[64], 12 bytes of sixteen 6-bit scale fields
+//         (each sc + 32), d; symmetric, 16 sub-blocks of 16, 3-bit codes c + 4.
+//   Q2_K  84 bytes: scales[16] (sc | mc << 4), qs[64], d, dmin; affine, 16
+//         sub-blocks of 16, 2-bit codes.
+// Every kernel gives lane l of a warp the weights 8l .. 8l + 7 of a
+// superblock.  The ISQ kernels take the plain definition's fp32 steps in its
+// order (IEEE division, round half away for the codes, binary16
+// round-to-nearest-even for the scales), so the bytes are bit-identical.
+// The linear layer is a CUDA-core kernel for every M: each weight is
+// dequantized exactly as the plain definition does (one fp32 rounding of
+// S q - Mn) and multiplied in fp32.  Q3_K and Q2_K superblocks are only 2- and
+// 4-byte aligned in a packed row, so no kernel here uses TMA boxes.
+#include "common.cuh"
+
+namespace qmm {
+
+constexpr int kKqThreads = 256;  // 8 warps
+
+__host__ __device__ constexpr int kq_bytes(int fmt) { return fmt == 5 ? 176 : fmt == 3 ? 110 : 84; }
+
+__device__ __forceinline__ float h2f_at(const uint8_t *p) {
+    return __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t *>(p)));
+}
+
+// ------------------------------------------------------------ decoding
+// The 6-bit scale / min codes of sub-block j of a Q4_K / Q5_K scale area.
+__device__ __forceinline__ void kq_scale_min_k4(const uint8_t *s12, int j, int &sc, int &mc) {
+    if (j < 4) {
+        sc = s12[j] & 63;
+        mc = s12[j + 4] & 63;
+    } else {
+        sc = (s12[j + 4] & 15) | ((s12[j - 4] >> 6) << 4);
+        mc = (s12[j + 4] >> 4) | ((s12[j] >> 6) << 4);
+    }
+}
+
+// Q3_K scale field j (0..15): low 4 bits in byte j mod 8 (high nibble for
+// j >= 8), high 2 bits at bit 2 (j div 4) of byte 8 + j mod 4.
+__device__ __forceinline__ int kq_q3_field(const uint8_t *s12, int j) {
+    return ((s12[j & 7] >> (j < 8 ? 0 : 4)) & 15) | (((s12[8 + (j & 3)] >> (2 * (j >> 2))) & 3) << 4);
+}
+
+// The 8 dequantized weights 8l .. 8l + 7 of superblock `blk` (lane l), each
+// the plain definition's fp32 value.
+template <int kFmt>
+__device__ __forceinline__ void kq_lane_values(const uint8_t *blk, int lane, float (&v)[8]) {
+    if constexpr (kFmt == 5) {
+        // sub-block j = l / 4, weights 8 (l % 4) + e of it
+        const int j = lane >> 2, o = 8 * (lane & 3);
+        int sc, mc;
+        kq_scale_min_k4(blk + 4, j, sc, mc);
+        const float S = h2f_at(blk) * (float)sc, Mn = h2f_at(blk + 2) * (float)mc;
+        const uint8_t *qs = blk + 48 + 32 * (j >> 1) + o;
+        const int nsh = 4 * (j & 1);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int q = ((qs[e] >> nsh) & 15) | (((blk[16 + o + e] >> j) & 1) << 4);
+            const float prod = S * (float)q;
+            v[e] = prod - Mn;
+        }
+    } else if constexpr (kFmt == 3) {
+        // weight w = 8l + e = 128 h + 32 s + l': h = l / 16, s = (l / 4) % 4,
+        // l' = 8 (l % 4) + e; sub-block l / 2
+        const int h = lane >> 4, s = (lane >> 2) & 3, o = 8 * (lane & 3);
+        const float S = h2f_at(blk + 108) * (float)(kq_q3_field(blk + 96, lane >> 1) - 32);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int q = ((blk[32 + 32 * h + o + e] >> (2 * s)) & 3) | (((blk[o + e] >> (4 * h + s)) & 1) << 2);
+            v[e] = S * (float)(q - 4);
+        }
+    } else {
+        const int h = lane >> 4, s = (lane >> 2) & 3, o = 8 * (lane & 3);
+        const uint8_t scb = blk[lane >> 1];
+        const float S = h2f_at(blk + 80) * (float)(scb & 15), Mn = h2f_at(blk + 82) * (float)(scb >> 4);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int q = (blk[16 + 32 * h + o + e] >> (2 * s)) & 3;
+            const float prod = S * (float)q;
+            v[e] = prod - Mn;
+        }
+    }
+}
+
+// ------------------------------------------------------------------- ISQ
+// One warp per superblock; lane l holds weights 8l .. 8l + 7.  Codes go to a
+// per-warp byte buffer, the block is assembled in shared memory and stored
+// as halfwords (every block size is even; a block is 2-byte aligned).
+template <int kFmt, bool kSrcF32>
+__global__ void __launch_bounds__(kKqThreads) qmm_quantize_kq_kernel(const void *__restrict__ src,
+                                                                     uint8_t *__restrict__ dst,
+                                                                     int64_t nblocks) {
+    constexpr int kB = kq_bytes(kFmt);
+    __shared__ uint8_t qbuf[kKqThreads / 32][256];
+    __shared__ __align__(4) uint8_t obuf[kKqThreads / 32][176];
+    __shared__ int scbuf[kKqThreads / 32][16], mcbuf[kKqThreads / 32][16];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint8_t *qw = qbuf[warp], *ow = obuf[warp];
+    int *scw = scbuf[warp], *mcw = mcbuf[warp];
+    for (int64_t b = (int64_t)blockIdx.x * (kKqThreads / 32) + warp; b < nblocks;
+         b += (int64_t)gridDim.x * (kKqThreads / 32)) {
+        float x[8];
+        if constexpr (kSrcF32) {
+            const float4 *p = reinterpret_cast<const float4 *>(static_cast<const float *>(src) + b * 256 + 8 * lane);
+            const float4 v0 = __ldg(p), v1 = __ldg(p + 1);
+            x[0] = v0.x; x[1] = v0.y; x[2] = v0.z; x[3] = v0.w;
+            x[4] = v1.x; x[5] = v1.y; x[6] = v1.z; x[7] = v1.w;
+        } else {
+            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(src) + b * 256) + lane);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                x[2 * e] = __uint_as_float(w[e] << 16);
+                x[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+            }
+        }
+        // lanes of one sub-block: 4 (Q5_K, 32 weights) or 2 (16 weights)
+        constexpr int kLanesPerSub = kFmt == 5 ? 4 : 2;
+        if constexpr (kFmt == 3) {
+            float amax = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[e]));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            const float sj = __fdiv_rn(amax, 3.0f);
+            float smax = sj;
+#pragma unroll
+            for (int o = 2; o < 32; o <<= 1) smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o));
+            const __half d16 = __float2half_rn(__fdiv_rn(smax, 31.0f));
+            const float df = __half2float(d16);
+            const int sc = df > 0.f ? (int)fminf(fmaxf(roundf(__fdiv_rn(sj, df)), 0.f), 31.f) : 0;
+            const float S = df * (float)sc;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int c = S > 0.f ? (int)fminf(fmaxf(roundf(__fdiv_rn(x[e], S)), -4.f), 3.f) : 0;
+                qw[8 * lane + e] = (uint8_t)(c + 4);
+            }
+            if ((lane & 1) == 0) scw[lane >> 1] = sc + 32;
+            if (lane == 0) *reinterpret_cast<uint16_t *>(ow + 108) = __half_as_ushort(d16);
+        } else {
+            constexpr float kLevels = kFmt == 5 ? 31.f : 3.f;
+            constexpr float kScaleCodes = kFmt == 5 ? 63.f : 15.f;
+            constexpr float kQMax = kFmt == 5 ? 31.f : 3.f;
+            float mx = x[0], mn = 0.f;  // max, and min(0, min)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                mx = fmaxf(mx, x[e]);
+                mn = fminf(mn, x[e]);
+            }
+#pragma unroll
+            for (int o = 1; o < kLanesPerSub; o <<= 1) {
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+            }
+            const float sj = __fdiv_rn(__fsub_rn(mx, mn), kLevels);
+            const float mj = __fsub_rn(0.f, mn);
+            float smax = sj, mmax = mj;
+#pragma unroll
+            for (int o = kLanesPerSub; o < 32; o <<= 1) {
+                smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o));
+                mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, o));
+            }
+            const __half d16 = __float2half_rn(__fdiv_rn(smax, kScaleCodes));
+            const __half m16 = __float2half_rn(__fdiv_rn(mmax, kScaleCodes));
+            const float df = __half2float(d16), dmf = __half2float(m16);
+            const int sc = df > 0.f ? (int)fminf(fmaxf(roundf(__fdiv_rn(sj, df)), 0.f), kScaleCodes) : 0;
+            const int mc = dmf > 0.f ? (int)fminf(fmaxf(roundf(__fdiv_rn(mj, dmf)), 0.f), kScaleCodes) : 0;
+            const float S = df * (float)sc, Mn = dmf * (float)mc;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int q = S > 0.f ? (int)fminf(fmaxf(roundf(__fdiv_rn(__fadd_rn(x[e], Mn), S)), 0.f), kQMax) : 0;
+                qw[8 * lane + e] = (uint8_t)q;
+            }
+            if (lane % kLanesPerSub == 0) {
+                scw[lane / kLanesPerSub] = sc;
+                mcw[lane / kLanesPerSub] = mc;
+            }
+            if (lane == 0) {
+                const int off = kFmt == 5 ? 0 : 80;
+                *reinterpret_cast<uint16_t *>(ow + off) = __half_as_ushort(d16);
+                *reinterpret_cast<uint16_t *>(ow + off + 2) = __half_as_ushort(m16);
+            }
+        }
+        __syncwarp();
+        if constexpr (kFmt == 5) {
+            if (lane < 4) {  // scale bytes j, j + 4, j + 8 (Q4_K's packing)
+                const int j = lane;
+                ow[4 + j] = (uint8_t)((scw[j] & 63) | ((scw[j + 4] >> 4) << 6));
+                ow[8 + j] = (uint8_t)((mcw[j] & 63) | ((mcw[j + 4] >> 4) << 6));
+                ow[12 + j] = (uint8_t)((scw[j + 4] & 15) | ((mcw[j + 4] & 15) << 4));
+            }
+            // qh byte l: bit j = bit 4 of weight l of sub-block j
+            uint32_t hb = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) hb |= (uint32_t)(qw[32 * j + lane] >> 4) << j;
+            ow[16 + lane] = (uint8_t)hb;
+            // qs bytes 4l .. 4l + 3: byte 32c + l' = sub-blocks 2c (low nibble), 2c + 1 (high)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int byte = 4 * lane + i, c = byte >> 5, l2 = byte & 31;
+                ow[48 + byte] = (uint8_t)((qw[64 * c + l2] & 15) | ((qw[64 * c + 32 + l2] & 15) << 4));
+            }
+        } else {
+            // low 2 bits: byte 32 h + l' holds weight 128 h + 32 s + l' at bit 2 s
+            const int lo_base = kFmt == 3 ? 32 : 16;
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int byte = 2 * lane + i, h = byte >> 5, l2 = byte & 31;
+                uint32_t v = 0;
+#pragma unroll
+                for (int s = 0; s < 4; ++s) v |= (uint32_t)(qw[128 * h + 32 * s + l2] & 3) << (2 * s);
+                ow[lo_base + byte] = (uint8_t)v;
+            }
+            if constexpr (kFmt == 3) {
+                // hmask byte l: bit 4 h + s = bit 2 of weight 128 h + 32 s + l
+                uint32_t hm = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) hm |= (uint32_t)(qw[32 * i + lane] >> 2) << i;
+                ow[lane] = (uint8_t)hm;
+                if (lane < 8) ow[96 + lane] = (uint8_t)((scw[lane] & 15) | ((scw[lane + 8] & 15) << 4));
+                if (lane < 4) {
+                    uint32_t v = 0;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) v |= (uint32_t)((scw[lane + 4 * k] >> 4) & 3) << (2 * k);
+                    ow[104 + lane] = (uint8_t)v;
+                }
+            } else {
+                if (lane < 16) ow[lane] = (uint8_t)(scw[lane] | (mcw[lane] << 4));
+            }
+        }
+        __syncwarp();
+        uint16_t *out = reinterpret_cast<uint16_t *>(dst + b * kB);
+        for (int i = lane; i < kB / 2; i += 32) out[i] = *reinterpret_cast<const uint16_t *>(ow + 2 * i);
+        __syncwarp();
+    }
+}
+
+// ---------------------------------------------------------- dequantization
+template <int kFmt>
+__global__ void __launch_bounds__(kKqThreads) qmm_dequantize_kq_kernel(const uint8_t *__restrict__ src,
+                                                                       float *__restrict__ dst, int64_t nblocks) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int64_t b = (int64_t)blockIdx.x * (kKqThreads / 32) + warp; b < nblocks;
+         b += (int64_t)gridDim.x * (kKqThreads / 32)) {
+        float v[8];
+        kq_lane_values<kFmt>(src + b * kq_bytes(kFmt), lane, v);
+        float4 *y = reinterpret_cast<float4 *>(dst + b * 256 + 8 * lane);
+        y[0] = make_float4(v[0], v[1], v[2], v[3]);
+        y[1] = make_float4(v[4], v[5], v[6], v[7]);
+    }
+}
+
+// ------------------------------------------------------------------ matmul
+// Y[M x N] = X[M x K] W^T.  A warp owns one weight row at a time; lane l takes
+// weights 8l .. 8l + 7 of each superblock, dequantized once per pass and
+// multiplied by up to kTok token rows; fp32 sums reduced across the warp.
+template <int kFmt, int kTok>
+__global__ void __launch_bounds__(kKqThreads) qmm_matmul_kq_kernel(const uint8_t *__restrict__ W,
+                                                                   const uint16_t *__restrict__ X,
+                                                                   float *__restrict__ Y, int M, int N, int K) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nsb = K / 256;
+    const int64_t row_bytes = (int64_t)nsb * kq_bytes(kFmt);
+    for (int64_t n = (int64_t)blockIdx.x * (kKqThreads / 32) + warp; n < N;
+         n += (int64_t)gridDim.x * (kKqThreads / 32)) {
+        const uint8_t *row = W + n * row_bytes;
+        for (int m0 = 0; m0 < M; m0 += kTok) {
+            const int mt = min(kTok, M - m0);
+            float acc[kTok];
+#pragma unroll
+            for (int t = 0; t < kTok; ++t) acc[t] = 0.f;
+            for (int sb = 0; sb < nsb; ++sb) {
+                float v[8];
+                kq_lane_values<kFmt>(row + (int64_t)sb * kq_bytes(kFmt), lane, v);
+#pragma unroll
+                for (int t = 0; t < kTok; ++t) {
+                    if (t < mt) {
+                        const uint4 xv =
+                            __ldg(reinterpret_cast<const uint4 *>(X + (int64_t)(m0 + t) * K + (int64_t)sb * 256 + 8 * lane));
+                        const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            acc[t] = fmaf(v[2 * e], __uint_as_float(w[e] << 16), acc[t]);
+                            acc[t] = fmaf(v[2 * e + 1], __uint_as_float(w[e] & 0xFFFF0000u), acc[t]);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < kTok; ++t) {
+                float s = acc[t];
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+                if (lane == 0 && t < mt) Y[(int64_t)(m0 + t) * N + n] = s;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------- embedding lookup
+// out[t][0 .. D) = the dequantized row ids[t]: one warp per (token, superblock).
+template <int kFmt, bool kBf16>
+__global__ void __launch_bounds__(kKqThreads) qmm_embedding_kq_kernel(const uint8_t *__restrict__ table,
+                                                                      const int64_t *__restrict__ ids,
+                                                                      void *__restrict__ out, int64_t T, int64_t V,
+                                                                      int64_t D) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t groups = D / 256;
+    const int64_t row_bytes = groups * kq_bytes(kFmt);
+    for (int64_t u = (int64_t)blockIdx.x * (kKqThreads / 32) + warp; u < T * groups;
+         u += (int64_t)gridDim.x * (kKqThreads / 32)) {
+        const int64_t t = u / groups, g = u - t * groups;
+        const int64_t id = __ldg(ids + t);
+        float v[8];
+        if (id < 0 || id >= V) {
+            if (lane == 0) record_error(kErrBadId);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = 0.f;
+        } else {
+            kq_lane_values<kFmt>(table + id * row_bytes + g * kq_bytes(kFmt), lane, v);
+        }
+        const int64_t base = t * D + g * 256 + 8 * lane;
+        if constexpr (kBf16) {
+            uint32_t p[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+                p[e] = *reinterpret_cast<const uint32_t *>(&h);
+            }
+            *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + base) = make_uint4(p[0], p[1], p[2], p[3]);
+        } else {
+            float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(out) + base);
+            o[0] = make_float4(v[0], v[1], v[2], v[3]);
+            o[1] = make_float4(v[4], v[5], v[6], v[7]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- launchers
+static int kq_grid(int64_t warps_of_work, int sms) {
+    const int64_t ctas = (warps_of_work + kKqThreads / 32 - 1) / (kKqThreads / 32);
+    const int64_t cap = (int64_t)sms * 8;
+    return (int)(ctas < 1 ? 1 : ctas < cap ? ctas : cap);
+}
+
+template <int kFmt>
+static cudaError_t kq_quantize_t(int src_f32, const void *src, void *dst, int64_t nblocks, int sms,
+                                 cudaStream_t stream) {
+    uint8_t *d = static_cast<uint8_t *>(dst);
+    if (src_f32)
+        qmm_quantize_kq_kernel<kFmt, true><<<kq_grid(nblocks, sms), kKqThreads, 0, stream>>>(src, d, nblocks);
+    else
+        qmm_quantize_kq_kernel<kFmt, false><<<kq_grid(nblocks, sms), kKqThreads, 0, stream>>>(src, d, nblocks);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_kq_quantize(int fmt, int src_f32, const void *src, void *dst, int64_t nweights, int sms,
+                               cudaStream_t stream) {
+    const int64_t nb = nweights / 256;
+    if (fmt == 5) return kq_quantize_t<5>(src_f32, src, dst, nb, sms, stream);
+    if (fmt == 3) return kq_quantize_t<3>(src_f32, src, dst, nb, sms, stream);
+    return kq_quantize_t<2>(src_f32, src, dst, nb, sms, stream);
+}
+
+cudaError_t launch_kq_dequantize(int fmt, const void *src, float *dst, int64_t nweights, int sms,
+                                 cudaStream_t stream) {
+    const int64_t nb = nweights / 256;
+    const uint8_t *s = static_cast<const uint8_t *>(src);
+    const int g = kq_grid(nb, sms);
+    if (fmt == 5) qmm_dequantize_kq_kernel<5><<<g, kKqThreads, 0, stream>>>(s, dst, nb);
+    else if (fmt == 3) qmm_dequantize_kq_kernel<3><<<g, kKqThreads, 0, stream>>>(s, dst, nb);
+    else qmm_dequantize_kq_kernel<2><<<g, kKqThreads, 0, stream>>>(s, dst, nb);
+    return cudaGetLastError();
+}
+
+template <int kFmt>
+static cudaError_t kq_matmul_t(const uint8_t *w, const uint16_t *X, float *Y, int M, int N, int K, int sms,
+                               cudaStream_t stream) {
+    const int g = kq_grid(N, sms);
+    if (M == 1) qmm_matmul_kq_kernel<kFmt, 1><<<g, kKqThreads, 0, stream>>>(w, X, Y, M, N, K);
+    else if (M <= 8) qmm_matmul_kq_kernel<kFmt, 8><<<g, kKqThreads, 0, stream>>>(w, X, Y, M, N, K);
+    else qmm_matmul_kq_kernel<kFmt, 16><<<g, kKqThreads, 0, stream>>>(w, X, Y, M, N, K);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_kq_matmul(int fmt, const void *W, const uint16_t *X, float *Y, int M, int N, int K, int sms,
+                             cudaStream_t stream) {
+    const uint8_t *w = static_cast<const uint8_t *>(W);
+    if (fmt == 5) return kq_matmul_t<5>(w, X, Y, M, N, K, sms, stream);
+    if (fmt == 3) return kq_matmul_t<3>(w, X, Y, M, N, K, sms, stream);
+    return kq_matmul_t<2>(w, X, Y, M, N, K, sms, stream);
+}
+
+template <int kFmt>
+static cudaError_t kq_embedding_t(const void *table, const int64_t *ids, void *out, int bf16, int64_t T, int64_t V,
+                                  int64_t D, int sms, cudaStream_t stream) {
+    const int g = kq_grid(T * (D / 256), sms);
+    const uint8_t *tb = static_cast<const uint8_t *>(table);
+    if (bf16) qmm_embedding_kq_kernel<kFmt, true><<<g, kKqThreads, 0, stream>>>(tb, ids, out, T, V, D);
+    else qmm_embedding_kq_kernel<kFmt, false><<<g, kKqThreads, 0, stream>>>(tb, ids, out, T, V, D);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_kq_embedding(int fmt, const void *table, const int64_t *ids, void *out, int bf16, int64_t T,
+                                int64_t V, int64_t D, int sms, cudaStream_t stream) {
+    if (fmt == 5) return kq_embedding_t<5>(table, ids, out, bf16, T, V, D, sms, stream);
+    if (fmt == 3) return kq_embedding_t<3>(table, ids, out, bf16, T, V, D, sms, stream);
+    return kq_embedding_t<2>(table, ids, out, bf16, T, V, D, sms, stream);
+}
+
+}  // namespace qmm

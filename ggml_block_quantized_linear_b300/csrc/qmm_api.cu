@@ -32,6 +32,14 @@ cudaError_t launch_fp8_quantize(int src_f32, const void *src, void *dst, int64_t
                                 cudaStream_t stream);
 cudaError_t launch_fp8_dequantize(const void *src, float *dst, int64_t rows, int64_t K, int sms,
                                   cudaStream_t stream);
+cudaError_t launch_kq_quantize(int fmt, int src_f32, const void *src, void *dst, int64_t nweights, int sms,
+                               cudaStream_t stream);
+cudaError_t launch_kq_dequantize(int fmt, const void *src, float *dst, int64_t nweights, int sms,
+                                 cudaStream_t stream);
+cudaError_t launch_kq_matmul(int fmt, const void *W, const uint16_t *X, float *Y, int M, int N, int K, int sms,
+                             cudaStream_t stream);
+cudaError_t launch_kq_embedding(int fmt, const void *table, const int64_t *ids, void *out, int bf16, int64_t T,
+                                int64_t V, int64_t D, int sms, cudaStream_t stream);
 
 constexpr int kMaxDecodeM = 16;
 // Largest dimension accepted (keeps every 32-bit index in the kernels exact).
@@ -77,10 +85,22 @@ static bool use_rows_kernel(int M, int N, int K, int sms) {
 
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 static bool known_fmt(qmm_format f) {
-    return f == QMM_Q8_0 || f == QMM_Q4_K || f == QMM_Q6_K || f == QMM_FP8_E4M3;
+    return f == QMM_Q8_0 || f == QMM_Q4_K || f == QMM_Q6_K || f == QMM_FP8_E4M3 || f == QMM_Q5_K || f == QMM_Q3_K ||
+           f == QMM_Q2_K;
 }
+// Q5_K / Q3_K / Q2_K: the CUDA-core kernels of kquant.cu
+static bool is_kq(qmm_format f) { return f == QMM_Q5_K || f == QMM_Q3_K || f == QMM_Q2_K; }
 static int64_t block_weights(qmm_format f) { return f == QMM_Q8_0 ? kQ8Weights : 256; }
-static int64_t block_bytes(qmm_format f) { return f == QMM_Q8_0 ? kQ8Bytes : f == QMM_Q4_K ? kQ4Bytes : 210; }
+static int64_t block_bytes(qmm_format f) {
+    switch (f) {
+    case QMM_Q8_0: return kQ8Bytes;
+    case QMM_Q4_K: return kQ4Bytes;
+    case QMM_Q5_K: return 176;
+    case QMM_Q3_K: return 110;
+    case QMM_Q2_K: return 84;
+    default: return 210;  // Q6_K
+    }
+}
 
 static qmm_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA; }
 
@@ -135,6 +155,9 @@ qmm_status qmm_quantize(qmm_format fmt, qmm_src_dtype st, const void *src, void 
     if (fmt == QMM_FP8_E4M3)
         return from_cuda(launch_fp8_quantize(st == QMM_SRC_F32, src, dst_packed, rows, cols, sm_count(),
                                              reinterpret_cast<cudaStream_t>(stream)));
+    if (is_kq(fmt))
+        return from_cuda(launch_kq_quantize((int)fmt, st == QMM_SRC_F32, src, dst_packed, rows * cols, sm_count(),
+                                            reinterpret_cast<cudaStream_t>(stream)));
     return from_cuda(launch_quantize((int)fmt, st == QMM_SRC_F32, src, dst_packed, rows * cols,
                                      sm_count(), reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -153,12 +176,15 @@ qmm_status qmm_dequantize(qmm_format fmt, const void *src_packed, float *dst, in
     if (fmt == QMM_FP8_E4M3)
         return from_cuda(launch_fp8_dequantize(src_packed, dst, rows, cols, sm_count(),
                                                reinterpret_cast<cudaStream_t>(stream)));
+    if (is_kq(fmt))
+        return from_cuda(launch_kq_dequantize((int)fmt, src_packed, dst, rows * cols, sm_count(),
+                                              reinterpret_cast<cudaStream_t>(stream)));
     return from_cuda(launch_dequantize((int)fmt, src_packed, dst, rows * cols, sm_count(),
                                        reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t qmm_matmul_workspace_bytes(qmm_format fmt, int64_t M, int64_t N, int64_t K) {
-    if (!known_fmt(fmt) || fmt == QMM_Q6_K || M <= kMaxDecodeM || N <= 0 || K <= 0 || M > kMaxDim ||
+    if (!known_fmt(fmt) || fmt == QMM_Q6_K || is_kq(fmt) || M <= kMaxDecodeM || N <= 0 || K <= 0 || M > kMaxDim ||
         N > kMaxDim || K > kMaxDim || K % kGroup != 0)
         return 0;
     return gemm_workspace_bytes((int)fmt, (int)M, (int)N, (int)K, sm_count());
@@ -177,6 +203,8 @@ qmm_status qmm_matmul(qmm_format fmt, const void *W_packed, const uint16_t *X_bf
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (fmt == QMM_Q6_K)
         return from_cuda(launch_q6k_matmul(W_packed, X_bf16, Y, (int)M, (int)N, (int)K, sm_count(), s));
+    if (is_kq(fmt))
+        return from_cuda(launch_kq_matmul((int)fmt, W_packed, X_bf16, Y, (int)M, (int)N, (int)K, sm_count(), s));
     if (M <= kMaxDecodeM) {
         // FP8 has only the row-tile decode kernel
         if (fmt == QMM_FP8_E4M3 || use_rows_kernel((int)M, (int)N, (int)K, sm_count()))
@@ -226,6 +254,9 @@ qmm_status qmm_embedding(qmm_format fmt, const void *table_packed, const int64_t
     if (V == 0 || table_packed == nullptr || ids == nullptr || out == nullptr) return QMM_ERR_INVALID_ARG;
     if (!aligned16(table_packed) || !aligned16(out) || (reinterpret_cast<uintptr_t>(ids) & 7u) != 0)
         return QMM_ERR_ALIGNMENT;
+    if (is_kq(fmt))
+        return from_cuda(launch_kq_embedding((int)fmt, table_packed, ids, out, out_dtype == QMM_OUT_BF16, T, V, D,
+                                             sm_count(), reinterpret_cast<cudaStream_t>(stream)));
     return from_cuda(launch_embedding((int)fmt, table_packed, ids, out, out_dtype == QMM_OUT_BF16, T, V, D,
                                       sm_count(), reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -233,8 +264,8 @@ qmm_status qmm_embedding(qmm_format fmt, const void *table_packed, const int64_t
 qmm_format qmm_embedding_format(qmm_format model_fmt) {
     // "Sensitive tensor precision": Q2K-Q4K models keep their embeddings and
     // output head in Q6K, Q5K / Q6K / Q8_0 models in Q8_0
-    if (model_fmt == QMM_Q4_K) return QMM_Q6_K;
-    if (model_fmt == QMM_Q6_K || model_fmt == QMM_Q8_0) return QMM_Q8_0;
+    if (model_fmt == QMM_Q2_K || model_fmt == QMM_Q3_K || model_fmt == QMM_Q4_K) return QMM_Q6_K;
+    if (model_fmt == QMM_Q5_K || model_fmt == QMM_Q6_K || model_fmt == QMM_Q8_0) return QMM_Q8_0;
     return (qmm_format)0;
 }
 
@@ -244,6 +275,6 @@ qmm_status qmm_selftest_bounded_wait(int64_t limit_ns, qmm_stream_t stream) {
     return from_cuda(cudaGetLastError());
 }
 
-const char *qmm_version(void) { return "qmm 0.2.0 sm_103a"; }
+const char *qmm_version(void) { return "qmm 0.3.0 sm_103a"; }
 
 }  // extern "C"

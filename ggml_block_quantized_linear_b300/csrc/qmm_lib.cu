@@ -7,4 +7,5 @@
 #include "gemm.cu"
 #include "q6k.cu"
 #include "fp8.cu"
+#include "kquant.cu"
 #include "static_scratch.cu"

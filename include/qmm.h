@@ -47,6 +47,30 @@
  *         byte 64h + 32(s & 1) + l (high nibble when s >= 2) and its high
  *         bits in bits 2s, 2s+1 of qh byte 32h + l.  Superblocks are only
  *         2-byte aligned inside a packed row.
+ *   Q5_K  256 weights -> 176 bytes: Q4_K's quantizer with 5-bit codes
+ *         (s_j = (max - min(0, min)) / 31, q in 0..31).  Bytes 0-1 d, 2-3
+ *         dmin, 4-15 the scale bytes (Q4_K's packing), 16-47 qh, 48-175 qs:
+ *         byte 48+32c+l holds the low 4 bits of weight l of sub-block 2c
+ *         (low nibble) and 2c+1 (high nibble); bit j of qh byte 16+l is bit 4
+ *         of weight l of sub-block j.  Value (d*sc_j) * q - dmin*mc_j.
+ *   Q3_K  256 weights -> 110 bytes, 16 sub-blocks of 16, symmetric:
+ *         s_j = max|x| / 3; d = fp16(max_j s_j / 31); sc_j = round(s_j / d)
+ *         in 0..31; c = clamp(round(x / (d*sc_j)), -4, 3), q = c + 4.  Bytes
+ *         0-31 hmask, 32-95 qs, 96-107 sixteen 6-bit fields sc_j + 32 (low 4
+ *         bits of field j in byte j mod 8, high nibble for j >= 8; high 2 bits
+ *         at bit 2 (j div 4) of byte 8 + j mod 4), 108-109 d.  Weight w =
+ *         128h + 32s + l: bits 0-1 of q at bit 2s of qs byte 32h + l, bit 2 at
+ *         bit 4h + s of hmask byte l.  Value (d*sc_j) * c (exact).
+ *   Q2_K  256 weights -> 84 bytes, 16 sub-blocks of 16, affine: s_j =
+ *         (max - min(0, min)) / 3, m_j = -min(0, min); d, dmin = fp16(max_j
+ *         s_j / 15), fp16(max_j m_j / 15); sc_j, mc_j in 0..15; q in 0..3.
+ *         Bytes 0-15 scales (sc_j | mc_j << 4), 16-79 qs (weight w = 128h +
+ *         32s + l at bit 2s of byte 16 + 32h + l), 80-81 d, 82-83 dmin.  Value
+ *         (d*sc_j) * q - dmin*mc_j.
+ *   Q5_K / Q3_K / Q2_K are the page's q5k / q3k / q2k (table "Q*K family";
+ *         `--isq 5 / 3 / 2` on CUDA).  Their superblocks are only 2- or 4-byte
+ *         aligned inside a row (Q3_K, Q2_K), and the library serves them with
+ *         CUDA-core kernels (see qmm_matmul).
  *   FP8_E4M3  (W8A16; the page's section "FP8": E4M3 produced by ISQ,
  *         symmetric weights with channel scales): one fp32 scale per row,
  *         s = max|x| / 448; code = E4M3(x / s), round to nearest even,
@@ -55,9 +79,9 @@
  *         A packed row is the K codes, s (fp32), 12 zero bytes: K + 16.
  *
  * A packed matrix is row-major in blocks: row n holds cols/32 Q8_0 blocks
- * (cols/32*34 bytes), cols/256 Q4_K superblocks (cols/256*144 bytes),
- * cols/256 Q6_K superblocks (cols/256*210 bytes) or the FP8 codes and row
- * scale (cols + 16 bytes), rows back to back.
+ * (cols/32*34 bytes), cols/256 K-quant superblocks (cols/256 * 144 / 210 /
+ * 176 / 110 / 84 bytes for Q4_K / Q6_K / Q5_K / Q3_K / Q2_K) or the FP8 codes
+ * and row scale (cols + 16 bytes), rows back to back.
  *
  * Conventions for every call:
  *  - Pointers are DEVICE pointers owned by the caller.  The library allocates
@@ -97,10 +121,18 @@ extern "C" {
 struct CUstream_st;
 typedef struct CUstream_st *qmm_stream_t;
 
-/* Block formats; the values mirror the ISQ shorthands `--isq 8` / `--isq 4`
- * / `--isq 6` (mistral.rs "Quantization types", section "Numeric
- * shorthands"). */
-typedef enum { QMM_Q8_0 = 8, QMM_Q4_K = 4, QMM_Q6_K = 6, QMM_FP8_E4M3 = 80 } qmm_format;
+/* Block formats; the values mirror the ISQ shorthands `--isq 8 / 6 / 5 / 4 /
+ * 3 / 2` (mistral.rs "Quantization types", section "Numeric shorthands":
+ * Q8_0, Q6K, Q5K, Q4K, Q3K, Q2K on CUDA). */
+typedef enum {
+    QMM_Q8_0 = 8,
+    QMM_Q4_K = 4,
+    QMM_Q6_K = 6,
+    QMM_Q5_K = 5,
+    QMM_Q3_K = 3,
+    QMM_Q2_K = 2,
+    QMM_FP8_E4M3 = 80
+} qmm_format;
 
 /* Element type of an embedding lookup's output. */
 typedef enum { QMM_OUT_F32 = 0, QMM_OUT_BF16 = 1 } qmm_out_dtype;
@@ -157,8 +189,8 @@ QMM_API qmm_status qmm_embedding(qmm_format fmt, const void *table_packed, const
 
 /* The format the page's section "Sensitive tensor precision" gives the token
  * embeddings and output head of a model quantized to model_fmt: QMM_Q6_K for
- * a Q4_K model, QMM_Q8_0 for Q6_K and Q8_0 models; 0 for an unknown format.
- * Host only. */
+ * Q2_K, Q3_K and Q4_K models, QMM_Q8_0 for Q5_K, Q6_K and Q8_0 models; 0 for
+ * any other format.  Host only. */
 QMM_API qmm_format qmm_embedding_format(qmm_format model_fmt);
 
 /* Workspace qmm_matmul needs for this problem, in bytes (0 = none; then
@@ -181,7 +213,10 @@ QMM_API size_t qmm_matmul_workspace_bytes(qmm_format fmt, int64_t M, int64_t N, 
  * to binary16 inside the GEMM, the row scale applied in the epilogue).
  * Q6_K (output heads) runs a CUDA-core kernel for every M: a warp per
  * weight row, exact integer codes times the activations, the sub-block
- * scale applied per superblock, fp32 sums.  For Q8_0 / Q4_K, larger M runs
+ * scale applied per superblock, fp32 sums.  Q5_K, Q3_K and Q2_K run a
+ * CUDA-core kernel for every M too: a warp per weight row, each weight
+ * dequantized exactly (one fp32 rounding, as qmm_dequantize gives it) and
+ * multiplied in fp32.  For Q8_0 / Q4_K, larger M runs
  * the tiled kernel (tcgen05 tensor cores, TMEM accumulators):
  * token tiles of 32, 64, 128 or 256 (the smallest of 32 / 64 / 128 that holds
  * M, else 256); when the output tiles are fewer than the SMs, K is split into

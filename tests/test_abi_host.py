@@ -62,7 +62,7 @@ S0 = ctypes.c_void_p(0)
 
 def test_quantize_argument_errors(lib):
     L = lib
-    assert L.qmm_quantize(5, 0, FAKE, FAKE, 4, 256, S0) == q.QMM_ERR_INVALID_ARG
+    assert L.qmm_quantize(7, 0, FAKE, FAKE, 4, 256, S0) == q.QMM_ERR_INVALID_ARG
     assert L.qmm_quantize(8, 3, FAKE, FAKE, 4, 256, S0) == q.QMM_ERR_INVALID_ARG
     assert L.qmm_quantize(8, 0, FAKE, FAKE, -1, 256, S0) == q.QMM_ERR_INVALID_ARG
     assert L.qmm_quantize(8, 0, FAKE, FAKE, 4, 0, S0) == q.QMM_ERR_SHAPE
@@ -77,7 +77,7 @@ def test_quantize_argument_errors(lib):
 
 def test_dequantize_argument_errors(lib):
     L = lib
-    assert L.qmm_dequantize(3, FAKE, FAKE, 4, 256, S0) == q.QMM_ERR_INVALID_ARG
+    assert L.qmm_dequantize(7, FAKE, FAKE, 4, 256, S0) == q.QMM_ERR_INVALID_ARG
     assert L.qmm_dequantize(8, FAKE, FAKE, 4, 100, S0) == q.QMM_ERR_SHAPE
     assert L.qmm_dequantize(8, NULL, FAKE, 4, 256, S0) == q.QMM_ERR_INVALID_ARG
     assert L.qmm_dequantize(4, FAKE, MISALIGNED, 4, 256, S0) == q.QMM_ERR_ALIGNMENT
@@ -128,10 +128,28 @@ def test_q6_k_sizes_and_policy(lib):
     assert q.qmm_matmul_workspace_bytes(q.QMM_Q6_K, 512, 4096, 4096) == 0
     # the pages' sensitive-tensor table, read from the golden file
     g = json.load(open(os.path.join(ROOT, "tests", "golden", "paper_widths.json")))
-    names = {"Q4K": q.QMM_Q4_K, "Q6K": q.QMM_Q6_K, "Q8_0": q.QMM_Q8_0}
+    names = {"Q2K": q.QMM_Q2_K, "Q3K": q.QMM_Q3_K, "Q4K": q.QMM_Q4_K, "Q5K": q.QMM_Q5_K, "Q6K": q.QMM_Q6_K,
+             "Q8_0": q.QMM_Q8_0}
     for model, emb in g["sensitive_tensor_type"].items():
         assert q.qmm_embedding_format(names[model]) == names[emb]
     assert q.qmm_embedding_format(7) == 0
+    assert q.qmm_embedding_format(q.QMM_FP8_E4M3) == 0
+
+
+def test_k_quant_sizes(lib):
+    # Q5_K 176, Q3_K 110, Q2_K 84 bytes per 256 weights; no workspace; the
+    # static prefill entry leaves them to qmm_matmul
+    L = lib
+    for fmt, nb in ((q.QMM_Q5_K, 176), (q.QMM_Q3_K, 110), (q.QMM_Q2_K, 84)):
+        assert q.qmm_packed_bytes(fmt, 4096, 4096) == 4096 * 16 * nb
+        assert q.qmm_packed_bytes(fmt, 3, 768) == 3 * 3 * nb
+        assert q.qmm_packed_bytes(fmt, 1, 256 + 32) == 0
+        assert q.qmm_matmul_workspace_bytes(fmt, 512, 4096, 4096) == 0
+        assert L.qmm_quantize(fmt, 0, FAKE, FAKE, 4, 200, S0) == q.QMM_ERR_SHAPE
+        assert L.qmm_quantize(fmt, 0, MISALIGNED, FAKE, 4, 256, S0) == q.QMM_ERR_ALIGNMENT
+        assert L.qmm_dequantize(fmt, NULL, FAKE, 4, 256, S0) == q.QMM_ERR_INVALID_ARG
+        assert L.qmm_matmul(fmt, FAKE, FAKE, NULL, 1, 64, 256, NULL, 0, S0) == q.QMM_ERR_INVALID_ARG
+        assert L.qmm_matmul_prefill_static(fmt, FAKE, FAKE, FAKE, 512, 64, 256, S0) == q.QMM_ERR_UNSUPPORTED
 
 
 def test_fp8_sizes(lib):
@@ -145,7 +163,7 @@ def test_embedding_argument_errors(lib):
     L = lib
     ids8 = ctypes.c_void_p(0x1000)
     ids_mis = ctypes.c_void_p(0x1004)
-    assert L.qmm_embedding(5, FAKE, ids8, 4, 10, 256, FAKE, 0, S0) == q.QMM_ERR_INVALID_ARG
+    assert L.qmm_embedding(7, FAKE, ids8, 4, 10, 256, FAKE, 0, S0) == q.QMM_ERR_INVALID_ARG
     assert L.qmm_embedding(8, FAKE, ids8, 4, 10, 256, FAKE, 2, S0) == q.QMM_ERR_INVALID_ARG
     assert L.qmm_embedding(8, FAKE, ids8, -1, 10, 256, FAKE, 0, S0) == q.QMM_ERR_INVALID_ARG
     assert L.qmm_embedding(8, FAKE, ids8, 4, 10, 300, FAKE, 0, S0) == q.QMM_ERR_SHAPE
