@@ -49,45 +49,113 @@ __device__ __forceinline__ int kq_q3_field(const uint8_t *s12, int j) {
     return ((s12[j & 7] >> (j < 8 ? 0 : 4)) & 15) | (((s12[8 + (j & 3)] >> (2 * (j >> 2))) & 3) << 4);
 }
 
-// The 8 dequantized weights 8l .. 8l + 7 of superblock `blk` (lane l), each
-// the plain definition's fp32 value.
+// The bytes lane l needs from a superblock for its weights 8l .. 8l + 7,
+// loaded with the widest loads the superblock's alignment allows (Q5_K 16,
+// Q2_K 4, Q3_K 2 bytes): first all loads, then the decoding, so that a
+// caller can put several superblocks' loads in flight before using any.
+struct KqRaw {
+    uint32_t a0, a1;  // Q5_K qs / Q3_K qs / Q2_K qs: the lane's 8 code bytes
+    uint32_t b0, b1;  // Q5_K qh / Q3_K hmask: the lane's 8 high-bit bytes
+    uint32_t s0, s1;  // scale words (see kq_lane_decode)
+};
+
+// 8 bytes at a 2-byte aligned address, as two words.
+__device__ __forceinline__ void kq_ld8_a2(const uint8_t *p, uint32_t &w0, uint32_t &w1) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    const uint32_t *w = reinterpret_cast<const uint32_t *>(a & ~(uintptr_t)3);
+    const uint32_t x0 = __ldg(w), x1 = __ldg(w + 1);
+    if ((a & 3) == 0) {
+        w0 = x0;
+        w1 = x1;
+    } else {
+        const uint32_t x2 = __ldg(w + 2);
+        w0 = __funnelshift_r(x0, x1, 16);
+        w1 = __funnelshift_r(x1, x2, 16);
+    }
+}
+
 template <int kFmt>
-__device__ __forceinline__ void kq_lane_values(const uint8_t *blk, int lane, float (&v)[8]) {
+__device__ __forceinline__ KqRaw kq_lane_load(const uint8_t *blk, int lane) {
+    KqRaw r;
+    const int h = lane >> 4, o = 8 * (lane & 3);
     if constexpr (kFmt == 5) {
-        // sub-block j = l / 4, weights 8 (l % 4) + e of it
-        const int j = lane >> 2, o = 8 * (lane & 3);
-        int sc, mc;
-        kq_scale_min_k4(blk + 4, j, sc, mc);
-        const float S = h2f_at(blk) * (float)sc, Mn = h2f_at(blk + 2) * (float)mc;
-        const uint8_t *qs = blk + 48 + 32 * (j >> 1) + o;
-        const int nsh = 4 * (j & 1);
+        const int j = lane >> 2;
+        const uint2 qs = __ldg(reinterpret_cast<const uint2 *>(blk + 48 + 32 * (j >> 1) + o));
+        const uint2 qh = __ldg(reinterpret_cast<const uint2 *>(blk + 16 + o));
+        const uint4 hd = __ldg(reinterpret_cast<const uint4 *>(blk));  // d, dmin, 12 scale bytes
+        r.a0 = qs.x; r.a1 = qs.y; r.b0 = qh.x; r.b1 = qh.y;
+        // Q4_K's scale packing: scale bytes 0-3 = hd.y, 4-7 = hd.z, 8-11 = hd.w
+        const uint32_t k = 8u * (uint32_t)(j & 3);
+        const uint32_t by = (hd.y >> k) & 0xFFu, bz = (hd.z >> k) & 0xFFu, bw = (hd.w >> k) & 0xFFu;
+        const uint32_t sc = j < 4 ? (by & 63u) : ((bw & 15u) | ((by >> 6) << 4));
+        const uint32_t mc = j < 4 ? (bz & 63u) : ((bw >> 4) | ((bz >> 6) << 4));
+        r.s0 = hd.x;  // d | dmin << 16
+        r.s1 = sc | (mc << 8);
+    } else if constexpr (kFmt == 3) {
+        kq_ld8_a2(blk + 32 + 32 * h + o, r.a0, r.a1);
+        kq_ld8_a2(blk + o, r.b0, r.b1);
+        const int j = lane >> 1;
+        r.s0 = (uint32_t)kq_q3_field(blk + 96, j);
+        r.s1 = (uint32_t)(*reinterpret_cast<const uint16_t *>(blk + 108));
+    } else {
+        const uint32_t *qs = reinterpret_cast<const uint32_t *>(blk + 16 + 32 * h + o);
+        r.a0 = __ldg(qs);
+        r.a1 = __ldg(qs + 1);
+        r.b0 = r.b1 = 0;
+        r.s0 = blk[lane >> 1];
+        r.s1 = __ldg(reinterpret_cast<const uint32_t *>(blk + 80));  // d | dmin << 16
+    }
+    return r;
+}
+
+// byte e of a word, exactly as a float (2^23 + b - 2^23)
+__device__ __forceinline__ float kq_byte_f(uint32_t w, int e) {
+    return __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7440u + e)) - 8388608.0f;
+}
+
+// The 8 dequantized weights of lane l, each the plain definition's fp32
+// value: Q5_K / Q2_K (d*sc) * q - dmin*mc, Q3_K (d*sc) * (q - 4).
+template <int kFmt>
+__device__ __forceinline__ void kq_lane_decode(const KqRaw &r, int lane, float (&v)[8]) {
+    const int s = (lane >> 2) & 3, h = lane >> 4;
+    if constexpr (kFmt == 5) {
+        const int j = lane >> 2, nsh = 4 * (j & 1);
+        const float S = __half2float(__ushort_as_half((unsigned short)(r.s0 & 0xFFFF))) * (float)(r.s1 & 0xFF);
+        const float Mn = __half2float(__ushort_as_half((unsigned short)(r.s0 >> 16))) * (float)(r.s1 >> 8);
+        const uint32_t q0 = ((r.a0 >> nsh) & 0x0F0F0F0Fu) | (((r.b0 >> j) & 0x01010101u) << 4);
+        const uint32_t q1 = ((r.a1 >> nsh) & 0x0F0F0F0Fu) | (((r.b1 >> j) & 0x01010101u) << 4);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int q = ((qs[e] >> nsh) & 15) | (((blk[16 + o + e] >> j) & 1) << 4);
-            const float prod = S * (float)q;
-            v[e] = prod - Mn;
+        for (int e = 0; e < 4; ++e) {
+            const float p0 = S * kq_byte_f(q0, e), p1 = S * kq_byte_f(q1, e);
+            v[e] = p0 - Mn;
+            v[4 + e] = p1 - Mn;
         }
     } else if constexpr (kFmt == 3) {
-        // weight w = 8l + e = 128 h + 32 s + l': h = l / 16, s = (l / 4) % 4,
-        // l' = 8 (l % 4) + e; sub-block l / 2
-        const int h = lane >> 4, s = (lane >> 2) & 3, o = 8 * (lane & 3);
-        const float S = h2f_at(blk + 108) * (float)(kq_q3_field(blk + 96, lane >> 1) - 32);
+        const float S = __half2float(__ushort_as_half((unsigned short)r.s1)) * (float)((int)r.s0 - 32);
+        const int hb = 4 * h + s;
+        const uint32_t q0 = ((r.a0 >> (2 * s)) & 0x03030303u) | (((r.b0 >> hb) & 0x01010101u) << 2);
+        const uint32_t q1 = ((r.a1 >> (2 * s)) & 0x03030303u) | (((r.b1 >> hb) & 0x01010101u) << 2);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int q = ((blk[32 + 32 * h + o + e] >> (2 * s)) & 3) | (((blk[o + e] >> (4 * h + s)) & 1) << 2);
-            v[e] = S * (float)(q - 4);
+        for (int e = 0; e < 4; ++e) {
+            v[e] = S * (kq_byte_f(q0, e) - 4.0f);
+            v[4 + e] = S * (kq_byte_f(q1, e) - 4.0f);
         }
     } else {
-        const int h = lane >> 4, s = (lane >> 2) & 3, o = 8 * (lane & 3);
-        const uint8_t scb = blk[lane >> 1];
-        const float S = h2f_at(blk + 80) * (float)(scb & 15), Mn = h2f_at(blk + 82) * (float)(scb >> 4);
+        const float S = __half2float(__ushort_as_half((unsigned short)(r.s1 & 0xFFFF))) * (float)(r.s0 & 15);
+        const float Mn = __half2float(__ushort_as_half((unsigned short)(r.s1 >> 16))) * (float)(r.s0 >> 4);
+        const uint32_t q0 = (r.a0 >> (2 * s)) & 0x03030303u, q1 = (r.a1 >> (2 * s)) & 0x03030303u;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int q = (blk[16 + 32 * h + o + e] >> (2 * s)) & 3;
-            const float prod = S * (float)q;
-            v[e] = prod - Mn;
+        for (int e = 0; e < 4; ++e) {
+            const float p0 = S * kq_byte_f(q0, e), p1 = S * kq_byte_f(q1, e);
+            v[e] = p0 - Mn;
+            v[4 + e] = p1 - Mn;
         }
     }
+}
+
+template <int kFmt>
+__device__ __forceinline__ void kq_lane_values(const uint8_t *blk, int lane, float (&v)[8]) {
+    kq_lane_decode<kFmt>(kq_lane_load<kFmt>(blk, lane), lane, v);
 }
 
 // ------------------------------------------------------------------- ISQ
@@ -262,7 +330,7 @@ __global__ void __launch_bounds__(kKqThreads) qmm_dequantize_kq_kernel(const uin
 // weights 8l .. 8l + 7 of each superblock, dequantized once per pass and
 // multiplied by up to kTok token rows; fp32 sums reduced across the warp.
 template <int kFmt, int kTok>
-__global__ void __launch_bounds__(kKqThreads) qmm_matmul_kq_kernel(const uint8_t *__restrict__ W,
+__global__ void __launch_bounds__(kKqThreads, kTok == 1 ? 3 : 2) qmm_matmul_kq_kernel(const uint8_t *__restrict__ W,
                                                                    const uint16_t *__restrict__ X,
                                                                    float *__restrict__ Y, int M, int N, int K) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -276,19 +344,29 @@ __global__ void __launch_bounds__(kKqThreads) qmm_matmul_kq_kernel(const uint8_t
             float acc[kTok];
 #pragma unroll
             for (int t = 0; t < kTok; ++t) acc[t] = 0.f;
-            for (int sb = 0; sb < nsb; ++sb) {
-                float v[8];
-                kq_lane_values<kFmt>(row + (int64_t)sb * kq_bytes(kFmt), lane, v);
+            // superblocks whose loads are in flight together
+            constexpr int kU = 4;
+            for (int sb0 = 0; sb0 < nsb; sb0 += kU) {
+                KqRaw raw[kU];
 #pragma unroll
-                for (int t = 0; t < kTok; ++t) {
-                    if (t < mt) {
-                        const uint4 xv =
-                            __ldg(reinterpret_cast<const uint4 *>(X + (int64_t)(m0 + t) * K + (int64_t)sb * 256 + 8 * lane));
-                        const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
+                for (int u = 0; u < kU; ++u)
+                    if (sb0 + u < nsb) raw[u] = kq_lane_load<kFmt>(row + (int64_t)(sb0 + u) * kq_bytes(kFmt), lane);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            acc[t] = fmaf(v[2 * e], __uint_as_float(w[e] << 16), acc[t]);
-                            acc[t] = fmaf(v[2 * e + 1], __uint_as_float(w[e] & 0xFFFF0000u), acc[t]);
+                for (int u = 0; u < kU; ++u) {
+                    if (sb0 + u >= nsb) break;
+                    float v[8];
+                    kq_lane_decode<kFmt>(raw[u], lane, v);
+#pragma unroll
+                    for (int t = 0; t < kTok; ++t) {
+                        if (t < mt) {
+                            const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(X + (int64_t)(m0 + t) * K +
+                                                                                   (int64_t)(sb0 + u) * 256 + 8 * lane));
+                            const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                acc[t] = fmaf(v[2 * e], __uint_as_float(w[e] << 16), acc[t]);
+                                acc[t] = fmaf(v[2 * e + 1], __uint_as_float(w[e] & 0xFFFF0000u), acc[t]);
+                            }
                         }
                     }
                 }
@@ -384,9 +462,10 @@ template <int kFmt>
 static cudaError_t kq_matmul_t(const uint8_t *w, const uint16_t *X, float *Y, int M, int N, int K, int sms,
                                cudaStream_t stream) {
     const int g = kq_grid(N, sms);
+    // more tokens run in further passes of 8 over the row (its bytes then
+    // come from L1 / L2): 16 token rows per pass cost registers and occupancy
     if (M == 1) qmm_matmul_kq_kernel<kFmt, 1><<<g, kKqThreads, 0, stream>>>(w, X, Y, M, N, K);
-    else if (M <= 8) qmm_matmul_kq_kernel<kFmt, 8><<<g, kKqThreads, 0, stream>>>(w, X, Y, M, N, K);
-    else qmm_matmul_kq_kernel<kFmt, 16><<<g, kKqThreads, 0, stream>>>(w, X, Y, M, N, K);
+    else qmm_matmul_kq_kernel<kFmt, 8><<<g, kKqThreads, 0, stream>>>(w, X, Y, M, N, K);
     return cudaGetLastError();
 }
 
