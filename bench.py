@@ -1,5 +1,6 @@
 #!/usr/bin/env python3
-"""Benchmark of the B300 GGML block-quantized linear layer (Q8_0, Q4_K).
+"""Benchmark of the B300 GGML block-quantized linear layer (Q8_0, Q4_K and
+the other block types).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -23,6 +24,8 @@ each stage captured as a CUDA graph and replayed back to back:
   gemm      prefill GEMM, M = 512 and 2048, 3 shapes x 2 formats
   fp8       FP8 E4M3 (row scales, W8A16) ISQ of the four decode weights, the
             M = 1 decode sweep over them and prefill at M = 2048
+  kq        Q5_K, Q3_K and Q2_K: ISQ of the four decode weights and the
+            M = 1 decode sweep over them
   embed     token-embedding lookup of 2048 tokens from the 128256 x 4096
             table, Q6_K and Q8_0, bf16 rows
   model     synthetic 8B-shape decoder (32 layers x 7 linears): ISQ of all
@@ -86,6 +89,8 @@ FAMILY_SOURCES = {
     "gemm_mid": ("common.cuh", "gemm.cu"),
     "head": ("common.cuh", "q6k.cu", "gemv_rows.cu"),
     "embed": ("common.cuh", "q6k.cu"),
+    "quantize_kq": ("common.cuh", "kquant.cu"),
+    "gemv_kq": ("common.cuh", "kquant.cu"),
 }
 
 
@@ -211,6 +216,11 @@ class Workload:
         self.fp8_isq_out = [torch.empty_like(p) for p in self.fp8]
         self.fp8_y = {m: [torch.empty((m, n), dtype=torch.float32, device=device)
                           for (n, k) in inputs.DECODE_SHAPES] for m in (1, 2048)}
+        # Q5_K / Q3_K / Q2_K (the other K-quants) of the same decode weights
+        self.kq_fmts = [q.QMM_Q5_K, q.QMM_Q3_K, q.QMM_Q2_K]
+        self.kq = {f: [q.qmm_quantize(f, w) for w in self.w_bf16] for f in self.kq_fmts}
+        self.kq_isq_out = {f: [torch.empty_like(p) for p in self.kq[f]] for f in self.kq_fmts}
+        self.kq_y = [torch.empty((1, n), dtype=torch.float32, device=device) for (n, k) in inputs.DECODE_SHAPES]
         # output head / embedding table of the 8B-shape decoder, in the types
         # of the sensitive-tensor policy (Q4_K model -> Q6_K, Q8_0 -> Q8_0)
         vocab, hidden = inputs.VOCAB, 4096
@@ -325,6 +335,22 @@ class Workload:
             S.append(("gemm_fp8_m2048", fp8_gemm, 6, 0, 2 * 2048.0 * sum(n * k for n, k in pshapes),
                       "gemm", sum(n * k for n, k in pshapes)))
 
+        kqb = {f: q.BLOCK[f][1] / q.BLOCK[f][0] for f in self.kq_fmts}
+
+        def kq_isq():
+            for f in self.kq_fmts:
+                for w, o in zip(self.w_bf16, self.kq_isq_out[f]):
+                    q.qmm_quantize(f, w, out=o)
+        S.append(("isq_kq", kq_isq, 12, sum(nw * (2 + kqb[f]) for f in self.kq_fmts), 0.0, "quantize_kq",
+                  3 * nw))
+
+        def kq_gemv():
+            for f in self.kq_fmts:
+                for (n, k), p, x, y in zip(shapes, self.kq[f], self.x[1], self.kq_y):
+                    q.qmm_matmul(f, p, x, n, out=y)
+        S.append(("gemv_kq_m1", kq_gemv, 12, sum(nw * kqb[f] for f in self.kq_fmts), 2.0 * 3 * nw, "gemv_kq",
+                  3 * nw))
+
         def embed():
             for f in self.head_fmts:
                 q.qmm_embedding(f, self.head[f], self.embed_ids, hidden, out=self.embed_out)
@@ -398,7 +424,8 @@ def parity_check(wl):
     """Sampled parity of the benchmarked kernels against the CPU oracle: the
     decode-shaped linears (packed bytes of 64 rows; outputs of 4 rows at
     M = 1, 16, 32 and 2048; FP8 bytes of 64 rows and outputs of 3 rows at
-    M = 1 and 2048), the output head (bytes and M = 1 outputs of 4
+    M = 1 and 2048), the Q5_K / Q3_K / Q2_K linears (bytes of 32 rows and
+    M = 1 outputs of 3 rows), the output head (bytes and M = 1 outputs of 4
     rows) and 4 embedding rows in each head format, and the last layer of
     the model (packed bytes and M = 1 outputs of 6 rows of each of its 7
     linears, both formats)."""
@@ -432,6 +459,16 @@ def parity_check(wl):
                 y = wl.y[m][f][si][:, ns].double().cpu().numpy()
                 r = float((np.abs(y - Y) / (1e-3 * A + 1e-6)).max())
                 worst = max(worst, r)
+    # the other K-quants: bytes of 32 rows and M = 1 outputs of 3 rows
+    for f in wl.kq_fmts:
+        for si, (n, k) in enumerate(inputs.DECODE_SHAPES):
+            want = oracle.quantize(f, inputs.bf16_bits(wl.w_bf16[si][:32].cpu()))
+            if not np.array_equal(wl.kq[f][si][:32].cpu().numpy(), want):
+                return "FAIL: packed bytes differ (fmt %d shape %d)" % (f, si)
+            y = q.qmm_matmul(f, wl.kq[f][si], wl.x[1][si], n)
+            ns = np.array([0, 1, 31], dtype=np.int64)
+            Y, A = oracle.matmul(f, want[ns], inputs.bf16_bits(wl.x[1][si]), ns.size, k)
+            worst = max(worst, float((np.abs(y[:, ns].double().cpu().numpy() - Y) / (1e-3 * A + 1e-6)).max()))
     # output head (sampled rows, bytes and M = 1 outputs) and embedding rows
     torch = wl.torch
     vocab, hidden = inputs.VOCAB, 4096
@@ -731,7 +768,7 @@ def main(argv=None):
         key = "model_decode_" + nm
         if key in rows:
             rows[key]["weight_GBps"] = rows[key].pop("GBps")
-    for key in ("gemm_m32", "gemm_m128", "head_m1", "gemv_fp8_m1"):
+    for key in ("gemm_m32", "gemm_m128", "head_m1", "gemv_fp8_m1", "gemv_kq_m1"):
         if key in rows:
             rows[key]["weight_GBps"] = rows[key].pop("GBps")
 

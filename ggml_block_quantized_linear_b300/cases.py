@@ -27,7 +27,7 @@ from ggml_block_quantized_linear_b300 import inputs
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--op", choices=["quantize", "dequantize", "matmul"], required=True)
-    ap.add_argument("--fmt", choices=["q8_0", "q4_k", "q6_k"], default="q8_0")
+    ap.add_argument("--fmt", choices=sorted(q.FORMATS), default="q8_0")
     ap.add_argument("--n", type=int, default=4096)
     ap.add_argument("--k", type=int, default=4096)
     ap.add_argument("--m", type=int, default=1)
