@@ -16,17 +16,20 @@
 //
 // Tile: 128 weight rows (the MMA's M side, "swap AB") x BN tokens (MMA N:
 // 32, 64, 128 or 256, the smallest that holds M up to 128; above that 256)
-// x 64 K per stage; persistent CTAs (one per SM) walk the work units.  The
-// dequantized weights go to tensor memory, not shared memory: each
-// dequantizing thread owns one weight row (one TMEM lane) and a 16-wide
-// slice of K, converts its 16 weights in registers and writes them with one
-// tcgen05.st; the MMA reads A from TMEM and only the activations from shared
-// memory (tcgen05.mma with A in TMEM).  That takes the A stores, their bank
-// conflicts and the MMA's A reads off the shared-memory port, which carried
-// every operand before.  TMEM holds the A stages (32 columns each) and the
-// fp32 accumulators: two of BN columns alternating between units for BN up
-// to 128, one of 256 columns for 256-token tiles (whose epilogue then does
-// not overlap the next unit's main loop).
+// x 128 K per stage (two 64-wide 128B-swizzled activation boxes); persistent
+// CTAs (one per SM) walk the work units.  The dequantized weights go to
+// tensor memory, not shared memory: each dequantizing thread owns one weight
+// row (one TMEM lane) and a 32-wide slice of the stage's K, converts its 32
+// weights in registers and writes them with tcgen05.st; the MMA reads A from
+// TMEM and only the activations from shared memory (tcgen05.mma with A in
+// TMEM).  That keeps the A stores, their bank conflicts and the MMA's A
+// reads off the shared-memory port.  One full barrier per stage counts the
+// activation bytes and the 16 dequantizing warps; one MMA commit frees it.
+// TMEM holds the A stages (64 columns each) and the fp32 accumulators: two
+// of BN columns alternating between units for BN up to 128 (three stages),
+// one of 256 columns for 256-token tiles (two stages), which the
+// dequantizing warps drain themselves where they would otherwise wait for
+// the unit's last MMA.
 // When the output tiles are fewer than the SMs, K is split into parts (a
 // unit is one part of one tile).  256-token tiles: at most two parts, both
 // added onto a Y zeroed by the conversion launch (two additions onto zero
@@ -39,8 +42,10 @@
 //                boxes)
 //   warp 1       TMEM allocator and single-thread MMA issuer
 //   warps 2-17   dequantize packed weights into the TMEM A stages (warp w
-//                writes TMEM lanes 32 (w mod 4) .. + 31, K slice (w - 2) / 4)
+//                writes TMEM lanes 32 (w mod 4) .. + 31, K slice (w - 2) / 4);
+//                with one 256-column accumulator they also drain it
 //   warps 18-21  epilogue: read an accumulator back (tcgen05.ld) and store Y
+//                (two accumulators)
 //   warp 22      TMA producer of the packed weights (separate from warp 0 so
 //                that the dequantizing warps never wait behind activation
 //                stages)
@@ -66,7 +71,7 @@ constexpr int kGemmThreads = (kGemmWarpPackedTma + 1) * 32;
 constexpr int kGemmStagesP = 2;     // packed weight groups
 constexpr int kGemmACols = kGemmBK / 2;  // TMEM columns of one A stage (two binary16 per column)
 constexpr int kGemmStepsPerGroup = kGroup / kGemmBK;  // K steps per packed 256-weight group
-static_assert(kGemmDeqWarps == 16, "four warps per TMEM lane quarter, one per 16-wide K slice");
+static_assert(kGemmDeqWarps == 16, "four warps per TMEM lane quarter, one per 32-wide K slice of a stage");
 // accumulators: two of BN columns (BN <= 128) or one of 256
 __host__ __device__ constexpr int gemm_nbuf(int bn) { return bn == 256 ? 1 : 2; }
 // K-step stages: an activation stage (BN x 256 bytes of shared memory) and
