@@ -74,7 +74,7 @@ def main(argv=None):
         ts.append(e0.elapsed_time(e1) * 1e-3)
     t = statistics.median(ts)
     nw = a.n * a.k
-    bw = {"q8_0": 34 / 32, "q4_k": 144 / 256, "q6_k": 210 / 256}[a.fmt]
+    bw = q.qmm_packed_bytes(fmt, a.n, a.k) / nw  # packed bytes per weight
     rec = {"op": a.op, "fmt": a.fmt, "N": a.n, "K": a.k, "M": a.m, "us": round(t * 1e6, 2)}
     if a.op == "quantize":
         rec["GBps"] = round(nw * (2 + bw) / t / 1e9, 1)

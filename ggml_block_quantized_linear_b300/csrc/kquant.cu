@@ -14,7 +14,11 @@
 // Every kernel gives lane l of a warp the weights 8l .. 8l + 7 of a
 // superblock.  The ISQ kernels take the plain definition's fp32 steps in its
 // order (IEEE division, round half away for the codes, binary16
-// round-to-nearest-even for the scales), so the bytes are bit-identical.
+// round-to-nearest-even for the scales), so the bytes are bit-identical; a
+// quotient that is only rounded to an integer (a weight code, a scale code)
+// is formed with the approximate reciprocal and decided exactly next to a
+// rounding tie (quantize.cu's exact_code and round_div), which gives the
+// integer that roundf of the IEEE quotient gives.
 // The linear layer is a CUDA-core kernel for every M: each weight is
 // dequantized exactly as the plain definition does (one fp32 rounding of
 // S q - Mn) and multiplied in fp32.  Q3_K and Q2_K superblocks are only 2- and
@@ -203,11 +207,12 @@ __global__ void __launch_bounds__(kKqThreads) qmm_quantize_kq_kernel(const void 
             for (int o = 2; o < 32; o <<= 1) smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o));
             const __half d16 = __float2half_rn(__fdiv_rn(smax, 31.0f));
             const float df = __half2float(d16);
-            const int sc = df > 0.f ? (int)fminf(fmaxf(roundf(__fdiv_rn(sj, df)), 0.f), 31.f) : 0;
+            const int sc = df > 0.f ? (int)fminf(fmaxf(round_div(sj, df), 0.f), 31.f) : 0;
             const float S = df * (float)sc;
+            const float r = S > 0.f ? rcp_approx(S) : 0.f;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                const int c = S > 0.f ? (int)fminf(fmaxf(roundf(__fdiv_rn(x[e], S)), -4.f), 3.f) : 0;
+                const int c = S > 0.f ? (int)fminf(fmaxf(exact_code(x[e], S, r, kTieGuardQ4), -4.f), 3.f) : 0;
                 qw[8 * lane + e] = (uint8_t)(c + 4);
             }
             if ((lane & 1) == 0) scw[lane >> 1] = sc + 32;
@@ -238,12 +243,14 @@ __global__ void __launch_bounds__(kKqThreads) qmm_quantize_kq_kernel(const void 
             const __half d16 = __float2half_rn(__fdiv_rn(smax, kScaleCodes));
             const __half m16 = __float2half_rn(__fdiv_rn(mmax, kScaleCodes));
             const float df = __half2float(d16), dmf = __half2float(m16);
-            const int sc = df > 0.f ? (int)fminf(fmaxf(roundf(__fdiv_rn(sj, df)), 0.f), kScaleCodes) : 0;
-            const int mc = dmf > 0.f ? (int)fminf(fmaxf(roundf(__fdiv_rn(mj, dmf)), 0.f), kScaleCodes) : 0;
+            const int sc = df > 0.f ? (int)fminf(fmaxf(round_div(sj, df), 0.f), kScaleCodes) : 0;
+            const int mc = dmf > 0.f ? (int)fminf(fmaxf(round_div(mj, dmf), 0.f), kScaleCodes) : 0;
             const float S = df * (float)sc, Mn = dmf * (float)mc;
+            const float r = S > 0.f ? rcp_approx(S) : 0.f;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                const int q = S > 0.f ? (int)fminf(fmaxf(roundf(__fdiv_rn(__fadd_rn(x[e], Mn), S)), 0.f), kQMax) : 0;
+                const float u = __fadd_rn(x[e], Mn);
+                const int q = S > 0.f ? (int)fminf(fmaxf(exact_code(u, S, r, kTieGuardQ4), 0.f), kQMax) : 0;
                 qw[8 * lane + e] = (uint8_t)q;
             }
             if (lane % kLanesPerSub == 0) {
