@@ -7,7 +7,8 @@
 // refill or an activation restage in between.
 //  * Producer warp (one thread): first the activations (bf16, one 1-D bulk
 //    copy per token row), then one 2-D tensor-map TMA copy per stage of
-//    16 rows x 2 chunks of 256 weights (8.5 KB Q8_0, 4.5 KB Q4_K).  In shared
+//    16 rows x 2 chunks of 256 weights (8.5 KB Q8_0, 4.5 KB Q4_K, 5.5 KB
+//    Q5_K).  In shared
 //    memory a stage row is 544 / 288 bytes long, which puts the 8 rows read by
 //    one 64-bit load of a warp on distinct banks.
 //  * Eight consumer warps: chunk i of a tile goes to warp i mod 8, so the two
@@ -56,8 +57,17 @@ struct RowsLayout {
 // Bytes a chunk advances in a packed row, and half the shared-memory pitch of
 // a stage row (FP8: two 256-byte chunks plus 32 bytes of the next, a 544-byte
 // pitch that keeps a warp's code loads on distinct banks, as Q8_0's does).
-__host__ __device__ constexpr int rows_chunk_bytes(int fmt) { return fmt == 8 ? kQ8GroupBytes : fmt == 4 ? kQ4Bytes : 256; }
-__host__ __device__ constexpr int rows_half_pitch(int fmt) { return fmt == 4 ? kQ4Bytes : kQ8GroupBytes; }
+// Q5_K: a 176-byte superblock per chunk, pitch 352 (88 words: the 8 rows of a
+// half-warp's 64-bit code loads land on distinct banks, as for Q4_K).
+constexpr int kQ5Bytes = 176;
+__host__ __device__ constexpr int rows_chunk_bytes(int fmt) {
+    return fmt == 8 ? kQ8GroupBytes : fmt == 4 ? kQ4Bytes : fmt == 5 ? kQ5Bytes : 256;
+}
+__host__ __device__ constexpr int rows_half_pitch(int fmt) {
+    return fmt == 4 ? kQ4Bytes : fmt == 5 ? kQ5Bytes : kQ8GroupBytes;
+}
+// the affine formats (codes times a sub-block scale minus a sub-block min)
+__host__ __device__ constexpr bool rows_affine(int fmt) { return fmt == 4 || fmt == 5; }
 
 // mt = 8 * (token tiles): the stride of the Q4_K block sums per 32-block.
 __host__ __device__ inline RowsLayout rows_layout(int fmt, int M, int dpp, int win, int mt, int nw) {
@@ -69,9 +79,9 @@ __host__ __device__ inline RowsLayout rows_layout(int fmt, int M, int dpp, int w
     L.xh = off;
     off += M * (win * kGroup + 32) * 2;       // token rows, 32 halves of padding between them
     L.xs = off;
-    off += fmt == 4 ? win * 8 * mt * 4 : 0;   // Q4_K: sum of x per 32-block and token
+    off += rows_affine(fmt) ? win * 8 * mt * 4 : 0;   // Q4_K / Q5_K: sum of x per 32-block and token
     L.coef = off;
-    off += fmt == 4 ? nw * kRowsR * kCoefStrideR * 4 : 0;
+    off += rows_affine(fmt) ? nw * kRowsR * kCoefStrideR * 4 : 0;
     L.ypart = off;
     off += kYBufsR * nw * kRowsR * M * 4;
     off = (off + 15) & ~15;
@@ -96,7 +106,7 @@ struct RowsParams {
 // Convert the raw bf16 activations of a window, landed by TMA at xh (token m
 // at xh + m * xstride), in place to binary16 (round to nearest), each group
 // of 4 stored in the order (0, 2, 1, 3) so that one 16-byte load yields both
-// B fragments of an MMA; Q4_K also sums each 32-weight block per token.
+// B fragments of an MMA; Q4_K and Q5_K also sum each 32-weight block per token.
 template <int kFmt, int kMT, int kW>
 __device__ __forceinline__ void rows_convert_x(int M, __half *xh, float *xs, int xstride, int wn,
                                                int tid) {
@@ -123,7 +133,7 @@ __device__ __forceinline__ void rows_convert_x(int M, __half *xh, float *xs, int
         o.z = *reinterpret_cast<const uint32_t *>(&h46);
         o.w = *reinterpret_cast<const uint32_t *>(&h57);
         *p = o;
-        if constexpr (kFmt == 4) {
+        if constexpr (rows_affine(kFmt)) {
             // lanes 4j .. 4j + 3 hold one 32-weight block (ngr is a multiple of 32)
             const float2 s02 = __half22float2(h02), s13 = __half22float2(h13);
             const float2 s46 = __half22float2(h46), s57 = __half22float2(h57);
@@ -279,6 +289,55 @@ __device__ __forceinline__ void rq4_group(const uint8_t *r0, const uint8_t *r1, 
     }
 }
 
+// Q5_K: rq4_group's 64 weights with 5-bit codes.  The chunk's codes sit at
+// byte 48 (16 of header, 32 of qh before them); bit j of qh byte l is bit 4
+// of weight l of sub-block j.  qh* hold the lane's qh bytes 8t .. 8t + 7 of
+// rows g and g + 8, qh*8 the same shifted down a byte (the odd bytes).  The
+// fifth bit joins the subnormal binary16 codes: bit 4 under the low nibble
+// (q * 2^-24), bit 8 under the high one (q * 2^-20), so rq4_coefs' scales
+// apply unchanged.
+template <int kSh>
+__device__ __forceinline__ uint32_t shl_c(uint32_t v) {
+    if constexpr (kSh >= 0) return v << kSh;
+    else return v >> -kSh;
+}
+template <int kC, int kNT>
+__device__ __forceinline__ void rq5_group(const uint8_t *r0, const uint8_t *r1, uint2 qha, uint2 qhb, uint2 qha8,
+                                          uint2 qhb8, const __half *xb, int xstride, const float *xsb,
+                                          const float *cw, int g, int t, bool v0, bool v1,
+                                          float (&acc)[kNT][4]) {
+    constexpr int kMT = 8 * kNT;
+    const uint2 qa = *reinterpret_cast<const uint2 *>(r0 + 48 + 32 * kC + 8 * t);
+    const uint2 qb = *reinterpret_cast<const uint2 *>(r1 + 48 + 32 * kC + 8 * t);
+    const float4 ca = *reinterpret_cast<const float4 *>(cw + g * kCoefStrideR + 4 * kC);
+    const float4 cb = *reinterpret_cast<const float4 *>(cw + (g + 8) * kCoefStrideR + 4 * kC);
+    const uint32_t qa0s = qa.x >> 8, qa1s = qa.y >> 8, qb0s = qb.x >> 8, qb1s = qb.y >> 8;
+    // sub-block 2c: low nibble | qh bit 2c at bit 4; sub-block 2c + 1: high nibble | qh bit 2c + 1 at bit 8
+    auto lo = [](uint32_t q, uint32_t h) { return (q & 0x000F000Fu) | (shl_c<4 - 2 * kC>(h) & 0x00100010u); };
+    auto hi = [](uint32_t q, uint32_t h) { return (q & 0x00F000F0u) | (shl_c<7 - 2 * kC>(h) & 0x01000100u); };
+    const uint32_t L0[4] = {lo(qa.x, qha.x), lo(qb.x, qhb.x), lo(qa0s, qha8.x), lo(qb0s, qhb8.x)};
+    const uint32_t L1[4] = {lo(qa.y, qha.y), lo(qb.y, qhb.y), lo(qa1s, qha8.y), lo(qb1s, qhb8.y)};
+    const uint32_t H0[4] = {hi(qa.x, qha.x), hi(qb.x, qhb.x), hi(qa0s, qha8.x), hi(qb0s, qhb8.x)};
+    const uint32_t H1[4] = {hi(qa.y, qha.y), hi(qb.y, qhb.y), hi(qa1s, qha8.y), hi(qb1s, qhb8.y)};
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt) {
+        const __half *xq = xb + nt * 8 * xstride + 64 * kC + 8 * t;
+        const uint4 xl = x_frag(xq, nt == 0 ? v0 : v1);
+        const uint4 xhv = x_frag(xq + 32, nt == 0 ? v0 : v1);
+        float cl[4] = {0.f, 0.f, 0.f, 0.f}, chh[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_f16_16816(cl, L0, xl.x, xl.y);
+        mma_f16_16816(cl, L1, xl.z, xl.w);
+        mma_f16_16816(chh, H0, xhv.x, xhv.y);
+        mma_f16_16816(chh, H1, xhv.z, xhv.w);
+        const float2 sl = *reinterpret_cast<const float2 *>(xsb + (2 * kC) * kMT + nt * 8 + 2 * t);
+        const float2 sh = *reinterpret_cast<const float2 *>(xsb + (2 * kC + 1) * kMT + nt * 8 + 2 * t);
+        acc[nt][0] = fmaf(ca.w, sh.x, fmaf(ca.y, sl.x, fmaf(ca.z, chh[0], fmaf(ca.x, cl[0], acc[nt][0]))));
+        acc[nt][1] = fmaf(ca.w, sh.y, fmaf(ca.y, sl.y, fmaf(ca.z, chh[1], fmaf(ca.x, cl[1], acc[nt][1]))));
+        acc[nt][2] = fmaf(cb.w, sh.x, fmaf(cb.y, sl.x, fmaf(cb.z, chh[2], fmaf(cb.x, cl[2], acc[nt][2]))));
+        acc[nt][3] = fmaf(cb.w, sh.y, fmaf(cb.y, sl.y, fmaf(cb.z, chh[3], fmaf(cb.x, cl[3], acc[nt][3]))));
+    }
+}
+
 // kNT token tiles of 8 (M <= 8 kNT); two tiles double the accumulators, so
 // their register budget allows two CTAs per SM instead of three.
 template <int kFmt, int kNT, int kW>
@@ -322,7 +381,7 @@ qmm_gemv_rows_kernel(const __grid_constant__ CUtensorMap wmap, const RowsParams 
     }
     // block sums of padding tokens (m >= M) stay zero for the whole kernel
     constexpr int kMT = 8 * kNT;
-    if constexpr (kFmt == 4)
+    if constexpr (rows_affine(kFmt))
         for (int idx = tid; idx < win * 8 * kMT; idx += kThreadsR) xs[idx] = 0.f;
     if (warp == kProdWarpR && lane == 0) {
         // descriptor fetch and L2 prefetch of the first tile's leading stages
@@ -466,6 +525,18 @@ qmm_gemv_rows_kernel(const __grid_constant__ CUtensorMap wmap, const RowsParams 
                             rq8_block<5, kNT>(r0, r1, xb, xstride, t, v0, v1, acc);
                             rq8_block<6, kNT>(r0, r1, xb, xstride, t, v0, v1, acc);
                             rq8_block<7, kNT>(r0, r1, xb, xstride, t, v0, v1, acc);
+                        } else if constexpr (kFmt == 5) {
+                            rq4_coefs(cbase, kPitch, cw, lane);  // Q5_K's header is Q4_K's
+                            __syncwarp();
+                            const float *xsb = xs + li * 8 * kMT;
+                            const uint2 qha = *reinterpret_cast<const uint2 *>(r0 + 16 + 8 * t);
+                            const uint2 qhb = *reinterpret_cast<const uint2 *>(r1 + 16 + 8 * t);
+                            const uint2 qha8 = make_uint2(qha.x >> 8, qha.y >> 8);
+                            const uint2 qhb8 = make_uint2(qhb.x >> 8, qhb.y >> 8);
+                            rq5_group<0, kNT>(r0, r1, qha, qhb, qha8, qhb8, xb, xstride, xsb, cw, g, t, v0, v1, acc);
+                            rq5_group<1, kNT>(r0, r1, qha, qhb, qha8, qhb8, xb, xstride, xsb, cw, g, t, v0, v1, acc);
+                            rq5_group<2, kNT>(r0, r1, qha, qhb, qha8, qhb8, xb, xstride, xsb, cw, g, t, v0, v1, acc);
+                            rq5_group<3, kNT>(r0, r1, qha, qhb, qha8, qhb8, xb, xstride, xsb, cw, g, t, v0, v1, acc);
                         } else {
                             rq4_coefs(cbase, kPitch, cw, lane);
                             __syncwarp();
@@ -590,7 +661,7 @@ static RowsPlan rows_plan_compute(int dev, int M, int K) {
     if (QMM_ROWS_WARPS != 16 && p8.dpp > 0 && p8.occ > 1) return p8;
     const RowsPlan p16 = rows_plan_warps<kFmt, kNT, 16>(dev, M, K);
     if (p16.dpp == 0) return p8;
-    if (QMM_ROWS_WARPS == 16 || p8.dpp == 0 || kFmt == 4) return p16;
+    if (QMM_ROWS_WARPS == 16 || p8.dpp == 0 || rows_affine(kFmt)) return p16;
     const long b8 = (long)p8.occ * 4 * p8.dpp, b16 = (long)p16.occ * 8 * p16.dpp;  // stages in flight per SM
     return b16 >= b8 ? p16 : p8;
 }
@@ -666,6 +737,8 @@ cudaError_t launch_gemv_rows(int fmt, const void *W, const uint16_t *X, float *Y
     p.K = K;
     if (fmt == kFp8)
         return M > 8 ? launch_rows_t<kFp8, 2>(W, p, sms, stream) : launch_rows_t<kFp8, 1>(W, p, sms, stream);
+    if (fmt == 5)
+        return M > 8 ? launch_rows_t<5, 2>(W, p, sms, stream) : launch_rows_t<5, 1>(W, p, sms, stream);
     if (M > 8)
         return fmt == 8 ? launch_rows_t<8, 2>(W, p, sms, stream) : launch_rows_t<4, 2>(W, p, sms, stream);
     return fmt == 8 ? launch_rows_t<8, 1>(W, p, sms, stream) : launch_rows_t<4, 1>(W, p, sms, stream);

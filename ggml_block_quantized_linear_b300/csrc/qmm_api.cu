@@ -203,6 +203,10 @@ qmm_status qmm_matmul(qmm_format fmt, const void *W_packed, const uint16_t *X_bf
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (fmt == QMM_Q6_K)
         return from_cuda(launch_q6k_matmul(W_packed, X_bf16, Y, (int)M, (int)N, (int)K, sm_count(), s));
+    // Q5_K decode runs on the row-tile kernel (its superblocks are 16-byte
+    // aligned, so TMA boxes fit); the other K-quants and Q5_K prefill on CUDA cores
+    if (fmt == QMM_Q5_K && M <= kMaxDecodeM)
+        return from_cuda(launch_gemv_rows((int)fmt, W_packed, X_bf16, Y, (int)M, (int)N, (int)K, sm_count(), s));
     if (is_kq(fmt))
         return from_cuda(launch_kq_matmul((int)fmt, W_packed, X_bf16, Y, (int)M, (int)N, (int)K, sm_count(), s));
     if (M <= kMaxDecodeM) {
