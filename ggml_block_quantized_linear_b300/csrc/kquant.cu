@@ -63,30 +63,40 @@ struct KqRaw {
     uint32_t s0, s1;  // scale words (see kq_lane_decode)
 };
 
-// 8 bytes at a 2-byte aligned address, as two words.
+// A load through the read-only path (global memory) or a plain one (kSm:
+// shared memory, where the superblocks sit after a TMA copy).
+template <bool kSm, typename T>
+__device__ __forceinline__ T kq_ld(const T *p) {
+    if constexpr (kSm) return *p;
+    else return __ldg(p);
+}
+
+// 8 bytes at a 2-byte aligned address, as two words (the aligned word below
+// is formed from the pointer itself, which keeps its address space visible).
+template <bool kSm = false>
 __device__ __forceinline__ void kq_ld8_a2(const uint8_t *p, uint32_t &w0, uint32_t &w1) {
     const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-    const uint32_t *w = reinterpret_cast<const uint32_t *>(a & ~(uintptr_t)3);
-    const uint32_t x0 = __ldg(w), x1 = __ldg(w + 1);
+    const uint32_t *w = reinterpret_cast<const uint32_t *>(p - (a & 3));
+    const uint32_t x0 = kq_ld<kSm>(w), x1 = kq_ld<kSm>(w + 1);
     if ((a & 3) == 0) {
         w0 = x0;
         w1 = x1;
     } else {
-        const uint32_t x2 = __ldg(w + 2);
+        const uint32_t x2 = kq_ld<kSm>(w + 2);
         w0 = __funnelshift_r(x0, x1, 16);
         w1 = __funnelshift_r(x1, x2, 16);
     }
 }
 
-template <int kFmt>
+template <int kFmt, bool kSm = false>
 __device__ __forceinline__ KqRaw kq_lane_load(const uint8_t *blk, int lane) {
     KqRaw r;
     const int h = lane >> 4, o = 8 * (lane & 3);
     if constexpr (kFmt == 5) {
         const int j = lane >> 2;
-        const uint2 qs = __ldg(reinterpret_cast<const uint2 *>(blk + 48 + 32 * (j >> 1) + o));
-        const uint2 qh = __ldg(reinterpret_cast<const uint2 *>(blk + 16 + o));
-        const uint4 hd = __ldg(reinterpret_cast<const uint4 *>(blk));  // d, dmin, 12 scale bytes
+        const uint2 qs = kq_ld<kSm>(reinterpret_cast<const uint2 *>(blk + 48 + 32 * (j >> 1) + o));
+        const uint2 qh = kq_ld<kSm>(reinterpret_cast<const uint2 *>(blk + 16 + o));
+        const uint4 hd = kq_ld<kSm>(reinterpret_cast<const uint4 *>(blk));  // d, dmin, 12 scale bytes
         r.a0 = qs.x; r.a1 = qs.y; r.b0 = qh.x; r.b1 = qh.y;
         // Q4_K's scale packing: scale bytes 0-3 = hd.y, 4-7 = hd.z, 8-11 = hd.w
         const uint32_t k = 8u * (uint32_t)(j & 3);
@@ -96,18 +106,18 @@ __device__ __forceinline__ KqRaw kq_lane_load(const uint8_t *blk, int lane) {
         r.s0 = hd.x;  // d | dmin << 16
         r.s1 = sc | (mc << 8);
     } else if constexpr (kFmt == 3) {
-        kq_ld8_a2(blk + 32 + 32 * h + o, r.a0, r.a1);
-        kq_ld8_a2(blk + o, r.b0, r.b1);
+        kq_ld8_a2<kSm>(blk + 32 + 32 * h + o, r.a0, r.a1);
+        kq_ld8_a2<kSm>(blk + o, r.b0, r.b1);
         const int j = lane >> 1;
         r.s0 = (uint32_t)kq_q3_field(blk + 96, j);
         r.s1 = (uint32_t)(*reinterpret_cast<const uint16_t *>(blk + 108));
     } else {
         const uint32_t *qs = reinterpret_cast<const uint32_t *>(blk + 16 + 32 * h + o);
-        r.a0 = __ldg(qs);
-        r.a1 = __ldg(qs + 1);
+        r.a0 = kq_ld<kSm>(qs);
+        r.a1 = kq_ld<kSm>(qs + 1);
         r.b0 = r.b1 = 0;
         r.s0 = blk[lane >> 1];
-        r.s1 = __ldg(reinterpret_cast<const uint32_t *>(blk + 80));  // d | dmin << 16
+        r.s1 = kq_ld<kSm>(reinterpret_cast<const uint32_t *>(blk + 80));  // d | dmin << 16
     }
     return r;
 }

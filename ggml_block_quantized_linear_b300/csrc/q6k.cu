@@ -19,14 +19,21 @@ namespace qmm {
 constexpr int kQ6Bytes = 210;
 constexpr int kQ6Threads = 256;  // 8 warps
 
-// 8 bytes at a 2-byte aligned address.
+// 8 bytes at a 2-byte aligned address, through the read-only path (global
+// memory) or with plain loads (kSm: shared memory).  The aligned word below
+// is formed from the pointer itself, which keeps its address space visible.
+template <bool kSm = false>
 __device__ __forceinline__ uint2 ld8_a2(const uint8_t *p) {
     const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-    const uint32_t *w = reinterpret_cast<const uint32_t *>(a & ~(uintptr_t)3);
+    const uint32_t *w = reinterpret_cast<const uint32_t *>(p - (a & 3));
     const uint32_t sh = (uint32_t)(a & 3) * 8u;  // 0 or 16
-    const uint32_t w0 = __ldg(w), w1 = __ldg(w + 1);
+    auto ld = [](const uint32_t *q) {
+        if constexpr (kSm) return *q;
+        else return __ldg(q);
+    };
+    const uint32_t w0 = ld(w), w1 = ld(w + 1);
     if (sh == 0) return make_uint2(w0, w1);
-    const uint32_t w2 = __ldg(w + 2);
+    const uint32_t w2 = ld(w + 2);
     return make_uint2(__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh));
 }
 
@@ -34,10 +41,11 @@ __device__ __forceinline__ uint2 ld8_a2(const uint8_t *p) {
 // h = l / 16, s = (l / 4) % 4, first weight 32 s' + 8 (l % 4) of its 128-half.
 // Low 4 bits: ql bytes 64 h + 32 (s & 1) + 8 (l % 4) + e (high nibble when
 // s >= 2); high 2 bits: bits 2s, 2s + 1 of qh bytes 128 + 32 h + 8 (l % 4) + e.
+template <bool kSm = false>
 __device__ __forceinline__ void q6_lane_codes(const uint8_t *blk, int lane, float (&c)[8]) {
     const int h = lane >> 4, s = (lane >> 2) & 3, o = 8 * (lane & 3);
-    const uint2 ql = ld8_a2(blk + 64 * h + 32 * (s & 1) + o);
-    const uint2 qh = ld8_a2(blk + 128 + 32 * h + o);
+    const uint2 ql = ld8_a2<kSm>(blk + 64 * h + 32 * (s & 1) + o);
+    const uint2 qh = ld8_a2<kSm>(blk + 128 + 32 * h + o);
     const uint32_t nsh = (uint32_t)(s >> 1) * 4u, hsh = 2u * (uint32_t)s;
     const uint32_t q0 = ((ql.x >> nsh) & 0x0F0F0F0Fu) | (((qh.x >> hsh) & 0x03030303u) << 4);
     const uint32_t q1 = ((ql.y >> nsh) & 0x0F0F0F0Fu) | (((qh.y >> hsh) & 0x03030303u) << 4);

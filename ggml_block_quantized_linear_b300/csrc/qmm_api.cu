@@ -40,6 +40,9 @@ cudaError_t launch_kq_matmul(int fmt, const void *W, const uint16_t *X, float *Y
                              cudaStream_t stream);
 cudaError_t launch_kq_embedding(int fmt, const void *table, const int64_t *ids, void *out, int bf16, int64_t T,
                                 int64_t V, int64_t D, int sms, cudaStream_t stream);
+bool sbrows_supported(int fmt, int M, int K);
+cudaError_t launch_sbrows(int fmt, const void *W, const uint16_t *X, float *Y, int N, int K, int sms,
+                          cudaStream_t stream);
 
 constexpr int kMaxDecodeM = 16;
 // Largest dimension accepted (keeps every 32-bit index in the kernels exact).
@@ -201,6 +204,10 @@ qmm_status qmm_matmul(qmm_format fmt, const void *W_packed, const uint16_t *X_bf
     if (W_packed == nullptr || X_bf16 == nullptr || Y == nullptr) return QMM_ERR_INVALID_ARG;
     if (!aligned16(W_packed) || !aligned16(X_bf16) || !aligned16(Y)) return QMM_ERR_ALIGNMENT;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // one token, Q6_K / Q3_K / Q2_K: TMA-fed CUDA-core kernel where the rows
+    // are 16-byte multiples; otherwise direct loads
+    if (sbrows_supported((int)fmt, (int)M, (int)K))
+        return from_cuda(launch_sbrows((int)fmt, W_packed, X_bf16, Y, (int)N, (int)K, sm_count(), s));
     if (fmt == QMM_Q6_K)
         return from_cuda(launch_q6k_matmul(W_packed, X_bf16, Y, (int)M, (int)N, (int)K, sm_count(), s));
     // Q5_K decode runs on the row-tile kernel (its superblocks are 16-byte

@@ -8,4 +8,5 @@
 #include "q6k.cu"
 #include "fp8.cu"
 #include "kquant.cu"
+#include "sbrows.cu"
 #include "static_scratch.cu"

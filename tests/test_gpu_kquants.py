@@ -141,3 +141,42 @@ def test_output_head_type_of_each_model(model, head):
     want = oracle.quantize(head, inputs.bf16_bits(w[ridx]))
     Y, A = oracle.matmul(head, want, inputs.bf16_bits(x), rows.size, D)
     check_matmul(y[:, ridx], Y, A, "head")
+
+
+# One token on the TMA-fed kernel (rows a 16-byte multiple): ragged row tiles
+# (N not a multiple of 8), several 8-superblock stages, a partial last stage
+# (Q2_K, 12 superblocks), many tiles per CTA (N = 9000), and K = 14336.
+@pytest.mark.parametrize("fmt,n,k", [(q.QMM_Q3_K, 300, 4096), (q.QMM_Q2_K, 300, 4096), (q.QMM_Q2_K, 77, 3072),
+                                     (q.QMM_Q3_K, 1001, 14336), (q.QMM_Q2_K, 1001, 14336),
+                                     (q.QMM_Q6_K, 301, 4096), (q.QMM_Q6_K, 203, 14336),
+                                     (q.QMM_Q3_K, 9000, 2048), (q.QMM_Q6_K, 9000, 2048)])
+def test_one_token_tma_path(fmt, n, k):
+    w = inputs.weights(n, k, 83 + n + k)
+    packed = oracle.quantize(fmt, inputs.bf16_bits(w))
+    xb = inputs.bf16_bits(inputs.activations(1, k, 84))
+    Y, A = oracle.matmul(fmt, packed, xb, n, k)
+    y = q.qmm_matmul(fmt, to_dev_u8(packed), bf16_from_bits(xb), n)
+    check_matmul(y, Y, A, "fmt=%d n=%d k=%d" % (fmt, n, k))
+    # repeated and chained calls stay identical (persistent CTAs, dependent launches)
+    y2 = q.qmm_matmul(fmt, to_dev_u8(packed), bf16_from_bits(xb), n)
+    assert torch.equal(y, y2)
+    assert q.qmm_device_error_take() == 0
+
+
+# Rows that are not 16-byte multiples take the direct-load kernel (Q3_K with
+# 12 superblocks: 1320 bytes); both kernels form each row's sum in the same
+# order, so a 16-byte-multiple row gives the same bits through either.
+def test_one_token_fallback_and_same_order():
+    n, k = 129, 3072
+    w = inputs.weights(n, k, 85)
+    packed = oracle.quantize(q.QMM_Q3_K, inputs.bf16_bits(w))
+    xb = inputs.bf16_bits(inputs.activations(1, k, 86))
+    Y, A = oracle.matmul(q.QMM_Q3_K, packed, xb, n, k)
+    check_matmul(q.qmm_matmul(q.QMM_Q3_K, to_dev_u8(packed), bf16_from_bits(xb), n), Y, A, "fallback")
+    # Q2_K, 12 superblocks (1008 bytes, TMA path) against the same rows at M = 2
+    # (direct loads, first token the same): identical first row of outputs
+    packed2 = oracle.quantize(q.QMM_Q2_K, inputs.bf16_bits(w))
+    x2 = inputs.activations(2, k, 87)
+    y1 = q.qmm_matmul(q.QMM_Q2_K, to_dev_u8(packed2), x2[:1].contiguous().to(DEV), n)
+    y2 = q.qmm_matmul(q.QMM_Q2_K, to_dev_u8(packed2), x2.to(DEV), n)
+    assert torch.equal(y1[0], y2[0])
