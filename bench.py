@@ -87,10 +87,10 @@ FAMILY_SOURCES = {
     "quantize_fp8": ("common.cuh", "fp8.cu"),
     "gemm": ("common.cuh", "gemm.cu"),
     "gemm_mid": ("common.cuh", "gemm.cu"),
-    "head": ("common.cuh", "q6k.cu", "gemv_rows.cu"),
+    "head": ("common.cuh", "q6k.cu", "gemv_rows.cu", "sbrows.cu"),
     "embed": ("common.cuh", "q6k.cu"),
     "quantize_kq": ("common.cuh", "kquant.cu"),
-    "gemv_kq": ("common.cuh", "kquant.cu"),
+    "gemv_kq": ("common.cuh", "kquant.cu", "gemv_rows.cu", "sbrows.cu"),
 }
 
 
