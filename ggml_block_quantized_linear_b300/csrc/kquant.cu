@@ -399,6 +399,150 @@ __global__ void __launch_bounds__(kKqThreads, kTok == 1 ? 3 : 2) qmm_matmul_kq_k
     }
 }
 
+// ------------------------------------------------------------- Q5_K ISQ
+// Q5_K quantizes like Q4_K with 5-bit codes, so it takes quantize.cu's Q4_K
+// structure: one lane per 32-weight sub-block (8 lanes a superblock, 4
+// superblocks a warp), codes four to a word from round2 with the same tie
+// flagging, the Q4_K scale bytes, and the superblock assembled in shared
+// memory and stored with 16-byte writes.  The fifth code bits (qh byte l,
+// bit j: bit 4 of weight l of sub-block j) are gathered with shuffles: lane
+// j moves its bits to bit j of each byte and the 8 lanes OR their words.
+template <bool kSrcF32>
+__global__ void __launch_bounds__(kQuantThreads, QMM_Q4_QUANT_MIN_BLOCKS)
+qmm_quantize_q5_k_kernel(const void *__restrict__ src, uint8_t *__restrict__ dst, int64_t nsuper) {
+    constexpr int kB = 176;
+    __shared__ __align__(16) uint8_t stage[kQuantWarps][4 * kB];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int sj = lane & 7, sbl = lane >> 3;  // sub-block j, superblock in the warp tile
+    uint8_t *st = stage[warp] + sbl * kB;
+    const int64_t nwarps = (int64_t)gridDim.x * kQuantWarps;
+    const int64_t step = nwarps * 4;
+    int64_t s0 = ((int64_t)blockIdx.x * kQuantWarps + warp) * 4;
+    Lane32<kSrcF32> Ln;
+    if (!kSrcF32) Ln.load(src, (s0 + sbl) * 256 + sj * 32, s0 + sbl < nsuper);
+    for (; s0 < nsuper; s0 += step) {
+        const int64_t sb = s0 + sbl;
+        const bool valid = sb < nsuper;  // uniform over each group of 8 lanes
+        const int nvalid = (int)min((int64_t)4, nsuper - s0);
+        Lane32<kSrcF32> L;
+        if constexpr (kSrcF32) {
+            L.load(src, sb * 256 + sj * 32, valid);
+        } else {
+            L = Ln;
+            Ln.load(src, (sb + step) * 256 + sj * 32, sb + step < nsuper);
+        }
+        float mx, mn;  // max_i x_i and min(0, min_i x_i)
+        L.extremes(mx, mn);
+        mn = fminf(0.0f, mn);
+        const float s = __fdiv_rn(__fsub_rn(mx, mn), 31.0f);
+        const float m = __fsub_rn(0.0f, mn);
+        float smax = s, mmax = m;
+#pragma unroll
+        for (int o = 1; o <= 4; o <<= 1) {
+            smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o));
+            mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, o));
+        }
+        smax = smax > 0.0f ? smax : 0.0f;
+        mmax = mmax > 0.0f ? mmax : 0.0f;
+        const __half dh = __float2half_rn(div_const<63>(smax));
+        const __half dminh = __float2half_rn(div_const<63>(mmax));
+        const float df = __half2float(dh), dminf = __half2float(dminh);
+        const float tsc = df > 0.0f ? round_div(s, df) : 0.0f;
+        const float tmc = dminf > 0.0f ? round_div(m, dminf) : 0.0f;
+        const int sc = (int)clamp_f(tsc, 0.0f, 63.0f);
+        const int mc = (int)clamp_f(tmc, 0.0f, 63.0f);
+        const float S = __fmul_rn(df, (float)sc);
+        const float Mn = __fmul_rn(dminf, (float)mc);
+        uint32_t w[8];  // 5-bit codes, one per byte
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[i] = 0u;
+        float r = 0.0f;
+        bool tie = false;
+        if (S > 0.0f) {
+            r = rcp_approx(S);
+            const uint64_t r2 = f2_pack(r, r), mn2 = f2_pack(Mn, Mn);
+            float dev = 0.0f;
+            // codes of u = x + Mn (its own rounding step) over S; monotone in x,
+            // so when the extremes' codes lie well inside int16 the clamp to
+            // [0, 31] runs on 16-bit pairs, otherwise on the floats
+            const float khi = __fmul_rn(__fadd_rn(mx, Mn), r), klo = __fmul_rn(__fadd_rn(mn, Mn), r);
+            if (khi < 30000.0f && klo > -30000.0f) {
+                auto code2 = [&](int i) {
+                    const uint64_t v = round2(f2_add(L.pair(i), mn2), r2, dev);
+                    return __vimin_s16x2_relu(prmt((uint32_t)v, (uint32_t)(v >> 32), 0x5410u), 0x001F001Fu);
+                };
+#pragma unroll
+                for (int i = 0; i < 8; ++i) w[i] = prmt(code2(4 * i), code2(4 * i + 2), 0x6420u);
+            } else {
+                auto code2 = [&](int i) { return clamp2(round2(f2_add(L.pair(i), mn2), r2, dev), 0.0f, 31.0f); };
+#pragma unroll
+                for (int i = 0; i < 8; ++i) w[i] = pack4_magic(code2(4 * i), code2(4 * i + 2));
+            }
+            // codes matter up to 31.5: 2^-23 * 31.75 + 2^-25 = 2^-18, Q4_K's guard
+            tie = valid && dev >= kTieGuardQ4;
+        }
+        // low nibbles: sub-block 2c (low) and 2c + 1 (high) share qs chunk c
+        uint32_t hw[8], hb[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            hw[i] = __shfl_xor_sync(0xffffffffu, w[i], 1);
+            hb[i] = ((w[i] >> 4) & 0x01010101u) << sj;  // bit 4 of each code to bit sj of its byte
+        }
+#pragma unroll
+        for (int o = 1; o <= 4; o <<= 1)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) hb[i] |= __shfl_xor_sync(0xffffffffu, hb[i], o);
+        const int sc4 = __shfl_down_sync(0xffffffffu, sc, 4);
+        const int mc4 = __shfl_down_sync(0xffffffffu, mc, 4);
+        if (valid) {
+            if ((sj & 1) == 0) {
+                uint4 *o = reinterpret_cast<uint4 *>(st + 48 + 32 * (sj >> 1));
+                o[0] = make_uint4((w[0] & 0x0F0F0F0Fu) | ((hw[0] & 0x0F0F0F0Fu) << 4),
+                                  (w[1] & 0x0F0F0F0Fu) | ((hw[1] & 0x0F0F0F0Fu) << 4),
+                                  (w[2] & 0x0F0F0F0Fu) | ((hw[2] & 0x0F0F0F0Fu) << 4),
+                                  (w[3] & 0x0F0F0F0Fu) | ((hw[3] & 0x0F0F0F0Fu) << 4));
+                o[1] = make_uint4((w[4] & 0x0F0F0F0Fu) | ((hw[4] & 0x0F0F0F0Fu) << 4),
+                                  (w[5] & 0x0F0F0F0Fu) | ((hw[5] & 0x0F0F0F0Fu) << 4),
+                                  (w[6] & 0x0F0F0F0Fu) | ((hw[6] & 0x0F0F0F0Fu) << 4),
+                                  (w[7] & 0x0F0F0F0Fu) | ((hw[7] & 0x0F0F0F0Fu) << 4));
+            }
+            if (sj == 1) {  // qh bytes 0-31
+                uint4 *o = reinterpret_cast<uint4 *>(st + 16);
+                o[0] = make_uint4(hb[0], hb[1], hb[2], hb[3]);
+                o[1] = make_uint4(hb[4], hb[5], hb[6], hb[7]);
+            }
+            if (sj < 4) {
+                st[4 + sj] = (uint8_t)(sc | ((sc4 >> 4) << 6));
+                st[8 + sj] = (uint8_t)(mc | ((mc4 >> 4) << 6));
+                st[12 + sj] = (uint8_t)((sc4 & 15) | ((mc4 & 15) << 4));
+            }
+            if (sj == 0)
+                *reinterpret_cast<uint32_t *>(st) =
+                    (uint32_t)__half_as_ushort(dh) | ((uint32_t)__half_as_ushort(dminh) << 16);
+        }
+        __syncwarp();
+        // sub-blocks with a possible tie: the warp recomputes them one at a
+        // time, lane l taking weight l, and overwrites its nibble and qh bit
+        for (uint32_t fl = __ballot_sync(0xffffffffu, tie); fl != 0; fl &= fl - 1) {
+            const int l = __ffs(fl) - 1, jl = l & 7;
+            const float Sl = __shfl_sync(0xffffffffu, S, l), rl = __shfl_sync(0xffffffffu, r, l);
+            const float Ml = __shfl_sync(0xffffffffu, Mn, l);
+            const float u = __fadd_rn(Lane32<kSrcF32>::reload(src, (s0 + (l >> 3)) * 256 + jl * 32, lane), Ml);
+            const uint32_t c = int_byte(clamp_f(exact_code(u, Sl, rl, kTieGuardQ4), 0.0f, 31.0f));
+            uint8_t *sbp = stage[warp] + (l >> 3) * kB;
+            uint8_t *q = sbp + 48 + 32 * (jl >> 1) + lane;
+            *q = (uint8_t)((jl & 1) ? ((*q & 0x0Fu) | ((c & 15u) << 4)) : ((*q & 0xF0u) | (c & 15u)));
+            uint8_t *h = sbp + 16 + lane;
+            *h = (uint8_t)((*h & ~(1u << jl)) | (((c >> 4) & 1u) << jl));
+            __syncwarp();
+        }
+        const int nvec = nvalid * kB / 16;
+        uint4 *out = reinterpret_cast<uint4 *>(dst + s0 * kB);
+        for (int v = lane; v < nvec; v += 32) out[v] = reinterpret_cast<const uint4 *>(stage[warp])[v];
+        __syncwarp();
+    }
+}
+
 // ---------------------------------------------------------- embedding lookup
 // out[t][0 .. D) = the dequantized row ids[t]: one warp per (token, superblock).
 template <int kFmt, bool kBf16>
@@ -459,7 +603,16 @@ static cudaError_t kq_quantize_t(int src_f32, const void *src, void *dst, int64_
 cudaError_t launch_kq_quantize(int fmt, int src_f32, const void *src, void *dst, int64_t nweights, int sms,
                                cudaStream_t stream) {
     const int64_t nb = nweights / 256;
-    if (fmt == 5) return kq_quantize_t<5>(src_f32, src, dst, nb, sms, stream);
+    if (fmt == 5) {
+        if (nb == 0) return cudaSuccess;
+        const int grid = grid_for(nb, 4 * kQuantWarps, sms);
+        uint8_t *d = static_cast<uint8_t *>(dst);
+        if (src_f32)
+            qmm_quantize_q5_k_kernel<true><<<grid, kQuantThreads, 0, stream>>>(src, d, nb);
+        else
+            qmm_quantize_q5_k_kernel<false><<<grid, kQuantThreads, 0, stream>>>(src, d, nb);
+        return cudaGetLastError();
+    }
     if (fmt == 3) return kq_quantize_t<3>(src_f32, src, dst, nb, sms, stream);
     return kq_quantize_t<2>(src_f32, src, dst, nb, sms, stream);
 }
