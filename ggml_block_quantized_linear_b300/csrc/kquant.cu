@@ -11,18 +11,22 @@
 //         (each sc + 32), d; symmetric, 16 sub-blocks of 16, 3-bit codes c + 4.
 //   Q2_K  84 bytes: scales[16] (sc | mc << 4), qs[64], d, dmin; affine, 16
 //         sub-blocks of 16, 2-bit codes.
-// Every kernel gives lane l of a warp the weights 8l .. 8l + 7 of a
-// superblock.  The ISQ kernels take the plain definition's fp32 steps in its
-// order (IEEE division, round half away for the codes, binary16
-// round-to-nearest-even for the scales), so the bytes are bit-identical; a
+// ISQ takes quantize.cu's word-level structure (one lane per sub-block,
+// codes four to a word, superblocks assembled in shared memory): the plain
+// definition's fp32 steps in its order (IEEE division or a correctly rounded
+// constant division for the scales, round half away for the codes, binary16
+// round-to-nearest-even for d and dmin), so the bytes are bit-identical; a
 // quotient that is only rounded to an integer (a weight code, a scale code)
-// is formed with the approximate reciprocal and decided exactly next to a
-// rounding tie (quantize.cu's exact_code and round_div), which gives the
-// integer that roundf of the IEEE quotient gives.
-// The linear layer is a CUDA-core kernel for every M: each weight is
+// comes from the approximate reciprocal with an exact decision next to a
+// rounding tie (round2 / exact_code / round_div), which gives the integer
+// that roundf of the IEEE quotient gives.
+// Dequantization, the embedding rows and the direct-load linear layer give
+// lane l of a warp the weights 8l .. 8l + 7 of a superblock: each weight is
 // dequantized exactly as the plain definition does (one fp32 rounding of
-// S q - Mn) and multiplied in fp32.  Q3_K and Q2_K superblocks are only 2- and
-// 4-byte aligned in a packed row, so no kernel here uses TMA boxes.
+// S q - Mn) and multiplied in fp32.  That linear layer serves what the
+// faster paths do not: Q5_K above 16 tokens (Q5_K decode runs the row-tile
+// kernel, gemv_rows.cu) and Q3_K / Q2_K above one token or with rows that
+// are not 16-byte multiples (one token runs sbrows.cu).
 #include "common.cuh"
 
 namespace qmm {
@@ -170,161 +174,6 @@ __device__ __forceinline__ void kq_lane_decode(const KqRaw &r, int lane, float (
 template <int kFmt>
 __device__ __forceinline__ void kq_lane_values(const uint8_t *blk, int lane, float (&v)[8]) {
     kq_lane_decode<kFmt>(kq_lane_load<kFmt>(blk, lane), lane, v);
-}
-
-// ------------------------------------------------------------------- ISQ
-// One warp per superblock; lane l holds weights 8l .. 8l + 7.  Codes go to a
-// per-warp byte buffer, the block is assembled in shared memory and stored
-// as halfwords (every block size is even; a block is 2-byte aligned).
-template <int kFmt, bool kSrcF32>
-__global__ void __launch_bounds__(kKqThreads) qmm_quantize_kq_kernel(const void *__restrict__ src,
-                                                                     uint8_t *__restrict__ dst,
-                                                                     int64_t nblocks) {
-    constexpr int kB = kq_bytes(kFmt);
-    __shared__ uint8_t qbuf[kKqThreads / 32][256];
-    __shared__ __align__(4) uint8_t obuf[kKqThreads / 32][176];
-    __shared__ int scbuf[kKqThreads / 32][16], mcbuf[kKqThreads / 32][16];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    uint8_t *qw = qbuf[warp], *ow = obuf[warp];
-    int *scw = scbuf[warp], *mcw = mcbuf[warp];
-    for (int64_t b = (int64_t)blockIdx.x * (kKqThreads / 32) + warp; b < nblocks;
-         b += (int64_t)gridDim.x * (kKqThreads / 32)) {
-        float x[8];
-        if constexpr (kSrcF32) {
-            const float4 *p = reinterpret_cast<const float4 *>(static_cast<const float *>(src) + b * 256 + 8 * lane);
-            const float4 v0 = __ldg(p), v1 = __ldg(p + 1);
-            x[0] = v0.x; x[1] = v0.y; x[2] = v0.z; x[3] = v0.w;
-            x[4] = v1.x; x[5] = v1.y; x[6] = v1.z; x[7] = v1.w;
-        } else {
-            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(src) + b * 256) + lane);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                x[2 * e] = __uint_as_float(w[e] << 16);
-                x[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
-            }
-        }
-        // lanes of one sub-block: 4 (Q5_K, 32 weights) or 2 (16 weights)
-        constexpr int kLanesPerSub = kFmt == 5 ? 4 : 2;
-        if constexpr (kFmt == 3) {
-            float amax = 0.f;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[e]));
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-            const float sj = __fdiv_rn(amax, 3.0f);
-            float smax = sj;
-#pragma unroll
-            for (int o = 2; o < 32; o <<= 1) smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o));
-            const __half d16 = __float2half_rn(__fdiv_rn(smax, 31.0f));
-            const float df = __half2float(d16);
-            const int sc = df > 0.f ? (int)fminf(fmaxf(round_div(sj, df), 0.f), 31.f) : 0;
-            const float S = df * (float)sc;
-            const float r = S > 0.f ? rcp_approx(S) : 0.f;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int c = S > 0.f ? (int)fminf(fmaxf(exact_code(x[e], S, r, kTieGuardQ4), -4.f), 3.f) : 0;
-                qw[8 * lane + e] = (uint8_t)(c + 4);
-            }
-            if ((lane & 1) == 0) scw[lane >> 1] = sc + 32;
-            if (lane == 0) *reinterpret_cast<uint16_t *>(ow + 108) = __half_as_ushort(d16);
-        } else {
-            constexpr float kLevels = kFmt == 5 ? 31.f : 3.f;
-            constexpr float kScaleCodes = kFmt == 5 ? 63.f : 15.f;
-            constexpr float kQMax = kFmt == 5 ? 31.f : 3.f;
-            float mx = x[0], mn = 0.f;  // max, and min(0, min)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                mx = fmaxf(mx, x[e]);
-                mn = fminf(mn, x[e]);
-            }
-#pragma unroll
-            for (int o = 1; o < kLanesPerSub; o <<= 1) {
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-                mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-            }
-            const float sj = __fdiv_rn(__fsub_rn(mx, mn), kLevels);
-            const float mj = __fsub_rn(0.f, mn);
-            float smax = sj, mmax = mj;
-#pragma unroll
-            for (int o = kLanesPerSub; o < 32; o <<= 1) {
-                smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o));
-                mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, o));
-            }
-            const __half d16 = __float2half_rn(__fdiv_rn(smax, kScaleCodes));
-            const __half m16 = __float2half_rn(__fdiv_rn(mmax, kScaleCodes));
-            const float df = __half2float(d16), dmf = __half2float(m16);
-            const int sc = df > 0.f ? (int)fminf(fmaxf(round_div(sj, df), 0.f), kScaleCodes) : 0;
-            const int mc = dmf > 0.f ? (int)fminf(fmaxf(round_div(mj, dmf), 0.f), kScaleCodes) : 0;
-            const float S = df * (float)sc, Mn = dmf * (float)mc;
-            const float r = S > 0.f ? rcp_approx(S) : 0.f;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float u = __fadd_rn(x[e], Mn);
-                const int q = S > 0.f ? (int)fminf(fmaxf(exact_code(u, S, r, kTieGuardQ4), 0.f), kQMax) : 0;
-                qw[8 * lane + e] = (uint8_t)q;
-            }
-            if (lane % kLanesPerSub == 0) {
-                scw[lane / kLanesPerSub] = sc;
-                mcw[lane / kLanesPerSub] = mc;
-            }
-            if (lane == 0) {
-                const int off = kFmt == 5 ? 0 : 80;
-                *reinterpret_cast<uint16_t *>(ow + off) = __half_as_ushort(d16);
-                *reinterpret_cast<uint16_t *>(ow + off + 2) = __half_as_ushort(m16);
-            }
-        }
-        __syncwarp();
-        if constexpr (kFmt == 5) {
-            if (lane < 4) {  // scale bytes j, j + 4, j + 8 (Q4_K's packing)
-                const int j = lane;
-                ow[4 + j] = (uint8_t)((scw[j] & 63) | ((scw[j + 4] >> 4) << 6));
-                ow[8 + j] = (uint8_t)((mcw[j] & 63) | ((mcw[j + 4] >> 4) << 6));
-                ow[12 + j] = (uint8_t)((scw[j + 4] & 15) | ((mcw[j + 4] & 15) << 4));
-            }
-            // qh byte l: bit j = bit 4 of weight l of sub-block j
-            uint32_t hb = 0;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) hb |= (uint32_t)(qw[32 * j + lane] >> 4) << j;
-            ow[16 + lane] = (uint8_t)hb;
-            // qs bytes 4l .. 4l + 3: byte 32c + l' = sub-blocks 2c (low nibble), 2c + 1 (high)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int byte = 4 * lane + i, c = byte >> 5, l2 = byte & 31;
-                ow[48 + byte] = (uint8_t)((qw[64 * c + l2] & 15) | ((qw[64 * c + 32 + l2] & 15) << 4));
-            }
-        } else {
-            // low 2 bits: byte 32 h + l' holds weight 128 h + 32 s + l' at bit 2 s
-            const int lo_base = kFmt == 3 ? 32 : 16;
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const int byte = 2 * lane + i, h = byte >> 5, l2 = byte & 31;
-                uint32_t v = 0;
-#pragma unroll
-                for (int s = 0; s < 4; ++s) v |= (uint32_t)(qw[128 * h + 32 * s + l2] & 3) << (2 * s);
-                ow[lo_base + byte] = (uint8_t)v;
-            }
-            if constexpr (kFmt == 3) {
-                // hmask byte l: bit 4 h + s = bit 2 of weight 128 h + 32 s + l
-                uint32_t hm = 0;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) hm |= (uint32_t)(qw[32 * i + lane] >> 2) << i;
-                ow[lane] = (uint8_t)hm;
-                if (lane < 8) ow[96 + lane] = (uint8_t)((scw[lane] & 15) | ((scw[lane + 8] & 15) << 4));
-                if (lane < 4) {
-                    uint32_t v = 0;
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) v |= (uint32_t)((scw[lane + 4 * k] >> 4) & 3) << (2 * k);
-                    ow[104 + lane] = (uint8_t)v;
-                }
-            } else {
-                if (lane < 16) ow[lane] = (uint8_t)(scw[lane] | (mcw[lane] << 4));
-            }
-        }
-        __syncwarp();
-        uint16_t *out = reinterpret_cast<uint16_t *>(dst + b * kB);
-        for (int i = lane; i < kB / 2; i += 32) out[i] = *reinterpret_cast<const uint16_t *>(ow + 2 * i);
-        __syncwarp();
-    }
 }
 
 // ---------------------------------------------------------- dequantization
@@ -543,6 +392,266 @@ qmm_quantize_q5_k_kernel(const void *__restrict__ src, uint8_t *__restrict__ dst
     }
 }
 
+// ------------------------------------------------------ Q3_K / Q2_K ISQ
+// The 16-weight sub-block formats on the same word-level structure: one lane
+// per sub-block (16 lanes a superblock, 2 superblocks a warp), the lane's 16
+// codes four to a word from round2 with the Q4_K tie flagging.  Lane j holds
+// weights 16j .. 16j + 15 = bytes l = 16 (j mod 2) .. + 15 of half h = j div 8
+// at shift s = (j div 2) mod 4; the low code bits of a byte come from the 4
+// lanes that differ in s, Q3_K's hmask bits from the 8 that differ in s and h,
+// gathered with shuffles (lane j moves its bits into place, the lanes OR).
+// Q3_K superblocks are 2-byte aligned in a row, Q2_K 4-byte: halfword and
+// word stores.
+template <bool kSrcF32> struct Lane16;
+template <> struct Lane16<true> {
+    float x[16];
+    __device__ __forceinline__ void load(const void *src, int64_t elem, bool valid) {
+        const float4 *p = reinterpret_cast<const float4 *>(static_cast<const float *>(src) + elem);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float4 v = valid ? __ldg(p + i) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            x[4 * i] = v.x;
+            x[4 * i + 1] = v.y;
+            x[4 * i + 2] = v.z;
+            x[4 * i + 3] = v.w;
+        }
+    }
+    __device__ __forceinline__ uint64_t pair(int i) const { return f2_pack(x[i], x[i + 1]); }
+    static __device__ __forceinline__ float reload(const void *src, int64_t elem, int j) {
+        return __ldg(static_cast<const float *>(src) + elem + j);
+    }
+    __device__ __forceinline__ void extremes(float &mx, float &mn) const {
+        mx = x[0];
+        mn = x[0];
+#pragma unroll
+        for (int i = 1; i < 16; ++i) {
+            mx = fmaxf(mx, x[i]);
+            mn = fminf(mn, x[i]);
+        }
+    }
+};
+template <> struct Lane16<false> {
+    uint32_t w[8];
+    __device__ __forceinline__ void load(const void *src, int64_t elem, bool valid) {
+        const uint4 *p = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(src) + elem);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const uint4 v = valid ? __ldg(p + i) : make_uint4(0u, 0u, 0u, 0u);
+            w[4 * i] = v.x;
+            w[4 * i + 1] = v.y;
+            w[4 * i + 2] = v.z;
+            w[4 * i + 3] = v.w;
+        }
+    }
+    __device__ __forceinline__ uint64_t pair(int i) const { return f2_from_bf16x2(w[i >> 1]); }
+    static __device__ __forceinline__ float reload(const void *src, int64_t elem, int j) {
+        return __uint_as_float((uint32_t)__ldg(static_cast<const unsigned short *>(src) + elem + j) << 16);
+    }
+    __device__ __forceinline__ void extremes(float &mx, float &mn) const {
+        __nv_bfloat162 vmax = *reinterpret_cast<const __nv_bfloat162 *>(&w[0]), vmin = vmax;
+#pragma unroll
+        for (int i = 1; i < 8; ++i) {
+            const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162 *>(&w[i]);
+            vmax = __hmax2(vmax, v);
+            vmin = __hmin2(vmin, v);
+        }
+        mx = fmaxf(__low2float(vmax), __high2float(vmax));
+        mn = fminf(__low2float(vmin), __high2float(vmin));
+    }
+};
+
+template <int kFmt, bool kSrcF32>
+__global__ void __launch_bounds__(kQuantThreads, QMM_Q4_QUANT_MIN_BLOCKS)
+qmm_quantize_k16_kernel(const void *__restrict__ src, uint8_t *__restrict__ dst, int64_t nsuper) {
+    static_assert(kFmt == 3 || kFmt == 2, "16-weight sub-block formats");
+    constexpr int kB = kq_bytes(kFmt);            // 110 / 84
+    constexpr int kLo = kFmt == 3 ? 32 : 16;      // the low-bit (qs) bytes
+    constexpr float kQLo = kFmt == 3 ? -4.0f : 0.0f, kQHi = 3.0f;
+    __shared__ __align__(16) uint8_t stage[kQuantWarps][2 * kB];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int sj = lane & 15, sbl = lane >> 4;  // sub-block j, superblock in the warp tile
+    const int hh = sj >> 3, ss = (sj >> 1) & 3, pp = sj & 1;
+    uint8_t *st = stage[warp] + sbl * kB;
+    const int64_t nwarps = (int64_t)gridDim.x * kQuantWarps;
+    const int64_t step = nwarps * 2;
+    int64_t s0 = ((int64_t)blockIdx.x * kQuantWarps + warp) * 2;
+    Lane16<kSrcF32> Ln;
+    if (!kSrcF32) Ln.load(src, (s0 + sbl) * 256 + sj * 16, s0 + sbl < nsuper);
+    for (; s0 < nsuper; s0 += step) {
+        const int64_t sb = s0 + sbl;
+        const bool valid = sb < nsuper;  // uniform over each half-warp
+        const int nvalid = (int)min((int64_t)2, nsuper - s0);
+        Lane16<kSrcF32> L;
+        if constexpr (kSrcF32) {
+            L.load(src, sb * 256 + sj * 16, valid);
+        } else {
+            L = Ln;
+            Ln.load(src, (sb + step) * 256 + sj * 16, sb + step < nsuper);
+        }
+        float mx, mn;
+        L.extremes(mx, mn);
+        float S = 0.0f, Mn = 0.0f, v0 = 0.0f, v1 = 0.0f;  // v0, v1: the lane's scale codes
+        __half dh, dminh = __ushort_as_half((unsigned short)0);
+        if constexpr (kFmt == 3) {
+            // symmetric: s_j = max |x| / 3, d = fp16(max_j s_j / 31), sc in 0..31
+            float amax = fmaxf(mx, -mn);
+            amax = amax > 0.0f ? amax : 0.0f;
+            const float s = __fdiv_rn(amax, 3.0f);
+            float smax = s;
+#pragma unroll
+            for (int o = 1; o <= 8; o <<= 1) smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o));
+            smax = smax > 0.0f ? smax : 0.0f;
+            dh = __float2half_rn(__fdiv_rn(smax, 31.0f));
+            const float df = __half2float(dh);
+            v0 = df > 0.0f ? clamp_f(round_div(s, df), 0.0f, 31.0f) : 0.0f;
+            S = __fmul_rn(df, v0);
+        } else {
+            // affine: s_j = (max - min(0, min)) / 3, m_j = 0 - min(0, min), d, dmin = fp16(max / 15)
+            mn = fminf(0.0f, mn);
+            const float s = __fdiv_rn(__fsub_rn(mx, mn), 3.0f);
+            const float m = __fsub_rn(0.0f, mn);
+            float smax = s, mmax = m;
+#pragma unroll
+            for (int o = 1; o <= 8; o <<= 1) {
+                smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o));
+                mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, o));
+            }
+            smax = smax > 0.0f ? smax : 0.0f;
+            mmax = mmax > 0.0f ? mmax : 0.0f;
+            dh = __float2half_rn(div_const<15>(smax));
+            dminh = __float2half_rn(div_const<15>(mmax));
+            const float df = __half2float(dh), dminf = __half2float(dminh);
+            v0 = df > 0.0f ? clamp_f(round_div(s, df), 0.0f, 15.0f) : 0.0f;
+            v1 = dminf > 0.0f ? clamp_f(round_div(m, dminf), 0.0f, 15.0f) : 0.0f;
+            S = __fmul_rn(df, v0);
+            Mn = __fmul_rn(dminf, v1);
+        }
+        // codes q (Q3_K: c + 4 with c in -4..3; Q2_K: 0..3), one per byte
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) w[i] = kFmt == 3 ? 0x04040404u : 0u;
+        float r = 0.0f;
+        bool tie = false;
+        if (S > 0.0f) {
+            r = rcp_approx(S);
+            const uint64_t r2 = f2_pack(r, r), mn2 = f2_pack(Mn, Mn);
+            float dev = 0.0f;
+            auto u2 = [&](int i) { return kFmt == 3 ? L.pair(i) : f2_add(L.pair(i), mn2); };
+            const float khi = __fmul_rn(kFmt == 3 ? mx : __fadd_rn(mx, Mn), r);
+            const float klo = __fmul_rn(kFmt == 3 ? mn : __fadd_rn(mn, Mn), r);
+            if (khi < 30000.0f && klo > -30000.0f) {
+                // 16-bit pairs: (k - lo) clamped to [0, hi - lo]
+                auto code2 = [&](int i) {
+                    const uint64_t v = round2(u2(i), r2, dev);
+                    uint32_t k2 = prmt((uint32_t)v, (uint32_t)(v >> 32), 0x5410u);
+                    if constexpr (kFmt == 3) k2 = __vadd2(k2, 0x00040004u);
+                    return __vimin_s16x2_relu(k2, kFmt == 3 ? 0x00070007u : 0x00030003u);
+                };
+#pragma unroll
+                for (int i = 0; i < 4; ++i) w[i] = prmt(code2(4 * i), code2(4 * i + 2), 0x6420u);
+            } else {
+                auto code2 = [&](int i) { return clamp2(round2(u2(i), r2, dev), kQLo, kQHi); };
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    w[i] = pack4_magic(code2(4 * i), code2(4 * i + 2));
+                    if constexpr (kFmt == 3) w[i] = __vadd4(w[i], 0x04040404u);
+                }
+            }
+            // codes matter up to |Q| = 4.5: Q4_K's guard holds
+            tie = valid && dev >= kTieGuardQ4;
+        }
+        // low 2 bits to bits 2s of their bytes, ORed over the 4 lanes that differ in s
+        uint32_t lo[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) lo[i] = (w[i] & 0x03030303u) << (2 * ss);
+#pragma unroll
+        for (int o = 2; o <= 4; o <<= 1)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) lo[i] |= __shfl_xor_sync(0xffffffffu, lo[i], o);
+        uint32_t hb[4];  // Q3_K: bit 2 of q to bit 4h + s, ORed over the 8 lanes that differ in s, h
+        if constexpr (kFmt == 3) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) hb[i] = ((w[i] >> 2) & 0x01010101u) << (4 * hh + ss);
+#pragma unroll
+            for (int o = 2; o <= 8; o <<= 1)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) hb[i] |= __shfl_xor_sync(0xffffffffu, hb[i], o);
+        }
+        const int iv0 = (int)v0, iv1 = (int)v1;
+        // Q3_K scale fields (sc + 32): byte j < 8 = field j | field j + 8 << 4; byte
+        // 8 + j (j < 4) = bits 4-5 of fields j, j + 4, j + 8, j + 12 at bits 0, 2, 4, 6
+        const int f0 = iv0 + 32;
+        const int f4 = __shfl_down_sync(0xffffffffu, f0, 4), f8 = __shfl_down_sync(0xffffffffu, f0, 8);
+        const int f12 = __shfl_down_sync(0xffffffffu, f0, 12);
+        if (valid) {
+            if ((sj & 6) == 0) {  // s == 0: 16 qs bytes at kLo + 32 h + 16 p
+                uint16_t *o = reinterpret_cast<uint16_t *>(st + kLo + 32 * hh + 16 * pp);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    o[2 * i] = (uint16_t)(lo[i] & 0xFFFFu);
+                    o[2 * i + 1] = (uint16_t)(lo[i] >> 16);
+                }
+            }
+            if constexpr (kFmt == 3) {
+                if ((sj & 14) == 0) {  // s == 0, h == 0: 16 hmask bytes at 16 p
+                    uint16_t *o = reinterpret_cast<uint16_t *>(st + 16 * pp);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        o[2 * i] = (uint16_t)(hb[i] & 0xFFFFu);
+                        o[2 * i + 1] = (uint16_t)(hb[i] >> 16);
+                    }
+                }
+                if (sj < 8) st[96 + sj] = (uint8_t)((f0 & 15) | ((f8 & 15) << 4));
+                if (sj < 4)
+                    st[104 + sj] = (uint8_t)(((f0 >> 4) & 3) | (((f4 >> 4) & 3) << 2) | (((f8 >> 4) & 3) << 4) |
+                                             (((f12 >> 4) & 3) << 6));
+                if (sj == 0) *reinterpret_cast<uint16_t *>(st + 108) = __half_as_ushort(dh);
+            } else {
+                st[sj] = (uint8_t)(iv0 | (iv1 << 4));
+                if (sj == 0) {
+                    *reinterpret_cast<uint16_t *>(st + 80) = __half_as_ushort(dh);
+                    *reinterpret_cast<uint16_t *>(st + 82) = __half_as_ushort(dminh);
+                }
+            }
+        }
+        __syncwarp();
+        // sub-blocks with a possible tie: lanes 0-15 recompute weight `lane` of
+        // the flagged sub-block and overwrite its code bits
+        for (uint32_t fl = __ballot_sync(0xffffffffu, tie); fl != 0; fl &= fl - 1) {
+            const int l = __ffs(fl) - 1, jl = l & 15;
+            const float Sl = __shfl_sync(0xffffffffu, S, l), rl = __shfl_sync(0xffffffffu, r, l);
+            const float Ml = __shfl_sync(0xffffffffu, Mn, l);
+            if (lane < 16) {
+                const float x = Lane16<kSrcF32>::reload(src, (s0 + (l >> 4)) * 256 + jl * 16, lane);
+                const float u = kFmt == 3 ? x : __fadd_rn(x, Ml);
+                const uint32_t q = (uint32_t)((int)clamp_f(exact_code(u, Sl, rl, kTieGuardQ4), kQLo, kQHi) -
+                                              (int)kQLo);
+                const int h = jl >> 3, s2 = 2 * ((jl >> 1) & 3), byte = 16 * (jl & 1) + lane;
+                uint8_t *sbp = stage[warp] + (l >> 4) * kB;
+                uint8_t *qb = sbp + kLo + 32 * h + byte;
+                *qb = (uint8_t)((*qb & ~(3u << s2)) | ((q & 3u) << s2));
+                if constexpr (kFmt == 3) {
+                    const int hbit = 4 * h + (s2 >> 1);
+                    uint8_t *hm = sbp + byte;
+                    *hm = (uint8_t)((*hm & ~(1u << hbit)) | (((q >> 2) & 1u) << hbit));
+                }
+            }
+            __syncwarp();
+        }
+        // the superblocks: halfwords (Q3_K, 2-byte aligned) or words (Q2_K)
+        if constexpr (kFmt == 3) {
+            const int n = nvalid * kB / 2;
+            uint16_t *out = reinterpret_cast<uint16_t *>(dst + s0 * kB);
+            for (int v = lane; v < n; v += 32) out[v] = reinterpret_cast<const uint16_t *>(stage[warp])[v];
+        } else {
+            const int n = nvalid * kB / 4;
+            uint32_t *out = reinterpret_cast<uint32_t *>(dst + s0 * kB);
+            for (int v = lane; v < n; v += 32) out[v] = reinterpret_cast<const uint32_t *>(stage[warp])[v];
+        }
+        __syncwarp();
+    }
+}
+
 // ---------------------------------------------------------- embedding lookup
 // out[t][0 .. D) = the dequantized row ids[t]: one warp per (token, superblock).
 template <int kFmt, bool kBf16>
@@ -589,17 +698,6 @@ static int kq_grid(int64_t warps_of_work, int sms) {
     return (int)(ctas < 1 ? 1 : ctas < cap ? ctas : cap);
 }
 
-template <int kFmt>
-static cudaError_t kq_quantize_t(int src_f32, const void *src, void *dst, int64_t nblocks, int sms,
-                                 cudaStream_t stream) {
-    uint8_t *d = static_cast<uint8_t *>(dst);
-    if (src_f32)
-        qmm_quantize_kq_kernel<kFmt, true><<<kq_grid(nblocks, sms), kKqThreads, 0, stream>>>(src, d, nblocks);
-    else
-        qmm_quantize_kq_kernel<kFmt, false><<<kq_grid(nblocks, sms), kKqThreads, 0, stream>>>(src, d, nblocks);
-    return cudaGetLastError();
-}
-
 cudaError_t launch_kq_quantize(int fmt, int src_f32, const void *src, void *dst, int64_t nweights, int sms,
                                cudaStream_t stream) {
     const int64_t nb = nweights / 256;
@@ -613,8 +711,17 @@ cudaError_t launch_kq_quantize(int fmt, int src_f32, const void *src, void *dst,
             qmm_quantize_q5_k_kernel<false><<<grid, kQuantThreads, 0, stream>>>(src, d, nb);
         return cudaGetLastError();
     }
-    if (fmt == 3) return kq_quantize_t<3>(src_f32, src, dst, nb, sms, stream);
-    return kq_quantize_t<2>(src_f32, src, dst, nb, sms, stream);
+    if (nb == 0) return cudaSuccess;
+    const int grid = grid_for(nb, 2 * kQuantWarps, sms);
+    uint8_t *d = static_cast<uint8_t *>(dst);
+    if (fmt == 3) {
+        if (src_f32) qmm_quantize_k16_kernel<3, true><<<grid, kQuantThreads, 0, stream>>>(src, d, nb);
+        else qmm_quantize_k16_kernel<3, false><<<grid, kQuantThreads, 0, stream>>>(src, d, nb);
+    } else {
+        if (src_f32) qmm_quantize_k16_kernel<2, true><<<grid, kQuantThreads, 0, stream>>>(src, d, nb);
+        else qmm_quantize_k16_kernel<2, false><<<grid, kQuantThreads, 0, stream>>>(src, d, nb);
+    }
+    return cudaGetLastError();
 }
 
 cudaError_t launch_kq_dequantize(int fmt, const void *src, float *dst, int64_t nweights, int sms,
