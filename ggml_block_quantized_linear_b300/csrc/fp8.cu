@@ -8,6 +8,8 @@
 // scales: one fp32 scale per output row, s = max |x| / 448, codes
 // E4M3(x / s) rounded to nearest even and saturated at +-448.  A packed row
 // is K codes, s, 12 zero bytes (K + 16 bytes, so rows stay 16-byte aligned).
+#include <atomic>
+
 #include "common.cuh"
 
 namespace qmm {
@@ -81,6 +83,124 @@ __global__ void __launch_bounds__(kFp8Threads) qmm_quantize_fp8_kernel(const voi
     }
 }
 
+// E4M3 codes of x / s for 8 weights (s > 0, rs = rcp_approx(s)), identical
+// to converting the IEEE quotient RN(x / s): y = RN(x rs) is within
+// 2^-22 |y| of it (rs within an ulp of 1 / s, two roundings), so RN(x / s)
+// lies between y (1 - 2^-21) and y (1 + 2^-21).  The conversion (round to
+// nearest even, saturating) is monotone, so when both ends give the same
+// code that is the code; otherwise (an E4M3 rounding boundary within the
+// interval) the pair is converted from the IEEE quotient.
+__device__ __forceinline__ uint32_t fp8_codes4(const float (&x)[8], int o, float s, float rs) {
+    uint32_t out = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const float a = x[o + 2 * h], b = x[o + 2 * h + 1];
+        const float ya = __fmul_rn(a, rs), yb = __fmul_rn(b, rs);
+        const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(__fmul_rn(ya, 0.99999952316284180f),
+                                                                 __fmul_rn(yb, 0.99999952316284180f)),
+                                                     __NV_SATFINITE, __NV_E4M3);
+        const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(__fmul_rn(ya, 1.00000047683715820f),
+                                                                 __fmul_rn(yb, 1.00000047683715820f)),
+                                                     __NV_SATFINITE, __NV_E4M3);
+        uint32_t c = lo & 0xFFFFu;
+        if (c != (hi & 0xFFFFu))
+            c = __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(a, s), __fdiv_rn(b, s)), __NV_SATFINITE, __NV_E4M3) &
+                0xFFFFu;
+        out |= c << (16 * h);
+    }
+    return out;
+}
+
+// Rows staged in shared memory: each CTA takes rows b, b + G, ...; one bulk
+// copy brings a whole row (K bf16 or fp32 values) into one of nbuf buffers
+// while the rows before it are quantized from the others, so every weight is
+// read from memory once and nbuf - 1 row copies stay in flight.
+template <bool kSrcF32>
+__global__ void __launch_bounds__(kFp8Threads) qmm_quantize_fp8_staged_kernel(const void *__restrict__ src,
+                                                                              uint8_t *__restrict__ dst,
+                                                                              int64_t rows, int64_t K, int nbuf) {
+    constexpr int kE = kSrcF32 ? 4 : 2;
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ float red[kFp8Threads / 32];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t rowb = (uint32_t)(K * kE);
+    const uint32_t bar0 = smem_addr(smem + nbuf * rowb);
+    const int64_t rb = K + kFp8RowPad;
+    const char *srcb = static_cast<const char *>(src);
+    if (tid == 0) {
+        for (int b = 0; b < nbuf; ++b) mbar_init(bar0 + 8u * b, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    // the first nbuf - 1 rows
+    if (tid == 0)
+        for (int j = 0; j < nbuf - 1; ++j) {
+            const int64_t rj = blockIdx.x + (int64_t)j * gridDim.x;
+            if (rj >= rows) break;
+            mbar_arrive_expect_tx(bar0 + 8u * j, rowb);
+            bulk_g2s(smem_addr(smem + j * rowb), srcb + rj * rowb, rowb, bar0 + 8u * j);
+        }
+    bool ok = true;
+    int i = 0;
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x, ++i) {
+        const int b = i % nbuf;
+        // the buffer of row i - 1 was last read in the previous iteration
+        // (closed by its final __syncthreads): bring row i + nbuf - 1 there
+        const int64_t rn = r + (int64_t)(nbuf - 1) * gridDim.x;
+        if (tid == 0 && rn < rows) {
+            const int bn = (i + nbuf - 1) % nbuf;
+            mbar_arrive_expect_tx(bar0 + 8u * bn, rowb);
+            bulk_g2s(smem_addr(smem + bn * rowb), srcb + rn * rowb, rowb, bar0 + 8u * bn);
+        }
+        if (ok) ok = mbar_wait(bar0 + 8u * b, (i / nbuf) & 1, kErrGemvFullWait);
+        const uint8_t *row = smem + b * rowb;
+        auto load8 = [&](int64_t k, float (&x)[8]) {
+            if constexpr (kSrcF32) {
+                const float4 v0 = *reinterpret_cast<const float4 *>(row + 4 * k);
+                const float4 v1 = *reinterpret_cast<const float4 *>(row + 4 * k + 16);
+                x[0] = v0.x; x[1] = v0.y; x[2] = v0.z; x[3] = v0.w;
+                x[4] = v1.x; x[5] = v1.y; x[6] = v1.z; x[7] = v1.w;
+            } else {
+                const uint4 v = *reinterpret_cast<const uint4 *>(row + 2 * k);
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    x[2 * e] = __uint_as_float(w[e] << 16);
+                    x[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+                }
+            }
+        };
+        float amax = 0.f;
+        if (ok)
+            for (int64_t k = 8 * (int64_t)tid; k < K; k += 8 * kFp8Threads) {
+                float x[8];
+                load8(k, x);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[e]));
+            }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        if (lane == 0) red[warp] = amax;
+        __syncthreads();
+        amax = red[0];
+#pragma unroll
+        for (int w = 1; w < kFp8Threads / 32; ++w) amax = fmaxf(amax, red[w]);
+        const float s = __fdiv_rn(amax, 448.0f);
+        const float rs = s > 0.f ? rcp_approx(s) : 0.f;
+        uint8_t *out = dst + r * rb;
+        if (ok)
+            for (int64_t k = 8 * (int64_t)tid; k < K; k += 8 * kFp8Threads) {
+                float x[8];
+                load8(k, x);
+                uint2 q = make_uint2(0u, 0u);
+                if (s > 0.f) q = make_uint2(fp8_codes4(x, 0, s, rs), fp8_codes4(x, 4, s, rs));
+                *reinterpret_cast<uint2 *>(out + k) = q;
+            }
+        if (tid == 0) *reinterpret_cast<uint4 *>(out + K) = make_uint4(__float_as_uint(s), 0u, 0u, 0u);
+        __syncthreads();  // buffer b and red are reused
+    }
+}
+
 // 8 weights per thread: value * row scale (one fp32 rounding).
 __global__ void __launch_bounds__(kFp8Threads) qmm_dequantize_fp8_kernel(const uint8_t *__restrict__ src,
                                                                          float *__restrict__ dst, int64_t rows,
@@ -115,8 +235,35 @@ static int fp8_grid(int64_t units, int sms) {
 
 cudaError_t launch_fp8_quantize(int src_f32, const void *src, void *dst, int64_t rows, int64_t K, int sms,
                                 cudaStream_t stream) {
-    const int grid = fp8_grid(rows, sms);
     uint8_t *d = static_cast<uint8_t *>(dst);
+    // two row buffers (and their barriers) in shared memory, while they fit;
+    // more buffers measured slower (fewer resident CTAs: the per-row
+    // reduction chain, not the copies, sets the pace)
+    const int64_t rowb = K * (src_f32 ? 4 : 2);
+    const int nbuf = 2;
+    const int64_t smem = nbuf * rowb + 8 * nbuf;
+    constexpr int kMaxSmem = 200 * 1024 + 32;  // the attribute covers every size this path launches
+    if (smem <= kMaxSmem) {
+        static std::atomic<uint64_t> done_f{0}, done_b{0};
+        const void *fn = src_f32 ? reinterpret_cast<const void *>(qmm_quantize_fp8_staged_kernel<true>)
+                                 : reinterpret_cast<const void *>(qmm_quantize_fp8_staged_kernel<false>);
+        cudaError_t e = set_smem_limit_once(fn, kMaxSmem, src_f32 ? done_f : done_b);
+        if (e != cudaSuccess) return e;
+        int occ = 0;
+        e = src_f32 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, qmm_quantize_fp8_staged_kernel<true>,
+                                                                     kFp8Threads, (size_t)smem)
+                    : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, qmm_quantize_fp8_staged_kernel<false>,
+                                                                     kFp8Threads, (size_t)smem);
+        if (e != cudaSuccess) return e;
+        const int64_t cap = (int64_t)sms * (occ < 1 ? 1 : occ);
+        const int grid = (int)(rows < cap ? rows : cap);
+        if (src_f32)
+            qmm_quantize_fp8_staged_kernel<true><<<grid, kFp8Threads, (size_t)smem, stream>>>(src, d, rows, K, nbuf);
+        else
+            qmm_quantize_fp8_staged_kernel<false><<<grid, kFp8Threads, (size_t)smem, stream>>>(src, d, rows, K, nbuf);
+        return cudaGetLastError();
+    }
+    const int grid = fp8_grid(rows, sms);
     if (src_f32)
         qmm_quantize_fp8_kernel<true><<<grid, kFp8Threads, 0, stream>>>(src, d, rows, K);
     else

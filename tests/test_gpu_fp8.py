@@ -37,6 +37,20 @@ def cases():
     row[200] = 448.0
     row[201:201 + 20] = -mids[-20:]
     c["midpoints"] = (np.tile(row, (3, 2)) * 2.0 ** -8).astype(np.float32)
+    # a scale that is not a power of two (amax 0.7): each E4M3 midpoint times s
+    # and its float neighbours 1 and 2 ulps away, where x / s rounds next to a
+    # rounding boundary of E4M3 (the quotient must be the IEEE one)
+    sc = np.float32(np.float32(0.7) / np.float32(448.0))
+    near = []
+    for mval in mids:
+        v = np.float32(mval * np.float64(sc))
+        near += [v, np.nextafter(v, np.float32(1)), np.nextafter(v, np.float32(-1)),
+                 np.nextafter(np.nextafter(v, np.float32(1)), np.float32(1)),
+                 np.nextafter(np.nextafter(v, np.float32(-1)), np.float32(-1))]
+    r2 = np.zeros(1024, dtype=np.float32)
+    r2[0] = 0.7
+    r2[1:1 + len(near)] = near
+    c["near_midpoints"] = np.stack([r2, -r2, r2[::-1].copy()])
     return c
 
 
