@@ -176,6 +176,65 @@ __device__ __forceinline__ void kq_lane_values(const uint8_t *blk, int lane, flo
     kq_lane_decode<kFmt>(kq_lane_load<kFmt>(blk, lane), lane, v);
 }
 
+// For the matmul: lane l's 8 codes as exact floats (Q3_K: q - 4) with the
+// sub-block's S (and Mn), so that its share of a dot product is
+// S * sum(c x) - Mn * sum(x) -- the scale and the min applied once per
+// superblock instead of once per weight.
+struct KqCodes {
+    float S, Mn;
+    float c[8];
+};
+template <int kFmt>
+__device__ __forceinline__ KqCodes kq_lane_codes(const KqRaw &r, int lane) {
+    KqCodes k;
+    const int s = (lane >> 2) & 3, h = lane >> 4;
+    uint32_t q0, q1;
+    float bias = 8388608.0f;  // byte b under the float 2^23 exponent is 2^23 + b
+    if constexpr (kFmt == 5) {
+        const int j = lane >> 2, nsh = 4 * (j & 1);
+        k.S = __half2float(__ushort_as_half((unsigned short)(r.s0 & 0xFFFF))) * (float)(r.s1 & 0xFF);
+        k.Mn = __half2float(__ushort_as_half((unsigned short)(r.s0 >> 16))) * (float)(r.s1 >> 8);
+        q0 = ((r.a0 >> nsh) & 0x0F0F0F0Fu) | (((r.b0 >> j) & 0x01010101u) << 4);
+        q1 = ((r.a1 >> nsh) & 0x0F0F0F0Fu) | (((r.b1 >> j) & 0x01010101u) << 4);
+    } else if constexpr (kFmt == 3) {
+        k.S = __half2float(__ushort_as_half((unsigned short)r.s1)) * (float)((int)r.s0 - 32);
+        k.Mn = 0.f;
+        const int hb = 4 * h + s;
+        q0 = ((r.a0 >> (2 * s)) & 0x03030303u) | (((r.b0 >> hb) & 0x01010101u) << 2);
+        q1 = ((r.a1 >> (2 * s)) & 0x03030303u) | (((r.b1 >> hb) & 0x01010101u) << 2);
+        bias = 8388612.0f;  // 2^23 + 4: the code minus 4, exactly
+    } else {
+        k.S = __half2float(__ushort_as_half((unsigned short)(r.s1 & 0xFFFF))) * (float)(r.s0 & 15);
+        k.Mn = __half2float(__ushort_as_half((unsigned short)(r.s1 >> 16))) * (float)(r.s0 >> 4);
+        q0 = (r.a0 >> (2 * s)) & 0x03030303u;
+        q1 = (r.a1 >> (2 * s)) & 0x03030303u;
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        k.c[e] = __uint_as_float(__byte_perm(q0, 0x4B000000u, 0x7440u + e)) - bias;
+        k.c[4 + e] = __uint_as_float(__byte_perm(q1, 0x4B000000u, 0x7440u + e)) - bias;
+    }
+    return k;
+}
+// acc + S * sum_k c_k x_k - Mn * sum_k x_k over the lane's 8 bf16 activations
+// (xw: pairs, lower index in the low half), the sums in k order.
+template <int kFmt>
+__device__ __forceinline__ float kq_codes_dot(const KqCodes &k, const uint32_t (&xw)[4], float acc) {
+    float p = 0.f, sx = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float xa = __uint_as_float(xw[e] << 16), xb = __uint_as_float(xw[e] & 0xFFFF0000u);
+        p = fmaf(k.c[2 * e], xa, p);
+        p = fmaf(k.c[2 * e + 1], xb, p);
+        if constexpr (kFmt != 3) {
+            sx = __fadd_rn(sx, xa);
+            sx = __fadd_rn(sx, xb);
+        }
+    }
+    if constexpr (kFmt == 3) return fmaf(k.S, p, acc);
+    else return fmaf(k.S, p, fmaf(-k.Mn, sx, acc));
+}
+
 // ---------------------------------------------------------- dequantization
 template <int kFmt>
 __global__ void __launch_bounds__(kKqThreads) qmm_dequantize_kq_kernel(const uint8_t *__restrict__ src,
@@ -193,8 +252,11 @@ __global__ void __launch_bounds__(kKqThreads) qmm_dequantize_kq_kernel(const uin
 
 // ------------------------------------------------------------------ matmul
 // Y[M x N] = X[M x K] W^T.  A warp owns one weight row at a time; lane l takes
-// weights 8l .. 8l + 7 of each superblock, dequantized once per pass and
-// multiplied by up to kTok token rows; fp32 sums reduced across the warp.
+// weights 8l .. 8l + 7 of each superblock, decoded once per pass for up to
+// kTok token rows: one token takes the exact codes and applies the sub-block
+// scale and min once (kq_codes_dot); a pass of 8 dequantizes each weight once
+// (one fp32 rounding) and multiplies it by the 8 tokens.  fp32 sums reduced
+// across the warp.
 template <int kFmt, int kTok>
 __global__ void __launch_bounds__(kKqThreads, kTok == 1 ? 3 : 2) qmm_matmul_kq_kernel(const uint8_t *__restrict__ W,
                                                                    const uint16_t *__restrict__ X,
@@ -220,18 +282,25 @@ __global__ void __launch_bounds__(kKqThreads, kTok == 1 ? 3 : 2) qmm_matmul_kq_k
 #pragma unroll
                 for (int u = 0; u < kU; ++u) {
                     if (sb0 + u >= nsb) break;
-                    float v[8];
-                    kq_lane_decode<kFmt>(raw[u], lane, v);
+                    if constexpr (kTok == 1) {
+                        const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(X + (int64_t)m0 * K +
+                                                                               (int64_t)(sb0 + u) * 256 + 8 * lane));
+                        const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
+                        acc[0] = kq_codes_dot<kFmt>(kq_lane_codes<kFmt>(raw[u], lane), w, acc[0]);
+                    } else {
+                        float v[8];
+                        kq_lane_decode<kFmt>(raw[u], lane, v);
 #pragma unroll
-                    for (int t = 0; t < kTok; ++t) {
-                        if (t < mt) {
-                            const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(X + (int64_t)(m0 + t) * K +
-                                                                                   (int64_t)(sb0 + u) * 256 + 8 * lane));
-                            const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
+                        for (int t = 0; t < kTok; ++t) {
+                            if (t < mt) {
+                                const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(
+                                    X + (int64_t)(m0 + t) * K + (int64_t)(sb0 + u) * 256 + 8 * lane));
+                                const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                acc[t] = fmaf(v[2 * e], __uint_as_float(w[e] << 16), acc[t]);
-                                acc[t] = fmaf(v[2 * e + 1], __uint_as_float(w[e] & 0xFFFF0000u), acc[t]);
+                                for (int e = 0; e < 4; ++e) {
+                                    acc[t] = fmaf(v[2 * e], __uint_as_float(w[e] << 16), acc[t]);
+                                    acc[t] = fmaf(v[2 * e + 1], __uint_as_float(w[e] & 0xFFFF0000u), acc[t]);
+                                }
                             }
                         }
                     }

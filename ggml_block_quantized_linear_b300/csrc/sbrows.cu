@@ -11,9 +11,10 @@
 // consumer warps each own one row of a box and decode it with the CUDA-core
 // lane decoders of q6k.cu and kquant.cu (lane l: weights 8l .. 8l + 7 of a
 // superblock), reading the superblocks from shared memory instead of global
-// memory.  A row's sum is formed in the same order as the direct-load
-// kernels (per lane over the superblocks in order, then a fixed butterfly
-// across the lanes), so the results are the same.
+// memory.  A row's sum is formed as in the direct-load kernels at one token
+// (per lane over the superblocks in order, exact codes with the sub-block
+// scale applied once per superblock, then a fixed butterfly across the
+// lanes), so the results are the same bits.
 // CTAs are persistent over 8-row tiles (CTA b takes tiles b, b + G, ...);
 // every wait is bounded (common.cuh); programmatic dependent launch as in
 // the other decode kernels.
@@ -49,7 +50,7 @@ struct SbParams {
 
 // One superblock of one row against the token: lane l's 8 weights times the
 // activations at xsb (the superblock's 256 bf16 values in shared memory),
-// added to acc in the direct-load kernels' order.
+// added to acc in the one-token direct-load kernels' order.
 template <int kFmt>
 __device__ __forceinline__ void sb_lane_dot(const uint8_t *blk, const uint16_t *xsb, int lane, float &acc) {
     if constexpr (kFmt == 6) {
@@ -67,15 +68,10 @@ __device__ __forceinline__ void sb_lane_dot(const uint8_t *blk, const uint16_t *
         }
         acc = fmaf(S, part, acc);
     } else {
-        float v[8];
-        kq_lane_decode<kFmt>(kq_lane_load<kFmt, true>(blk, lane), lane, v);
+        const KqCodes kc = kq_lane_codes<kFmt>(kq_lane_load<kFmt, true>(blk, lane), lane);
         const uint4 xv = *reinterpret_cast<const uint4 *>(xsb + 8 * lane);
         const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            acc = fmaf(v[2 * e], __uint_as_float(w[e] << 16), acc);
-            acc = fmaf(v[2 * e + 1], __uint_as_float(w[e] & 0xFFFF0000u), acc);
-        }
+        acc = kq_codes_dot<kFmt>(kc, w, acc);
     }
 }
 

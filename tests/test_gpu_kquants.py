@@ -163,20 +163,25 @@ def test_one_token_tma_path(fmt, n, k):
     assert q.qmm_device_error_take() == 0
 
 
-# Rows that are not 16-byte multiples take the direct-load kernel (Q3_K with
-# 12 superblocks: 1320 bytes); both kernels form each row's sum in the same
-# order, so a 16-byte-multiple row gives the same bits through either.
+# Rows that are not 16-byte multiples take the direct-load kernel (Q3_K and
+# Q2_K with 12 superblocks: 1320 bytes; Q2_K's 1008 bytes are a multiple and
+# take the TMA path); one token on the direct-load kernel forms each row's sum
+# exactly as the TMA path does, which a TMA-path row of the same weights shows.
 def test_one_token_fallback_and_same_order():
     n, k = 129, 3072
     w = inputs.weights(n, k, 85)
-    packed = oracle.quantize(q.QMM_Q3_K, inputs.bf16_bits(w))
     xb = inputs.bf16_bits(inputs.activations(1, k, 86))
-    Y, A = oracle.matmul(q.QMM_Q3_K, packed, xb, n, k)
-    check_matmul(q.qmm_matmul(q.QMM_Q3_K, to_dev_u8(packed), bf16_from_bits(xb), n), Y, A, "fallback")
-    # Q2_K, 12 superblocks (1008 bytes, TMA path) against the same rows at M = 2
-    # (direct loads, first token the same): identical first row of outputs
-    packed2 = oracle.quantize(q.QMM_Q2_K, inputs.bf16_bits(w))
-    x2 = inputs.activations(2, k, 87)
-    y1 = q.qmm_matmul(q.QMM_Q2_K, to_dev_u8(packed2), x2[:1].contiguous().to(DEV), n)
-    y2 = q.qmm_matmul(q.QMM_Q2_K, to_dev_u8(packed2), x2.to(DEV), n)
-    assert torch.equal(y1[0], y2[0])
+    for fmt in (q.QMM_Q3_K, q.QMM_Q2_K):
+        packed = oracle.quantize(fmt, inputs.bf16_bits(w))
+        Y, A = oracle.matmul(fmt, packed, xb, n, k)
+        check_matmul(q.qmm_matmul(fmt, to_dev_u8(packed), bf16_from_bits(xb), n), Y, A, "fmt=%d" % fmt)
+    # Q3_K rows of 16 superblocks (TMA path) against the same superblocks as the
+    # first 16 of 20 (a 2200-byte row: direct loads) with zero activations beyond
+    w2 = inputs.weights(n, 5120, 88)
+    x2 = inputs.activations(1, 5120, 89)
+    x2[:, 4096:] = 0
+    p2 = q.qmm_quantize(q.QMM_Q3_K, w2.to(DEV))
+    y_direct = q.qmm_matmul(q.QMM_Q3_K, p2, x2.to(DEV), n)
+    p1 = q.qmm_quantize(q.QMM_Q3_K, w2[:, :4096].contiguous().to(DEV))
+    y_tma = q.qmm_matmul(q.QMM_Q3_K, p1, x2[:, :4096].contiguous().to(DEV), n)
+    assert torch.equal(y_direct, y_tma)
