@@ -657,8 +657,8 @@ def workload_config():
     return {"workload": "decode-shaped Q8_0/Q4_K linears (N x K = 4096x4096, 1024x4096, "
                         "14336x4096, 4096x14336), GEMV at M=1 (headline) plus M=4/16, ISQ, "
                         "dequant, mid-batch matmul M=32/128, prefill GEMM M=512/2048, FP8 "
-                        "E4M3 W8A16 ISQ + M=1 sweep + M=2048 prefill, a "
-                        "128256x4096 output head (Q6_K / Q8_0, M=1), a 2048-token embedding "
+                        "E4M3 W8A16 ISQ + M=1 sweep + M=2048 prefill, Q5_K/Q3_K/Q2_K ISQ + M=1 "
+                        "sweep, a 128256x4096 output head (Q6_K / Q8_0, M=1), a 2048-token embedding "
                         "lookup and a 32-layer 8B-shape model (ISQ + 224-GEMV decode step) in "
                         "each step",
             "weights": "bf16 ~N(0,0.02) with 0.1% x20 outliers, seeded",
