@@ -104,3 +104,21 @@ def test_matmul_full_shapes_sampled(shape, m):
     Y, A = oracle.matmul(oracle.FP8, want, inputs.bf16_bits(x), rows.size, k)
     check_matmul(y[:, ridx], Y, A, "fp8 %s m=%d" % (shape, m))
     assert q.qmm_device_error_take() == 0
+
+
+# ISQ rows staged in shared memory up to the largest row that fits twice
+# (51200 bf16 values: 200 KB), and the direct kernel beyond (53248); fp32
+# sources switch at half the length.
+@pytest.mark.parametrize("rows,k,src", [(3, 51200, "bf16"), (3, 53248, "bf16"), (2, 25600, "f32"),
+                                        (2, 26624, "f32")])
+def test_quantize_long_rows(rows, k, src):
+    x = inputs.weights(rows, k, 91 + k, fp32=True).numpy()
+    if src == "bf16":
+        t = torch.from_numpy(x).to(torch.bfloat16)
+        want = oracle.quantize(oracle.FP8, inputs.bf16_bits(t))
+        got = q.qmm_quantize(F, t.to(DEV)).cpu().numpy()
+    else:
+        want = oracle.quantize(oracle.FP8, x)
+        got = q.qmm_quantize(F, torch.from_numpy(x).to(DEV)).cpu().numpy()
+    assert np.array_equal(got, want)
+    assert q.qmm_device_error_take() == 0

@@ -185,3 +185,17 @@ def test_one_token_fallback_and_same_order():
     p1 = q.qmm_quantize(q.QMM_Q3_K, w2[:, :4096].contiguous().to(DEV))
     y_tma = q.qmm_matmul(q.QMM_Q3_K, p1, x2[:, :4096].contiguous().to(DEV), n)
     assert torch.equal(y_direct, y_tma)
+
+
+# One token with a K whose activations do not fit the TMA-fed kernel's
+# shared memory (K * 2 bytes > 64 KB): the direct-load kernel takes it.
+@pytest.mark.parametrize("fmt,k", [(q.QMM_Q6_K, 34816), (q.QMM_Q2_K, 33792), (q.QMM_Q3_K, 34816)])
+def test_one_token_long_k(fmt, k):
+    n = 64
+    w = inputs.weights(n, k, 93)
+    packed = oracle.quantize(fmt, inputs.bf16_bits(w))
+    xb = inputs.bf16_bits(inputs.activations(1, k, 94))
+    Y, A = oracle.matmul(fmt, packed, xb, n, k)
+    y = q.qmm_matmul(fmt, to_dev_u8(packed), bf16_from_bits(xb), n)
+    check_matmul(y, Y, A, "fmt=%d k=%d" % (fmt, k))
+    assert q.qmm_device_error_take() == 0
