@@ -296,8 +296,13 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b16) {
 
 // Two E4M3 codes (low byte first) -> their values as a binary16 pair, exactly.
 __device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t two_codes) {
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two_codes & 0xFFFFu), __NV_E4M3);
-    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+    // the packed conversion (exact: every E4M3 value is a binary16 value), its
+    // 32-bit result used as is
+    uint32_t r;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}"
+        : "=r"(r)
+        : "r"(two_codes));
+    return r;
 }
 
 }  // namespace qmm
