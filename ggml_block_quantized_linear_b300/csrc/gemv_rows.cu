@@ -23,10 +23,12 @@
 //    partial sums in a double-buffered shared array and moves on; the reducer
 //    adds the eight partials in warp order (deterministic) and stores the
 //    tile's outputs.  There is no cluster and no workspace.
-// Used when the row tiles alone fill the GPU's SMs, for up to 8 tokens (one
-// 8-token MMA column tile) or, while up to 128 KB of activations stay
-// resident, up to 16 (two tiles).  The ring depth and the activation window
-// are planned per (M, K) from the resident CTAs per SM.
+// Q8_0 / Q4_K use it when the row tiles alone fill the GPU's SMs, for up to
+// 8 tokens (one 8-token MMA column tile) or, while up to 128 KB of
+// activations stay resident, up to 16 (two tiles); Q5_K and FP8 (which have
+// no cluster kernel) for every M <= 16.  The ring depth, the consumer warps
+// and the activation window are planned per (M, K) from the resident CTAs
+// per SM.
 #include <atomic>
 #include <mutex>
 
