@@ -1,5 +1,6 @@
 // gemm.cu -- prefill-shaped quantized matmul (M > 16 tokens) on the 5th-
-// generation tensor cores: Y[M x N] = X[M x K] * W^T, W packed Q8_0 / Q4_K.
+// generation tensor cores: Y[M x N] = X[M x K] * W^T, W packed Q8_0, Q4_K,
+// Q5_K or FP8 E4M3 with row scales.
 //
 // The mistral.rs documentation ("Quantization types") sends larger dense
 // batches to tiled matrix multiplication (section NVFP4) and describes FP8
@@ -90,8 +91,15 @@ static_assert(2 * 128 + 3 * 64 <= 512 && 256 + 2 * 64 <= 512, "accumulators and 
 // Shared-memory pitch of a packed weight row in a stage (FP8: a 256-byte group
 // plus 16 bytes of the next, which keeps the dequantizing warps' loads on
 // distinct banks as Q8_0's 272 bytes do), and a group's advance in a row.
-__host__ __device__ constexpr int gemm_group_bytes(int fmt) { return fmt == 4 ? kQ4Bytes : kQ8GroupBytes; }
-__host__ __device__ constexpr int gemm_group_advance(int fmt) { return fmt == 8 ? kQ8GroupBytes : fmt == 4 ? kQ4Bytes : 256; }
+// (Q5_K: 176 bytes, 44 words: the 8 rows of a quarter-warp's 16-byte loads
+// land on distinct banks.)
+constexpr int kGemmQ5Bytes = 176;
+__host__ __device__ constexpr int gemm_group_bytes(int fmt) {
+    return fmt == 4 ? kQ4Bytes : fmt == 5 ? kGemmQ5Bytes : kQ8GroupBytes;
+}
+__host__ __device__ constexpr int gemm_group_advance(int fmt) {
+    return fmt == 8 ? kQ8GroupBytes : fmt == 4 ? kQ4Bytes : fmt == 5 ? kGemmQ5Bytes : 256;
+}
 
 struct GemmLayout {
     int b, p, bars, total;  // offsets from the 1024-aligned base
@@ -282,6 +290,34 @@ __device__ __forceinline__ void deq16_q4_k(const uint8_t *prow, int j, int kq, f
     const int sh = (kq >> 1) * 4;
     const uint32_t n[4] = {(q.x >> sh) & 0x0F0F0F0Fu, (q.y >> sh) & 0x0F0F0F0Fu, (q.z >> sh) & 0x0F0F0F0Fu,
                            (q.w >> sh) & 0x0F0F0F0Fu};
+    const uint64_t s2 = f2_pack(S, S), nm2 = f2_pack(-Mn, -Mn);
+    const uint64_t k2 = f2_pack(-8388608.0f, -8388608.0f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const uint32_t nw = n[e >> 1];
+        const int b0 = (2 * e) & 3;
+        const uint64_t qq = f2_add(f2_pack(__uint_as_float(prmt(nw, 0x4B000000u, 0x7440u + b0)),
+                                           __uint_as_float(prmt(nw, 0x4B000000u, 0x7440u + b0 + 1))),
+                                   k2);
+        float v0, v1;
+        f2_unpack(f2_fma(s2, qq, nm2), v0, v1);
+        const __half2 hv = __floats2half2_rn(v0, v1);
+        r[e] = *reinterpret_cast<const uint32_t *>(&hv);
+    }
+}
+
+// Q5_K: Q4_K's slice with the fifth code bits: the codes sit at byte 48 of
+// the superblock, and bit sb (the sub-block) of qh byte l (16 + l) is bit 4
+// of weight l.
+__device__ __forceinline__ void deq16_q5_k(const uint8_t *prow, int j, int kq, float S, float Mn,
+                                           uint32_t (&r)[8]) {
+    const uint4 q = *reinterpret_cast<const uint4 *>(prow + 48 + 32 * j + 16 * (kq & 1));
+    const uint4 h = *reinterpret_cast<const uint4 *>(prow + 16 + 16 * (kq & 1));
+    const int sh = (kq >> 1) * 4, sb = 2 * j + (kq >> 1);
+    const uint32_t n[4] = {((q.x >> sh) & 0x0F0F0F0Fu) | (((h.x >> sb) & 0x01010101u) << 4),
+                           ((q.y >> sh) & 0x0F0F0F0Fu) | (((h.y >> sb) & 0x01010101u) << 4),
+                           ((q.z >> sh) & 0x0F0F0F0Fu) | (((h.z >> sb) & 0x01010101u) << 4),
+                           ((q.w >> sh) & 0x0F0F0F0Fu) | (((h.w >> sb) & 0x01010101u) << 4)};
     const uint64_t s2 = f2_pack(S, S), nm2 = f2_pack(-Mn, -Mn);
     const uint64_t k2 = f2_pack(-8388608.0f, -8388608.0f);
 #pragma unroll
@@ -540,8 +576,8 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
                 const int sp = gi % kGemmStagesP;
                 if (ok) ok = mbar_wait_warp(p_full(sp), (gi / kGemmStagesP) & 1, kErrGemmWait);
                 const uint8_t *prow = smem + L.p + sp * kPBytes + r * kCB;
-                float S[2], Mn[2];  // Q4_K: (S_j, Mn_j) of this thread's sub-block 4 j + kq in each K step
-                if constexpr (kFmt == 4) {
+                float S[2], Mn[2];  // Q4_K / Q5_K: (S_j, Mn_j) of this thread's sub-block 4 j + kq in each K step
+                if constexpr (kFmt == 4 || kFmt == 5) {
                     if (ok) {
                         const uint4 h = *reinterpret_cast<const uint4 *>(prow);
 #pragma unroll
@@ -575,6 +611,9 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
                                 if (kq & 1) { deq16_q8_0<2 * j, 1>(prow, 0, v0); deq16_q8_0<2 * j, 1>(prow, 1, v1); }
                                 else        { deq16_q8_0<2 * j, 0>(prow, 0, v0); deq16_q8_0<2 * j, 0>(prow, 1, v1); }
                             }
+                        } else if constexpr (kFmt == 5) {
+                            deq16_q5_k(prow, J, pc, S[j], Mn[j], v0);
+                            deq16_q5_k(prow, J, pc + 1, S[j], Mn[j], v1);
                         } else {
                             deq16_q4_k(prow, J, pc, S[j], Mn[j], v0);
                             deq16_q4_k(prow, J, pc + 1, S[j], Mn[j], v1);
@@ -835,6 +874,7 @@ cudaError_t launch_gemm(int fmt, const void *W, const uint16_t *X, float *Y, int
     if (workspace_bytes < gemm_workspace_bytes(fmt, M, N, K, sms)) return cudaErrorInvalidValue;
     if (fmt == 8) return launch_gemm_f<8>(W, X, Y, M, N, K, workspace, sms, stream);
     if (fmt == kFp8) return launch_gemm_f<kFp8>(W, X, Y, M, N, K, workspace, sms, stream);
+    if (fmt == 5) return launch_gemm_f<5>(W, X, Y, M, N, K, workspace, sms, stream);
     return launch_gemm_f<4>(W, X, Y, M, N, K, workspace, sms, stream);
 }
 

@@ -23,10 +23,10 @@
 // Dequantization, the embedding rows and the direct-load linear layer give
 // lane l of a warp the weights 8l .. 8l + 7 of a superblock: each weight is
 // dequantized exactly as the plain definition does (one fp32 rounding of
-// S q - Mn) and multiplied in fp32.  That linear layer serves what the
-// faster paths do not: Q5_K above 16 tokens (Q5_K decode runs the row-tile
-// kernel, gemv_rows.cu) and Q3_K / Q2_K above one token or with rows that
-// are not 16-byte multiples (one token runs sbrows.cu).
+// S q - Mn) and multiplied in fp32.  That linear layer serves Q3_K / Q2_K
+// above one token or with rows that are not 16-byte multiples (one token runs
+// sbrows.cu); Q5_K runs the row-tile decode kernel (gemv_rows.cu) and the
+// tiled kernel (gemm.cu).
 #include "common.cuh"
 
 namespace qmm {
@@ -818,7 +818,6 @@ static cudaError_t kq_matmul_t(const uint8_t *w, const uint16_t *X, float *Y, in
 cudaError_t launch_kq_matmul(int fmt, const void *W, const uint16_t *X, float *Y, int M, int N, int K, int sms,
                              cudaStream_t stream) {
     const uint8_t *w = static_cast<const uint8_t *>(W);
-    if (fmt == 5) return kq_matmul_t<5>(w, X, Y, M, N, K, sms, stream);
     if (fmt == 3) return kq_matmul_t<3>(w, X, Y, M, N, K, sms, stream);
     return kq_matmul_t<2>(w, X, Y, M, N, K, sms, stream);
 }

@@ -187,7 +187,8 @@ qmm_status qmm_dequantize(qmm_format fmt, const void *src_packed, float *dst, in
 }
 
 size_t qmm_matmul_workspace_bytes(qmm_format fmt, int64_t M, int64_t N, int64_t K) {
-    if (!known_fmt(fmt) || fmt == QMM_Q6_K || is_kq(fmt) || M <= kMaxDecodeM || N <= 0 || K <= 0 || M > kMaxDim ||
+    if (!known_fmt(fmt) || fmt == QMM_Q6_K || fmt == QMM_Q3_K || fmt == QMM_Q2_K || M <= kMaxDecodeM || N <= 0 ||
+        K <= 0 || M > kMaxDim ||
         N > kMaxDim || K > kMaxDim || K % kGroup != 0)
         return 0;
     return gemm_workspace_bytes((int)fmt, (int)M, (int)N, (int)K, sm_count());
@@ -210,11 +211,11 @@ qmm_status qmm_matmul(qmm_format fmt, const void *W_packed, const uint16_t *X_bf
         return from_cuda(launch_sbrows((int)fmt, W_packed, X_bf16, Y, (int)N, (int)K, sm_count(), s));
     if (fmt == QMM_Q6_K)
         return from_cuda(launch_q6k_matmul(W_packed, X_bf16, Y, (int)M, (int)N, (int)K, sm_count(), s));
-    // Q5_K decode runs on the row-tile kernel (its superblocks are 16-byte
-    // aligned, so TMA boxes fit); the other K-quants and Q5_K prefill on CUDA cores
+    // Q5_K runs the row-tile decode kernel and the tiled kernel (its
+    // superblocks are 16-byte aligned, so TMA boxes fit); Q3_K / Q2_K on CUDA cores
     if (fmt == QMM_Q5_K && M <= kMaxDecodeM)
         return from_cuda(launch_gemv_rows((int)fmt, W_packed, X_bf16, Y, (int)M, (int)N, (int)K, sm_count(), s));
-    if (is_kq(fmt))
+    if (fmt == QMM_Q3_K || fmt == QMM_Q2_K)
         return from_cuda(launch_kq_matmul((int)fmt, W_packed, X_bf16, Y, (int)M, (int)N, (int)K, sm_count(), s));
     if (M <= kMaxDecodeM) {
         // FP8 has only the row-tile decode kernel

@@ -42,8 +42,8 @@ extern "C" qmm_status qmm_matmul_prefill_static(qmm_format fmt, const void *W_pa
         return QMM_ERR_INVALID_ARG;
     if (K == 0 || K % kGroup != 0) return QMM_ERR_SHAPE;
     if (M == 0 || N == 0) return QMM_OK;
-    // decode (and every Q6_K, Q5_K, Q3_K, Q2_K product) needs no scratch: use qmm_matmul
-    if (M <= kMaxDecodeM || fmt == QMM_Q6_K || is_kq(fmt)) return QMM_ERR_UNSUPPORTED;
+    // decode (and every Q6_K, Q3_K, Q2_K product) needs no scratch: use qmm_matmul
+    if (M <= kMaxDecodeM || fmt == QMM_Q6_K || fmt == QMM_Q3_K || fmt == QMM_Q2_K) return QMM_ERR_UNSUPPORTED;
     if (W_packed == nullptr || X_bf16 == nullptr || Y == nullptr) return QMM_ERR_INVALID_ARG;
     if (!aligned16(W_packed) || !aligned16(X_bf16) || !aligned16(Y)) return QMM_ERR_ALIGNMENT;
     const size_t need = gemm_workspace_bytes((int)fmt, (int)M, (int)N, (int)K, sm_count());

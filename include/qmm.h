@@ -69,9 +69,9 @@
  *         (d*sc_j) * q - dmin*mc_j.
  *   Q5_K / Q3_K / Q2_K are the page's q5k / q3k / q2k (table "Q*K family";
  *         `--isq 5 / 3 / 2` on CUDA).  Q5_K superblocks are 16-byte aligned
- *         and its decode matmul runs the row-tile kernel; Q3_K and Q2_K
- *         superblocks are only 2- or 4-byte aligned inside a row, and the
- *         library serves them (and Q5_K above 16 tokens) with CUDA-core
+ *         and its matmul runs the row-tile decode kernel and the tiled
+ *         tensor-core kernel; Q3_K and Q2_K superblocks are only 2- or 4-byte
+ *         aligned inside a row, and the library serves them with CUDA-core
  *         kernels (see qmm_matmul).
  *   FP8_E4M3  (W8A16; the page's section "FP8": E4M3 produced by ISQ,
  *         symmetric weights with channel scales): one fp32 scale per row,
@@ -214,13 +214,15 @@ QMM_API size_t qmm_matmul_workspace_bytes(qmm_format fmt, int64_t M, int64_t N, 
  * finished sums) and the tiled kernel above that (each weight tile converted
  * to binary16 inside the GEMM, the row scale applied in the epilogue).
  * Q5_K runs the row-tile decode kernel for M <= 16 (5-bit codes exactly in
- * the MMA fragments, Q4_K's scale and min handling).  Q6_K (output heads)
- * runs a CUDA-core kernel for every M: a warp per weight row, exact integer
- * codes times the activations, the sub-block scale applied per superblock,
- * fp32 sums.  Q3_K and Q2_K, and Q5_K above 16 tokens, run a CUDA-core
- * kernel: a warp per weight row, each weight dequantized exactly (one fp32
- * rounding, as qmm_dequantize gives it) and multiplied in fp32, with the
- * activations exact (no binary16 rounding).  For Q8_0 / Q4_K, larger M runs
+ * the MMA fragments, Q4_K's scale and min handling) and the tiled kernel
+ * above.  Q6_K (output heads) runs a CUDA-core kernel for every M: a warp
+ * per weight row, exact integer codes times the activations, the sub-block
+ * scale applied per superblock, fp32 sums.  Q3_K and Q2_K run a CUDA-core
+ * kernel: a warp per weight row, exact codes with the sub-block scale and
+ * min applied once per superblock at one token, each weight dequantized
+ * exactly (one fp32 rounding, as qmm_dequantize gives it) for more tokens,
+ * fp32 products with the activations exact (no binary16 rounding).  For
+ * Q8_0 / Q4_K / Q5_K, larger M runs
  * the tiled kernel (tcgen05 tensor cores, TMEM accumulators):
  * token tiles of 32, 64, 128 or 256 (the smallest of 32 / 64 / 128 that holds
  * M, else 256); when the output tiles are fewer than the SMs, K is split into
@@ -231,8 +233,7 @@ QMM_API size_t qmm_matmul_workspace_bytes(qmm_format fmt, int64_t M, int64_t N, 
  *   |y - y_exact| <= 1e-3 * sum_k |w^_k x_k| + 1e-6 + 2^-25 * T,
  * where T = sum over k of |x_k| for the weights with |w^_k| < 2^-14 (prefill
  * path, M > 16, only) plus |w^_k| for the activations with |x_k| < 2^-14 (both
- * paths; the CUDA-core kernels of Q6_K, Q3_K, Q2_K and of Q5_K above 16
- * tokens have no T term).  Both paths round each activation to binary16
+ * paths; the CUDA-core kernels of Q6_K, Q3_K and Q2_K have no T term).  Both paths round each activation to binary16
  * once, and the prefill path also rounds each dequantized weight to
  * binary16 once: a relative error
  * of at most 2^-11 for values in binary16's normal range, an absolute error

@@ -137,18 +137,25 @@ def test_q6_k_sizes_and_policy(lib):
 
 
 def test_k_quant_sizes(lib):
-    # Q5_K 176, Q3_K 110, Q2_K 84 bytes per 256 weights; no workspace; the
-    # static prefill entry leaves them to qmm_matmul
+    # Q5_K 176, Q3_K 110, Q2_K 84 bytes per 256 weights.  Q5_K prefill runs the
+    # tiled kernel (the binary16 copy of X as workspace, the static entry
+    # serves it); Q3_K / Q2_K need no workspace and the static entry leaves
+    # them to qmm_matmul
     L = lib
     for fmt, nb in ((q.QMM_Q5_K, 176), (q.QMM_Q3_K, 110), (q.QMM_Q2_K, 84)):
         assert q.qmm_packed_bytes(fmt, 4096, 4096) == 4096 * 16 * nb
         assert q.qmm_packed_bytes(fmt, 3, 768) == 3 * 3 * nb
         assert q.qmm_packed_bytes(fmt, 1, 256 + 32) == 0
-        assert q.qmm_matmul_workspace_bytes(fmt, 512, 4096, 4096) == 0
+        assert q.qmm_matmul_workspace_bytes(fmt, 16, 4096, 4096) == 0
         assert L.qmm_quantize(fmt, 0, FAKE, FAKE, 4, 200, S0) == q.QMM_ERR_SHAPE
         assert L.qmm_quantize(fmt, 0, MISALIGNED, FAKE, 4, 256, S0) == q.QMM_ERR_ALIGNMENT
         assert L.qmm_dequantize(fmt, NULL, FAKE, 4, 256, S0) == q.QMM_ERR_INVALID_ARG
         assert L.qmm_matmul(fmt, FAKE, FAKE, NULL, 1, 64, 256, NULL, 0, S0) == q.QMM_ERR_INVALID_ARG
+    assert q.qmm_matmul_workspace_bytes(q.QMM_Q5_K, 512, 4096, 4096) == 512 * 4096 * 2
+    assert L.qmm_matmul(q.QMM_Q5_K, FAKE, FAKE, FAKE, 32, 64, 256, NULL, 0, S0) == q.QMM_ERR_WORKSPACE
+    assert L.qmm_matmul_prefill_static(q.QMM_Q5_K, NULL, FAKE, FAKE, 512, 64, 256, S0) == q.QMM_ERR_INVALID_ARG
+    for fmt in (q.QMM_Q3_K, q.QMM_Q2_K):
+        assert q.qmm_matmul_workspace_bytes(fmt, 512, 4096, 4096) == 0
         assert L.qmm_matmul_prefill_static(fmt, FAKE, FAKE, FAKE, 512, 64, 256, S0) == q.QMM_ERR_UNSUPPORTED
 
 

@@ -199,3 +199,23 @@ def test_one_token_long_k(fmt, k):
     y = q.qmm_matmul(fmt, to_dev_u8(packed), bf16_from_bits(xb), n)
     check_matmul(y, Y, A, "fmt=%d k=%d" % (fmt, k))
     assert q.qmm_device_error_take() == 0
+
+
+# Q5_K prefill on the tiled tensor-core kernel at decode and prefill shapes
+# (a K split at 512 tokens on 4096 x 4096, 2048 tokens filling the SMs, a
+# 300-token ragged tile on K = 14336): sampled rows, every token.
+@pytest.mark.parametrize("n,k,m", [(4096, 4096, 512), (14336, 4096, 2048), (4096, 14336, 300), (1024, 4096, 40)])
+def test_q5_k_prefill_sampled(n, k, m):
+    w = inputs.weights(n, k, 95 + m, device=DEV)
+    packed = q.qmm_quantize(q.QMM_Q5_K, w)
+    x = inputs.activations(m, k, 96 + m, device=DEV)
+    y = q.qmm_matmul(q.QMM_Q5_K, packed, x, n)
+    rng = np.random.default_rng(n + k + m)
+    rows = np.unique(np.concatenate([rng.choice(n, 16, replace=False), [0, 127, 128, n - 1]])).astype(np.int64)
+    ridx = torch.from_numpy(rows).to(DEV)
+    want = oracle.quantize(q.QMM_Q5_K, inputs.bf16_bits(w[ridx]))
+    assert np.array_equal(packed[ridx].cpu().numpy(), want)
+    Y, A = oracle.matmul(q.QMM_Q5_K, want, inputs.bf16_bits(x), rows.size, k)
+    check_matmul(y[:, ridx], Y, A, "Q5_K n=%d k=%d m=%d" % (n, k, m))
+    assert torch.equal(y, q.qmm_matmul(q.QMM_Q5_K, packed, x, n))
+    assert q.qmm_device_error_take() == 0
