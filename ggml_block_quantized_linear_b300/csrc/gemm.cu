@@ -31,14 +31,19 @@
 // one of 256 columns for 256-token tiles (two stages), which the
 // dequantizing warps drain themselves where they would otherwise wait for
 // the unit's last MMA.
-// When the output tiles are fewer than the SMs, K is split into parts (a
-// unit is one part of one tile).  256-token tiles: at most two parts, both
-// added onto a Y zeroed by the conversion launch (two additions onto zero
-// commute, so the result does not depend on their order).  Smaller tiles:
-// up to 8 parts; each part stores its partial tile in the workspace and takes
-// a ticket, and the last part of a tile to arrive adds all parts in part
-// order and writes Y.  Both are deterministic and nothing ever waits for
-// another CTA.
+// 256-token tiles, at least as many as the CTAs (stream-K): the (tile,
+// packed group) pairs, token tile fastest, are cut into one contiguous run
+// per CTA, so every CTA has the same K work and the last wave is not left
+// part-empty.  A run is at least one tile long, so a tile falls to at most
+// two CTAs; both add their parts onto a Y tile that the conversion launch
+// zeroed.  With fewer output tiles than SMs, K is split into parts (a unit is
+// one part of one tile).  256-token tiles: at most two parts, both added onto
+// a Y zeroed by the conversion launch.  (Two additions onto zero commute, so
+// neither result depends on the order of the parts.)  Smaller tiles: up to
+// 8 parts; each part stores its partial tile in the workspace and takes a
+// ticket, and the last part of a tile to arrive adds all parts in part order
+// and writes Y.  All are deterministic and nothing ever waits for another
+// CTA.
 //   warp 0       TMA producer of the binary16 activation tiles (128B-swizzled
 //                boxes)
 //   warp 1       TMEM allocator and single-thread MMA issuer
@@ -57,6 +62,9 @@
 
 namespace qmm {
 
+#ifndef QMM_GEMM_MAX_PARTS  // K parts per tile for token tiles below 256
+#define QMM_GEMM_MAX_PARTS 8
+#endif
 constexpr int kGemmBM = 128;        // weight rows per CTA (MMA M)
 constexpr int kGemmBK = 128;        // K per stage: two 128-byte swizzle atoms of f16
 constexpr int kGemmAtomK = 64;      // K of one 128B-swizzled atom (one TMA box, one descriptor base)
@@ -220,18 +228,48 @@ __device__ __forceinline__ void fence_async_smem() {
 }
 
 // ----------------------------------------------------- activation conversion
+// Stream-K tiles shared by two CTAs: the tile holding pair c G / ctas for
+// each CTA boundary c = 1 .. ctas - 1 that falls inside a tile (tile t =
+// weight tile * tiles_m + token tile, BN tokens x 128 weight rows).
+struct SplitTiles {
+    int ctas;        // 0: none
+    int gtot, tiles_m, bn, M, N;
+    int64_t gall;    // (tile, group) pairs
+};
+
 // X bf16 -> binary16 (round to nearest), 8 elements per thread.  With a K
 // split, the same launch also clears the tiles' tickets (nt words) or zeroes
-// Y (ny floats) for the parts to add onto.
+// Y (ny floats) for the parts to add onto; with stream-K it zeroes the Y
+// tiles that two CTAs share.
 __global__ void __launch_bounds__(256) qmm_x_to_f16_kernel(const uint16_t *__restrict__ X,
                                                            __half *__restrict__ Xh, int64_t n8,
                                                            int *__restrict__ tickets, int nt,
-                                                           float *__restrict__ Yz, int64_t ny) {
+                                                           float *__restrict__ Yz, int64_t ny,
+                                                           const SplitTiles st) {
     for (int i = blockIdx.x * 256 + threadIdx.x; i < nt; i += gridDim.x * 256) tickets[i] = 0;
     const int64_t y4 = ny / 4;  // Y is 16-byte aligned
     for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < y4; i += (int64_t)gridDim.x * 256)
         reinterpret_cast<float4 *>(Yz)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (blockIdx.x == 0 && threadIdx.x < ny - 4 * y4) Yz[4 * y4 + threadIdx.x] = 0.f;
+    // one boundary per block: its tile, then 128 consecutive n per token row
+    for (int c = 1 + (int)blockIdx.x; c < st.ctas; c += (int)gridDim.x) {
+        const int64_t b = st.gall * c / st.ctas;
+        if (b % st.gtot == 0) continue;  // the boundary falls between tiles
+        const int t = (int)(b / st.gtot);
+        const int m0 = (t % st.tiles_m) * st.bn, n0 = (t / st.tiles_m) * 128;
+        const int rows = min(st.bn, st.M - m0);
+        if ((st.N & 3) == 0) {  // whole float4s (n0 is a multiple of 128)
+            const int c4 = min(32, (st.N - n0) / 4);
+            for (int e = threadIdx.x; e < rows * 32; e += 256)
+                if ((e & 31) < c4)
+                    reinterpret_cast<float4 *>(Yz + (int64_t)(m0 + (e >> 5)) * st.N + n0)[e & 31] =
+                        make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+            const int cn = min(128, st.N - n0);
+            for (int e = threadIdx.x; e < rows * 128; e += 256)
+                if ((e & 127) < cn) Yz[(int64_t)(m0 + (e >> 7)) * st.N + n0 + (e & 127)] = 0.f;
+        }
+    }
     for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n8; i += (int64_t)gridDim.x * 256) {
         const uint4 v = __ldg(reinterpret_cast<const uint4 *>(X) + i);
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -382,7 +420,7 @@ struct GemmParams {
 // A stages) runs on across tiles, and the two TMEM accumulators alternate
 // between tiles, so the epilogue of one tile overlaps the main loop of the
 // next.
-template <int kFmt, int kBN>
+template <int kFmt, int kBN, bool kSK>
 __global__ void __launch_bounds__(kGemmThreads, 1)
 qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
                 const GemmParams p) {
@@ -405,19 +443,50 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
     // CTA b takes units b, b + gridDim.x, ...  Consecutive CTAs run
     // neighbouring weight tiles against the same token tile, so an
     // activation tile is read from DRAM about once and then from L2.
+    // Stream-K: tile t = weight tile * tiles_m + token tile, and CTA b takes
+    // the pairs [b G / gridDim.x, (b + 1) G / gridDim.x) of the G = tiles x
+    // groups (tile, group) pairs, i.e. a few consecutive tiles, mostly of one
+    // weight tile (read from DRAM once, then from L2) against every token
+    // tile (all of X stays in L2).
     const int cid = (int)blockIdx.x, nctas = (int)gridDim.x;
-    const int tiles_n = (p.N + kGemmBM - 1) / kGemmBM;
+    const int tiles_n = (p.N + kGemmBM - 1) / kGemmBM, tiles_m = (p.M + kBN - 1) / kBN;
     const int ksplit = p.ksplit;
-    const int units = tiles_n * ((p.M + kBN - 1) / kBN) * ksplit;
-    const int my_tiles = units > cid ? (units - 1 - cid) / nctas + 1 : 0;
-    auto tile_base = [&](int lt) { return (cid + lt * nctas) / ksplit; };
-    auto tile_n0 = [&](int lt) { return (tile_base(lt) % tiles_n) * kGemmBM; };
-    auto tile_m0 = [&](int lt) { return (tile_base(lt) / tiles_n) * kBN; };
-    auto kpart = [&](int lt) { return (cid + lt * nctas) % ksplit; };
-    // packed groups [kg0, kg1) of the unit's K part (parts differ by at most one group)
     const int gtot = p.K / kGroup;
-    auto kg0 = [&](int lt) { return (int)((int64_t)gtot * kpart(lt) / ksplit); };
-    auto kg1 = [&](int lt) { return (int)((int64_t)gtot * (kpart(lt) + 1) / ksplit); };
+    const int units = tiles_n * tiles_m * ksplit;
+    static_assert(!kSK || kBN == 256, "stream-K runs 256-token tiles");
+    constexpr bool sk = kSK;
+    // stream-K run [s0, s1): tiles t_first .. t_first + my_tiles - 1, from
+    // group g_first of the first to group g_end of the last (exclusive)
+    int t_first = 0, g_first = 0, g_end = gtot, my_tiles;
+    if (sk) {
+        const int64_t gall = (int64_t)tiles_n * tiles_m * gtot;
+        const int64_t s0 = gall * cid / nctas, s1 = gall * (cid + 1) / nctas;
+        t_first = (int)(s0 / gtot);
+        const int t_last = (int)((s1 - 1) / gtot);
+        my_tiles = s1 > s0 ? t_last - t_first + 1 : 0;
+        g_first = (int)(s0 - (int64_t)t_first * gtot);
+        g_end = (int)(s1 - (int64_t)t_last * gtot);
+    } else {
+        my_tiles = units > cid ? (units - 1 - cid) / nctas + 1 : 0;
+    }
+    auto tile_base = [&](int lt) { return sk ? t_first + lt : (cid + lt * nctas) / ksplit; };
+    auto tile_n0 = [&](int lt) {
+        return (sk ? tile_base(lt) / tiles_m : tile_base(lt) % tiles_n) * kGemmBM;
+    };
+    auto tile_m0 = [&](int lt) { return (sk ? tile_base(lt) % tiles_m : tile_base(lt) / tiles_n) * kBN; };
+    auto kpart = [&](int lt) { return (cid + lt * nctas) % ksplit; };
+    // packed groups [kg0, kg1) of the unit's K part (parts differ by at most
+    // one group), or of the tile's share of the stream-K run
+    auto kg0 = [&](int lt) {
+        if (sk) return lt == 0 ? g_first : 0;
+        return (int)((int64_t)gtot * kpart(lt) / ksplit);
+    };
+    auto kg1 = [&](int lt) {
+        if (sk) return lt == my_tiles - 1 ? g_end : gtot;
+        return (int)((int64_t)gtot * (kpart(lt) + 1) / ksplit);
+    };
+    // the unit covers all of K: store Y; otherwise add onto the zeroed Y (or, with tickets, a partial tile)
+    auto whole = [&](int lt) { return kg0(lt) == 0 && kg1(lt) == gtot; };
 
     const uint32_t bar = smem_addr(smem + L.bars);
     // stage s is full when its activation copy has landed and all dequantizing
@@ -432,6 +501,7 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
     volatile int *last_slot = reinterpret_cast<volatile int *>(smem + L.bars + 8 * 25);
 
     if (tid == 0) {
+        *last_slot = 0;
         for (int s = 0; s < kSA; ++s) {
             mbar_init(full(s), kGemmDeqWarps + 1);
             mbar_init(empty(s), 1);
@@ -546,6 +616,7 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
             if (ok) ok = mbar_wait_warp(acc_full(0), lt & 1, kErrGemmWait);
             tc_fence_after();
             const int n = tile_n0(lt) + r, m0 = tile_m0(lt);
+            const bool wh = sk ? whole(lt) : ksplit == 1;
             float rs = 1.f;
             if constexpr (kFmt == kFp8)
                 if (n < p.N) rs = __ldg(reinterpret_cast<const float *>(p.W + (int64_t)n * p.row_bytes + p.K));
@@ -561,7 +632,7 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
                             const int m = m0 + col + i;
                             if (m >= p.M) continue;
                             const float y = __uint_as_float(v[i]) * rs;
-                            if (ksplit == 1) p.Y[(int64_t)m * p.N + n] = y;
+                            if (wh) p.Y[(int64_t)m * p.N + n] = y;
                             else atomicAdd(p.Y + (int64_t)m * p.N + n, y);
                         }
                     }
@@ -677,12 +748,9 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
                             }
                         }
                     } else {
-                        // this part's sums, row-major (one row's BN columns contiguous)
-                        float4 *pr = reinterpret_cast<float4 *>(pw + r * kBN + col);
+                        // this part's sums, column-major (a token's 128 rows contiguous)
 #pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            pr[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                                __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+                        for (int i = 0; i < 32; ++i) pw[(col + i) * kGemmBM + r] = __uint_as_float(v[i]);
                     }
                 }
             }
@@ -690,50 +758,11 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_empty(buf));
             if (p.tickets_mode) {
-                // ticket: the last part of the tile to finish adds all parts in order
+                // ticket: the last part of the tile to finish adds all parts
+                // in order, with every warp of the CTA (after the roles end)
                 __threadfence();
                 named_bar_sync(2, kGemmEpiWarps * 32);
                 if (etid == 0) *last_slot = atomicAdd(p.tickets + tile, 1) == ksplit - 1;
-                named_bar_sync(2, kGemmEpiWarps * 32);
-                if (*last_slot && ok && n < p.N) {
-                    __threadfence();
-                    const float *pt = p.partials + (int64_t)tile * ksplit * (kBN * kGemmBM) + r * kBN;
-#pragma unroll 1
-                    for (int col = 0; col < kBN; col += 16) {
-                        // 4 float4 of two parts in flight before their sums
-                        float4 acc[4];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-                        for (int q0 = 0; q0 < ksplit; q0 += 2) {
-                            const float4 *a = reinterpret_cast<const float4 *>(pt + (int64_t)q0 * (kBN * kGemmBM) + col);
-                            const float4 *b = reinterpret_cast<const float4 *>(pt + (int64_t)(q0 + 1) * (kBN * kGemmBM) + col);
-                            const bool two = q0 + 1 < ksplit;
-                            float4 va[4], vb[4];
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                va[i] = __ldcg(a + i);
-                                vb[i] = two ? __ldcg(b + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-                            }
-                            // parts in order: acc + part q0, then + part q0 + 1
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                acc[i].x += va[i].x; acc[i].y += va[i].y; acc[i].z += va[i].z; acc[i].w += va[i].w;
-                                if (two) {
-                                    acc[i].x += vb[i].x; acc[i].y += vb[i].y; acc[i].z += vb[i].z; acc[i].w += vb[i].w;
-                                }
-                            }
-                        }
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const float o[4] = {acc[i].x, acc[i].y, acc[i].z, acc[i].w};
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int m = m0 + col + 4 * i + e;
-                                if (m < p.M) p.Y[(int64_t)m * p.N + n] = o[e];
-                            }
-                        }
-                    }
-                }
             }
         }
     }
@@ -744,18 +773,51 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+    if constexpr (kNbuf == 2) {
+        if (p.tickets_mode && *last_slot) {
+            // this CTA's unit (with tickets, every CTA has one) finished its
+            // tile last: Y = part 0 + part 1 + ... in part order, four rows
+            // (one float4 of each column-major partial tile) per thread and
+            // step, with every warp of the CTA
+            __threadfence();
+            const int lt = my_tiles - 1, n0 = tile_n0(lt), m0 = tile_m0(lt);
+            constexpr int kQ = kBN * kGemmBM / 4;  // float4s per partial tile
+            const float4 *pt = reinterpret_cast<const float4 *>(p.partials) + (int64_t)tile_base(lt) * ksplit * kQ;
+#pragma unroll 1
+            for (int e = tid; e < kQ; e += kGemmThreads) {
+                float4 a[QMM_GEMM_MAX_PARTS];
+#pragma unroll
+                for (int q = 0; q < QMM_GEMM_MAX_PARTS; ++q)
+                    if (q < ksplit) a[q] = __ldcg(pt + (int64_t)q * kQ + e);
+#pragma unroll
+                for (int q = 1; q < QMM_GEMM_MAX_PARTS; ++q) {
+                    if (q < ksplit) {
+                        a[0].x += a[q].x; a[0].y += a[q].y; a[0].z += a[q].z; a[0].w += a[q].w;
+                    }
+                }
+                const int m = m0 + e / (kGemmBM / 4), n = n0 + 4 * (e % (kGemmBM / 4));
+                if (m >= p.M || n >= p.N) continue;
+                float *y = p.Y + (int64_t)m * p.N + n;
+                if ((p.N & 3) == 0) {
+                    *reinterpret_cast<float4 *>(y) = a[0];
+                } else {
+                    const float o[4] = {a[0].x, a[0].y, a[0].z, a[0].w};
+                    for (int i = 0; i < 4 && n + i < p.N; ++i) y[i] = o[i];
+                }
+            }
+        }
+    }
 }
 
 // ---------------------------------------------------------------- launcher
 // Token tile and K split of a problem.  BN: the smallest of 32 / 64 / 128
-// that holds M, else 256.  K parts: as many as fill the SMs with one unit
-// each when the output tiles alone do not (at most one part per packed
-// group of K).
-#ifndef QMM_GEMM_MAX_PARTS  // K parts per tile for token tiles below 256
-#define QMM_GEMM_MAX_PARTS 8
-#endif
+// that holds M, else 256.  256-token tiles at least as many as the SMs:
+// stream-K.  Otherwise K parts: as many as fill the SMs with one unit each
+// when the output tiles alone do not (at most one part per packed group of
+// K; two for 256-token tiles).
+constexpr int kGemmStreamKWaves = 4;  // 256-token tiles per SM from which stream-K runs
 struct GemmPlan {
-    int bn, ksplit, tiles, tickets;
+    int bn, ksplit, tiles, tickets, stream_k;
 };
 static GemmPlan gemm_plan(int M, int N, int K, int sms) {
     GemmPlan pl;
@@ -771,10 +833,16 @@ static GemmPlan gemm_plan(int M, int N, int K, int sms) {
     };
     pl.bn = M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
     pl.tiles = tiles_n * ((M + pl.bn - 1) / pl.bn);
+    pl.stream_k = 0;
     if (pl.bn == 256) {
-        pl.ksplit = halves(pl.tiles);
+        // four or more waves of tiles: stream-K (it recovers the idle part of
+        // the last wave, up to one unit; its cut tiles cost a few microseconds)
+        pl.stream_k = pl.tiles >= kGemmStreamKWaves * sms;
+        pl.ksplit = pl.stream_k ? 1 : halves(pl.tiles);
         pl.tickets = 0;
     } else {
+        // (tiles x parts <= SMs: each CTA runs one unit, which the final
+        // reduction of the kernel relies on)
         int ks = sms / pl.tiles;
         if (ks > groups) ks = groups;
         if (ks > QMM_GEMM_MAX_PARTS) ks = QMM_GEMM_MAX_PARTS;
@@ -816,12 +884,23 @@ static cudaError_t launch_gemm_t(const void *W, const uint16_t *X, float *Y, int
     const int nt = pl.tickets ? pl.tiles : 0;
     const int64_t ny = (!pl.tickets && pl.ksplit > 1) ? (int64_t)M * N : 0;  // Y to add the halves onto
     const int64_t n8 = (int64_t)M * K / 8;
+    const int grid = pl.stream_k ? sms : (pl.tiles * pl.ksplit < sms ? pl.tiles * pl.ksplit : sms);
+    if (pl.tickets && pl.tiles * pl.ksplit > grid) return cudaErrorInvalidConfiguration;  // one unit per CTA
+    SplitTiles st;
+    st.ctas = pl.stream_k ? grid : 0;
+    st.gtot = K / kGroup;
+    st.tiles_m = (M + kBN - 1) / kBN;
+    st.bn = kBN;
+    st.M = M;
+    st.N = N;
+    st.gall = (int64_t)pl.tiles * st.gtot;
     const int64_t work = n8 > ny / 4 ? n8 : ny / 4;
     int cgrid = (int)((work + 255) / 256);
     if (cgrid > 148 * 16) cgrid = 148 * 16;
+    if (cgrid < st.ctas - 1) cgrid = st.ctas - 1;  // a block per stream-K boundary
     if (cgrid < 1) cgrid = 1;
     qmm_x_to_f16_kernel<<<cgrid, 256, 0, stream>>>(X, Xh, n8, reinterpret_cast<int *>(wb + ws.tickets), nt,
-                                                   Y, ny);
+                                                   Y, ny, st);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
@@ -838,9 +917,16 @@ static cudaError_t launch_gemm_t(const void *W, const uint16_t *X, float *Y, int
     if (e != cudaSuccess) return e;
 
     const GemmLayout L = gemm_layout(kFmt, kBN);
-    static std::atomic<uint64_t> attr_done{0};
-    e = set_smem_limit_once(reinterpret_cast<const void *>(qmm_gemm_kernel<kFmt, kBN>), L.total, attr_done);
+    static std::atomic<uint64_t> attr_done{0}, attr_done_sk{0};
+    e = set_smem_limit_once(reinterpret_cast<const void *>(qmm_gemm_kernel<kFmt, kBN, false>), L.total, attr_done);
     if (e != cudaSuccess) return e;
+    if constexpr (kBN == 256) {
+        if (pl.stream_k) {
+            e = set_smem_limit_once(reinterpret_cast<const void *>(qmm_gemm_kernel<kFmt, 256, true>), L.total,
+                                    attr_done_sk);
+            if (e != cudaSuccess) return e;
+        }
+    }
     GemmParams p;
     p.Y = Y;
     p.W = static_cast<const uint8_t *>(W);
@@ -852,9 +938,14 @@ static cudaError_t launch_gemm_t(const void *W, const uint16_t *X, float *Y, int
     p.K = K;
     p.ksplit = pl.ksplit;
     p.tickets_mode = pl.tickets;
-    const int units = pl.tiles * pl.ksplit;
-    const int grid = units < sms ? units : sms;  // one persistent CTA per SM
-    qmm_gemm_kernel<kFmt, kBN><<<grid, kGemmThreads, (size_t)L.total, stream>>>(xmap, wmap, p);
+    // one persistent CTA per SM (stream-K: exactly one per SM, the runs' divisor)
+    if constexpr (kBN == 256) {
+        if (pl.stream_k) {
+            qmm_gemm_kernel<kFmt, 256, true><<<grid, kGemmThreads, (size_t)L.total, stream>>>(xmap, wmap, p);
+            return cudaGetLastError();
+        }
+    }
+    qmm_gemm_kernel<kFmt, kBN, false><<<grid, kGemmThreads, (size_t)L.total, stream>>>(xmap, wmap, p);
     return cudaGetLastError();
 }
 

@@ -174,18 +174,34 @@ def test_prefill_split_k_full(fmt, n, k, m):
     assert torch.equal(y, run(fmt, packed, xb, n))  # parts added in a fixed order
 
 
-# 512-token units (two 256-token MMA tiles sharing each dequantized weight
-# stage), which the planner picks where they need fewer waves: ragged last
-# unit (1000 = 512 + 488 tokens; 1500 = 2 x 512 + 476), a unit whose second
-# MMA tile is entirely past M (1100 = 2 x 512 + 76), and K halves.
+# 256-token tiles with a ragged last token tile (1000 = 3 x 256 + 232;
+# 1500 = 5 x 256 + 220; 1100 = 4 x 256 + 76): 128 and 96 tiles take K halves
+# added onto a zeroed Y; 160 tiles (4096 x 1100) run whole, in two waves.
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("n,k,m", [(4096, 512, 1000), (2048, 1024, 1500), (4096, 512, 1100)])
-def test_prefill_512_token_units_full(fmt, n, k, m):
+def test_prefill_256_token_ragged_full(fmt, n, k, m):
     packed, xb = problem(fmt, n, k, m, 5000 + n + k + m)
     Y, A = oracle.matmul(fmt, packed, xb, n, k)
     y = run(fmt, packed, xb, n)
     check_matmul(y, Y, A, "fmt=%d n=%d k=%d m=%d" % (fmt, n, k, m))
     assert torch.equal(y, run(fmt, packed, xb, n))
+
+
+# Stream-K (256-token tiles, four waves or more on the 148 SMs): each CTA
+# runs an equal share of the (tile, packed group) pairs, and a tile cut
+# between two CTAs is the sum of both parts on a zeroed Y.  600 tiles of 2
+# groups and 608 of 3 (in the second N is ragged and not a multiple of 4, and
+# M is ragged); all four formats of the tiled kernel, compared in full, and
+# run twice.
+@pytest.mark.parametrize("fmt", FMTS + [q.QMM_Q5_K, q.QMM_FP8_E4M3])
+@pytest.mark.parametrize("n,k,m", [(9600, 512, 2048), (9602, 768, 1900)])
+def test_prefill_stream_k_full(fmt, n, k, m):
+    packed, xb = problem(fmt, n, k, m, 8000 + n + k + m)
+    Y, A = oracle.matmul(fmt, packed, xb, n, k)
+    y = run(fmt, packed, xb, n)
+    check_matmul(y, Y, A, "fmt=%d n=%d k=%d m=%d" % (fmt, n, k, m))
+    assert torch.equal(y, run(fmt, packed, xb, n))  # two parts on zero: either order, the same sum
+    assert q.qmm_device_error_take() == 0
 
 
 @pytest.mark.parametrize("fmt", FMTS)
