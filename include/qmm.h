@@ -225,9 +225,12 @@ QMM_API size_t qmm_matmul_workspace_bytes(qmm_format fmt, int64_t M, int64_t N, 
  * Q8_0 / Q4_K / Q5_K, larger M runs
  * the tiled kernel (tcgen05 tensor cores, TMEM accumulators):
  * token tiles of 32, 64, 128 or 256 (the smallest of 32 / 64 / 128 that holds
- * M, else 256); when the output tiles are fewer than the SMs, K is split into
- * parts whose partial tiles the last part to finish adds in part order, so
- * the result is still deterministic.
+ * M, else 256).  When the output tiles are fewer than the SMs, K is split:
+ * 256-token tiles into two halves added onto a zeroed Y, smaller tiles into
+ * parts whose partial tiles the last part to finish adds in part order.  From
+ * four waves of 256-token tiles, each CTA takes an equal run of K work and a
+ * tile cut between two CTAs is the sum of both parts on a zeroed Y.  Two
+ * additions onto zero commute, so every result is deterministic.
  *
  * Accuracy, per element, with w^ the dequantized weights:
  *   |y - y_exact| <= 1e-3 * sum_k |w^_k x_k| + 1e-6 + 2^-25 * T,
