@@ -209,30 +209,42 @@ __device__ __forceinline__ KqCodes kq_lane_codes(const KqRaw &r, int lane) {
         q0 = (r.a0 >> (2 * s)) & 0x03030303u;
         q1 = (r.a1 >> (2 * s)) & 0x03030303u;
     }
+    const uint64_t b2 = f2_pack(bias, bias);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        k.c[e] = __uint_as_float(__byte_perm(q0, 0x4B000000u, 0x7440u + e)) - bias;
-        k.c[4 + e] = __uint_as_float(__byte_perm(q1, 0x4B000000u, 0x7440u + e)) - bias;
+    for (int e = 0; e < 4; e += 2) {  // code pairs, one packed subtraction each
+        f2_unpack(f2_sub(f2_pack(__uint_as_float(__byte_perm(q0, 0x4B000000u, 0x7440u + e)),
+                                 __uint_as_float(__byte_perm(q0, 0x4B000000u, 0x7441u + e))),
+                         b2),
+                  k.c[e], k.c[e + 1]);
+        f2_unpack(f2_sub(f2_pack(__uint_as_float(__byte_perm(q1, 0x4B000000u, 0x7440u + e)),
+                                 __uint_as_float(__byte_perm(q1, 0x4B000000u, 0x7441u + e))),
+                         b2),
+                  k.c[4 + e], k.c[5 + e]);
     }
     return k;
 }
 // acc + S * sum_k c_k x_k - Mn * sum_k x_k over the lane's 8 bf16 activations
-// (xw: pairs, lower index in the low half), the sums in k order.
+// (xw: pairs, lower index in the low half).  Each sum runs as two packed
+// fp32 lanes (even k, odd k, each in k order), added at the end.
 template <int kFmt>
 __device__ __forceinline__ float kq_codes_dot(const KqCodes &k, const uint32_t (&xw)[4], float acc) {
-    float p = 0.f, sx = 0.f;
+    uint64_t p2 = f2_pack(0.f, 0.f), s2 = f2_pack(0.f, 0.f);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-        const float xa = __uint_as_float(xw[e] << 16), xb = __uint_as_float(xw[e] & 0xFFFF0000u);
-        p = fmaf(k.c[2 * e], xa, p);
-        p = fmaf(k.c[2 * e + 1], xb, p);
-        if constexpr (kFmt != 3) {
-            sx = __fadd_rn(sx, xa);
-            sx = __fadd_rn(sx, xb);
-        }
+        const uint64_t x2 = f2_pack(__uint_as_float(xw[e] << 16), __uint_as_float(xw[e] & 0xFFFF0000u));
+        p2 = f2_fma(f2_pack(k.c[2 * e], k.c[2 * e + 1]), x2, p2);
+        if constexpr (kFmt != 3) s2 = f2_add(s2, x2);
     }
-    if constexpr (kFmt == 3) return fmaf(k.S, p, acc);
-    else return fmaf(k.S, p, fmaf(-k.Mn, sx, acc));
+    float pe, po;
+    f2_unpack(p2, pe, po);
+    const float p = pe + po;
+    if constexpr (kFmt == 3) {
+        return fmaf(k.S, p, acc);
+    } else {
+        float se, so;
+        f2_unpack(s2, se, so);
+        return fmaf(k.S, p, fmaf(-k.Mn, se + so, acc));
+    }
 }
 
 // ---------------------------------------------------------- dequantization

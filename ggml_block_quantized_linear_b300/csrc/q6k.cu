@@ -49,12 +49,35 @@ __device__ __forceinline__ void q6_lane_codes(const uint8_t *blk, int lane, floa
     const uint32_t nsh = (uint32_t)(s >> 1) * 4u, hsh = 2u * (uint32_t)s;
     const uint32_t q0 = ((ql.x >> nsh) & 0x0F0F0F0Fu) | (((qh.x >> hsh) & 0x03030303u) << 4);
     const uint32_t q1 = ((ql.y >> nsh) & 0x0F0F0F0Fu) | (((qh.y >> hsh) & 0x03030303u) << 4);
+    // byte b under the float 2^23 exponent is 2^23 + b; minus 2^23 + 32 gives
+    // b - 32 exactly (code pairs, one packed subtraction each)
+    const uint64_t b2 = f2_pack(8388640.0f, 8388640.0f);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        // byte b under the float 2^23 exponent is 2^23 + b; minus 2^23 + 32 gives b - 32 exactly
-        c[e] = __uint_as_float(__byte_perm(q0, 0x4B000000u, 0x7440u + e)) - 8388640.0f;
-        c[4 + e] = __uint_as_float(__byte_perm(q1, 0x4B000000u, 0x7440u + e)) - 8388640.0f;
+    for (int e = 0; e < 4; e += 2) {
+        f2_unpack(f2_sub(f2_pack(__uint_as_float(__byte_perm(q0, 0x4B000000u, 0x7440u + e)),
+                                 __uint_as_float(__byte_perm(q0, 0x4B000000u, 0x7441u + e))),
+                         b2),
+                  c[e], c[e + 1]);
+        f2_unpack(f2_sub(f2_pack(__uint_as_float(__byte_perm(q1, 0x4B000000u, 0x7440u + e)),
+                                 __uint_as_float(__byte_perm(q1, 0x4B000000u, 0x7441u + e))),
+                         b2),
+                  c[4 + e], c[5 + e]);
     }
+}
+
+// sum_k c_k x_k over a lane's 8 codes and bf16 activations (xw: pairs, lower
+// index in the low half), as two packed fp32 lanes (even k, odd k, each in k
+// order) added at the end; the one-token kernels of q6k.cu and sbrows.cu
+// share it, so their sums are the same bits.
+__device__ __forceinline__ float q6_codes_dot(const float (&c)[8], const uint32_t (&xw)[4]) {
+    uint64_t p2 = f2_pack(0.f, 0.f);
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        p2 = f2_fma(f2_pack(c[2 * e], c[2 * e + 1]),
+                    f2_pack(__uint_as_float(xw[e] << 16), __uint_as_float(xw[e] & 0xFFFF0000u)), p2);
+    float pe, po;
+    f2_unpack(p2, pe, po);
+    return pe + po;
 }
 
 // S = d * sc of lane l's sub-block (l / 2); exact in fp32.
@@ -200,13 +223,7 @@ __global__ void __launch_bounds__(kQ6Threads) qmm_matmul_q6_k_kernel(const uint8
                                 const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(
                                     X + (int64_t)(m0 + t) * K + (int64_t)(sb0 + u) * 256 + koff));
                                 const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
-                                float part = 0.f;
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    part = fmaf(c[u][2 * e], __uint_as_float(w[e] << 16), part);
-                                    part = fmaf(c[u][2 * e + 1], __uint_as_float(w[e] & 0xFFFF0000u), part);
-                                }
-                                acc[t] = fmaf(S[u], part, acc[t]);
+                                acc[t] = fmaf(S[u], q6_codes_dot(c[u], w), acc[t]);
                             }
                         }
                     }

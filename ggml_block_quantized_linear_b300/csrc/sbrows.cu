@@ -60,13 +60,7 @@ __device__ __forceinline__ void sb_lane_dot(const uint8_t *blk, const uint16_t *
         const int koff = 128 * (lane >> 4) + 32 * ((lane >> 2) & 3) + 8 * (lane & 3);
         const uint4 xv = *reinterpret_cast<const uint4 *>(xsb + koff);
         const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
-        float part = 0.f;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            part = fmaf(c[2 * e], __uint_as_float(w[e] << 16), part);
-            part = fmaf(c[2 * e + 1], __uint_as_float(w[e] & 0xFFFF0000u), part);
-        }
-        acc = fmaf(S, part, acc);
+        acc = fmaf(S, q6_codes_dot(c, w), acc);
     } else {
         const KqCodes kc = kq_lane_codes<kFmt>(kq_lane_load<kFmt, true>(blk, lane), lane);
         const uint4 xv = *reinterpret_cast<const uint4 *>(xsb + 8 * lane);
