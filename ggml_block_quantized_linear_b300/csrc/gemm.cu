@@ -445,9 +445,9 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
     // activation tile is read from DRAM about once and then from L2.
     // Stream-K: tile t = weight tile * tiles_m + token tile, and CTA b takes
     // the pairs [b G / gridDim.x, (b + 1) G / gridDim.x) of the G = tiles x
-    // groups (tile, group) pairs, i.e. a few consecutive tiles, mostly of one
-    // weight tile (read from DRAM once, then from L2) against every token
-    // tile (all of X stays in L2).
+    // groups (tile, group) pairs, i.e. a few consecutive tiles, mostly one
+    // weight tile against consecutive token tiles (the weight tile is then
+    // often still in L2; X, a few MB to tens of MB, mostly stays there).
     const int cid = (int)blockIdx.x, nctas = (int)gridDim.x;
     const int tiles_n = (p.N + kGemmBM - 1) / kGemmBM, tiles_m = (p.M + kBN - 1) / kBN;
     const int ksplit = p.ksplit;
