@@ -223,6 +223,9 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
         : "memory");
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+// Wait for the conversion launch (programmatic dependent launch): its
+// activations, zeroed Y tiles and cleared tickets are visible afterwards.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -246,6 +249,8 @@ __global__ void __launch_bounds__(256) qmm_x_to_f16_kernel(const uint16_t *__res
                                                            int *__restrict__ tickets, int nt,
                                                            float *__restrict__ Yz, int64_t ny,
                                                            const SplitTiles st) {
+    // the GEMM behind this launch may start its prologue and weight stages now
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     for (int i = blockIdx.x * 256 + threadIdx.x; i < nt; i += gridDim.x * 256) tickets[i] = 0;
     const int64_t y4 = ny / 4;  // Y is 16-byte aligned
     for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < y4; i += (int64_t)gridDim.x * 256)
@@ -529,6 +534,7 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
         // ------------------------------------------------ activation TMA producer
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
+            griddep_wait();  // the binary16 activations of the conversion launch
             bool ok = true;
             int bi = 0;  // running activation stage counter
             for (int lt = 0; lt < my_tiles && ok; ++lt) {
@@ -613,6 +619,7 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
         // each storing 64 of the 256 columns of its 32 rows.
         int epi_unit = -1, epi_at = 0;
         auto drain = [&](int lt) {
+            griddep_wait();  // Y (zeroed by the conversion launch for K parts)
             if (ok) ok = mbar_wait_warp(acc_full(0), lt & 1, kErrGemmWait);
             tc_fence_after();
             const int n = tile_n0(lt) + r, m0 = tile_m0(lt);
@@ -715,6 +722,7 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
         const int quarter = warp & 3;  // this warp may read TMEM lanes 32*quarter .. +31
         const int r = 32 * quarter + lane;  // weight row within the tile
         const int etid = tid - 32 * (2 + kGemmDeqWarps);  // 0 .. 127
+        griddep_wait();  // Y and the tickets (cleared by the conversion launch)
         bool ok = true;
         for (int lt = 0; lt < (kNbuf == 1 ? 0 : my_tiles); ++lt) {
             const int buf = lt % kNbuf, use = lt / kNbuf;
@@ -775,6 +783,7 @@ qmm_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
     }
     if constexpr (kNbuf == 2) {
         if (p.tickets_mode && *last_slot) {
+            griddep_wait();
             // this CTA's unit (with tickets, every CTA has one) finished its
             // tile last: Y = part 0 + part 1 + ... in part order, four rows
             // (one float4 of each column-major partial tile) per thread and
@@ -938,15 +947,24 @@ static cudaError_t launch_gemm_t(const void *W, const uint16_t *X, float *Y, int
     p.K = K;
     p.ksplit = pl.ksplit;
     p.tickets_mode = pl.tickets;
-    // one persistent CTA per SM (stream-K: exactly one per SM, the runs' divisor)
+    // one persistent CTA per SM (stream-K: exactly one per SM, the runs'
+    // divisor), by programmatic dependent launch: the CTAs' prologue and
+    // weight stages overlap the conversion launch, and the roles that read X
+    // or write Y, the tickets or the partial tiles wait for it (griddep_wait)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(kGemmThreads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)L.total;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if constexpr (kBN == 256) {
-        if (pl.stream_k) {
-            qmm_gemm_kernel<kFmt, 256, true><<<grid, kGemmThreads, (size_t)L.total, stream>>>(xmap, wmap, p);
-            return cudaGetLastError();
-        }
+        if (pl.stream_k) return cudaLaunchKernelEx(&cfg, qmm_gemm_kernel<kFmt, 256, true>, xmap, wmap, p);
     }
-    qmm_gemm_kernel<kFmt, kBN, false><<<grid, kGemmThreads, (size_t)L.total, stream>>>(xmap, wmap, p);
-    return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, qmm_gemm_kernel<kFmt, kBN, false>, xmap, wmap, p);
 }
 
 template <int kFmt>
