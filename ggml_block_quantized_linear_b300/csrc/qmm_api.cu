@@ -45,6 +45,20 @@ cudaError_t launch_sbrows(int fmt, const void *W, const uint16_t *X, float *Y, i
                           cudaStream_t stream);
 
 constexpr int kMaxDecodeM = 16;
+
+// The tiled (tcgen05) kernel's batches: above 16 tokens, and from 9 tokens
+// on long rows (K >= 12288, where 9-16 tokens of activations no longer stay
+// resident in a decode CTA) for FP8 and Q5_K, from 12 for Q8_0 (4096 x 14336
+// on a B300: the tiled kernel 25.6 / 30.7 / 26.3 us against the decode
+// kernels' 29.5-40.3 / 37.1-57.6 / 30.2 at 9-16 tokens).  Q4_K stays on the
+// decode kernels (even there); Q6_K, Q3_K, Q2_K have no tiled kernel.
+static bool tiled_batch(qmm_format fmt, int64_t M, int64_t K) {
+    if (fmt == QMM_Q6_K || fmt == QMM_Q3_K || fmt == QMM_Q2_K) return false;
+    if (M > kMaxDecodeM) return true;
+    if (K < 12288) return false;
+    if (fmt == QMM_FP8_E4M3 || fmt == QMM_Q5_K) return M >= 9;
+    return fmt == QMM_Q8_0 && M >= 12;
+}
 // Largest dimension accepted (keeps every 32-bit index in the kernels exact).
 constexpr int64_t kMaxDim = (int64_t)1 << 30;
 
@@ -187,8 +201,7 @@ qmm_status qmm_dequantize(qmm_format fmt, const void *src_packed, float *dst, in
 }
 
 size_t qmm_matmul_workspace_bytes(qmm_format fmt, int64_t M, int64_t N, int64_t K) {
-    if (!known_fmt(fmt) || fmt == QMM_Q6_K || fmt == QMM_Q3_K || fmt == QMM_Q2_K || M <= kMaxDecodeM || N <= 0 ||
-        K <= 0 || M > kMaxDim ||
+    if (!known_fmt(fmt) || M <= 0 || !tiled_batch(fmt, M, K) || N <= 0 || K <= 0 || M > kMaxDim ||
         N > kMaxDim || K > kMaxDim || K % kGroup != 0)
         return 0;
     return gemm_workspace_bytes((int)fmt, (int)M, (int)N, (int)K, sm_count());
@@ -213,11 +226,12 @@ qmm_status qmm_matmul(qmm_format fmt, const void *W_packed, const uint16_t *X_bf
         return from_cuda(launch_q6k_matmul(W_packed, X_bf16, Y, (int)M, (int)N, (int)K, sm_count(), s));
     // Q5_K runs the row-tile decode kernel and the tiled kernel (its
     // superblocks are 16-byte aligned, so TMA boxes fit); Q3_K / Q2_K on CUDA cores
-    if (fmt == QMM_Q5_K && M <= kMaxDecodeM)
+    const bool tiled = tiled_batch(fmt, M, K);
+    if (fmt == QMM_Q5_K && !tiled)
         return from_cuda(launch_gemv_rows((int)fmt, W_packed, X_bf16, Y, (int)M, (int)N, (int)K, sm_count(), s));
     if (fmt == QMM_Q3_K || fmt == QMM_Q2_K)
         return from_cuda(launch_kq_matmul((int)fmt, W_packed, X_bf16, Y, (int)M, (int)N, (int)K, sm_count(), s));
-    if (M <= kMaxDecodeM) {
+    if (!tiled) {
         // FP8 has only the row-tile decode kernel
         if (fmt == QMM_FP8_E4M3 || use_rows_kernel((int)M, (int)N, (int)K, sm_count()))
             return from_cuda(launch_gemv_rows((int)fmt, W_packed, X_bf16, Y, (int)M, (int)N, (int)K,

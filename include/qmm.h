@@ -205,11 +205,13 @@ QMM_API size_t qmm_matmul_workspace_bytes(qmm_format fmt, int64_t M, int64_t N, 
  * "NVFP4" (a dedicated matrix-vector kernel for small decode batches, tiled
  * matrix multiplication for larger ones), and the large-batch kernel converts
  * each weight tile inside the GEMM as that page's section "FP8" describes for
- * W8A16.  M <= 16 runs a decode kernel: persistent CTAs over 16-row tiles
+ * W8A16.  M <= 16 runs a decode kernel (except on long rows, K >= 12288,
+ * where FP8 and Q5_K from M = 9 and Q8_0 from M = 12 run the tiled kernel,
+ * measured faster there): persistent CTAs over 16-row tiles
  * when the tiles fill the GPU (each tile's partial sums added in a fixed
  * order), otherwise split-K over a thread-block cluster reduced in
  * distributed shared memory in a fixed order; both are deterministic.
- * FP8 runs the row-tile decode kernel for every M <= 16 (codes converted
+ * FP8 runs the row-tile decode kernel for M <= 16 (codes converted
  * exactly to binary16 in the MMA fragments, the row scale applied to the
  * finished sums) and the tiled kernel above that (each weight tile converted
  * to binary16 inside the GEMM, the row scale applied in the epilogue).

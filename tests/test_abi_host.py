@@ -110,10 +110,20 @@ def test_workspace_query(lib):
         # tiles and one ticket per tile follow (256-byte aligned regions)
         # 512 x 4096: 256-token tiles, K halves added onto a zeroed Y
         assert q.qmm_matmul_workspace_bytes(fmt, 512, 4096, 4096) == 512 * 4096 * 2
-        # 2048 x 14336: 112 x 8 tiles fill the SMs, no split
+        # 2048 x 14336: 112 x 8 tiles, stream-K onto a zeroed Y (no partial tiles)
         assert q.qmm_matmul_workspace_bytes(fmt, 2048, 14336, 4096) == 2048 * 4096 * 2
         # 32 tokens: a 32-token tile; 8 weight tiles, K in min(16, 148 // 8, 8) = 8 parts
         assert q.qmm_matmul_workspace_bytes(fmt, 32, 1024, 4096) == 32 * 4096 * 2 + 8 * 8 * 32 * 128 * 4 + 256
+    # long rows (K >= 12288) at decode batch sizes: FP8 and Q5_K from 9 tokens,
+    # Q8_0 from 12 run the tiled kernel (workspace); Q4_K and shorter rows do not
+    F8 = q.QMM_FP8_E4M3
+    assert q.qmm_matmul_workspace_bytes(F8, 8, 4096, 14336) == 0
+    assert q.qmm_matmul_workspace_bytes(F8, 9, 4096, 14336) > 9 * 14336 * 2
+    assert q.qmm_matmul_workspace_bytes(q.QMM_Q5_K, 9, 4096, 12288) > 0
+    assert q.qmm_matmul_workspace_bytes(q.QMM_Q8_0, 11, 4096, 14336) == 0
+    assert q.qmm_matmul_workspace_bytes(q.QMM_Q8_0, 12, 4096, 14336) > 0
+    assert q.qmm_matmul_workspace_bytes(q.QMM_Q4_K, 16, 4096, 14336) == 0
+    assert q.qmm_matmul_workspace_bytes(F8, 16, 4096, 11264) == 0
     L = lib
     assert L.qmm_matmul(8, FAKE, FAKE, FAKE, 32, 64, 256, NULL, 0, S0) == q.QMM_ERR_WORKSPACE
     assert L.qmm_matmul(4, FAKE, FAKE, FAKE, 32, 64, 256, FAKE, 100, S0) == q.QMM_ERR_WORKSPACE

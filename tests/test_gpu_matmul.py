@@ -230,6 +230,21 @@ def test_mid_batch_full(fmt, n, k, m):
     assert torch.equal(y, run(fmt, packed, xb, n))  # same parts, same order
 
 
+# Long rows (K >= 12288) at 9-16 tokens: FP8 and Q5_K from 9 tokens and
+# Q8_0 from 12 take the tiled kernel, the others (and shorter rows) the
+# decode kernels; both sides of each threshold, compared in full.
+@pytest.mark.parametrize("fmt", FMTS + [q.QMM_Q5_K, q.QMM_FP8_E4M3])
+@pytest.mark.parametrize("n,k,m", [(300, 14336, 8), (300, 14336, 9), (300, 14336, 11), (300, 12288, 12),
+                                   (257, 14336, 16), (300, 11264, 16)])
+def test_long_rows_decode_batches_full(fmt, n, k, m):
+    packed, xb = problem(fmt, n, k, m, 9500 + n + k + m)
+    Y, A = oracle.matmul(fmt, packed, xb, n, k)
+    y = run(fmt, packed, xb, n)
+    check_matmul(y, Y, A, "fmt=%d n=%d k=%d m=%d" % (fmt, n, k, m))
+    assert torch.equal(y, run(fmt, packed, xb, n))
+    assert q.qmm_device_error_take() == 0
+
+
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("shape", inputs.DECODE_SHAPES)
 @pytest.mark.parametrize("m", [17, 32, 64, 128])
