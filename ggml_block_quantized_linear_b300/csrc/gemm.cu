@@ -6,14 +6,17 @@
 // batches to tiled matrix multiplication (section NVFP4) and describes FP8
 // W8A16 GEMMs that convert each weight tile to BF16 / F16 inside the GEMM
 // (section FP8).  This kernel does the same for the GGML block formats: the
-// packed weight tile is dequantized in shared memory and fed to tcgen05.mma.
+// packed weight tile is dequantized in registers into tensor memory and fed
+// to tcgen05.mma.
 //
 // Operand precision.  The dequantized weights are rounded to binary16 (not
 // bf16): the relative error 2^-11 per weight keeps every output inside
 // 1e-3 * sum|w x| even for a one-hot activation row, which bf16's 2^-9 does
 // not.  tcgen05 kind::f16 needs both operands in one type, so the bf16
 // activations are converted to binary16 once per call (first kernel below)
-// into the caller's workspace.
+// into the caller's workspace.  The GEMM follows that launch by programmatic
+// dependent launch: its prologue and weight stages overlap the conversion,
+// and the roles that read X or write Y, tickets or partial tiles wait for it.
 //
 // Tile: 128 weight rows (the MMA's M side, "swap AB") x BN tokens (MMA N:
 // 32, 64, 128 or 256, the smallest that holds M up to 128; above that 256)
@@ -31,7 +34,7 @@
 // one of 256 columns for 256-token tiles (two stages), which the
 // dequantizing warps drain themselves where they would otherwise wait for
 // the unit's last MMA.
-// 256-token tiles, at least as many as the CTAs (stream-K): the (tile,
+// 256-token tiles, four waves or more (stream-K): the (tile,
 // packed group) pairs, token tile fastest, are cut into one contiguous run
 // per CTA, so every CTA has the same K work and the last wave is not left
 // part-empty.  A run is at least one tile long, so a tile falls to at most
@@ -40,10 +43,10 @@
 // one part of one tile).  256-token tiles: at most two parts, both added onto
 // a Y zeroed by the conversion launch.  (Two additions onto zero commute, so
 // neither result depends on the order of the parts.)  Smaller tiles: up to
-// 8 parts; each part stores its partial tile in the workspace and takes a
-// ticket, and the last part of a tile to arrive adds all parts in part order
-// and writes Y.  All are deterministic and nothing ever waits for another
-// CTA.
+// 8 parts, one unit per CTA; each part stores its partial tile in the
+// workspace and takes a ticket, and in the CTA whose part arrives last every
+// warp, once its role has ended, helps add all parts in part order into Y.
+// All are deterministic and nothing ever waits for another CTA.
 //   warp 0       TMA producer of the binary16 activation tiles (128B-swizzled
 //                boxes)
 //   warp 1       TMEM allocator and single-thread MMA issuer
