@@ -302,7 +302,11 @@ class Workload:
                         q.qmm_matmul(f, p, x, n, out=y)
             wbytes = sum(nw * bw[f] for f in self.fmts)
             io = 2 * sum((2 * m * k + 4 * m * n) for n, k in shapes)
-            S.append(("gemv_m%d" % m, gemv, 8, wbytes + io, 2.0 * 2 * m * nw, "gemv", 2 * nw))
+            # a call that takes the tiled kernel (it needs a workspace: long rows
+            # from 12 tokens for Q8_0) launches the activation conversion too
+            nl = sum(2 if q.qmm_matmul_workspace_bytes(f, m, n, k) > 0 else 1
+                     for f in self.fmts for (n, k) in shapes)
+            S.append(("gemv_m%d" % m, gemv, nl, wbytes + io, 2.0 * 2 * m * nw, "gemv", 2 * nw))
 
         if self.gemm_ok:
             for m in inputs.MID_MS:
